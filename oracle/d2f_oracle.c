@@ -1,0 +1,360 @@
+/*
+ * CPU oracle for the per-step hot path of Discrete Diffusion Forcing (D2F)
+ * block-diffusion decoding.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing in the product path links, loads or calls
+ * this file; only the tests, the smoke check and the benchmark's CPU-baseline
+ * leg do. It shares no code, header, table or helper with the CUDA library.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [P1] "D2F: 확산 언어 모델이 KV 캐시를 얻고 자기회귀 모델보다 2.5배 빨라지는
+ *        방법 (arXiv:2508.09192)" (llm-wiki.hwlabs.dev)
+ *   [P2] "D2F 논문 리뷰: 확산 LLM이 자기회귀 모델보다 빠른 추론을 처음으로
+ *        달성한 방식" (allinfo.ai.kr)
+ *   [P3] "확산 언어 모델(Diffusion LLM)이란 무엇인가" (discuss.pytorch.kr)
+ *
+ * Every function below is the plain definition written out: no blocking, no
+ * fusion, no reordering. Floating-point attention is done in double precision;
+ * the commit widens logits to float (exact for bf16), accumulates the softmax
+ * denominator in double and rounds the confidence to float.
+ *
+ * Parity pins for every function live in tests/ (brute force, closed forms,
+ * hand-worked examples, invariants); none of them is "parity unpinned".
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_DT_BF16 0
+#define ORACLE_DT_F32 1
+#define ORACLE_DT_F64 2
+
+/* Element access that widens the stored value exactly. bf16 is the upper half
+ * of an IEEE binary32, so shifting its bits left by 16 gives the same number. */
+static double load_elem(const void *base, int64_t idx, int dtype) {
+  if (dtype == ORACLE_DT_BF16) {
+    uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+  }
+  if (dtype == ORACLE_DT_F64) return ((const double *)base)[idx];
+  return (double)((const float *)base)[idx];
+}
+
+static float load_elem_f32(const void *base, int64_t idx, int dtype) {
+  if (dtype == ORACLE_DT_BF16) {
+    uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return f;
+  }
+  return ((const float *)base)[idx];
+}
+
+/*
+ * Block-causal attention of the active window over [cached context ; window].
+ *
+ * [P1] §블록 단위 인과 어텐션: the output is cut into fixed-size blocks; tokens
+ * of one block attend to each other in both directions, a block attends only to
+ * earlier blocks, so a finished block's K/V never change and go into an
+ * ordinary KV cache. [P2] §쉽게 이해하기: a window of active blocks is decoded
+ * together, each seeing its own block and the blocks before it.
+ *
+ * For sequence b with cached length C_b = ctx_len[b] and window rows
+ * q_start[b] .. q_start[b+1]-1 (n_b rows, window block of row i is i / B), query
+ * head h (KV head g = h / (Hq/Hkv)) of window row i sees:
+ *   - every cached token t < C_b, stored in pool page page_table[b][t / B] at
+ *     slot t % B, and
+ *   - every window row i2 of the same sequence whose block i2 / B is not later
+ *     than i / B.
+ * Score = scale * <q, k>; output = softmax-weighted sum of v (max-subtracted
+ * softmax in double); lse = natural-log normaliser (max + log(sum)).
+ *
+ * Operands are bf16, float or double (dtype 0 / 1 / 2), all of one type.
+ * Layouts (row-major): q [total_q, Hq, D]; k_win, v_win [total_q, Hkv, D];
+ * k_pool, v_pool [num_pages, Hkv, B, D]; page_table [batch, max_pages_per_seq];
+ * out [total_q, Hq, D] double; lse [total_q, Hq] double (may be NULL).
+ *
+ * Returns 0, or a negative code: -1 bad sizes, -2 inconsistent q_start,
+ * -3 page id out of range, -4 out of memory.
+ */
+int d2f_oracle_block_attn(const void *q, const void *k_win, const void *v_win,
+                          const void *k_pool, const void *v_pool,
+                          const int32_t *page_table, int max_pages_per_seq,
+                          const int32_t *ctx_len, const int32_t *q_start,
+                          int batch, int total_q, int num_heads_q,
+                          int num_heads_kv, int head_dim, int block_size,
+                          int num_pages, int dtype, double scale, double *out,
+                          double *lse, int nthreads) {
+  if (batch < 0 || num_heads_q <= 0 || num_heads_kv <= 0 || head_dim <= 0 ||
+      block_size <= 0 || num_heads_q % num_heads_kv != 0)
+    return -1;
+  if (q_start[0] != 0 || q_start[batch] != total_q) return -2;
+  for (int b = 0; b < batch; ++b) {
+    if (q_start[b + 1] < q_start[b]) return -2;
+    if (ctx_len[b] < 0 || ctx_len[b] > max_pages_per_seq * block_size) return -1;
+    int used_pages = (ctx_len[b] + block_size - 1) / block_size;
+    for (int p = 0; p < used_pages; ++p) {
+      int32_t pg = page_table[(int64_t)b * max_pages_per_seq + p];
+      if (pg < 0 || pg >= num_pages) return -3;
+    }
+  }
+  const int G = num_heads_q / num_heads_kv;
+  const int H = num_heads_q, Hk = num_heads_kv, D = head_dim, B = block_size;
+  const int64_t n_items = (int64_t)total_q * H;
+  int err = 0;
+
+#pragma omp parallel for schedule(dynamic, 4) num_threads(nthreads > 0 ? nthreads : 1)
+  for (int64_t item = 0; item < n_items; ++item) {
+    const int R = (int)(item / H); /* global window row */
+    const int h = (int)(item % H);
+    const int g = h / G;
+    int b = 0;
+    while (q_start[b + 1] <= R) ++b;
+    const int i = R - q_start[b];
+    const int n_b = q_start[b + 1] - q_start[b];
+    const int C = ctx_len[b];
+    const int max_keys = C + n_b;
+
+    double *s = (double *)malloc(sizeof(double) * (size_t)(max_keys > 0 ? max_keys : 1));
+    int64_t *koff = (int64_t *)malloc(sizeof(int64_t) * (size_t)(max_keys > 0 ? max_keys : 1));
+    int *kwin = (int *)malloc(sizeof(int) * (size_t)(max_keys > 0 ? max_keys : 1));
+    if (!s || !koff || !kwin) {
+#pragma omp atomic write
+      err = -4;
+      free(s); free(koff); free(kwin);
+      continue;
+    }
+
+    /* Build the visible key set K(i). */
+    int nk = 0;
+    for (int t = 0; t < C; ++t) {
+      int32_t page = page_table[(int64_t)b * max_pages_per_seq + t / B];
+      int slot = t % B;
+      koff[nk] = (((int64_t)page * Hk + g) * B + slot) * D;
+      kwin[nk] = 0;
+      ++nk;
+    }
+    for (int i2 = 0; i2 < n_b; ++i2) {
+      if (i2 / B <= i / B) {
+        koff[nk] = ((int64_t)(q_start[b] + i2) * Hk + g) * D;
+        kwin[nk] = 1;
+        ++nk;
+      }
+    }
+
+    const int64_t qoff = ((int64_t)R * H + h) * D;
+    double mx = -INFINITY;
+    for (int kk = 0; kk < nk; ++kk) {
+      const void *kb = kwin[kk] ? k_win : k_pool;
+      double dot = 0.0;
+      for (int d = 0; d < D; ++d)
+        dot += load_elem(q, qoff + d, dtype) * load_elem(kb, koff[kk] + d, dtype);
+      s[kk] = scale * dot;
+      if (s[kk] > mx) mx = s[kk];
+    }
+    double denom = 0.0;
+    for (int kk = 0; kk < nk; ++kk) {
+      s[kk] = exp(s[kk] - mx);
+      denom += s[kk];
+    }
+    double *o = out + qoff;
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    for (int kk = 0; kk < nk; ++kk) {
+      const void *vb = kwin[kk] ? v_win : v_pool;
+      const double w = s[kk] / denom;
+      for (int d = 0; d < D; ++d) o[d] += w * load_elem(vb, koff[kk] + d, dtype);
+    }
+    if (lse) lse[(int64_t)R * H + h] = mx + log(denom);
+    free(s);
+    free(koff);
+    free(kwin);
+  }
+  return err;
+}
+
+/*
+ * Per-position confidence of a still-masked position.
+ *
+ * [P3] §양방향 어텐션과 사라진 KV 캐시 and §토큰 순서의 이론: LLaDA's default
+ * low-confidence remasking ranks positions by the largest softmax probability
+ * of the prediction. For a logit row l: m = max_v l_v, a = the lowest v with
+ * l_v = m (greedy token), p_max = exp(m - logsumexp(l)) = 1 / sum_v exp(l_v - m).
+ * Comparisons are exact in float; the sum is accumulated in double and the
+ * reciprocal rounded to float once.
+ */
+static void row_confidence(const void *logits, int64_t row_off, int dtype,
+                           int vocab, float *p_out, int32_t *a_out) {
+  float m = -INFINITY;
+  int32_t a = -1;
+  for (int v = 0; v < vocab; ++v) {
+    float x = load_elem_f32(logits, row_off + v, dtype);
+    if (x > m || a < 0) {
+      m = x;
+      a = v;
+    }
+  }
+  double S = 0.0;
+  for (int v = 0; v < vocab; ++v) {
+    double x = (double)load_elem_f32(logits, row_off + v, dtype);
+    S += exp(x - (double)m);
+  }
+  *p_out = (float)(1.0 / S);
+  *a_out = a;
+}
+
+/*
+ * Confidence commit with conservative / aggressive phases, then remasking.
+ *
+ * [P2] §쉽게 이해하기 (pipelined decoding): a block that has just entered the
+ * window is conservative and fixes only the tokens whose confidence is above
+ * the threshold; once its predecessor has progressed enough it turns
+ * aggressive and also fixes the relatively most confident token even when that
+ * one is below the threshold; every token not fixed is masked again for the
+ * next step. [P3] §양방향 어텐션과 사라진 KV 캐시: confidence is the maximum
+ * softmax probability (low-confidence remasking).
+ *
+ * Readings where the pages are silent: "above" is strict (p > tau, in float);
+ * the aggressive set is {p > tau} plus the masked position of highest p (lowest
+ * position on ties); a block with no masked position commits nothing; positions
+ * that were already committed are neither read nor changed.
+ *
+ * Window block jb covers rows jb*B .. jb*B+B-1 (q_start values are multiples of
+ * B); its sequence b is the one whose rows contain it, tau[b] its threshold and
+ * block_phase[jb] its phase (0 conservative, 1 aggressive).
+ *
+ * On return: committed rows get tokens[r] = a_r, masked[r] = 0; rows still
+ * masked get tokens[r] = mask_id; rows not masked on entry keep their token.
+ * conf_out[r] / argmax_out[r] = p_max / a for rows masked on entry and
+ * -1 / -1 for the others (either may be NULL); block_remaining[jb] = masked
+ * rows of block jb after the commit (may be NULL). logit_row (may be NULL)
+ * maps position r to the logit row holding its prediction (identity when NULL).
+ *
+ * Returns 0, or -1 bad sizes, -2 inconsistent q_start, -3 logit row out of range.
+ */
+int d2f_oracle_commit(const void *logits, int64_t row_stride, int dtype,
+                      int vocab, int num_logit_rows, const int32_t *logit_row,
+                      int32_t *tokens, uint8_t *masked, const int32_t *q_start,
+                      const uint8_t *block_phase, const float *tau, int batch,
+                      int total_q, int block_size, int32_t mask_id,
+                      float *conf_out, int32_t *argmax_out,
+                      int32_t *block_remaining, int nthreads) {
+  if (batch < 0 || total_q < 0 || vocab <= 0 || block_size <= 0 ||
+      block_size > 1024 || total_q % block_size != 0 || row_stride < vocab)
+    return -1;
+  if (q_start[0] != 0 || q_start[batch] != total_q) return -2;
+  for (int b = 0; b < batch; ++b)
+    if (q_start[b + 1] < q_start[b] || q_start[b] % block_size != 0) return -2;
+  for (int r = 0; r < total_q; ++r) {
+    int lr = logit_row ? logit_row[r] : r;
+    if (masked[r] && (lr < 0 || lr >= num_logit_rows)) return -3;
+  }
+
+  float *conf = (float *)malloc(sizeof(float) * (size_t)(total_q > 0 ? total_q : 1));
+  int32_t *amax = (int32_t *)malloc(sizeof(int32_t) * (size_t)(total_q > 0 ? total_q : 1));
+  if (!conf || !amax) {
+    free(conf);
+    free(amax);
+    return -4;
+  }
+
+  /* Confidence and greedy token of every position that is still masked. */
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads > 0 ? nthreads : 1)
+  for (int r = 0; r < total_q; ++r) {
+    if (masked[r]) {
+      int lr = logit_row ? logit_row[r] : r;
+      row_confidence(logits, (int64_t)lr * row_stride, dtype, vocab, &conf[r], &amax[r]);
+    } else {
+      conf[r] = -1.0f;
+      amax[r] = -1;
+    }
+  }
+
+  /* Block-level commit decision, then remasking. */
+  const int n_blocks = total_q / block_size;
+  for (int jb = 0; jb < n_blocks; ++jb) {
+    const int r0 = jb * block_size;
+    int b = 0;
+    while (q_start[b + 1] <= r0) ++b;
+    const float t = tau[b];
+    uint8_t commit[1024];
+    int any_masked = 0;
+    for (int u = 0; u < block_size; ++u) {
+      const int r = r0 + u;
+      commit[u] = 0;
+      if (!masked[r]) continue;
+      any_masked = 1;
+      if (conf[r] > t) commit[u] = 1;
+    }
+    if (block_phase[jb] == 1 && any_masked) {
+      int best = -1;
+      for (int u = 0; u < block_size; ++u) {
+        const int r = r0 + u;
+        if (!masked[r]) continue;
+        if (best < 0 || conf[r] > conf[r0 + best]) best = u;
+      }
+      commit[best] = 1;
+    }
+    int remaining = 0;
+    for (int u = 0; u < block_size; ++u) {
+      const int r = r0 + u;
+      if (!masked[r]) continue;
+      if (commit[u]) {
+        tokens[r] = amax[r];
+        masked[r] = 0;
+      } else {
+        tokens[r] = mask_id;
+        ++remaining;
+      }
+    }
+    if (block_remaining) block_remaining[jb] = remaining;
+  }
+  for (int r = 0; r < total_q; ++r) {
+    if (conf_out) conf_out[r] = conf[r];
+    if (argmax_out) argmax_out[r] = amax[r];
+  }
+  free(conf);
+  free(amax);
+  return 0;
+}
+
+/*
+ * Append finished blocks' K/V to the paged cache.
+ *
+ * [P1] §블록 단위 인과 어텐션 and §운영 관점 (KV 캐시 관리 방식): a completed
+ * block's K/V are final and are stored permanently; with a paged cache whose
+ * page is one block, completion of a block is the signal to persist it.
+ *
+ * For append a: rows src_row[a] .. src_row[a]+B-1 of k_win / v_win
+ * ([total_q, Hkv, D]) are copied into page dst_page[a] of k_pool / v_pool
+ * ([num_pages, Hkv, B, D]) as pool[dst][g][s][:] = win[src + s][g][:].
+ * elem_bytes is 2 (bf16), 4 (float) or 8 (double); the copy is bitwise.
+ * Returns 0, or -1 bad sizes, -3 page or row out of range.
+ */
+int d2f_oracle_kv_append(const void *k_win, const void *v_win,
+                         const int32_t *src_row, const int32_t *dst_page,
+                         int n_append, int total_q, void *k_pool, void *v_pool,
+                         int num_heads_kv, int head_dim, int block_size,
+                         int num_pages, int elem_bytes) {
+  if (n_append < 0 || num_heads_kv <= 0 || head_dim <= 0 || block_size <= 0 ||
+      (elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8))
+    return -1;
+  for (int a = 0; a < n_append; ++a) {
+    if (dst_page[a] < 0 || dst_page[a] >= num_pages) return -3;
+    if (src_row[a] < 0 || src_row[a] + block_size > total_q) return -3;
+  }
+  const int64_t row_bytes = (int64_t)head_dim * elem_bytes;
+  for (int a = 0; a < n_append; ++a) {
+    for (int g = 0; g < num_heads_kv; ++g) {
+      for (int s = 0; s < block_size; ++s) {
+        int64_t src = ((int64_t)(src_row[a] + s) * num_heads_kv + g) * row_bytes;
+        int64_t dst = (((int64_t)dst_page[a] * num_heads_kv + g) * block_size + s) * row_bytes;
+        memcpy((char *)k_pool + dst, (const char *)k_win + src, (size_t)row_bytes);
+        memcpy((char *)v_pool + dst, (const char *)v_win + src, (size_t)row_bytes);
+      }
+    }
+  }
+  return 0;
+}
