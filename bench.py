@@ -1,0 +1,613 @@
+#!/usr/bin/env python
+"""Benchmark of the D2F decoding hot path: block-attn + commit steps/s.
+
+One step = d2f_block_attn (one layer, the whole active window) + d2f_commit
+(every still-masked window position), + d2f_kv_append where the workload
+appends, preceded by a 2-copy reset of the decode state (tokens, masked) so that
+every step does the same work. Default workload: the LLaDA-8B-shaped layer
+(batch 1, 32 MHA heads, head_dim 128, bf16, context 1024 in 16-token pages,
+window 3 blocks = 48 queries, vocabulary 126464).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload llada]
+    python bench.py --impl reference ...   # the CPU oracle, timed the same way
+
+Timing: inputs resident in HBM; the step cycles through enough independent
+input sets (> 4x L2) that no step finds its inputs in L2; K steps replayed from
+CUDA graphs between CUDA events, barrier + synchronize on both sides, max over
+ranks. Per-kernel durations come from CUDA events captured in the same graphs.
+Prints one JSON line (rank 0).
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "block-attn + commit steps/sec and achieved HBM GB/s (% of GB300 roofline)"
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llada")
+    ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--commit-splits", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--profile-steps", type=int, default=0,
+                    help="run this many eager steps and exit (for ncu captures)")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU, replicas: no data-path collective)
+# ---------------------------------------------------------------------------
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# workload accounting
+# ---------------------------------------------------------------------------
+def algorithmic_bytes(p):
+    """Bytes a step must move at minimum: cached K+V once per (sequence, KV
+    head), window K/V, Q, O, page ids; logits of masked rows; appended blocks."""
+    w = p.w
+    elt = 2 if w.dtype == torch.bfloat16 else 4
+    Hk, H, D = w.num_heads_kv, w.num_heads_q, w.head_dim
+    ctx = sum(w.ctx_lens)
+    tq = w.total_q
+    pages = sum((c + w.block_size - 1) // w.block_size for c in w.ctx_lens)
+    attn = 2 * ctx * Hk * D * elt + 2 * tq * Hk * D * elt + 2 * tq * H * D * elt + pages * 4 * Hk
+    masked_rows = int(p.masked.sum())
+    commit = masked_rows * w.vocab * elt + tq * 6
+    append = 2 * 2 * len(p.src_row) * w.block_size * Hk * D * elt
+    return attn, commit, append
+
+
+def flops(p):
+    w = p.w
+    f = 0
+    for c, nb in zip(w.ctx_lens, w.window_blocks):
+        n = nb * w.block_size
+        keys = sum(c + (i // w.block_size + 1) * w.block_size for i in range(n))
+        f += 4 * w.num_heads_q * w.head_dim * keys
+    return f
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "attn": ["block_causal_kv_gb300/csrc/attn_tc.cu", "block_causal_kv_gb300/csrc/attn_common.cuh",
+             "block_causal_kv_gb300/csrc/d2f_internal.cuh"],
+    "commit": ["block_causal_kv_gb300/csrc/commit.cu", "block_causal_kv_gb300/csrc/d2f_internal.cuh"],
+}
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel source is
+    unchanged since the counters were taken; else None."""
+    path = os.path.join(PROFILES, "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel + ":" + workload]
+    except Exception:
+        return None
+    if rec.get("source_sha") != source_sha(KERNEL_SOURCES[kernel]):
+        return None
+    return rec.get("bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+CLOCK_FIELDS = ("timestamp,index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,"
+                "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+                "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                "clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, out_path=None):
+        self.proc = None
+        self.out_path = out_path or os.path.join("/tmp", "d2f_clocks_%d.csv" % os.getpid())
+
+    def start(self):
+        try:
+            self.fh = open(self.out_path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + CLOCK_FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self, bus_id=None):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.out_path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 11:
+                    continue
+                if bus_id is not None:
+                    try:  # "DDDDDDDD:BB:DD.F" -> bus number
+                        if int(parts[2].split(":")[1], 16) != int(bus_id):
+                            continue
+                    except (ValueError, IndexError):
+                        pass
+                try:
+                    rows.append(dict(sm=float(parts[3]), smax=float(parts[4]),
+                                     power=float(parts[5]) if parts[5] not in ("[N/A]", "") else None,
+                                     hw=parts[7], hwt=parts[8], swt=parts[9], swp=parts[10]))
+                except ValueError:
+                    continue
+        if not rows:
+            return None
+        busy = [r for r in rows if r["power"] is None or r["power"] > 0] or rows
+        reasons = set()
+        for r in busy:
+            for k, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                            ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[k].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in busy),
+                "sm_max_mhz": max(r["smax"] for r in busy), "reasons": sorted(reasons),
+                "samples": len(busy)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+def time_oracle(p, seconds, nthreads):
+    """Time the CPU oracle on a bounded sample of one step and extrapolate to
+    full steps: attention over a subset of KV heads (its cost is linear in heads)
+    and the commit over a subset of rows (linear in rows)."""
+    import oracle
+    w = p.w
+    Hk, G = w.num_heads_kv, w.num_heads_q // w.num_heads_kv
+    # calibrate with one KV head and one block of rows
+    def attn_sample(nh):
+        hk = list(range(nh))
+        hq = [h for g in hk for h in range(g * G, (g + 1) * G)]
+        t0 = time.perf_counter()
+        oracle.block_attn(p.q[:, hq], p.k_win[:, hk], p.v_win[:, hk], p.k_pool[:, hk],
+                          p.v_pool[:, hk], p.page_table, p.ctx_len, p.q_start, w.block_size,
+                          nthreads=nthreads, want_lse=False)
+        return time.perf_counter() - t0
+
+    def commit_sample(nb):
+        B = w.block_size
+        rows = nb * B
+        qs = torch.tensor([0, rows], dtype=torch.int32)
+        t0 = time.perf_counter()
+        oracle.commit(p.logits[:rows], p.tokens[:rows], p.masked[:rows], qs,
+                      p.block_phase[:nb], p.tau[:1], B, p.mask_id, nthreads=nthreads)
+        return time.perf_counter() - t0
+
+    ta1 = attn_sample(1)
+    tc1 = commit_sample(1)
+    n_blocks = w.total_q // w.block_size
+    # grow the sample so that the whole measurement takes about `seconds`
+    est_step = ta1 * Hk + tc1 * n_blocks
+    nh = max(1, min(Hk, int(Hk * min(1.0, seconds / 2 / max(est_step, 1e-9)))))
+    nb = max(1, min(n_blocks, int(n_blocks * min(1.0, seconds / 2 / max(est_step, 1e-9)))))
+    reps = 0
+    ta = tc = 0.0
+    t_start = time.perf_counter()
+    while True:
+        ta += attn_sample(nh)
+        tc += commit_sample(nb)
+        reps += 1
+        if time.perf_counter() - t_start >= seconds:
+            break
+    step_s = (ta / reps) * Hk / nh + (tc / reps) * n_blocks / nb
+    sample = ("%d x [attention for %d of %d KV heads + commit for %d of %d window blocks], "
+              "extrapolated linearly to full steps" % (reps, nh, Hk, nb, n_blocks))
+    return 1.0 / step_s, sample
+
+
+def oracle_threads():
+    return max(1, len(os.sched_getaffinity(0)))
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    from block_causal_kv_gb300 import synth
+    import oracle
+    oracle._load()
+    w = synth.workload(args.workload)
+    p = synth.make_problem(w)
+    nthreads = oracle_threads()
+    # bounded: the whole run takes about a minute regardless of K
+    budget = 60.0
+    for _ in range(max(0, min(args.warmup, 1))):
+        time_oracle(p, 0.1, nthreads)
+    value, sample = time_oracle(p, budget, nthreads)
+    ms = 1000.0 / value
+    cfg = workload_config(p, args)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "config": cfg,
+            "cpu_baseline": {"value": value, "unit": "steps/s", "cores": nthreads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(p, args):
+    w = p.w
+    return {"workload": "%s: batch %d, Hq %d / Hkv %d, head_dim %d, block %d, context %s, "
+                        "window %s blocks, vocab %d" % (
+                            w.name, w.batch, w.num_heads_q, w.num_heads_kv, w.head_dim,
+                            w.block_size, "/".join(str(c) for c in sorted(set(w.ctx_lens))),
+                            "/".join(str(x) for x in sorted(set(w.window_blocks))), w.vocab),
+            "batch": w.batch, "window_queries": w.total_q, "context": max(w.ctx_lens),
+            "parallelism": "replica per GPU (no collective)"}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+class StepSet:
+    """Device buffers of one independent input set."""
+
+    def __init__(self, p, dev, clone_from=None):
+        src = clone_from
+        for name in ("q", "k_win", "v_win", "k_pool", "v_pool", "page_table", "ctx_len", "q_start",
+                     "tokens", "masked", "block_phase", "tau", "src_row", "dst_page"):
+            if src is None:
+                setattr(self, name, getattr(p, name).to(dev))
+            else:
+                setattr(self, name, getattr(src, name).clone())
+        if src is None:
+            self.logits = p.logits.contiguous().to(dev)
+        else:
+            self.logits = src.logits.clone()
+        self.out = torch.empty_like(self.q)
+
+    def nbytes(self):
+        return sum(t.numel() * t.element_size() for t in
+                   (self.q, self.k_win, self.v_win, self.k_pool, self.v_pool, self.logits, self.out))
+
+
+def run_ours(args, world, rank, local):
+    from block_causal_kv_gb300 import d2f, synth
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = synth.workload(args.workload)
+    big = w.name.startswith("long") or w.name in ("dream", "ragged")
+    p = synth.make_problem(w, device="cuda" if big else "cpu")
+    base = StepSet(p, dev)
+    tokens0, masked0 = base.tokens.clone(), base.masked.clone()
+    B = w.block_size
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
+    per_set = base.nbytes()
+    n_sets = max(1, min(64, -(-4 * l2 // per_set)))
+    sets = [base] + [StepSet(p, dev, clone_from=base) for _ in range(n_sets - 1)]
+    appends = len(p.src_row) > 0
+
+    ws_attn = d2f.attn_workspace(dev, batch=w.batch, total_q=w.total_q,
+                                 max_q_per_seq=p.max_q_per_seq, max_ctx=p.max_ctx,
+                                 num_heads_q=w.num_heads_q, num_heads_kv=w.num_heads_kv,
+                                 head_dim=w.head_dim, block_size=B, num_splits=args.num_splits)
+    ws_commit = d2f.commit_workspace(dev, total_q=w.total_q, vocab=w.vocab, block_size=B,
+                                     num_splits=args.commit_splits)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    conf = torch.empty(w.total_q, dtype=torch.float32, device=dev)
+    amax = torch.empty(w.total_q, dtype=torch.int32, device=dev)
+    rem = torch.empty(w.total_q // B, dtype=torch.int32, device=dev)
+
+    def attn(s):
+        d2f.block_attn(s.q, s.k_win, s.v_win, s.k_pool, s.v_pool, s.page_table, s.ctx_len,
+                       s.q_start, block_size=B, max_q_per_seq=p.max_q_per_seq, max_ctx=p.max_ctx,
+                       num_splits=args.num_splits, out=s.out, want_lse=False, workspace=ws_attn,
+                       err=err)
+
+    def commit(s):
+        d2f.commit(s.logits, s.tokens, s.masked, s.q_start, s.block_phase, s.tau, block_size=B,
+                   mask_id=p.mask_id, num_splits=args.commit_splits, conf=conf, argmax=amax,
+                   block_remaining=rem, workspace=ws_commit, err=err)
+
+    def append(s):
+        d2f.kv_append(s.k_win, s.v_win, s.src_row, s.dst_page, s.k_pool, s.v_pool, block_size=B,
+                      err=err)
+
+    def reset(s):
+        s.tokens.copy_(tokens0)
+        s.masked.copy_(masked0)
+
+    if args.profile_steps:
+        for i in range(args.profile_steps):
+            s = sets[i % n_sets]
+            reset(s)
+            attn(s)
+            commit(s)
+            if appends:
+                append(s)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0, "device error %d" % int(err.item())
+        return
+
+    stream = torch.cuda.Stream(device=dev)
+    # warm-up (library init, function attributes) outside capture
+    with torch.cuda.stream(stream):
+        for i in range(max(3, min(args.warmup, n_sets))):
+            s = sets[i % n_sets]
+            reset(s)
+            attn(s)
+            commit(s)
+            if appends:
+                append(s)
+    stream.synchronize()
+
+    try:
+        ev_kw = dict(enable_timing=True, external=True)
+        torch.cuda.Event(**ev_kw)
+        have_ext = True
+    except TypeError:
+        have_ext = False
+
+    def capture(indices, with_events):
+        g = torch.cuda.CUDAGraph()
+        evs = []
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+            for i in indices:
+                s = sets[i]
+                reset(s)
+                e = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)] \
+                    if with_events else None
+                if e:
+                    e[0].record()
+                attn(s)
+                if e:
+                    e[1].record()
+                commit(s)
+                if e:
+                    e[2].record()
+                if appends:
+                    append(s)
+                if e:
+                    evs.append(e)
+        return g, evs
+
+    g_all, evs_all = capture(range(n_sets), have_ext)
+    singles = [capture([i], have_ext) for i in range(n_sets)]
+
+    K, W = args.steps, args.warmup
+    full, rest = divmod(K, n_sets)
+
+    # warm-up replays (untimed) plus a short pre-roll so clock samples overlap load
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            singles[i % n_sets][0].replay()
+    stream.synchronize()
+    sampler = ClockSampler()
+    sampler.start()
+    t_pre = time.time()
+    with torch.cuda.stream(stream):
+        while time.time() - t_pre < 0.6:
+            g_all.replay()
+            stream.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(full):
+            g_all.replay()
+        for i in range(rest):
+            singles[i][0].replay()
+        stop.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    bus = getattr(props, "pci_bus_id", None)
+    clocks = sampler.stop(bus if isinstance(bus, int) else None)
+    elapsed_ms = start.elapsed_time(stop)
+    elapsed_ms = max_over_ranks(elapsed_ms, world)
+    if int(err.item()) != 0:
+        raise RuntimeError("device error word %d after the timed region" % int(err.item()))
+
+    # per-kernel durations from the events captured inside the graphs (last replay)
+    attn_us, commit_us = [], []
+    if have_ext:
+        ev_sets = evs_all if full > 0 else []
+        if rest:
+            ev_sets = ev_sets[rest:] + [e for gi in range(rest) for e in singles[gi][1]]
+        for e in ev_sets:
+            attn_us.append(e[0].elapsed_time(e[1]) * 1000.0)
+            commit_us.append(e[1].elapsed_time(e[2]) * 1000.0)
+    else:
+        # fall back: time attention-only and commit-only graphs over the same sets
+        for which, acc in (("attn", attn_us), ("commit", commit_us)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+                for i in range(n_sets):
+                    reset(sets[i])
+                    (attn if which == "attn" else commit)(sets[i])
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                for _ in range(20):
+                    g.replay()
+                b.record(stream)
+            torch.cuda.synchronize()
+            acc.append(a.elapsed_time(b) * 1000.0 / (20 * n_sets))
+
+    steps_total = K * world
+    value = steps_total / (elapsed_ms / 1000.0)
+    ms_per_step = elapsed_ms / K
+    attn_b, commit_b, append_b = algorithmic_bytes(p)
+    hbm, tflops, peak_kind = peaks()
+    t_attn = statistics.mean(attn_us) if attn_us else None
+    t_commit = statistics.mean(commit_us) if commit_us else None
+    kernels = {}
+    if t_attn:
+        kernels["block_attn"] = {"us": t_attn, "bytes": attn_b, "GB/s": attn_b / t_attn / 1e3,
+                                 "frac": attn_b / t_attn / 1e3 / hbm,
+                                 "TFLOP/s": flops(p) / t_attn / 1e6}
+    if t_commit:
+        kernels["commit"] = {"us": t_commit, "bytes": commit_b, "GB/s": commit_b / t_commit / 1e3,
+                             "frac": commit_b / t_commit / 1e3 / hbm}
+    dom = "block_attn" if (t_attn or 0) >= (t_commit or 0) else "commit"
+    dk = kernels.get(dom, {})
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": dk.get("GB/s"), "peak": hbm,
+                "unit": "GB/s", "frac": dk.get("frac"), "peak_kind": peak_kind,
+                "traffic": recorded_traffic("attn" if dom == "block_attn" else "commit", w.name)}
+
+    # end to end through the C ABI from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(p, dev, sets[0], attn, commit, append if appends else None, K, stream,
+                      tokens0, masked0)
+
+    line = {"metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": K,
+            "warmup": W, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
+            "data": "synthetic (seeded; no dataset, no weights)",
+            "config": dict(workload_config(p, args),
+                           l2="%d rotating input sets of %.1f MB (%.0f MB > 4x L2 %.0f MB)" % (
+                               n_sets, per_set / 1e6, n_sets * per_set / 1e6, l2 / 1e6),
+                           state_reset="2 device copies (tokens, masked: %d B) per step" % (
+                               5 * w.total_q),
+                           attn_splits=args.num_splits or "auto",
+                           commit_splits=args.commit_splits or "auto"),
+            "roofline": roofline, "kernels": kernels,
+            "gpu_launches": K * (2 + (1 if appends else 0)),
+            "clocks": clocks, "e2e": e2e}
+    if rank == 0 and not args.no_cpu_baseline:
+        value_cpu, sample = time_oracle(p if p.q.device.type == "cpu" else p.to("cpu"),
+                                        args.cpu_seconds, oracle_threads())
+        line["cpu_baseline"] = {"value": value_cpu, "unit": "steps/s", "cores": oracle_threads(),
+                                "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(p, dev, s, attn, commit, append, K, stream, tokens0, masked0):
+    """Same step through the public API with host inputs: every step copies its
+    inputs (Q, window K/V, logits, decode state) from pinned host memory and
+    reads back its results (output, tokens, masked, block_remaining)."""
+    pin = lambda t: t.detach().to("cpu").contiguous().pin_memory()  # noqa: E731
+    h_q, h_kw, h_vw = pin(s.q), pin(s.k_win), pin(s.v_win)
+    h_logits = pin(s.logits)
+    h_tok, h_msk = pin(tokens0), pin(masked0)
+    h_out = torch.empty(s.out.shape, dtype=s.out.dtype).pin_memory()
+    h_tok_o = torch.empty_like(h_tok).pin_memory()
+    h_msk_o = torch.empty_like(h_msk).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kw, h_vw, h_logits, h_tok, h_msk))
+    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_tok_o, h_msk_o))
+    n = max(10, min(K, 2000))
+
+    def step():
+        s.q.copy_(h_q, non_blocking=True)
+        s.k_win.copy_(h_kw, non_blocking=True)
+        s.v_win.copy_(h_vw, non_blocking=True)
+        s.logits.copy_(h_logits, non_blocking=True)
+        s.tokens.copy_(h_tok, non_blocking=True)
+        s.masked.copy_(h_msk, non_blocking=True)
+        attn(s)
+        commit(s)
+        if append:
+            append(s)
+        h_out.copy_(s.out, non_blocking=True)
+        h_tok_o.copy_(s.tokens, non_blocking=True)
+        h_msk_o.copy_(s.masked, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    stream.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(n):
+            step()
+        b.record(stream)
+    stream.synchronize()
+    ms = a.elapsed_time(b)
+    return {"value": n / (ms / 1000.0), "unit": "steps/s", "steps": n,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,377 @@
+// Host side of the libd2f C ABI: argument validation, split planning,
+// workspace layout and kernel dispatch. No allocation, no host<->device copy,
+// no synchronisation happens here.
+#include <stdarg.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "d2f_internal.cuh"
+
+namespace d2f {
+
+static thread_local char g_last_error[512] = "";
+
+void set_last_error(const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+}
+
+int num_sms_current_device() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int cdiv(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+int fail(int status, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return status;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+  return fail(D2F_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// ---------------------------------------------------------------------------
+// Attention plan
+// ---------------------------------------------------------------------------
+struct AttnPlan {
+  bool tc;        // tensor-core path
+  int m_tiles;
+  int splits;
+  int n_counters;
+  size_t off_ml, off_o, bytes;
+};
+
+bool force_simt() {
+  const char *e = getenv("D2F_ATTN_PATH");
+  return e && strcmp(e, "simt") == 0;
+}
+
+int plan_attn(int batch, int total_q, int max_q, int max_ctx, int Hq, int Hkv, int D, int B,
+              int dtype, int num_splits, AttnPlan *p) {
+  if (batch < 0 || total_q < 0 || max_q < 0 || max_ctx < 0)
+    return fail(D2F_ERR_INVALID_ARG, "negative size (batch %d, total_q %d, max_q %d, max_ctx %d)",
+                batch, total_q, max_q, max_ctx);
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
+    return fail(D2F_ERR_INVALID_ARG, "num_heads_q (%d) must be a positive multiple of num_heads_kv (%d)",
+                Hq, Hkv);
+  if (dtype != D2F_BF16 && dtype != D2F_F32)
+    return fail(D2F_ERR_INVALID_ARG, "dtype must be D2F_BF16 or D2F_F32");
+  if (B < 1 || num_splits < 0 || num_splits > 4096)
+    return fail(D2F_ERR_INVALID_ARG, "block_size %d / num_splits %d out of range", B, num_splits);
+  if (max_q > total_q)
+    return fail(D2F_ERR_INVALID_ARG, "max_q_per_seq %d exceeds total_q %d", max_q, total_q);
+  if ((long long)batch * Hkv > 65535)
+    return fail(D2F_ERR_UNSUPPORTED, "batch * num_heads_kv must be <= 65535");
+  const bool tc = dtype == D2F_BF16 && (D == 64 || D == 128) && (B == 8 || B == 16 || B == 32) &&
+                  !force_simt();
+  if (!tc) {
+    if (!(D == 32 || D == 64 || D == 128))
+      return fail(D2F_ERR_UNSUPPORTED, "head_dim %d: supported are 64, 128 (bf16, B in {8,16,32}) "
+                  "and 32, 64, 128 (CUDA-core path)", D);
+    if (B > 256) return fail(D2F_ERR_UNSUPPORTED, "block_size %d > 256", B);
+  }
+  const int rows = tc ? kTcRows : kSimtRows;
+  const int keys = tc ? kTcKeys : kSimtKeys;
+  const int G = Hq / Hkv;
+  p->tc = tc;
+  p->m_tiles = max(1, cdiv((long long)G * max_q, rows));
+  const int t_max = max(1, cdiv(max_ctx, keys) + cdiv(max_q, keys));
+  int splits = num_splits;
+  if (splits == 0) {
+    const int sms = num_sms_current_device();
+    const long long base = (long long)max(batch, 1) * Hkv * p->m_tiles;
+    const long long target = sms > 0 ? (tc ? sms : 4LL * sms) : 1;
+    splits = (int)max(1LL, target / base);
+    splits = min(splits, t_max);
+  }
+  p->splits = splits;
+  p->n_counters = max(batch, 1) * Hkv * max(1, cdiv((long long)G * max_q, kSimtRows));
+  const size_t n_hr = (size_t)total_q * Hq;
+  p->off_ml = align_up((size_t)p->n_counters * sizeof(int32_t));
+  if (splits > 1) {
+    p->off_o = p->off_ml + align_up((size_t)splits * n_hr * sizeof(float2));
+    p->bytes = p->off_o + align_up((size_t)splits * n_hr * D * sizeof(float));
+  } else {
+    p->off_o = p->off_ml;
+    p->bytes = p->off_ml;
+  }
+  return D2F_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Commit plan
+// ---------------------------------------------------------------------------
+constexpr int kCommitThreads = 256;
+constexpr int kCommitMaxSplits = 64;
+
+struct CommitPlan {
+  int splits, chunk;
+  size_t off_partial, off_conf, off_arg, off_rowcnt, off_blkcnt, bytes;
+};
+
+int plan_commit(int total_q, int vocab, int dtype, int B, int num_splits, CommitPlan *p) {
+  if (total_q < 0 || vocab <= 0)
+    return fail(D2F_ERR_INVALID_ARG, "total_q %d / vocab %d out of range", total_q, vocab);
+  if (dtype != D2F_BF16 && dtype != D2F_F32)
+    return fail(D2F_ERR_INVALID_ARG, "dtype must be D2F_BF16 or D2F_F32");
+  if (B < 1 || B > 32) return fail(D2F_ERR_UNSUPPORTED, "commit supports block_size 1..32 (got %d)", B);
+  if (total_q % B != 0)
+    return fail(D2F_ERR_INVALID_ARG, "total_q %d is not a multiple of block_size %d", total_q, B);
+  if (total_q > 65535) return fail(D2F_ERR_UNSUPPORTED, "total_q must be <= 65535");
+  if (num_splits < 0 || num_splits > kCommitMaxSplits)
+    return fail(D2F_ERR_INVALID_ARG, "num_splits must be in [0, %d]", kCommitMaxSplits);
+  const int vec = dtype == D2F_BF16 ? 8 : 4;
+  int splits = num_splits;
+  int chunk;
+  if (splits == 0) {
+    const int sms = num_sms_current_device();
+    const long long target = 4LL * (sms > 0 ? sms : 1);
+    const long long rows = total_q > 0 ? total_q : 1;
+    long long want = (target + rows - 1) / rows;
+    if (want < 1) want = 1;
+    if (want > kCommitMaxSplits) want = kCommitMaxSplits;
+    splits = (int)want;
+    chunk = cdiv(cdiv(vocab, splits), vec * kCommitThreads) * vec * kCommitThreads;
+  } else {
+    chunk = cdiv(cdiv(vocab, splits), vec) * vec;
+  }
+  splits = cdiv(vocab, chunk);
+  p->splits = splits;
+  p->chunk = chunk;
+  // Counters first: their place does not depend on the split count, so one
+  // zeroed workspace stays valid across calls with different splits.
+  const size_t nq = (size_t)total_q;
+  p->off_rowcnt = 0;
+  p->off_blkcnt = align_up(nq * sizeof(int32_t));
+  p->off_conf = p->off_blkcnt + align_up((nq / B + 1) * sizeof(int32_t));
+  p->off_arg = p->off_conf + align_up(nq * sizeof(float));
+  p->off_partial = p->off_arg + align_up(nq * sizeof(int32_t));
+  p->bytes = p->off_partial + align_up(nq * splits * sizeof(float4));
+  return D2F_OK;
+}
+
+}  // namespace
+}  // namespace d2f
+
+using namespace d2f;
+
+extern "C" {
+
+int d2f_version(void) { return 100; }
+
+const char *d2f_status_string(int status) {
+  switch (status) {
+    case D2F_OK: return "ok";
+    case D2F_ERR_INVALID_ARG: return "invalid argument";
+    case D2F_ERR_UNSUPPORTED: return "unsupported configuration";
+    case D2F_ERR_CUDA: return "CUDA error";
+    case D2F_ERR_BAD_INDEX: return "index out of range (device)";
+    case D2F_ERR_TIMEOUT: return "bounded wait timed out (device)";
+    case D2F_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+const char *d2f_last_error_string(void) { return g_last_error; }
+
+int d2f_block_attn_workspace_size(int batch, int total_q, int max_q_per_seq, int max_ctx,
+                                  int num_heads_q, int num_heads_kv, int head_dim, int block_size,
+                                  int dtype, int num_splits, size_t *bytes) {
+  if (!bytes) return fail(D2F_ERR_INVALID_ARG, "bytes is NULL");
+  AttnPlan p{};
+  const int st = plan_attn(batch, total_q, max_q_per_seq, max_ctx, num_heads_q, num_heads_kv,
+                           head_dim, block_size, dtype, num_splits, &p);
+  if (st != D2F_OK) return st;
+  *bytes = p.bytes;
+  return D2F_OK;
+}
+
+int d2f_block_attn(const void *q, const void *k_win, const void *v_win, const void *k_pool,
+                   const void *v_pool, const int32_t *page_table, int max_pages_per_seq,
+                   const int32_t *ctx_len, const int32_t *q_start, void *out, float *lse_out,
+                   int batch, int total_q, int max_q_per_seq, int max_ctx, int num_heads_q,
+                   int num_heads_kv, int head_dim, int block_size, int num_pages, int dtype,
+                   float softmax_scale, int num_splits, void *workspace, size_t workspace_bytes,
+                   int32_t *err_word, void *stream) {
+  AttnPlan p{};
+  int st = plan_attn(batch, total_q, max_q_per_seq, max_ctx, num_heads_q, num_heads_kv, head_dim,
+                     block_size, dtype, num_splits, &p);
+  if (st != D2F_OK) return st;
+  if (batch == 0 || total_q == 0) return D2F_OK;
+  if (!q || !k_win || !v_win || !out || !ctx_len || !q_start)
+    return fail(D2F_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (max_pages_per_seq < 0 || num_pages < 0)
+    return fail(D2F_ERR_INVALID_ARG, "max_pages_per_seq / num_pages negative");
+  if ((long long)max_pages_per_seq * block_size < max_ctx)
+    return fail(D2F_ERR_INVALID_ARG, "max_ctx %d exceeds max_pages_per_seq * block_size", max_ctx);
+  if (max_ctx > 0 && (!k_pool || !v_pool || !page_table || num_pages <= 0))
+    return fail(D2F_ERR_INVALID_ARG, "a cached context needs k_pool, v_pool, page_table and pages");
+  if (!(softmax_scale > 0.f)) return fail(D2F_ERR_INVALID_ARG, "softmax_scale must be > 0");
+  const void *ptrs[] = {q, k_win, v_win, k_pool, v_pool, out};
+  for (const void *x : ptrs)
+    if (x && !aligned16(x)) return fail(D2F_ERR_INVALID_ARG, "device buffers must be 16-byte aligned");
+  if (p.bytes > 0 && (!workspace || workspace_bytes < p.bytes))
+    return fail(D2F_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", p.bytes,
+                workspace ? workspace_bytes : (size_t)0);
+
+  AttnArgs a;
+  a.q = q;
+  a.k_win = k_win;
+  a.v_win = v_win;
+  // With no pages at all, the pool maps point at the window so they stay encodable;
+  // no cached tile is ever read then (every ctx_len must be 0).
+  a.k_pool = (num_pages > 0 && k_pool) ? k_pool : k_win;
+  a.v_pool = (num_pages > 0 && v_pool) ? v_pool : v_win;
+  a.page_table = page_table;
+  a.max_pages_per_seq = max_pages_per_seq;
+  a.ctx_len = ctx_len;
+  a.q_start = q_start;
+  a.out = out;
+  a.lse_out = lse_out;
+  a.batch = batch;
+  a.total_q = total_q;
+  a.max_q_per_seq = max_q_per_seq;
+  a.num_heads_q = num_heads_q;
+  a.num_heads_kv = num_heads_kv;
+  a.head_dim = head_dim;
+  a.block_size = block_size;
+  a.num_pages = num_pages > 0 ? num_pages : 1;
+  a.group = num_heads_q / num_heads_kv;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.num_splits = p.splits;
+  a.m_tiles = p.m_tiles;
+  a.counters = reinterpret_cast<int32_t *>(workspace);
+  a.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) + p.off_ml);
+  a.ws_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + p.off_o);
+  a.err = err_word;
+  if (num_pages <= 0 && max_ctx > 0) return fail(D2F_ERR_INVALID_ARG, "no pages");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (p.tc) {
+    char why[256] = "";
+    e = launch_attn_tc(a, s, why, sizeof why);
+    if (e != cudaSuccess) {
+      if (why[0]) return fail(D2F_ERR_CUDA, "tensor-core attention: %s (%s)", why, cudaGetErrorString(e));
+      return cuda_fail(e, "tensor-core attention launch");
+    }
+  } else {
+    e = launch_attn_simt(a, dtype, s);
+    if (e != cudaSuccess) return cuda_fail(e, "CUDA-core attention launch");
+  }
+  return D2F_OK;
+}
+
+int d2f_commit_workspace_size(int total_q, int vocab, int dtype, int block_size, int num_splits,
+                              size_t *bytes) {
+  if (!bytes) return fail(D2F_ERR_INVALID_ARG, "bytes is NULL");
+  CommitPlan p{};
+  const int st = plan_commit(total_q, vocab, dtype, block_size, num_splits, &p);
+  if (st != D2F_OK) return st;
+  *bytes = p.bytes;
+  return D2F_OK;
+}
+
+int d2f_commit(const void *logits, int64_t row_stride, int dtype, int vocab, int num_logit_rows,
+               const int32_t *logit_row, int32_t *tokens, uint8_t *masked,
+               const int32_t *q_start, const uint8_t *block_phase, const float *tau, int batch,
+               int total_q, int block_size, int32_t mask_id, float *conf_out,
+               int32_t *argmax_out, int32_t *block_remaining, int num_splits, void *workspace,
+               size_t workspace_bytes, int32_t *err_word, void *stream) {
+  CommitPlan p{};
+  int st = plan_commit(total_q, vocab, dtype, block_size, num_splits, &p);
+  if (st != D2F_OK) return st;
+  if (batch < 1) return fail(D2F_ERR_INVALID_ARG, "batch must be >= 1");
+  if (total_q == 0) return D2F_OK;
+  if (!logits || !tokens || !masked || !q_start || !block_phase || !tau)
+    return fail(D2F_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (row_stride < vocab) return fail(D2F_ERR_INVALID_ARG, "row_stride < vocab");
+  if (num_logit_rows <= 0) return fail(D2F_ERR_INVALID_ARG, "num_logit_rows must be > 0");
+  if (!workspace || workspace_bytes < p.bytes)
+    return fail(D2F_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", p.bytes,
+                workspace ? workspace_bytes : (size_t)0);
+  const int elt = dtype == D2F_BF16 ? 2 : 4;
+  const bool vec_ok = aligned16(logits) && ((row_stride * elt) % 16 == 0);
+  CommitArgs a;
+  a.logits = logits;
+  a.row_stride = row_stride;
+  a.vocab = vocab;
+  a.num_logit_rows = num_logit_rows;
+  a.logit_row = logit_row;
+  a.tokens = tokens;
+  a.masked = masked;
+  a.q_start = q_start;
+  a.block_phase = block_phase;
+  a.tau = tau;
+  a.batch = batch;
+  a.total_q = total_q;
+  a.block_size = block_size;
+  a.mask_id = mask_id;
+  a.conf_out = conf_out;
+  a.argmax_out = argmax_out;
+  a.block_remaining = block_remaining;
+  a.splits = p.splits;
+  a.chunk = p.chunk;
+  char *ws = static_cast<char *>(workspace);
+  a.partial = reinterpret_cast<float4 *>(ws + p.off_partial);
+  a.row_conf = reinterpret_cast<float *>(ws + p.off_conf);
+  a.row_arg = reinterpret_cast<int32_t *>(ws + p.off_arg);
+  a.row_cnt = reinterpret_cast<int32_t *>(ws + p.off_rowcnt);
+  a.blk_cnt = reinterpret_cast<int32_t *>(ws + p.off_blkcnt);
+  a.err = err_word;
+  const cudaError_t e = launch_commit(a, dtype, vec_ok, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "commit launch");
+  return D2F_OK;
+}
+
+int d2f_kv_append(const void *k_win, const void *v_win, const int32_t *src_row,
+                  const int32_t *dst_page, int n_append, int total_q, void *k_pool,
+                  void *v_pool, int num_heads_kv, int head_dim, int block_size, int num_pages,
+                  int dtype, int32_t *err_word, void *stream) {
+  if (n_append < 0 || total_q < 0 || num_heads_kv <= 0 || head_dim <= 0 || block_size < 1 ||
+      num_pages < 0)
+    return fail(D2F_ERR_INVALID_ARG, "size out of range");
+  if (dtype != D2F_BF16 && dtype != D2F_F32)
+    return fail(D2F_ERR_INVALID_ARG, "dtype must be D2F_BF16 or D2F_F32");
+  if ((long long)n_append * num_heads_kv > 0x7fffffffLL)
+    return fail(D2F_ERR_UNSUPPORTED, "n_append * num_heads_kv too large");
+  if (n_append == 0) return D2F_OK;
+  if (!k_win || !v_win || !src_row || !dst_page || !k_pool || !v_pool)
+    return fail(D2F_ERR_INVALID_ARG, "a required pointer is NULL");
+  const int elt = dtype == D2F_BF16 ? 2 : 4;
+  AppendArgs a;
+  a.k_win = k_win;
+  a.v_win = v_win;
+  a.src_row = src_row;
+  a.dst_page = dst_page;
+  a.n_append = n_append;
+  a.total_q = total_q;
+  a.k_pool = k_pool;
+  a.v_pool = v_pool;
+  a.num_heads_kv = num_heads_kv;
+  a.block_size = block_size;
+  a.num_pages = num_pages;
+  a.row_bytes = head_dim * elt;
+  a.err = err_word;
+  const bool vec_ok = aligned16(k_win) && aligned16(v_win) && aligned16(k_pool) &&
+                      aligned16(v_pool) && (a.row_bytes % 16 == 0);
+  const cudaError_t e = launch_append(a, vec_ok, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
+  return D2F_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,303 @@
+// Internal declarations shared by the libd2f translation units: launch
+// argument structs, status plumbing and thin inline-PTX wrappers for the
+// Blackwell (sm_103a) async machinery (mbarrier, TMA, tcgen05 / TMEM).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "d2f.h"
+
+namespace d2f {
+
+// ---------------------------------------------------------------------------
+// Host-side plumbing
+// ---------------------------------------------------------------------------
+void set_last_error(const char *fmt, ...);
+int num_sms_current_device();
+
+// Bounded waits give up after this many SM clock cycles (about one second at
+// the GB300's clocks), set D2F_ERR_TIMEOUT in the error word and unwind.
+constexpr long long kWaitCycles = 2000000000LL;
+
+// ---------------------------------------------------------------------------
+// Launch arguments
+// ---------------------------------------------------------------------------
+struct AttnArgs {
+  const void *q, *k_win, *v_win, *k_pool, *v_pool;
+  const int32_t *page_table;
+  int max_pages_per_seq;
+  const int32_t *ctx_len, *q_start;
+  void *out;
+  float *lse_out;
+  int batch, total_q, max_q_per_seq, num_heads_q, num_heads_kv, head_dim, block_size, num_pages;
+  int group;             // num_heads_q / num_heads_kv
+  float scale_log2;      // softmax_scale * log2(e)
+  int num_splits;        // split count requested (each sequence uses <= this many)
+  int m_tiles;           // grid.x: row tiles per (sequence, KV head)
+  int32_t *counters;     // [batch * Hkv * m_tiles] merge arrival counters (zero at rest)
+  float2 *ws_ml;         // [num_splits][total_q * Hq] (max in log2 units, sum)
+  float *ws_o;           // [num_splits][total_q * Hq][head_dim] unnormalised partial output
+  int32_t *err;
+};
+
+struct CommitArgs {
+  const void *logits;
+  int64_t row_stride;
+  int vocab, num_logit_rows;
+  const int32_t *logit_row;
+  int32_t *tokens;
+  uint8_t *masked;
+  const int32_t *q_start;
+  const uint8_t *block_phase;
+  const float *tau;
+  int batch, total_q, block_size;
+  int32_t mask_id;
+  float *conf_out;
+  int32_t *argmax_out, *block_remaining;
+  int splits;            // CTAs per row
+  int chunk;             // vocabulary entries per CTA
+  float4 *partial;       // [total_q][splits] (max, argmax bits, sum, unused)
+  float *row_conf;       // [total_q]
+  int32_t *row_arg;      // [total_q]
+  int32_t *row_cnt;      // [total_q] (zero at rest)
+  int32_t *blk_cnt;      // [total_q / block_size] (zero at rest)
+  int32_t *err;
+};
+
+struct AppendArgs {
+  const void *k_win, *v_win;
+  const int32_t *src_row, *dst_page;
+  int n_append, total_q;
+  void *k_pool, *v_pool;
+  int num_heads_kv, block_size, num_pages;
+  int row_bytes;         // head_dim * element size
+  int32_t *err;
+};
+
+// Launchers (one per translation unit). Return cudaSuccess or the launch error.
+cudaError_t launch_commit(const CommitArgs &a, int dtype, bool vec_ok, cudaStream_t s);
+cudaError_t launch_append(const AppendArgs &a, bool vec_ok, cudaStream_t s);
+cudaError_t launch_attn_simt(const AttnArgs &a, int dtype, cudaStream_t s);
+cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t s, char *why, size_t why_len);
+
+// Tile and row sizes of the two attention paths (also used for workspace sizing).
+constexpr int kSimtRows = 16;   // query rows per CTA, CUDA-core path
+constexpr int kSimtKeys = 32;   // keys per tile, CUDA-core path
+constexpr int kTcRows = 128;    // query rows per CTA (UMMA M), tensor-core path
+constexpr int kTcKeys = 64;     // keys per tile (UMMA N of Q.K^T), tensor-core path
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+#ifdef __CUDACC__
+__device__ __forceinline__ void set_err(int32_t *err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
+  return __uint_as_float(bits16 << 16);
+}
+
+// Round-to-nearest-even float -> bf16 bits (the cvt.rn.bf16.f32 instruction).
+__device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
+  uint16_t r;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(f));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Sequence metadata check shared by the attention kernels: returns false (and
+// records D2F_ERR_INVALID_ARG) when the window rows of sequence b contradict the
+// host sizes.
+__device__ __forceinline__ bool load_seq_meta(const AttnArgs &a, int b, int &q0, int &n, int &C) {
+  q0 = a.q_start[b];
+  const int q1 = a.q_start[b + 1];
+  C = a.ctx_len[b];
+  n = q1 - q0;
+  const bool ok = q0 >= 0 && q1 >= q0 && q1 <= a.total_q && (q0 % a.block_size) == 0 &&
+                  (n % a.block_size) == 0 && n <= a.max_q_per_seq && C >= 0 &&
+                  (long long)C <= (long long)a.max_pages_per_seq * a.block_size;
+  return ok;
+}
+
+// ----- mbarrier --------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for the phase with the given parity; gives up after kWaitCycles or when
+// another thread of the CTA has already given up (shared abort flag).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          int32_t *err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort_flag = 1;
+      set_err(err, D2F_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// ----- TMA (tensor copies global -> shared, completion on an mbarrier) -------
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+// Generic-proxy shared-memory writes -> visible to the async proxy (UMMA reads).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ----- tcgen05 / TMEM ---------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem], bf16 inputs, f32 accumulate.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on an mbarrier once every tcgen05 operation issued so far by this thread completes.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// 32 consecutive 32-bit TMEM columns of this thread's lane, waited for in the
+// same asm block so no use of the registers can be scheduled before the wait.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+// Shared-memory matrix descriptor for tcgen05.mma, 128-byte swizzle.
+//   start address >> 4 in bits 0-13, leading byte offset >> 4 in 16-29,
+//   stride byte offset >> 4 in 32-45, descriptor version 1 in bits 46-47,
+//   swizzle mode 2 (128B) in bits 61-63.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16 with bf16 A/B and f32 accumulator.
+//   D format f32 (bits 4-5 = 1), A and B format bf16 (bits 7-9 = 1, 10-12 = 1),
+//   A major (bit 15) and B major (bit 16): 0 = K-major, 1 = MN-major,
+//   N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_major,
+                                                      int b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn_major << 15) |
+         ((uint32_t)b_mn_major << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+#endif  // __CUDACC__
+
+}  // namespace d2f

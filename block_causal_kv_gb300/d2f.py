@@ -1,0 +1,246 @@
+"""Python binding of libd2f (ctypes): argument marshalling only.
+
+Every function takes torch CUDA tensors, passes their device pointers, sizes
+and the current CUDA stream to the C entry point of the same name, and raises
+D2FError on a non-OK status. No computation happens here; there is no CPU
+fallback: if libd2f.so is missing the import fails.
+
+    from block_causal_kv_gb300 import d2f
+    out, lse = d2f.block_attn(q, k_win, v_win, k_pool, v_pool, page_table, ctx_len,
+                              q_start, block_size=16, max_q_per_seq=48, max_ctx=1024)
+    res = d2f.commit(logits, tokens, masked, q_start, block_phase, tau,
+                     block_size=16, mask_id=126464)
+    d2f.kv_append(k_win, v_win, src_row, dst_page, k_pool, v_pool, block_size=16)
+"""
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libd2f.so")
+
+BF16 = 0
+F32 = 1
+PHASE_CONSERVATIVE = 0
+PHASE_AGGRESSIVE = 1
+
+STATUS = {0: "D2F_OK", 1: "D2F_ERR_INVALID_ARG", 2: "D2F_ERR_UNSUPPORTED", 3: "D2F_ERR_CUDA",
+          4: "D2F_ERR_BAD_INDEX", 5: "D2F_ERR_TIMEOUT", 6: "D2F_ERR_WORKSPACE"}
+
+# Every symbol include/d2f.h declares.
+EXPORTS = ("d2f_version", "d2f_status_string", "d2f_last_error_string",
+           "d2f_block_attn_workspace_size", "d2f_block_attn", "d2f_commit_workspace_size",
+           "d2f_commit", "d2f_kv_append")
+
+
+class D2FError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__("%s: %s" % (STATUS.get(status, status), message))
+        self.status = status
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SZ = ctypes.c_size_t
+
+
+def load(path=LIB_PATH):
+    """Load libd2f.so (built in-tree by __graft_entry__.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError("libd2f.so is not built (%s); run __graft_entry__.build()" % path)
+    lib = ctypes.CDLL(path)
+    lib.d2f_version.restype = _I
+    lib.d2f_status_string.restype = ctypes.c_char_p
+    lib.d2f_status_string.argtypes = [_I]
+    lib.d2f_last_error_string.restype = ctypes.c_char_p
+    lib.d2f_block_attn_workspace_size.restype = _I
+    lib.d2f_block_attn_workspace_size.argtypes = [_I] * 10 + [ctypes.POINTER(_SZ)]
+    lib.d2f_block_attn.restype = _I
+    lib.d2f_block_attn.argtypes = ([_P] * 6 + [_I] + [_P] * 2 + [_P, _P] + [_I] * 10 +
+                                   [ctypes.c_float, _I, _P, _SZ, _P, _P])
+    lib.d2f_commit_workspace_size.restype = _I
+    lib.d2f_commit_workspace_size.argtypes = [_I] * 5 + [ctypes.POINTER(_SZ)]
+    lib.d2f_commit.restype = _I
+    lib.d2f_commit.argtypes = ([_P, ctypes.c_int64, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I,
+                                ctypes.c_int32, _P, _P, _P, _I, _P, _SZ, _P, _P])
+    lib.d2f_kv_append.restype = _I
+    lib.d2f_kv_append.argtypes = [_P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P]
+    _lib = lib
+    return lib
+
+
+def _check(status):
+    if status != 0:
+        raise D2FError(status, _lib.d2f_last_error_string().decode())
+
+
+def _dtype_code(t):
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError("libd2f takes bfloat16 or float32 tensors, got %s" % t.dtype)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _dev(t, name, dtype=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+
+
+def status_string(status):
+    return load().d2f_status_string(status).decode()
+
+
+def version():
+    return load().d2f_version()
+
+
+# ---------------------------------------------------------------------------
+# block attention
+# ---------------------------------------------------------------------------
+def attn_workspace_size(batch, total_q, max_q_per_seq, max_ctx, num_heads_q, num_heads_kv,
+                        head_dim, block_size, dtype=BF16, num_splits=0):
+    lib = load()
+    n = _SZ(0)
+    _check(lib.d2f_block_attn_workspace_size(batch, total_q, max_q_per_seq, max_ctx, num_heads_q,
+                                             num_heads_kv, head_dim, block_size, dtype,
+                                             num_splits, ctypes.byref(n)))
+    return n.value
+
+
+def attn_workspace(device, **kw):
+    """A zero-filled workspace of the size attn_workspace_size(**kw) returns."""
+    return torch.zeros(max(attn_workspace_size(**kw), 1), dtype=torch.uint8, device=device)
+
+
+def block_attn(q, k_win, v_win, k_pool, v_pool, page_table, ctx_len, q_start, *, block_size,
+               max_q_per_seq, max_ctx, softmax_scale=None, num_splits=0, out=None, lse=None,
+               want_lse=True, workspace=None, err=None, stream=None):
+    """Block-causal attention of the window over [paged cache ; window] (one layer).
+
+    Returns (out [total_q, Hq, D] like q, lse [total_q, Hq] float32 or None)."""
+    lib = load()
+    for name, t in (("q", q), ("k_win", k_win), ("v_win", v_win), ("k_pool", k_pool),
+                    ("v_pool", v_pool)):
+        _dev(t, name, q.dtype)
+    _dev(page_table, "page_table", torch.int32)
+    _dev(ctx_len, "ctx_len", torch.int32)
+    _dev(q_start, "q_start", torch.int32)
+    total_q, hq, d = q.shape
+    hkv = k_win.shape[1]
+    batch = ctx_len.shape[0]
+    dt = _dtype_code(q)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    _dev(out, "out", q.dtype)
+    if lse is None and want_lse:
+        lse = torch.empty((total_q, hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = attn_workspace(q.device, batch=batch, total_q=total_q,
+                                   max_q_per_seq=max_q_per_seq, max_ctx=max_ctx,
+                                   num_heads_q=hq, num_heads_kv=hkv, head_dim=d,
+                                   block_size=block_size, dtype=dt, num_splits=num_splits)
+    _check(lib.d2f_block_attn(
+        _ptr(q), _ptr(k_win), _ptr(v_win), _ptr(k_pool), _ptr(v_pool), _ptr(page_table),
+        page_table.shape[1] if page_table is not None else 0, _ptr(ctx_len), _ptr(q_start),
+        _ptr(out), _ptr(lse), batch, total_q, max_q_per_seq, max_ctx, hq, hkv, d, block_size,
+        k_pool.shape[0] if k_pool is not None else 0, dt, float(softmax_scale), num_splits,
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream)))
+    return out, lse
+
+
+# ---------------------------------------------------------------------------
+# commit
+# ---------------------------------------------------------------------------
+def commit_workspace_size(total_q, vocab, block_size, dtype=BF16, num_splits=0):
+    lib = load()
+    n = _SZ(0)
+    _check(lib.d2f_commit_workspace_size(total_q, vocab, dtype, block_size, num_splits,
+                                         ctypes.byref(n)))
+    return n.value
+
+
+def commit_workspace(device, **kw):
+    return torch.zeros(max(commit_workspace_size(**kw), 1), dtype=torch.uint8, device=device)
+
+
+def commit(logits, tokens, masked, q_start, block_phase, tau, *, block_size, mask_id,
+           logit_row=None, num_splits=0, conf=None, argmax=None, block_remaining=None,
+           want_outputs=True, workspace=None, err=None, stream=None):
+    """Confidence commit + remask, in place on tokens / masked.
+
+    logits may be a row-strided view ([rows, vocab] with stride(1) == 1).
+    Returns dict(conf, argmax, block_remaining) (device tensors, or None)."""
+    lib = load()
+    if not logits.is_cuda or logits.stride(-1) != 1:
+        raise ValueError("logits must be a CUDA tensor with unit stride along the vocabulary")
+    _dev(tokens, "tokens", torch.int32)
+    _dev(masked, "masked", torch.uint8)
+    _dev(q_start, "q_start", torch.int32)
+    _dev(block_phase, "block_phase", torch.uint8)
+    _dev(tau, "tau", torch.float32)
+    _dev(logit_row, "logit_row", torch.int32)
+    total_q = tokens.shape[0]
+    rows, vocab = logits.shape
+    dt = _dtype_code(logits)
+    dev = tokens.device
+    if want_outputs:
+        if conf is None:
+            conf = torch.empty(total_q, dtype=torch.float32, device=dev)
+        if argmax is None:
+            argmax = torch.empty(total_q, dtype=torch.int32, device=dev)
+        if block_remaining is None:
+            block_remaining = torch.empty(max(total_q // block_size, 1), dtype=torch.int32,
+                                          device=dev)
+    if workspace is None:
+        workspace = commit_workspace(dev, total_q=total_q, vocab=vocab, block_size=block_size,
+                                     dtype=dt, num_splits=num_splits)
+    _check(lib.d2f_commit(
+        _ptr(logits), logits.stride(0), dt, vocab, rows, _ptr(logit_row), _ptr(tokens),
+        _ptr(masked), _ptr(q_start), _ptr(block_phase), _ptr(tau), q_start.shape[0] - 1, total_q,
+        block_size, int(mask_id), _ptr(conf), _ptr(argmax), _ptr(block_remaining), num_splits,
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err),
+        _stream(stream)))
+    return {"conf": conf, "argmax": argmax, "block_remaining": block_remaining}
+
+
+# ---------------------------------------------------------------------------
+# KV append
+# ---------------------------------------------------------------------------
+def kv_append(k_win, v_win, src_row, dst_page, k_pool, v_pool, *, block_size, err=None,
+              stream=None):
+    """Copy finished blocks (rows src_row[a] .. +B of the window K/V) into pages dst_page[a]."""
+    lib = load()
+    for name, t in (("k_win", k_win), ("v_win", v_win), ("k_pool", k_pool), ("v_pool", v_pool)):
+        _dev(t, name, k_win.dtype)
+    _dev(src_row, "src_row", torch.int32)
+    _dev(dst_page, "dst_page", torch.int32)
+    total_q, hkv, d = k_win.shape
+    _check(lib.d2f_kv_append(
+        _ptr(k_win), _ptr(v_win), _ptr(src_row), _ptr(dst_page), src_row.shape[0], total_q,
+        _ptr(k_pool), _ptr(v_pool), hkv, d, block_size, k_pool.shape[0], _dtype_code(k_win),
+        _ptr(err), _stream(stream)))

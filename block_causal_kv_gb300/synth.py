@@ -256,9 +256,12 @@ def small(name: str, **over) -> Workload:
                        window_blocks=[1, 3, 2, 1, 2], vocab=3001),
         "dream": dict(batch=2, num_heads_q=14, num_heads_kv=2, ctx_lens=[512, 300],
                       window_blocks=[3, 3], vocab=4099, appends_per_seq=1),
-        "long_b8": dict(batch=2, num_heads_q=2, num_heads_kv=2, ctx_lens=[1000, 1024], vocab=2048),
-        "long_b16": dict(batch=2, num_heads_q=2, num_heads_kv=2, ctx_lens=[1000, 1024], vocab=2048),
-        "long_b32": dict(batch=2, num_heads_q=2, num_heads_kv=2, ctx_lens=[1000, 1024], vocab=2048),
+        "long_b8": dict(batch=2, num_heads_q=2, num_heads_kv=2, ctx_lens=[1000, 1024],
+                         window_blocks=[4, 4], vocab=2048),
+        "long_b16": dict(batch=2, num_heads_q=2, num_heads_kv=2, ctx_lens=[1000, 1024],
+                         window_blocks=[4, 4], vocab=2048),
+        "long_b32": dict(batch=2, num_heads_q=2, num_heads_kv=2, ctx_lens=[1000, 1024],
+                         window_blocks=[4, 4], vocab=2048),
     }[name]
     defaults.update(over)
     return replace(base, name=name + "_small", **defaults)

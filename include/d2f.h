@@ -1,0 +1,211 @@
+/*
+ * d2f.h -- C ABI of libd2f, the GB300 (sm_103a) hot path of Discrete Diffusion
+ * Forcing (D2F) block-diffusion decoding.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [P1] "D2F: 확산 언어 모델이 KV 캐시를 얻고 자기회귀 모델보다 2.5배 빨라지는
+ *        방법 (arXiv:2508.09192)"
+ *   [P2] "D2F 논문 리뷰: 확산 LLM이 자기회귀 모델보다 빠른 추론을 처음으로
+ *        달성한 방식"
+ *   [P3] "확산 언어 모델(Diffusion LLM)이란 무엇인가"
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers named as device buffers are CUDA device (or managed) memory owned
+ *   by the caller. The library never allocates, frees or copies between host
+ *   and device; it only enqueues kernels.
+ * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream). Every call is asynchronous: it validates its host-side arguments,
+ *   enqueues its kernel(s) on `stream` and returns without synchronising.
+ * - Return value: a d2f_status. D2F_ERR_INVALID_ARG, D2F_ERR_UNSUPPORTED and
+ *   D2F_ERR_WORKSPACE are detected on the host before anything is enqueued;
+ *   D2F_ERR_CUDA means a launch failed. d2f_last_error_string() gives a
+ *   one-line reason for the last non-OK return in the calling thread.
+ * - `err_word` (nullable) is a device int32 the caller zeroes. Problems found
+ *   on the device (a page id outside [0, num_pages), window metadata that
+ *   contradicts the host sizes, a bounded wait that gave up) store the first
+ *   error code there with an atomic compare-and-swap; the offending work is
+ *   skipped without any out-of-range access, and the caller reads the word
+ *   after its own synchronisation. Kernels never trap or assert.
+ * - Window metadata: sequence b owns window rows q_start[b] .. q_start[b+1]-1
+ *   (n_b rows; q_start[0] = 0, q_start[batch] = total_q, every q_start value a
+ *   multiple of block_size). Row i of sequence b lies in window block i / B.
+ *   Global window block jb covers rows jb*B .. jb*B+B-1.
+ * - K/V pool layout: [num_pages][num_heads_kv][block_size][head_dim], one page
+ *   = one block of B tokens of one sequence ([P1] §운영 관점: block completion
+ *   is the cache-persistence signal, so a page holds exactly one block). Token t
+ *   of sequence b lives in page page_table[b*max_pages_per_seq + t/B], slot t%B.
+ * - GQA: query head h reads KV head h / (num_heads_q / num_heads_kv).
+ * - Workspace: caller-provided device memory of at least the size the matching
+ *   *_workspace_size query returns. It must be zero-filled before its first use
+ *   (e.g. cudaMemsetAsync); every call leaves it ready for the next call on the
+ *   same stream. Calls that share one workspace must not overlap in time.
+ */
+#ifndef D2F_H
+#define D2F_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum d2f_status {
+  D2F_OK = 0,
+  D2F_ERR_INVALID_ARG = 1, /* bad sizes, null required pointer, bad metadata */
+  D2F_ERR_UNSUPPORTED = 2, /* valid request this build does not implement      */
+  D2F_ERR_CUDA = 3,        /* a CUDA runtime / launch error                      */
+  D2F_ERR_BAD_INDEX = 4,   /* device: page id / row index out of range          */
+  D2F_ERR_TIMEOUT = 5,     /* device: a bounded wait gave up                     */
+  D2F_ERR_WORKSPACE = 6    /* workspace missing or smaller than required         */
+} d2f_status;
+
+typedef enum d2f_dtype { D2F_BF16 = 0, D2F_F32 = 1 } d2f_dtype;
+
+/* Block phases ([P2] §쉽게 이해하기). */
+enum { D2F_PHASE_CONSERVATIVE = 0, D2F_PHASE_AGGRESSIVE = 1 };
+
+/* Library version, e.g. 100 for 0.1.0. */
+int d2f_version(void);
+
+/* Static description of a status code. */
+const char *d2f_status_string(int status);
+
+/* One-line reason for the last non-OK status returned in this thread
+ * (empty string if none). The pointer stays valid until the next call. */
+const char *d2f_last_error_string(void);
+
+/* ------------------------------------------------------------------------- */
+/* Block-causal attention over [paged cache ; window]                        */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Workspace bytes for d2f_block_attn with the same size arguments. num_splits
+ * = 0 selects the automatic split count for the current CUDA device (the same
+ * one d2f_block_attn picks for num_splits = 0 on that device).
+ */
+int d2f_block_attn_workspace_size(int batch, int total_q, int max_q_per_seq, int max_ctx,
+                                  int num_heads_q, int num_heads_kv, int head_dim,
+                                  int block_size, int dtype, int num_splits, size_t *bytes);
+
+/*
+ * d2f_block_attn -- one layer's attention for the active window.
+ *
+ * [P1] §블록 단위 인과 어텐션, [P2] §쉽게 이해하기: query head h of window row i
+ * of sequence b attends to
+ *   (a) every cached token t < ctx_len[b] (prompt and committed blocks, read
+ *       through the page table), and
+ *   (b) every window row i2 of the same sequence with i2/B <= i/B (its own
+ *       block in both directions, earlier window blocks, no later ones);
+ * scores = softmax_scale * <q, k>, out = softmax(scores) . v. The cached part
+ * is split over several CTAs whose partial (O, max, sum) are composed in log
+ * space ([P3] §FlashBlock: log-space composition of attention parts).
+ *
+ *   q           device [total_q][num_heads_q][head_dim], dtype
+ *   k_win,v_win device [total_q][num_heads_kv][head_dim], dtype (this step's
+ *               window K/V)
+ *   k_pool,
+ *   v_pool      device [num_pages][num_heads_kv][block_size][head_dim], dtype
+ *   page_table  device int32 [batch][max_pages_per_seq]; entries at or past
+ *               ceil(ctx_len[b]/B) are not read
+ *   ctx_len     device int32 [batch], 0 <= ctx_len[b] <= max_pages_per_seq*B;
+ *               need not be a multiple of B (slots past it are masked)
+ *   q_start     device int32 [batch+1]
+ *   out         device [total_q][num_heads_q][head_dim], dtype
+ *   lse_out     device float [total_q][num_heads_q] natural-log normaliser, or NULL
+ *   max_q_per_seq  host upper bound on n_b (rows past it are reported through
+ *               err_word as D2F_ERR_INVALID_ARG and left unwritten)
+ *   max_ctx     host hint used only to pick the split count
+ *   dtype       D2F_BF16 (tensor-core path, head_dim 64 or 128) or D2F_F32
+ *               (CUDA-core path, head_dim <= 256 and a multiple of 32)
+ *   softmax_scale  > 0, typically 1/sqrt(head_dim)
+ *   num_splits  0 = automatic, else the number of CTAs sharing one sequence's keys
+ *   block_size  8, 16 or 32 on the tensor-core path; 1..256 on the CUDA-core path
+ *   workspace   device, >= d2f_block_attn_workspace_size(...) bytes, zeroed once
+ *
+ * Alignment: every device buffer 16-byte aligned.
+ */
+int d2f_block_attn(const void *q, const void *k_win, const void *v_win, const void *k_pool,
+                   const void *v_pool, const int32_t *page_table, int max_pages_per_seq,
+                   const int32_t *ctx_len, const int32_t *q_start, void *out, float *lse_out,
+                   int batch, int total_q, int max_q_per_seq, int max_ctx, int num_heads_q,
+                   int num_heads_kv, int head_dim, int block_size, int num_pages, int dtype,
+                   float softmax_scale, int num_splits, void *workspace, size_t workspace_bytes,
+                   int32_t *err_word, void *stream);
+
+/* ------------------------------------------------------------------------- */
+/* Confidence commit over the vocabulary                                    */
+/* ------------------------------------------------------------------------- */
+
+/* Workspace bytes for d2f_commit (num_splits 0 = automatic for the current device). */
+int d2f_commit_workspace_size(int total_q, int vocab, int dtype, int block_size, int num_splits,
+                              size_t *bytes);
+
+/*
+ * d2f_commit -- confidence, greedy token, commit and remask for every
+ * still-masked window position.
+ *
+ * [P3] §양방향 어텐션과 사라진 KV 캐시, §토큰 순서의 이론: confidence is the largest
+ * softmax probability of the position's prediction (LLaDA low-confidence
+ * remasking). [P2] §쉽게 이해하기: a conservative block commits the positions
+ * whose confidence is above the threshold; an aggressive block also commits its
+ * relatively most confident position; every position not committed is masked
+ * again for the next step.
+ *
+ * For each row r with masked[r] != 0, with l = the logit row logit_row[r]
+ * (or r when logit_row is NULL):
+ *   m = max_v l_v, a = lowest v with l_v = m (bf16 widened exactly to float),
+ *   p = 1 / sum_v exp(l_v - m) (float accumulation).
+ * For each window block jb of sequence b (tau[b], block_phase[jb]):
+ *   commit {r masked : p_r > tau[b]} (strict, in float); if aggressive and the
+ *   block has a masked row, also the masked row with the largest p (lowest row
+ *   on ties). Committed rows: tokens[r] = a, masked[r] = 0. Other masked rows:
+ *   tokens[r] = mask_id. Rows not masked on entry are left unchanged.
+ *
+ *   logits          device [num_logit_rows][row_stride] dtype; columns >= vocab are not read
+ *   row_stride      elements between logit rows (>= vocab)
+ *   logit_row       device int32 [total_q] or NULL (e.g. Dream's one-position shift)
+ *   tokens, masked  device int32 / uint8 [total_q], in/out
+ *   q_start         device int32 [batch+1]
+ *   block_phase     device uint8 [total_q / block_size] (D2F_PHASE_*)
+ *   tau             device float [batch]
+ *   conf_out        device float [total_q] or NULL: p for rows masked on entry, -1 otherwise
+ *   argmax_out      device int32 [total_q] or NULL: a for rows masked on entry, -1 otherwise
+ *   block_remaining device int32 [total_q / block_size] or NULL: masked rows left per block
+ *   block_size      1..32
+ */
+int d2f_commit(const void *logits, int64_t row_stride, int dtype, int vocab, int num_logit_rows,
+               const int32_t *logit_row, int32_t *tokens, uint8_t *masked,
+               const int32_t *q_start, const uint8_t *block_phase, const float *tau, int batch,
+               int total_q, int block_size, int32_t mask_id, float *conf_out,
+               int32_t *argmax_out, int32_t *block_remaining, int num_splits, void *workspace,
+               size_t workspace_bytes, int32_t *err_word, void *stream);
+
+/* ------------------------------------------------------------------------- */
+/* KV append of finished blocks                                             */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * d2f_kv_append -- copy finished blocks from the window K/V into their pages.
+ *
+ * [P1] §블록 단위 인과 어텐션 and §운영 관점: a completed block's K/V never change
+ * and are stored permanently; with pages of one block, completion is the signal
+ * to persist. For append a: k_pool[dst_page[a]][g][s][:] = k_win[src_row[a]+s][g][:]
+ * for every KV head g and slot s < block_size (same for V); a bitwise copy.
+ * The caller then extends page_table / ctx_len.
+ *
+ *   src_row, dst_page  device int32 [n_append]; src_row[a] + block_size <= total_q,
+ *                      0 <= dst_page[a] < num_pages (else err_word = D2F_ERR_BAD_INDEX
+ *                      and that append is skipped). Destination pages must be distinct.
+ */
+int d2f_kv_append(const void *k_win, const void *v_win, const int32_t *src_row,
+                  const int32_t *dst_page, int n_append, int total_q, void *k_pool,
+                  void *v_pool, int num_heads_kv, int head_dim, int block_size, int num_pages,
+                  int dtype, int32_t *err_word, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* D2F_H */

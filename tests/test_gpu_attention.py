@@ -1,0 +1,146 @@
+"""GPU parity of d2f_block_attn against the CPU oracle (element by element).
+
+Covers every workload at reduced size (several tiles, ragged tails, GQA with
+more than 128 packed rows, permuted page tables, contexts that are not a
+multiple of the block, empty contexts), forced split counts (the log-space
+composition path), both the tensor-core and the CUDA-core path, and the
+full-size LLaDA-shaped layer in the launch configuration the benchmark times.
+"""
+import os
+
+import pytest
+import torch
+
+import oracle
+from block_causal_kv_gb300 import d2f, synth
+from gpu_common import check_attention, device
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(p, dev, num_splits=0, want_lse=True):
+    g = p.to(dev)
+    out, lse = d2f.block_attn(g.q, g.k_win, g.v_win, g.k_pool, g.v_pool, g.page_table,
+                              g.ctx_len, g.q_start, block_size=p.w.block_size,
+                              max_q_per_seq=p.max_q_per_seq, max_ctx=p.max_ctx,
+                              num_splits=num_splits, want_lse=want_lse)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+_REF = {}
+
+
+def _ref(p):
+    key = (p.w.name, p.w.seed, p.w.block_size, p.w.head_dim, str(p.w.dtype))
+    if key not in _REF:
+        _REF[key] = oracle.block_attn(p.q, p.k_win, p.v_win, p.k_pool, p.v_pool, p.page_table,
+                                      p.ctx_len, p.q_start, p.w.block_size)
+    return _REF[key]
+
+
+SMALL = ["tiny", "llada", "ragged", "dream", "long_b8", "long_b16", "long_b32"]
+
+
+@pytest.mark.parametrize("name", SMALL)
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_small_workloads(name, splits):
+    dev = device()
+    w = synth.workload("tiny") if name == "tiny" else synth.small(name)
+    p = synth.make_problem(w)
+    out, lse = _run(p, dev, splits)
+    ref, ref_lse = _ref(p)
+    check_attention(out, lse, ref, ref_lse, w.dtype, "%s/s%d" % (name, splits))
+
+
+@pytest.mark.parametrize("name", ["llada", "ragged", "dream", "long_b16"])
+def test_cuda_core_path_bf16(name, monkeypatch):
+    """The CUDA-core kernel on bf16 operands, cross-checked like the main path."""
+    dev = device()
+    monkeypatch.setenv("D2F_ATTN_PATH", "simt")
+    p = synth.make_problem(synth.small(name))
+    out, lse = _run(p, dev, 2)
+    ref, ref_lse = _ref(p)
+    check_attention(out, lse, ref, ref_lse, torch.bfloat16, "simt/" + name)
+
+
+@pytest.mark.parametrize("B", [8, 16, 32])
+@pytest.mark.parametrize("D", [64, 128])
+def test_block_and_head_sizes(B, D):
+    dev = device()
+    w = synth.Workload("bd", 2, 4, 2, D, B, torch.bfloat16, [5 * B + 3, 130], [3, 2], 64,
+                       permute_pages=True, extra_pages=2, seed=400 + B + D)
+    p = synth.make_problem(w)
+    for splits in (1, 2, 5):
+        out, lse = _run(p, dev, splits)
+        ref, ref_lse = _ref(p)
+        check_attention(out, lse, ref, ref_lse, torch.bfloat16, "B%d D%d s%d" % (B, D, splits))
+
+
+def test_many_splits_more_than_tiles():
+    """Requested splits beyond the number of key tiles: each sequence uses only
+    as many non-empty splits as it has tiles."""
+    dev = device()
+    w = synth.Workload("ms", 3, 4, 4, 128, 16, torch.bfloat16, [0, 16, 700], [1, 2, 3], 64,
+                       seed=77)
+    p = synth.make_problem(w)
+    out, lse = _run(p, dev, 64)
+    ref, ref_lse = _ref(p)
+    check_attention(out, lse, ref, ref_lse, torch.bfloat16, "splits64")
+
+
+def test_lse_optional_and_repeatable():
+    """lse_out may be NULL; back-to-back calls with one workspace give identical
+    results (merge counters reset themselves)."""
+    dev = device()
+    p = synth.make_problem(synth.small("ragged"))
+    g = p.to(dev)
+    ws = d2f.attn_workspace(dev, batch=p.w.batch, total_q=p.w.total_q,
+                            max_q_per_seq=p.max_q_per_seq, max_ctx=p.max_ctx,
+                            num_heads_q=p.w.num_heads_q, num_heads_kv=p.w.num_heads_kv,
+                            head_dim=p.w.head_dim, block_size=p.w.block_size, num_splits=4)
+    outs = []
+    for _ in range(3):
+        out, lse = d2f.block_attn(g.q, g.k_win, g.v_win, g.k_pool, g.v_pool, g.page_table,
+                                  g.ctx_len, g.q_start, block_size=p.w.block_size,
+                                  max_q_per_seq=p.max_q_per_seq, max_ctx=p.max_ctx,
+                                  num_splits=4, want_lse=False, workspace=ws)
+        outs.append(out.clone())
+    torch.cuda.synchronize()
+    assert lse is None
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+    # merge counters (one per sequence x KV head x 16-row group, at offset 0) back at zero
+    n_counters = p.w.batch * p.w.num_heads_kv * -(-p.max_q_per_seq * p.w.num_heads_q
+                                                   // p.w.num_heads_kv // 16)
+    assert int(ws[:4 * n_counters].view(torch.int32).abs().sum()) == 0
+    ref, _ = _ref(p)
+    check_attention(outs[0], None, ref, None, torch.bfloat16, "repeat")
+
+
+def test_full_size_llada_layer():
+    """The LLaDA-8B-shaped layer at full size, automatic splits (the benchmark's
+    launch configuration), every output element against the oracle."""
+    dev = device()
+    p = synth.make_problem(synth.workload("llada"))
+    out, lse = _run(p, dev, 0)
+    ref, ref_lse = _ref(p)
+    mx, mean = check_attention(out, lse, ref, ref_lse, torch.bfloat16, "llada full")
+    print("llada full: max-abs %.3e mean-abs %.3e" % (mx, mean))
+
+
+@pytest.mark.parametrize("name", ["dream", "ragged", "long_b16"])
+def test_full_size_sampled(name):
+    """Full-size workloads: the GPU runs the whole batch; the oracle recomputes
+    one sampled sequence (its window rows, all heads) one by one."""
+    dev = device()
+    p = synth.make_problem(synth.workload(name))
+    out, _ = _run(p, dev, 0, want_lse=False)
+    b = p.w.batch // 2
+    qs = p.q_start.tolist()
+    rows = slice(qs[b], qs[b + 1])
+    ref, _ = oracle.block_attn(p.q[rows], p.k_win[rows], p.v_win[rows], p.k_pool, p.v_pool,
+                               p.page_table[b:b + 1], p.ctx_len[b:b + 1],
+                               torch.tensor([0, qs[b + 1] - qs[b]], dtype=torch.int32),
+                               p.w.block_size, want_lse=False)
+    mx, mean = check_attention(out[rows], None, ref, None, torch.bfloat16, name + " full")
+    print("%s full (sequence %d): max-abs %.3e mean-abs %.3e" % (name, b, mx, mean))

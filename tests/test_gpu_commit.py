@@ -1,0 +1,145 @@
+"""GPU parity of d2f_commit against the CPU oracle.
+
+Greedy tokens bit-exact; confidence within 1e-5 relative; committed tokens and
+masks bit-exact outside the reported |p - tau| < 1e-5 band and aggressive
+near-ties. Covers every workload's logits (full size for LLaDA, Dream and the
+ragged batch), tie-heavy rows, tau = 0 / 1, Dream's shifted logit rows, padded
+and unaligned row strides, float32 logits, split counts, block sizes 1..32.
+"""
+import pytest
+import torch
+
+import oracle
+from block_causal_kv_gb300 import d2f, synth
+from gpu_common import commit_compare, device
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu_commit(p, dev, phase=None, tau=None, num_splits=0, logit_row=None, logits=None):
+    g = p.to(dev)
+    phase = g.block_phase if phase is None else phase.to(dev)
+    tau = g.tau if tau is None else tau.to(dev)
+    lg = g.logits if logits is None else logits.to(dev)
+    lr = None if logit_row is None else logit_row.to(dev)
+    res = d2f.commit(lg, g.tokens, g.masked, g.q_start, phase, tau, block_size=p.w.block_size,
+                     mask_id=p.mask_id, logit_row=lr, num_splits=num_splits)
+    torch.cuda.synchronize()
+    return g, res, phase, tau
+
+
+def _check(p, dev, phase=None, tau=None, num_splits=0, logit_row=None, logits=None):
+    g, res, phase, tau = _gpu_commit(p, dev, phase, tau, num_splits, logit_row, logits)
+    ref = oracle.commit(p.logits if logits is None else logits, p.tokens, p.masked, p.q_start,
+                        phase.cpu(), tau.cpu(), p.w.block_size, p.mask_id,
+                        logit_row=logit_row)
+    return commit_compare(p, g.tokens, g.masked, res["conf"], res["argmax"],
+                          res["block_remaining"], phase, tau, ref)
+
+
+@pytest.mark.parametrize("name", ["tiny", "llada", "ragged", "dream", "long_b8", "long_b32"])
+@pytest.mark.parametrize("splits", [0, 1, 7])
+def test_small_workloads(name, splits):
+    dev = device()
+    w = synth.workload("tiny") if name == "tiny" else synth.small(name)
+    nb, nt = _check(synth.make_problem(w), dev, num_splits=splits)
+    print("%s s%d: band %d tie %d" % (name, splits, nb, nt))
+
+
+@pytest.mark.parametrize("name", ["llada", "ragged", "dream"])
+def test_full_size(name):
+    dev = device()
+    p = synth.make_problem(synth.workload(name))
+    nb, nt = _check(p, dev)
+    print("%s full: rows %d, excluded band %d tie %d" % (name, p.w.total_q, nb, nt))
+
+
+def _tiny_vocab(seed, B=8, vocab=300, **over):
+    kw = dict(masked_frac=0.6, taus=(0.05, 0.3, 0.6), logit_sigma=1.5)
+    kw.update(over)
+    w = synth.Workload("c", 3, 1, 1, 8, B, torch.bfloat16, [0, 0, 0], [2, 1, 3], vocab,
+                       seed=seed, **kw)
+    return synth.make_problem(w)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_random_phases_and_thresholds(seed):
+    dev = device()
+    p = _tiny_vocab(seed)
+    phase = torch.randint(0, 2, p.block_phase.shape, generator=torch.Generator().manual_seed(seed),
+                          dtype=torch.uint8)
+    _check(p, dev, phase=phase)
+
+
+def test_argmax_ties_take_lowest_index():
+    dev = device()
+    p = _tiny_vocab(3, vocab=4096)
+    g = torch.Generator().manual_seed(5)
+    tied = (torch.randint(0, 3, p.logits.shape, generator=g).float() * 0.5).to(torch.bfloat16)
+    _check(p, dev, logits=tied, num_splits=5)
+
+
+def test_tau_zero_and_one():
+    dev = device()
+    p = _tiny_vocab(8)
+    all_aggr = torch.ones_like(p.block_phase)
+    _check(p, dev, phase=all_aggr, tau=torch.ones_like(p.tau))
+    _check(p, dev, tau=torch.zeros_like(p.tau))
+
+
+def test_logit_row_shift_and_padded_stride():
+    dev = device()
+    w = synth.Workload("s", 2, 1, 1, 8, 16, torch.bfloat16, [0, 0], [2, 1], 1001,
+                       logit_row_pad=24, masked_frac=0.8, seed=21)
+    p = synth.make_problem(w)
+    shift = torch.clamp(torch.arange(p.w.total_q, dtype=torch.int32) - 1, min=0)
+    _check(p, dev, logit_row=shift)
+
+
+def test_unaligned_rows_use_the_scalar_path():
+    dev = device()
+    w = synth.Workload("u", 1, 1, 1, 8, 8, torch.bfloat16, [0], [2], 999, logit_row_pad=2,
+                       seed=22)
+    p = synth.make_problem(w)  # row stride 1001 elements: rows not 16-byte aligned
+    _check(p, dev, num_splits=3)
+
+
+def test_float32_logits():
+    dev = device()
+    p = synth.make_problem(synth.workload("tiny"))
+    _check(p, dev, num_splits=2)
+
+
+@pytest.mark.parametrize("B", [1, 4, 32])
+def test_block_sizes(B):
+    dev = device()
+    p = _tiny_vocab(30 + B, B=B)
+    phase = torch.randint(0, 2, p.block_phase.shape, generator=torch.Generator().manual_seed(B),
+                          dtype=torch.uint8)
+    _check(p, dev, phase=phase, num_splits=2)
+
+
+def test_nothing_masked_and_repeated_calls():
+    """Three calls in a row on the evolving state match the oracle applied three
+    times (counters reset themselves); a batch with every position committed
+    commits nothing, also with a different split count on the same workspace."""
+    dev = device()
+    p = _tiny_vocab(11)
+    g = p.to(dev)
+    ws = d2f.commit_workspace(dev, total_q=p.w.total_q, vocab=p.w.vocab, block_size=p.w.block_size,
+                              num_splits=4)
+    ref = {"tokens": p.tokens, "masked": p.masked}
+    for _ in range(3):
+        d2f.commit(g.logits, g.tokens, g.masked, g.q_start, g.block_phase, g.tau,
+                   block_size=p.w.block_size, mask_id=p.mask_id, num_splits=4, workspace=ws)
+        ref = oracle.commit(p.logits, ref["tokens"], ref["masked"], p.q_start, p.block_phase,
+                            p.tau, p.w.block_size, p.mask_id)
+    torch.cuda.synchronize()
+    assert torch.equal(g.tokens.cpu(), ref["tokens"])
+    assert torch.equal(g.masked.cpu(), ref["masked"])
+    done = torch.zeros_like(g.masked)
+    res = d2f.commit(g.logits, g.tokens, done, g.q_start, torch.ones_like(g.block_phase), g.tau,
+                     block_size=p.w.block_size, mask_id=p.mask_id, num_splits=2, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(res["block_remaining"].sum()) == 0
+    assert torch.all(res["conf"] == -1)
