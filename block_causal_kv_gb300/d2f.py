@@ -32,7 +32,7 @@ STATUS = {0: "D2F_OK", 1: "D2F_ERR_INVALID_ARG", 2: "D2F_ERR_UNSUPPORTED", 3: "D
 # Every symbol include/d2f.h declares.
 EXPORTS = ("d2f_version", "d2f_status_string", "d2f_last_error_string",
            "d2f_block_attn_workspace_size", "d2f_block_attn", "d2f_commit_workspace_size",
-           "d2f_commit", "d2f_kv_append")
+           "d2f_commit", "d2f_commit_noalloc", "d2f_kv_append")
 
 
 class D2FError(RuntimeError):
@@ -69,6 +69,9 @@ def load(path=LIB_PATH):
     lib.d2f_commit.restype = _I
     lib.d2f_commit.argtypes = ([_P, ctypes.c_int64, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I,
                                 ctypes.c_int32, _P, _P, _P, _I, _P, _SZ, _P, _P])
+    lib.d2f_commit_noalloc.restype = _I
+    lib.d2f_commit_noalloc.argtypes = ([_P, ctypes.c_int64, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I,
+                                        _I, _I, ctypes.c_int32, _P, _P, _P, _I, _P, _P])
     lib.d2f_kv_append.restype = _I
     lib.d2f_kv_append.argtypes = [_P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P]
     _lib = lib
@@ -225,6 +228,25 @@ def commit(logits, tokens, masked, q_start, block_phase, tau, *, block_size, mas
         block_size, int(mask_id), _ptr(conf), _ptr(argmax), _ptr(block_remaining), num_splits,
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err),
         _stream(stream)))
+    return {"conf": conf, "argmax": argmax, "block_remaining": block_remaining}
+
+
+def commit_noalloc(logits, tokens, masked, q_start, block_phase, tau, *, block_size, mask_id,
+                   logit_row=None, num_splits=0, conf=None, argmax=None, block_remaining=None,
+                   err=None, stream=None):
+    """d2f_commit_noalloc: the commit without a workspace, for callers that cannot
+    allocate device memory; its scratch is a fixed array inside the library (see
+    include/d2f.h for the size limit and the rule that calls must not overlap)."""
+    lib = load()
+    if not logits.is_cuda or logits.stride(-1) != 1:
+        raise ValueError("logits must be a CUDA tensor with unit stride along the vocabulary")
+    total_q = tokens.shape[0]
+    rows, vocab = logits.shape
+    _check(lib.d2f_commit_noalloc(
+        _ptr(logits), logits.stride(0), _dtype_code(logits), vocab, rows, _ptr(logit_row),
+        _ptr(tokens), _ptr(masked), _ptr(q_start), _ptr(block_phase), _ptr(tau),
+        q_start.shape[0] - 1, total_q, block_size, int(mask_id), _ptr(conf), _ptr(argmax),
+        _ptr(block_remaining), num_splits, _ptr(err), _stream(stream)))
     return {"conf": conf, "argmax": argmax, "block_remaining": block_remaining}
 
 

@@ -182,6 +182,30 @@ int d2f_commit(const void *logits, int64_t row_stride, int dtype, int vocab, int
                int32_t *argmax_out, int32_t *block_remaining, int num_splits, void *workspace,
                size_t workspace_bytes, int32_t *err_word, void *stream);
 
+/*
+ * d2f_commit_noalloc -- d2f_commit without a caller workspace, for callers that
+ * cannot allocate device memory (a plugin or callback that may only use the
+ * buffers its host framework passes in, a runtime that must not allocate once it
+ * serves, a caller with no allocator at hand). The pages describe no such entry
+ * point; it exists only for those callers.
+ *
+ * Same arguments and result as d2f_commit, minus workspace / workspace_bytes.
+ * Its scratch is a fixed 2 MiB array in the library's device image, held by
+ * every GPU that loads the library until the process exits. Requests whose
+ * d2f_commit_workspace_size exceeds 2 MiB return D2F_ERR_WORKSPACE (use
+ * d2f_commit instead). The first call on each device looks up the array's
+ * device address (cudaGetSymbolAddress); make that first call before any
+ * stream capture. Each call clears the scratch it uses with cudaMemsetAsync on
+ * `stream`; nothing is allocated or freed. All calls share the one array:
+ * calls that may overlap on the GPU race and must be serialised.
+ */
+int d2f_commit_noalloc(const void *logits, int64_t row_stride, int dtype, int vocab,
+                       int num_logit_rows, const int32_t *logit_row, int32_t *tokens,
+                       uint8_t *masked, const int32_t *q_start, const uint8_t *block_phase,
+                       const float *tau, int batch, int total_q, int block_size, int32_t mask_id,
+                       float *conf_out, int32_t *argmax_out, int32_t *block_remaining,
+                       int num_splits, int32_t *err_word, void *stream);
+
 /* ------------------------------------------------------------------------- */
 /* KV append of finished blocks                                             */
 /* ------------------------------------------------------------------------- */
