@@ -4,28 +4,34 @@
 // 모델보다 2.5배 빨라지는 방법", §블록 단위 인과 어텐션 (bidirectional inside a
 // block, causal between blocks, finished blocks in a KV cache) and §운영 관점
 // (paged cache, one block per page); "D2F 논문 리뷰", §쉽게 이해하기 (a window of
-// several active blocks decoded together).
+// several active blocks decoded together); "확산 언어 모델(Diffusion LLM)이란
+// 무엇인가", §FlashBlock (attention parts recombined in log space).
 //
-// One CTA = (row tile of <= 128 query rows, split, sequence x KV head). The
-// G = Hq/Hkv query heads of a KV group are packed into the rows (row r = query
-// r / G, head r % G), so every K/V byte is read once per row tile. The CTA's key
-// tiles (64 keys: 64/B cache pages, or 64/B window blocks) stream through a
-// 4-stage shared-memory ring:
+// Work decomposition. A row tile is <= 128 query rows of one (sequence, KV
+// head): the G = Hq/Hkv query heads of the group are packed into the rows
+// (row r = query r / G, head r % G), so every K/V byte is read once per row
+// tile. The key tiles of the row tile (64 keys = 64/B cache pages or 64/B window
+// blocks, cache first) are split among the `cs` CTAs of one thread-block
+// cluster; each CTA streams its share through a 4-stage shared-memory ring:
 //
-//   warp 0 (one lane)  TMA producer: page ids -> cp.async.bulk.tensor loads of
-//                      the K and V tiles (128-byte swizzle), completion counted
-//                      on the stage's mbarrier; slots past the sequence are skipped.
-//   warp 1 (one lane)  MMA issuer: S = Q K^T into TMEM (double-buffered), then
-//                      O += P V into TMEM once the softmax has written P.
-//   warps 2-5          one thread per query row (= TMEM lane): read S from TMEM,
-//                      mask, online softmax in log2 units with lazy rescaling
-//                      of O (only when the running max grows by > 2^8), write
-//                      bf16 P to shared memory for the second MMA.
+//   warp 0       TMA producer: page ids (32 at a time, prefetched) ->
+//                cp.async.bulk.tensor loads of the K and V tiles, 128-byte
+//                swizzle, completion counted on the stage's mbarrier.
+//   warp 1       MMA issuer (one lane): S = Q K^T into TMEM (double-buffered),
+//                then O += P V into TMEM once the softmax has written P.
+//   warps 2-5    one thread per query row (= TMEM lane): load the Q row, then per
+//                tile read S from TMEM, apply the block-causal mask as a per-row
+//                key limit, online softmax in log2 units with lazy rescaling of
+//                O (only when the running max grows by more than 2^8), write bf16
+//                P to shared memory for the second MMA.
 //
-// Splits of one row tile write unnormalised partials; the last-arriving CTA
-// composes them in log space. Every mbarrier wait is bounded; on time-out the
-// CTA records D2F_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and
-// returns.
+// Composition. With cs > 1 every CTA stages its unnormalised O and (max, sum)
+// in its own shared memory; after a cluster barrier CTA k composes the rows
+// r = k mod cs by reading all cs partials through distributed shared memory and
+// writes the normalised output. No partial ever goes to global memory.
+//
+// Every mbarrier wait is bounded; on time-out the CTA records D2F_ERR_TIMEOUT,
+// drains its own copies and MMAs, frees TMEM and returns.
 #include <string.h>
 
 #include <cstdio>
@@ -37,36 +43,45 @@ namespace d2f {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int NS = 4;             // K/V ring stages
-constexpr int M = kTcRows;        // 128 query rows per tile
-constexpr int N = kTcKeys;        // 64 keys per tile
+constexpr int NS = 4;                // K/V ring stages
+constexpr int M = kTcRows;           // 128 query rows per tile
+constexpr int N = kTcKeys;           // 64 keys per tile
 constexpr uint32_t kTmemCols = 256;  // S double buffer (2 x 64) + O (<= 128)
 constexpr uint32_t kTmemO = 128;     // first TMEM column of O
 constexpr int kEpiThreads = 128;
+constexpr int kMaxCluster = 8;
 
 template <int D>
 struct Layout {
-  static constexpr int kHalves = D / 64;               // 64-element (128-byte) swizzle columns
-  static constexpr int kQHalf = M * 128;               // one 64-wide column block of Q
+  static constexpr int kHalves = D / 64;         // 64-element (128-byte) swizzle columns
+  static constexpr int kQHalf = M * 128;         // one 64-wide column block of Q
   static constexpr int kQBytes = kHalves * kQHalf;
-  static constexpr int kKVHalf = N * 128;              // 64 key rows x 128 bytes
+  static constexpr int kKVHalf = N * 128;        // 64 key rows x 128 bytes
   static constexpr int kKBytes = kHalves * kKVHalf;
-  static constexpr int kStage = 2 * kKBytes;           // K tile then V tile
-  static constexpr int kPBytes = M * N * 2;            // bf16 P, 128 rows x 128 bytes
+  static constexpr int kStage = 2 * kKBytes;     // K tile then V tile
+  static constexpr int kPBytes = M * N * 2;      // bf16 P, 128 rows x 128 bytes
+  static constexpr int kChunks = D / 4;          // 16-byte chunks of one fp32 O row
   static constexpr int kQ = 0;
-  static constexpr int kRing = kQ + kQBytes;
+  static constexpr int kRing = kQ + kQBytes;     // also the fp32 O staging area
   static constexpr int kP = kRing + NS * kStage;
-  static constexpr int kBars = kP + 2 * kPBytes;
+  static constexpr int kML = kP + 2 * kPBytes;   // float2 (max, sum) per row
+  static constexpr int kBars = kML + M * 8;
   static constexpr int kBytes = kBars + 256;
-  static constexpr int kAlloc = kBytes + 1024;          // slack for 1024-byte alignment
+  static constexpr int kAlloc = kBytes + 1024;   // slack for 1024-byte alignment
+  static_assert(NS * kStage >= M * D * 4, "O staging must fit in the ring");
 };
 
 struct Bars {
-  uint64_t full[NS], empty[NS], s_full[2], p_full[2], pv_done[2], drain;
+  uint64_t full[NS], empty[NS], s_full[2], p_full[2], pv_done[2], q_full, drain;
   uint32_t tmem_base;
   int abort_flag;
-  int is_last;
 };
+
+template <int D>
+__device__ __forceinline__ uint32_t o_stage_addr(uint32_t sb, int row, int chunk) {
+  using L = Layout<D>;
+  return sb + L::kRing + row * (D * 4) + ((chunk ^ (row % L::kChunks)) << 4);
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -81,12 +96,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sb = smem_u32(smem);
   Bars *bars = reinterpret_cast<Bars *>(smem + L::kBars);
   volatile int *abort_flag = &bars->abort_flag;
+  float2 *ml_s = reinterpret_cast<float2 *>(smem + L::kML);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int mt = blockIdx.x, split = blockIdx.y;
+  const int cs = gridDim.x;  // CTAs of the cluster = splits of this row tile
+  const int split = blockIdx.x;
+  const int mt = blockIdx.y;
   const int b = blockIdx.z / a.num_heads_kv, g = blockIdx.z % a.num_heads_kv;
 
-  // ---- work of this CTA (uniform across the CTA) ----------------------------
+  if (tid == 0) D2F_TRACE_MARK(0, 0);
+  grid_dependency_wait();  // inputs may come from the previous kernel in the stream
+  if (tid == 0) D2F_TRACE_MARK(0, 1);
+
+  // ---- work of this CTA (uniform across the cluster except has_work) ---------
   int q0, n, C;
   if (!load_seq_meta(a, b, q0, n, C)) {
     if (tid == 0 && mt == 0 && split == 0 && g == 0) set_err(a.err, D2F_ERR_INVALID_ARG);
@@ -98,11 +120,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (r_begin >= rows_total) return;
   const int nrows = min(M, rows_total - r_begin);
   const int Tc = (C + N - 1) / N, Tw = (n + N - 1) / N;
-  int t0, t1, s_eff;
-  if (!split_range(Tc + Tw, a.num_splits, split, t0, t1, s_eff)) return;
-  const int T = t1 - t0;
+  int t0 = 0, t1 = 0, s_eff = 1;
+  const bool has_work = split_range(Tc + Tw, cs, split, t0, t1, s_eff);
+  const int T = has_work ? t1 - t0 : 0;
+  grid_launch_dependents();
 
-  // ---- set-up: barriers, TMEM, Q tile ---------------------------------------
+  // ---- set-up: barriers, TMEM --------------------------------------------------
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(&bars->full[i]), 1);
@@ -113,115 +136,114 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bars->p_full[i]), kEpiThreads);
       mbar_init(smem_u32(&bars->pv_done[i]), 1);
     }
+    mbar_init(smem_u32(&bars->q_full), kEpiThreads);
     mbar_init(smem_u32(&bars->drain), 1);
     bars->abort_flag = 0;
     mbar_fence_init();
   }
-  if (warp == 0 && lane == 0) {
+  if (has_work && warp == 1) {
+    tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  if (has_work && warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_kpool);
     tma_prefetch_desc(&tm_vpool);
     tma_prefetch_desc(&tm_kwin);
     tma_prefetch_desc(&tm_vwin);
   }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
-    tmem_relinquish();
-  }
-  {
-    // Q rows into the 128-byte-swizzled K-major layout the MMA reads:
-    // row rr, 16-byte chunk c of column block h lands at
-    //   h*kQHalf + (rr/8)*1024 + (rr%8)*128 + ((c ^ (rr%8)) * 16).
-    const uint16_t *Q = reinterpret_cast<const uint16_t *>(a.q);
-    constexpr int kChunks = D / 8;
-    for (int e = tid; e < M * kChunks; e += kThreads) {
-      const int rr = e / kChunks, c = e % kChunks;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (rr < nrows) {
-        const int r = r_begin + rr;
-        const int64_t off = ((int64_t)(q0 + r / G) * H + g * G + r % G) * D + c * 8;
-        v = *reinterpret_cast<const uint4 *>(Q + off);
-      }
-      const int h = c >> 3, cc = c & 7;
-      const uint32_t dst =
-          sb + L::kQ + h * L::kQHalf + (rr >> 3) * 1024 + (rr & 7) * 128 + ((cc ^ (rr & 7)) << 4);
-      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y),
-                   "r"(v.z), "r"(v.w)
-                   : "memory");
-    }
-  }
-  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  if (tid == 0) D2F_TRACE_MARK(0, 2);
 
-  if (warp == 0) {
-    // ======================= TMA producer ======================================
-    if (lane == 0) {
-      int issued = 0;
-      const int pages_per_tile = N / B;
-      for (int u = 0; u < T; ++u) {
-        const int stage = u % NS;
-        if (u >= NS &&
-            !mbar_wait(smem_u32(&bars->empty[stage]), ((u / NS) - 1) & 1, abort_flag, a.err))
-          break;
-        const uint32_t full = smem_u32(&bars->full[stage]);
-        const uint32_t kdst = sb + L::kRing + stage * L::kStage;
-        const uint32_t vdst = kdst + L::kKBytes;
-        const int t = t0 + u;
-        // Source of each B-row slot of the tile: a physical page (cache tiles) or a
-        // window row (window tiles); -1 = nothing to load (past the sequence, or a
-        // bad page id). Skipped slots keep stale shared memory: their keys are
-        // masked and their V rows are cleared by the softmax warps.
-        int src[N / 8];
-        uint32_t bytes = 0;
-        for (int p = 0; p < pages_per_tile; ++p) {
-          src[p] = -1;
-          if (t < Tc) {
-            const int lp = t * pages_per_tile + p;  // logical page of the sequence
-            if (lp * B < C) {
-              const int pg = a.page_table[(int64_t)b * a.max_pages_per_seq + lp];
-              if (pg >= 0 && pg < a.num_pages)
-                src[p] = pg;
-              else
-                set_err(a.err, D2F_ERR_BAD_INDEX);
-            }
-          } else {
-            const int w0 = (t - Tc) * N + p * B;  // first window row of this block
-            if (w0 < n) src[p] = q0 + w0;
-          }
-          if (src[p] >= 0) bytes += 2u * L::kHalves * B * 128;
-        }
-        mbar_arrive_expect_tx(full, bytes);
-        for (int p = 0; p < pages_per_tile; ++p) {
-          if (src[p] < 0) continue;
-          const uint32_t row_off = p * B * 128;
-#pragma unroll
-          for (int h = 0; h < L::kHalves; ++h) {
-            if (t < Tc) {
-              tma_load_4d(kdst + h * L::kKVHalf + row_off, &tm_kpool, full, h * 64, 0, g, src[p]);
-              tma_load_4d(vdst + h * L::kKVHalf + row_off, &tm_vpool, full, h * 64, 0, g, src[p]);
-            } else {
-              tma_load_3d(kdst + h * L::kKVHalf + row_off, &tm_kwin, full, h * 64, g, src[p]);
-              tma_load_3d(vdst + h * L::kKVHalf + row_off, &tm_vwin, full, h * 64, g, src[p]);
-            }
-          }
-        }
-        issued = u + 1;
+  // softmax-thread identity (warps 2-5)
+  const int quad = warp & 3;         // TMEM lanes 32*quad .. 32*quad+31
+  const int row = quad * 32 + lane;  // row of the tile = TMEM lane
+  const bool row_valid = row < nrows;
+  const int r = r_begin + row;
+  const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
+  float m_ref = -INFINITY, l = 0.f;
+
+  if (has_work && warp == 0) {
+    // ======================= TMA producer (whole warp) =========================
+    const int ppt = N / B;                        // pages (or window blocks) per tile
+    const int n_pages = (C + B - 1) / B;          // cached pages of the sequence
+    const int p_first = t0 * ppt;                 // first logical page of this CTA
+    const int32_t *pt = a.page_table + (int64_t)b * a.max_pages_per_seq;
+    auto fetch = [&](int base) -> int {
+      const int lp = base + lane;
+      return (lp < n_pages && lp < p_first + T * ppt) ? __ldg(pt + lp) : -1;
+    };
+    int chunk = p_first;                          // logical page held by lane 0 of ids_cur
+    int ids_cur = fetch(chunk);
+    int ids_next = fetch(chunk + 32);
+    int issued = 0;
+    for (int u = 0; u < T; ++u) {
+      const int stage = u % NS;
+      const int t = t0 + u;
+      if (u >= NS) {
+        bool ok = true;
+        if (lane == 0)
+          ok = mbar_wait(smem_u32(&bars->empty[stage]), ((u / NS) - 1) & 1, abort_flag, a.err);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       }
-      // Drain: every issued stage must have landed before the CTA may exit.
+      // Source of slot p (lane p < ppt): a physical page or a window row; -1 =
+      // nothing to load (past the sequence, or a bad page id). Skipped slots keep
+      // stale shared memory: their keys are masked and their V rows cleared.
+      int src = -1;
+      if (t < Tc) {
+        const int lp0 = t * ppt;
+        if (lp0 - chunk >= 32) {                  // warp-uniform: move to the next 32 ids
+          chunk += 32;
+          ids_cur = ids_next;
+          ids_next = fetch(chunk + 32);
+        }
+        const int pg = __shfl_sync(0xffffffffu, ids_cur, (lp0 - chunk + lane) & 31);
+        if (lane < ppt && (lp0 + lane) * B < C) {
+          if (pg >= 0 && pg < a.num_pages)
+            src = pg;
+          else
+            set_err(a.err, D2F_ERR_BAD_INDEX);
+        }
+      } else if (lane < ppt) {
+        const int w0 = (t - Tc) * N + lane * B;   // first window row of this block
+        if (w0 < n) src = q0 + w0;
+      }
+      const unsigned have = __ballot_sync(0xffffffffu, src >= 0);
+      const uint32_t full = smem_u32(&bars->full[stage]);
+      if (lane == 0) mbar_arrive_expect_tx(full, __popc(have) * 2u * L::kHalves * B * 128);
+      __syncwarp();
+      if (src >= 0) {
+        const uint32_t kdst = sb + L::kRing + stage * L::kStage + lane * B * 128;
+        const uint32_t vdst = kdst + L::kKBytes;
+#pragma unroll
+        for (int h = 0; h < L::kHalves; ++h) {
+          if (t < Tc) {
+            tma_load_4d(kdst + h * L::kKVHalf, &tm_kpool, full, h * 64, 0, g, src);
+            tma_load_4d(vdst + h * L::kKVHalf, &tm_vpool, full, h * 64, 0, g, src);
+          } else {
+            tma_load_3d(kdst + h * L::kKVHalf, &tm_kwin, full, h * 64, g, src);
+            tma_load_3d(vdst + h * L::kKVHalf, &tm_vwin, full, h * 64, g, src);
+          }
+        }
+      }
+      issued = u + 1;
+    }
+    // Drain: every issued stage must have landed before the CTA moves on.
+    if (lane == 0) {
       for (int u = max(0, issued - NS); u < issued; ++u) {
         volatile int no_abort = 0;
         mbar_wait(smem_u32(&bars->full[u % NS]), (u / NS) & 1, &no_abort, a.err);
       }
     }
-  } else if (warp == 1) {
+  } else if (has_work && warp == 1) {
     // ======================= MMA issuer ========================================
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(M, N, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(M, D, 0, 1);
       const uint32_t q_base = sb + L::kQ;
-      bool ok = true;
+      bool ok = mbar_wait(smem_u32(&bars->q_full), 0, abort_flag, a.err);
       auto issue_pv = [&](int v) -> bool {
         if (!mbar_wait(smem_u32(&bars->p_full[v & 1]), (v >> 1) & 1, abort_flag, a.err))
           return false;
@@ -246,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
+        if (u == 0) D2F_TRACE_MARK(0, 10);
         const uint32_t k_base = sb + L::kRing + stage * L::kStage;
 #pragma unroll
         for (int h = 0; h < L::kHalves; ++h) {
@@ -265,23 +288,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       volatile int no_abort = 0;
       mbar_wait(smem_u32(&bars->drain), 0, &no_abort, a.err);
     }
-  } else {
-    // ======================= softmax / epilogue (128 threads) ====================
-    const int quad = warp & 3;            // TMEM lanes 32*quad .. 32*quad+31
-    const int row = quad * 32 + lane;     // row of the tile = TMEM lane
-    const bool row_valid = row < nrows;
-    const int r = r_begin + row;
+  } else if (has_work) {
+    // ======================= softmax (128 threads, one per row) ================
+    {
+      // Q row into the 128-byte-swizzled K-major layout the MMA reads: 16-byte
+      // chunk c of column block h lands at
+      //   h*kQHalf + (row/8)*1024 + (row%8)*128 + ((c ^ (row%8)) * 16).
+      constexpr int kQc = D / 8;
+      uint4 qv[kQc];
+      const uint4 *src = reinterpret_cast<const uint4 *>(
+          reinterpret_cast<const uint16_t *>(a.q) +
+          ((int64_t)(q0 + r / G) * H + g * G + r % G) * D);
+#pragma unroll
+      for (int c = 0; c < kQc; ++c) qv[c] = row_valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int c = 0; c < kQc; ++c) {
+        const uint32_t dst = sb + L::kQ + (c >> 3) * L::kQHalf + (row >> 3) * 1024 +
+                             (row & 7) * 128 + (((c & 7) ^ (row & 7)) << 4);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(qv[c].x),
+                     "r"(qv[c].y), "r"(qv[c].z), "r"(qv[c].w)
+                     : "memory");
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&bars->q_full));
+      if (tid == 64) D2F_TRACE_MARK(0, 3);
+    }
     const int win_end = row_valid ? ((r / G) / B + 1) * B : 0;
-    const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
     const float sl2 = a.scale_log2;
-    float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-
     for (int u = 0; u < T; ++u) {
       const int t = t0 + u;
       ok = mbar_wait(smem_u32(&bars->s_full[u & 1]), (u >> 1) & 1, abort_flag, a.err);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
+      if (tid == 64 && u == 0) D2F_TRACE_MARK(0, 4);
+      if (tid == 64 && u == T - 1) D2F_TRACE_MARK(0, 5);
       uint32_t s_lo[32], s_hi[32];
       tmem_ld32(lane_addr + (u & 1) * N, s_lo);
       tmem_ld32(lane_addr + (u & 1) * N + 32, s_hi);
@@ -328,8 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float p0 = c0 < lim ? fast_exp2(fmaf(__uint_as_float(s_lo[c0]), sl2, -m_ref)) : 0.f;
         const float p1 = c1 < lim ? fast_exp2(fmaf(__uint_as_float(s_lo[c1]), sl2, -m_ref)) : 0.f;
         pk[j] = pack_bf16x2(p0, p1);
-        const float p2 = c0 + 32 < lim ? fast_exp2(fmaf(__uint_as_float(s_hi[c0]), sl2, -m_ref)) : 0.f;
-        const float p3 = c1 + 32 < lim ? fast_exp2(fmaf(__uint_as_float(s_hi[c1]), sl2, -m_ref)) : 0.f;
+        const float p2 =
+            c0 + 32 < lim ? fast_exp2(fmaf(__uint_as_float(s_hi[c0]), sl2, -m_ref)) : 0.f;
+        const float p3 =
+            c1 + 32 < lim ? fast_exp2(fmaf(__uint_as_float(s_hi[c1]), sl2, -m_ref)) : 0.f;
         pk[16 + j] = pack_bf16x2(p2, p3);
       }
 #pragma unroll
@@ -342,10 +385,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(smem_u32(&bars->pv_done[u & 1]), ((u - 2) >> 1) & 1, abort_flag, a.err);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       }
-      const uint32_t p_row = sb + L::kP + (u & 1) * L::kPBytes + (row >> 3) * 1024 + (row & 7) * 128;
+      const uint32_t p_row =
+          sb + L::kP + (u & 1) * L::kPBytes + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(p_row + ((c ^ (row & 7)) << 4)),
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(p_row +
+                                                                       ((c ^ (row & 7)) << 4)),
                      "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
                      : "memory");
       }
@@ -368,64 +413,106 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(smem_u32(&bars->p_full[u & 1]));
     }
+    // wait for the last P.V product
+    if (tid == 64) D2F_TRACE_MARK(0, 6);
     if (ok) {
       ok = mbar_wait(smem_u32(&bars->pv_done[(T - 1) & 1]), ((T - 1) >> 1) & 1, abort_flag, a.err);
       ok = __all_sync(0xffffffffu, ok);
     }
-    __syncwarp();
-    asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
-    const bool aborted = *abort_flag != 0;
-    if (!aborted) {
-      tc_fence_after();
+    tc_fence_after();
+  }
+
+  // ---- epilogue ---------------------------------------------------------------
+  __syncwarp();
+  __syncthreads();  // every role is done; the ring and P buffers are free
+  if (tid == 0) D2F_TRACE_MARK(0, 7);
+  const bool aborted = *abort_flag != 0;
+  if (cs == 1) {
+    if (warp >= 2 && has_work && !aborted) {
       const int64_t hr = (int64_t)(q0 + r / G) * H + g * G + r % G;
-      const int64_t n_hr = (int64_t)a.total_q * H;
-      if (s_eff == 1) {
-        const float inv = 1.0f / l;
-        uint16_t *dst = reinterpret_cast<uint16_t *>(a.out) + hr * D;
+      const float inv = 1.0f / l;
+      uint16_t *dst = reinterpret_cast<uint16_t *>(a.out) + hr * D;
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t o[32];
+        tmem_ld32(lane_addr + kTmemO + ch * 32, o);
+        if (row_valid) {
+          uint32_t w[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            w[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
+          uint4 *d4 = reinterpret_cast<uint4 *>(dst + ch * 32);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            d4[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+        }
+      }
+      if (row_valid && a.lse_out) a.lse_out[hr] = (m_ref + __log2f(l)) * 0.6931471805599453f;
+    }
+  } else {
+    // Stage this CTA's partial: fp32 O rows (16-byte chunks XOR-swizzled by row)
+    // and (max, sum) per row; an empty or aborted CTA contributes nothing.
+    if (warp >= 2) {
+      const bool mine = has_work && !aborted;
+      ml_s[row] = mine ? make_float2(m_ref, l) : make_float2(-INFINITY, 0.f);
+      if (mine) {
 #pragma unroll
         for (int ch = 0; ch < D / 32; ++ch) {
           uint32_t o[32];
           tmem_ld32(lane_addr + kTmemO + ch * 32, o);
-          if (row_valid) {
-            uint32_t w[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              w[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
-            uint4 *d4 = reinterpret_cast<uint4 *>(dst + ch * 32);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) d4[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-          }
-        }
-        if (row_valid && a.lse_out) a.lse_out[hr] = (m_ref + __log2f(l)) * 0.6931471805599453f;
-      } else {
-        float *dst = a.ws_o + ((int64_t)split * n_hr + hr) * D;
-#pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t o[32];
-          tmem_ld32(lane_addr + kTmemO + ch * 32, o);
-          if (row_valid) {
-            uint4 *d4 = reinterpret_cast<uint4 *>(dst + ch * 32);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) d4[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-          }
-        }
-        if (row_valid) a.ws_ml[split * n_hr + hr] = make_float2(m_ref, l);
-        __threadfence();
-        asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
-        int32_t *cnt = a.counters + ((int64_t)blockIdx.z * a.m_tiles + mt);
-        if (tid == 64) bars->is_last = atomicAdd(cnt, 1) == s_eff - 1;
-        asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
-        if (bars->is_last) {
-          __threadfence();
-          for (int rr = warp - 2; rr < nrows; rr += 4) {
-            const int r2 = r_begin + rr;
-            const int64_t hr2 = (int64_t)(q0 + r2 / G) * H + g * G + r2 % G;
-            merge_head_row<uint16_t, D>(a, hr2, s_eff);
-          }
-          if (tid == 64) *cnt = 0;
+          for (int j = 0; j < 8; ++j)
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             o_stage_addr<D>(sb, row, ch * 8 + j)),
+                         "r"(o[4 * j]), "r"(o[4 * j + 1]), "r"(o[4 * j + 2]), "r"(o[4 * j + 3])
+                         : "memory");
         }
       }
     }
+    __syncwarp();
+    cluster_sync();
+    if (tid == 0) D2F_TRACE_MARK(0, 8);
+    if (warp >= 2) {
+      // CTA `split` composes rows split, split + cs, ...: one warp per row, lane c
+      // holds 16-byte chunk c of the row.
+      for (int rr = split + cs * (warp - 2); rr < nrows; rr += cs * 4) {
+        const int r2 = r_begin + rr;
+        const uint32_t ml_local = smem_u32(ml_s + rr);
+        float2 ml = make_float2(-INFINITY, 0.f);
+        if (lane < cs) ml = dsmem_ld_f2(dsmem_addr(ml_local, lane));
+        float mx = ml.x;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const float w = (lane < cs && ml.y > 0.f) ? fast_exp2(ml.x - mx) : 0.f;
+        float ls = w * ml.y;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const uint32_t o_local = o_stage_addr<D>(sb, rr, lane % L::kChunks);
+#pragma unroll
+        for (int j = 0; j < kMaxCluster; ++j) {
+          const float wj = __shfl_sync(0xffffffffu, w, j);
+          if (j < cs && wj > 0.f && lane < L::kChunks) {
+            const float4 v = dsmem_ld_f4(dsmem_addr(o_local, j));
+            acc.x = fmaf(wj, v.x, acc.x);
+            acc.y = fmaf(wj, v.y, acc.y);
+            acc.z = fmaf(wj, v.z, acc.z);
+            acc.w = fmaf(wj, v.w, acc.w);
+          }
+        }
+        if (lane < L::kChunks && !aborted) {
+          const float inv = 1.0f / ls;
+          const int64_t hr2 = (int64_t)(q0 + r2 / G) * H + g * G + r2 % G;
+          const uint2 packed = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv),
+                                          pack_bf16x2(acc.z * inv, acc.w * inv));
+          *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(a.out) + hr2 * D + lane * 4) =
+              packed;
+          if (lane == 0 && a.lse_out) a.lse_out[hr2] = (mx + __log2f(ls)) * 0.6931471805599453f;
+        }
+      }
+    }
+    __syncwarp();
+    cluster_sync();  // keep this CTA's shared memory alive until every peer has read it
   }
 
   // ---- teardown ---------------------------------------------------------------
@@ -433,7 +520,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (has_work && warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (tid == 0) D2F_TRACE_MARK(0, 9);
 }
 
 // ---------------------------------------------------------------------------
@@ -468,6 +556,22 @@ bool encode(EncodeTiledFn fn, CUtensorMap *map, const void *base, int rank, cons
   return r == CUDA_SUCCESS;
 }
 
+// The shared-memory opt-in is a per-device function attribute; set it once per device.
+template <int D>
+cudaError_t ensure_smem_attr() {
+  static std::mutex mu;
+  static bool done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Layout<D>::kAlloc);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+  return e;
+}
+
 template <int D>
 cudaError_t launch_d(const AttnArgs &a, cudaStream_t s, char *why, size_t why_len) {
   EncodeTiledFn fn = get_encode_fn();
@@ -491,12 +595,25 @@ cudaError_t launch_d(const AttnArgs &a, cudaStream_t s, char *why, size_t why_le
     snprintf(why, why_len, "cuTensorMapEncodeTiled rejected a K/V tensor (alignment or size)");
     return cudaErrorInvalidValue;
   }
-  const int smem = Layout<D>::kAlloc;
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_smem_attr<D>();
   if (e != cudaSuccess) return e;
-  dim3 grid(a.m_tiles, a.num_splits, a.batch * a.num_heads_kv), block(kThreads);
-  attn_tc_kernel<D><<<grid, block, smem, s>>>(a, kp, vp, kw, vw);
+  const int cs = a.num_splits;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs, a.m_tiles, a.batch * a.num_heads_kv);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Layout<D>::kAlloc;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<D>, a, kp, vp, kw, vw);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -504,6 +621,10 @@ cudaError_t launch_d(const AttnArgs &a, cudaStream_t s, char *why, size_t why_le
 
 cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t s, char *why, size_t why_len) {
   if (a.batch == 0 || a.total_q == 0) return cudaSuccess;
+  if (a.num_splits < 1 || a.num_splits > kMaxCluster) {
+    snprintf(why, why_len, "tensor-core path takes 1..%d splits", kMaxCluster);
+    return cudaErrorInvalidValue;
+  }
   if (a.head_dim == 128) return launch_d<128>(a, s, why, why_len);
   if (a.head_dim == 64) return launch_d<64>(a, s, why, why_len);
   snprintf(why, why_len, "tensor-core path supports head_dim 64 or 128");

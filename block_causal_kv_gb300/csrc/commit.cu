@@ -6,13 +6,16 @@
 // "D2F 논문 리뷰: 확산 LLM이 자기회귀 모델보다 빠른 추론을 처음으로 달성한 방식",
 // §쉽게 이해하기 (conservative threshold commit, aggressive top-1, remask).
 //
-// Grid (splits, total_q): CTA (s, r) reduces vocabulary slice s of row r to a
-// running (max, first argmax, sum of exp(l - max)) with 128-bit streaming loads.
-// The last CTA of a row (arrival counter) composes the slices; the last row of a
-// block (second counter) makes the block's commit decision with one warp. There
-// is no spin-wait anywhere: arrival counters hand the work to whoever arrives
-// last, and every counter is reset by its last arriver so the next call (or a
-// graph replay) starts from zero.
+// Grid (slices, rows): CTA (s, r) reduces vocabulary slice s of row r to
+// (max, first argmax, sum of exp(l - max)). On the staged path one thread issues
+// a single 1-D bulk copy (TMA) of the whole slice into shared memory, so every
+// byte of the slice is in flight at once, and the CTA then folds it from shared
+// memory; the direct path (unaligned rows) folds 128-bit or scalar global loads.
+// Every CTA of a window block then bumps one arrival counter; the last one to
+// arrive composes the slices of all rows of the block and decides the block with
+// one warp (lane = row). The decision's metadata (sequence, tau, phase) is
+// fetched while the slice streams. There is no spin-wait on another CTA: the
+// counter hands the work to whoever arrives last and is reset by it.
 #include "d2f_internal.cuh"
 
 namespace d2f {
@@ -83,42 +86,41 @@ __device__ __forceinline__ void fold(const float (&x)[N], int v0, float &m, int 
 }
 
 template <int DT>
+__device__ __forceinline__ void unpack(const uint4 raw, float (&x)[DT == D2F_BF16 ? 8 : 4]) {
+  if (DT == D2F_BF16) {
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[2 * j] = __uint_as_float(w[j] << 16);
+      x[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+    }
+  } else {
+    x[0] = __uint_as_float(raw.x);
+    x[1] = __uint_as_float(raw.y);
+    x[2] = __uint_as_float(raw.z);
+    x[3] = __uint_as_float(raw.w);
+  }
+}
+
+template <int DT>
 __device__ __forceinline__ float load_scalar(const void *base, int64_t i) {
-  if (DT == D2F_BF16)
-    return bf16_bits_to_float(((const uint16_t *)base)[i]);
+  if (DT == D2F_BF16) return bf16_bits_to_float(((const uint16_t *)base)[i]);
   return ((const float *)base)[i];
 }
 
-// One warp (lane u = row u of the block) decides block jb. Called by all 32
-// lanes of one warp after every row of the block has its result.
-__device__ void decide_block(const CommitArgs &a, int jb) {
+// One warp (lane u = row u of the block) decides block jb from the composed row
+// results in shared memory.
+__device__ void decide_block(const CommitArgs &a, int jb, const float *conf_s, const int *arg_s,
+                             float t, int phase) {
   const int lane = threadIdx.x & 31;
-  const int B = a.block_size;
-  const int r = jb * B + lane;
-  const bool in = lane < B;
+  const int r = jb * a.block_size + lane;
+  const bool in = lane < a.block_size;
   const bool m = in && a.masked[r] != 0;
-  float c = -1.0f;
-  int am = -1;
-  if (m) {
-    c = __ldcg(a.row_conf + r);
-    am = __ldcg(a.row_arg + r);
-  }
-  // sequence of the block (q_start values are multiples of B, blocks never straddle)
-  int b = 0;
-  if (lane == 0) {
-    int lo = 0, hi = a.batch - 1;
-    const int r0 = jb * B;
-    while (lo < hi) {  // largest b with q_start[b] <= r0
-      const int mid = (lo + hi + 1) >> 1;
-      if (a.q_start[mid] <= r0) lo = mid; else hi = mid - 1;
-    }
-    b = lo;
-  }
-  b = __shfl_sync(0xffffffffu, b, 0);
-  const float t = a.tau[b];
+  const float c = m ? conf_s[lane] : -1.0f;
+  const int am = m ? arg_s[lane] : -1;
   bool take = m && (c > t);
   const unsigned any_masked = __ballot_sync(0xffffffffu, m);
-  if (a.block_phase[jb] == D2F_PHASE_AGGRESSIVE && any_masked) {
+  if (phase == D2F_PHASE_AGGRESSIVE && any_masked) {
     float bv = m ? c : -INFINITY;
     int bl = m ? lane : 64;
 #pragma unroll
@@ -142,63 +144,95 @@ __device__ void decide_block(const CommitArgs &a, int jb) {
   }
   const unsigned left = __ballot_sync(0xffffffffu, m && !take);
   if (in) {
-    if (a.conf_out) a.conf_out[r] = m ? c : -1.0f;
-    if (a.argmax_out) a.argmax_out[r] = m ? am : -1;
+    if (a.conf_out) a.conf_out[r] = c;
+    if (a.argmax_out) a.argmax_out[r] = am;
   }
   if (lane == 0 && a.block_remaining) a.block_remaining[jb] = __popc(left);
 }
 
-// Called by warp 0 of the CTA that completed row r.
-__device__ void row_done(const CommitArgs &a, int r) {
-  const int lane = threadIdx.x & 31;
-  const int jb = r / a.block_size;
-  int old = 0;
-  if (lane == 0) {
-    __threadfence();
-    old = atomicAdd(a.blk_cnt + jb, 1);
-  }
-  old = __shfl_sync(0xffffffffu, old, 0);
-  if (old != a.block_size - 1) return;
-  __threadfence();
-  decide_block(a, jb);
-  if (lane == 0) a.blk_cnt[jb] = 0;
-}
-
-template <int DT, bool VEC>
+template <int DT, int PATH>  // PATH 0: scalar loads, 1: 128-bit loads, 2: bulk-staged
 __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
+  constexpr int N = (DT == D2F_BF16) ? 8 : 4;  // values per 16-byte vector
+  extern __shared__ __align__(128) uint8_t stage[];
+  __shared__ RowState red[kThreads / 32];
+  __shared__ float conf_s[32];
+  __shared__ int arg_s[32];
+  __shared__ uint64_t bar;
+  __shared__ int is_last;
+  __shared__ int abort_flag;
+
   const int s = blockIdx.x;
   const int r = blockIdx.y;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  __shared__ RowState red[kThreads / 32];
-  __shared__ int is_last;
+  const int B = a.block_size;
+  const int jb = r / B;
 
-  if (a.masked[r] == 0) {
-    if (s == 0 && warp == 0) row_done(a, r);
-    return;
-  }
-  int lr = a.logit_row ? a.logit_row[r] : r;
-  const bool row_ok = lr >= 0 && lr < a.num_logit_rows;
-  if (!row_ok) {
-    if (tid == 0 && s == 0) set_err(a.err, D2F_ERR_BAD_INDEX);
-    lr = 0;
-  }
+  if (tid == 0) D2F_TRACE_MARK(1, 0);
+  grid_dependency_wait();  // logits / state may come from the previous kernel
+  if (tid == 0) D2F_TRACE_MARK(1, 1);
 
-  // ---- streaming reduction of this CTA's vocabulary slice ------------------
-  constexpr int N = (DT == D2F_BF16) ? 8 : 4;  // values per 16-byte vector
-  const int v0 = s * a.chunk;
-  const int v1 = min(a.vocab, v0 + a.chunk);
-  float m = -INFINITY;
-  int idx = 0x7fffffff;
-  float acc[N];
+  // Decision metadata of this block, fetched now, used only by the last arriver.
+  float tau_b = 0.f;
+  int phase = 0;
+  if (tid == 0) {
+    int lo = 0, hi = a.batch - 1;
+    const int r0 = jb * B;
+    while (lo < hi) {  // largest b with q_start[b] <= r0 (blocks never straddle sequences)
+      const int mid = (lo + hi + 1) >> 1;
+      if (__ldg(a.q_start + mid) <= r0) lo = mid; else hi = mid - 1;
+    }
+    tau_b = __ldg(a.tau + lo);
+    phase = __ldg(a.block_phase + jb);
+  }
+  const bool is_masked = a.masked[r] != 0;
+  grid_launch_dependents();
+
+  if (is_masked) {
+    int lr = a.logit_row ? a.logit_row[r] : r;
+    const bool row_ok = lr >= 0 && lr < a.num_logit_rows;
+    if (!row_ok) {
+      if (tid == 0 && s == 0) set_err(a.err, D2F_ERR_BAD_INDEX);
+      lr = 0;
+    }
+    const int v0 = s * a.chunk;
+    const int v1 = min(a.vocab, v0 + a.chunk);
+    const char *row = (const char *)a.logits + (int64_t)lr * a.row_stride * (DT == D2F_BF16 ? 2 : 4);
+    float m = -INFINITY;
+    int idx = 0x7fffffff;
+    float acc[N];
 #pragma unroll
-  for (int j = 0; j < N; ++j) acc[j] = 0.f;
-  const char *row = (const char *)a.logits + (int64_t)lr * a.row_stride * (DT == D2F_BF16 ? 2 : 4);
+    for (int j = 0; j < N; ++j) acc[j] = 0.f;
+    int v_tail = v0;  // first index left for the scalar loop
 
-  if (row_ok && v0 < v1) {
-    int v = v0;
-    if (VEC) {
-      // v0 and chunk are multiples of N, the row start is 16-byte aligned.
+    if (PATH == 2) {
+      // Bulk-staged slice: whole 16-byte vectors [v0, v0 + nvec*N).
+      const int nvec = (v1 - v0) / N;
+      if (tid == 0) {
+        abort_flag = 0;
+        mbar_init(smem_u32(&bar), 1);
+        mbar_fence_init();
+      }
+      __syncthreads();
+      if (row_ok && nvec > 0) {
+        if (tid == 0) {
+          mbar_arrive_expect_tx(smem_u32(&bar), nvec * 16u);
+          bulk_load(smem_u32(stage), row + (int64_t)v0 * (DT == D2F_BF16 ? 2 : 4), nvec * 16u,
+                    smem_u32(&bar));
+        }
+        if (tid == 0) D2F_TRACE_MARK(1, 2);
+        mbar_wait(smem_u32(&bar), 0, &abort_flag, a.err);
+        if (tid == 0) D2F_TRACE_MARK(1, 3);
+        const uint4 *sv = reinterpret_cast<const uint4 *>(stage);
+        for (int k = tid; k < nvec; k += kThreads) {
+          float x[N];
+          unpack<DT>(sv[k], x);
+          fold<N>(x, v0 + k * N, m, idx, acc);
+        }
+        v_tail = v0 + nvec * N;
+      }
+    } else if (PATH == 1 && row_ok) {
+      // v0 and chunk are multiples of N and the row start is 16-byte aligned.
       const uint4 *vec = reinterpret_cast<const uint4 *>(row);
       const int nvec_end = v1 / N;  // vectors fully inside [v0, v1)
       int k = v0 / N + tid;
@@ -209,111 +243,116 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
           float x[N];
-          if (DT == D2F_BF16) {
-            const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              x[2 * j] = __uint_as_float(w[j] << 16);
-              x[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
-            }
-          } else {
-            x[0] = __uint_as_float(raw[u].x);
-            x[1] = __uint_as_float(raw[u].y);
-            x[2] = __uint_as_float(raw[u].z);
-            x[3] = __uint_as_float(raw[u].w);
-          }
+          unpack<DT>(raw[u], x);
           fold<N>(x, (k + u * kThreads) * N, m, idx, acc);
         }
       }
       for (; k < nvec_end; k += kThreads) {
-        const uint4 raw = __ldcs(vec + k);
         float x[N];
-        if (DT == D2F_BF16) {
-          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            x[2 * j] = __uint_as_float(w[j] << 16);
-            x[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
-          }
-        } else {
-          x[0] = __uint_as_float(raw.x);
-          x[1] = __uint_as_float(raw.y);
-          x[2] = __uint_as_float(raw.z);
-          x[3] = __uint_as_float(raw.w);
-        }
+        unpack<DT>(__ldcs(vec + k), x);
         fold<N>(x, k * N, m, idx, acc);
       }
-      v = max(v0, nvec_end * N);
+      v_tail = max(v0, nvec_end * N);
     }
-    // scalar part (whole slice when not vectorised, else the ragged tail)
-    for (int e = v + tid; e < v1; e += kThreads) {
-      const float x = load_scalar<DT>(row, e);
-      if (x > m) {  // new maximum: rescale every lane accumulator
-        const float alpha = fast_exp2((m - x) * kLog2e);
+    // scalar part: the whole slice on the scalar path, else the ragged tail
+    if (row_ok) {
+      for (int e = v_tail + tid; e < v1; e += kThreads) {
+        const float x = load_scalar<DT>(row, e);
+        if (x > m) {  // new maximum: rescale every lane accumulator
+          const float alpha = fast_exp2((m - x) * kLog2e);
 #pragma unroll
-        for (int j = 0; j < N; ++j) acc[j] *= alpha;
-        m = x;
-        idx = e;
+          for (int j = 0; j < N; ++j) acc[j] *= alpha;
+          m = x;
+          idx = e;
+        }
+        acc[0] += fast_exp2((x - m) * kLog2e);
       }
-      acc[0] += fast_exp2((x - m) * kLog2e);
     }
-  }
-  float tot = 0.f;
+    float tot = 0.f;
 #pragma unroll
-  for (int j = 0; j < N; ++j) tot += acc[j];
-  RowState st = {m, idx, tot};
-  st = warp_combine(st);
-  if (lane == 0) red[warp] = st;
-  __syncthreads();
-  if (warp != 0) return;
-  st = lane < kThreads / 32 ? red[lane] : RowState{-INFINITY, 0x7fffffff, 0.f};
-  st = warp_combine(st);
+    for (int j = 0; j < N; ++j) tot += acc[j];
+    if (tid == 0) D2F_TRACE_MARK(1, 4);
+    RowState st = {m, idx, tot};
+    st = warp_combine(st);
+    if (lane == 0) red[warp] = st;
+    __syncthreads();
+    if (warp == 0) {
+      st = lane < kThreads / 32 ? red[lane] : RowState{-INFINITY, 0x7fffffff, 0.f};
+      st = warp_combine(st);
+      if (lane == 0) {
+        if (!row_ok) st = RowState{-INFINITY, 0x7fffffff, 0.f};
+        a.partial[(int64_t)r * a.splits + s] = make_float4(st.m, __int_as_float(st.idx), st.s, 0.f);
+      }
+    }
+  }
 
-  // ---- compose the slices of the row --------------------------------------
-  if (a.splits > 1) {
-    if (lane == 0) {
-      a.partial[(int64_t)r * a.splits + s] =
-          make_float4(st.m, __int_as_float(st.idx), st.s, 0.f);
-      __threadfence();
-      is_last = atomicAdd(a.row_cnt + r, 1) == a.splits - 1;
-    }
-    __syncwarp();
-    if (!__shfl_sync(0xffffffffu, is_last, 0)) return;
+  // ---- arrival on the block's counter ----------------------------------------
+  if (tid == 0) D2F_TRACE_MARK(1, 5);
+  if (tid == 0) {
     __threadfence();
+    is_last = atomicAdd(a.blk_cnt + jb, 1) == B * a.splits - 1;
+  }
+  __syncthreads();
+  if (tid == 0) D2F_TRACE_MARK(1, 6);
+  if (!is_last) return;
+  __threadfence();
+  // Compose the slices of every masked row of the block: one warp per row.
+  for (int u = warp; u < B; u += kThreads / 32) {
+    const int rr = jb * B + u;
+    const bool mu = a.masked[rr] != 0;  // warp-uniform
     RowState acc2 = {-INFINITY, 0x7fffffff, 0.f};
-    for (int j = lane; j < a.splits; j += 32) {
-      const float4 p = __ldcg(a.partial + (int64_t)r * a.splits + j);
-      acc2 = combine(acc2, RowState{p.x, __float_as_int(p.y), p.z});
+    if (mu) {
+      for (int j = lane; j < a.splits; j += 32) {
+        const float4 p = __ldcg(a.partial + (int64_t)rr * a.splits + j);
+        acc2 = combine(acc2, RowState{p.x, __float_as_int(p.y), p.z});
+      }
     }
-    st = warp_combine(acc2);
-    if (lane == 0) a.row_cnt[r] = 0;
+    acc2 = warp_combine(acc2);
+    if (lane == 0) {
+      const bool ok = mu && acc2.s > 0.f;
+      conf_s[u] = ok ? 1.0f / acc2.s : -1.0f;
+      arg_s[u] = ok ? acc2.idx : -1;
+    }
   }
-  if (lane == 0) {
-    const bool ok = row_ok && st.s > 0.f;
-    a.row_conf[r] = ok ? 1.0f / st.s : -1.0f;
-    a.row_arg[r] = ok ? st.idx : -1;
+  __syncthreads();
+  if (warp == 0) {
+    tau_b = __shfl_sync(0xffffffffu, tau_b, 0);
+    phase = __shfl_sync(0xffffffffu, phase, 0);
+    decide_block(a, jb, conf_s, arg_s, tau_b, phase);
+    if (lane == 0) a.blk_cnt[jb] = 0;
+    if (lane == 0) D2F_TRACE_MARK(1, 7);
   }
-  __syncwarp();
-  row_done(a, r);
+}
+
+template <int DT, int PATH>
+cudaError_t launch_path(const CommitArgs &a, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.splits, a.total_q);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = PATH == 2 ? (size_t)a.chunk * (DT == D2F_BF16 ? 2 : 4) : 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, commit_kernel<DT, PATH>, a);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_commit(const CommitArgs &a, int dtype, bool vec_ok, cudaStream_t stream) {
+cudaError_t launch_commit(const CommitArgs &a, int dtype, int path, cudaStream_t stream) {
   if (a.total_q == 0) return cudaSuccess;
-  dim3 grid(a.splits, a.total_q), block(kThreads);
   if (dtype == D2F_BF16) {
-    if (vec_ok)
-      commit_kernel<D2F_BF16, true><<<grid, block, 0, stream>>>(a);
-    else
-      commit_kernel<D2F_BF16, false><<<grid, block, 0, stream>>>(a);
-  } else {
-    if (vec_ok)
-      commit_kernel<D2F_F32, true><<<grid, block, 0, stream>>>(a);
-    else
-      commit_kernel<D2F_F32, false><<<grid, block, 0, stream>>>(a);
+    if (path == 2) return launch_path<D2F_BF16, 2>(a, stream);
+    if (path == 1) return launch_path<D2F_BF16, 1>(a, stream);
+    return launch_path<D2F_BF16, 0>(a, stream);
   }
-  return cudaGetLastError();
+  if (path == 2) return launch_path<D2F_F32, 2>(a, stream);
+  if (path == 1) return launch_path<D2F_F32, 1>(a, stream);
+  return launch_path<D2F_F32, 0>(a, stream);
 }
 
 }  // namespace d2f

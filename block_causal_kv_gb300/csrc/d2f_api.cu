@@ -92,10 +92,24 @@ int plan_attn(int batch, int total_q, int max_q, int max_ctx, int Hq, int Hkv, i
   p->m_tiles = max(1, cdiv((long long)G * max_q, rows));
   const int t_max = max(1, cdiv(max_ctx, keys) + cdiv(max_q, keys));
   int splits = num_splits;
+  const long long base = (long long)max(batch, 1) * Hkv * p->m_tiles;
+  if (tc) {
+    // The splits of one row tile form a thread-block cluster (at most 8 CTAs)
+    // and compose their partials in distributed shared memory: no workspace.
+    if (splits == 0) {
+      const int sms = num_sms_current_device();
+      splits = 1;
+      while (splits * 2 <= kTcMaxSplits && splits * 2 <= t_max && base * splits * 2 <= sms)
+        splits *= 2;
+    }
+    p->splits = min(splits, kTcMaxSplits);
+    p->n_counters = 0;
+    p->off_ml = p->off_o = p->bytes = 0;
+    return D2F_OK;
+  }
   if (splits == 0) {
     const int sms = num_sms_current_device();
-    const long long base = (long long)max(batch, 1) * Hkv * p->m_tiles;
-    const long long target = sms > 0 ? (tc ? sms : 4LL * sms) : 1;
+    const long long target = sms > 0 ? 4LL * sms : 1;
     splits = (int)max(1LL, target / base);
     splits = min(splits, t_max);
   }
@@ -121,7 +135,8 @@ constexpr int kCommitMaxSplits = 64;
 
 struct CommitPlan {
   int splits, chunk;
-  size_t off_partial, off_conf, off_arg, off_rowcnt, off_blkcnt, bytes;
+  bool stageable;  // slice fits the bulk-staged path
+  size_t off_blkcnt, off_partial, bytes;
 };
 
 int plan_commit(int total_q, int vocab, int dtype, int B, int num_splits, CommitPlan *p) {
@@ -135,32 +150,35 @@ int plan_commit(int total_q, int vocab, int dtype, int B, int num_splits, Commit
   if (total_q > 65535) return fail(D2F_ERR_UNSUPPORTED, "total_q must be <= 65535");
   if (num_splits < 0 || num_splits > kCommitMaxSplits)
     return fail(D2F_ERR_INVALID_ARG, "num_splits must be in [0, %d]", kCommitMaxSplits);
-  const int vec = dtype == D2F_BF16 ? 8 : 4;
+  const int elt = dtype == D2F_BF16 ? 2 : 4;
+  const int vec = 16 / elt;
+  const int max_chunk = kCommitMaxStageBytes / elt;  // a slice the staged path can hold
   int splits = num_splits;
   int chunk;
   if (splits == 0) {
+    // about four CTAs per SM, and slices small enough to stage in shared memory
     const int sms = num_sms_current_device();
     const long long target = 4LL * (sms > 0 ? sms : 1);
     const long long rows = total_q > 0 ? total_q : 1;
     long long want = (target + rows - 1) / rows;
+    want = max(want, (long long)cdiv(vocab, max_chunk));
     if (want < 1) want = 1;
     if (want > kCommitMaxSplits) want = kCommitMaxSplits;
     splits = (int)want;
     chunk = cdiv(cdiv(vocab, splits), vec * kCommitThreads) * vec * kCommitThreads;
+    if (chunk > max_chunk) chunk = cdiv(cdiv(vocab, splits), vec) * vec;
   } else {
     chunk = cdiv(cdiv(vocab, splits), vec) * vec;
   }
   splits = cdiv(vocab, chunk);
   p->splits = splits;
   p->chunk = chunk;
+  p->stageable = chunk <= max_chunk;
   // Counters first: their place does not depend on the split count, so one
   // zeroed workspace stays valid across calls with different splits.
   const size_t nq = (size_t)total_q;
-  p->off_rowcnt = 0;
-  p->off_blkcnt = align_up(nq * sizeof(int32_t));
-  p->off_conf = p->off_blkcnt + align_up((nq / B + 1) * sizeof(int32_t));
-  p->off_arg = p->off_conf + align_up(nq * sizeof(float));
-  p->off_partial = p->off_arg + align_up(nq * sizeof(int32_t));
+  p->off_blkcnt = 0;
+  p->off_partial = align_up((nq / B + 1) * sizeof(int32_t));
   p->bytes = p->off_partial + align_up(nq * splits * sizeof(float4));
   return D2F_OK;
 }
@@ -169,6 +187,15 @@ int plan_commit(int total_q, int vocab, int dtype, int B, int num_splits, Commit
 }  // namespace d2f
 
 using namespace d2f;
+
+#ifdef D2F_TRACE
+// Development builds only: the phase-trace array and its address.
+__device__ unsigned long long d2f::g_d2f_trace[2][d2f::kTraceCtas * d2f::kTraceSlots];
+extern "C" void *d2f_trace_buffer(void) {
+  void *p = nullptr;
+  return cudaGetSymbolAddress(&p, d2f::g_d2f_trace) == cudaSuccess ? p : nullptr;
+}
+#endif
 
 extern "C" {
 
@@ -306,6 +333,7 @@ int d2f_commit(const void *logits, int64_t row_stride, int dtype, int vocab, int
                 workspace ? workspace_bytes : (size_t)0);
   const int elt = dtype == D2F_BF16 ? 2 : 4;
   const bool vec_ok = aligned16(logits) && ((row_stride * elt) % 16 == 0);
+  const int path = !vec_ok ? 0 : (p.stageable ? 2 : 1);
   CommitArgs a;
   a.logits = logits;
   a.row_stride = row_stride;
@@ -328,12 +356,9 @@ int d2f_commit(const void *logits, int64_t row_stride, int dtype, int vocab, int
   a.chunk = p.chunk;
   char *ws = static_cast<char *>(workspace);
   a.partial = reinterpret_cast<float4 *>(ws + p.off_partial);
-  a.row_conf = reinterpret_cast<float *>(ws + p.off_conf);
-  a.row_arg = reinterpret_cast<int32_t *>(ws + p.off_arg);
-  a.row_cnt = reinterpret_cast<int32_t *>(ws + p.off_rowcnt);
   a.blk_cnt = reinterpret_cast<int32_t *>(ws + p.off_blkcnt);
   a.err = err_word;
-  const cudaError_t e = launch_commit(a, dtype, vec_ok, reinterpret_cast<cudaStream_t>(stream));
+  const cudaError_t e = launch_commit(a, dtype, path, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "commit launch");
   return D2F_OK;
 }

@@ -59,10 +59,7 @@ struct CommitArgs {
   int splits;            // CTAs per row
   int chunk;             // vocabulary entries per CTA
   float4 *partial;       // [total_q][splits] (max, argmax bits, sum, unused)
-  float *row_conf;       // [total_q]
-  int32_t *row_arg;      // [total_q]
-  int32_t *row_cnt;      // [total_q] (zero at rest)
-  int32_t *blk_cnt;      // [total_q / block_size] (zero at rest)
+  int32_t *blk_cnt;      // [total_q / block_size] arrivals per block (zero at rest)
   int32_t *err;
 };
 
@@ -77,7 +74,9 @@ struct AppendArgs {
 };
 
 // Launchers (one per translation unit). Return cudaSuccess or the launch error.
-cudaError_t launch_commit(const CommitArgs &a, int dtype, bool vec_ok, cudaStream_t s);
+// path: 0 scalar loads, 1 128-bit loads, 2 bulk-staged slices (see commit.cu)
+cudaError_t launch_commit(const CommitArgs &a, int dtype, int path, cudaStream_t s);
+constexpr int kCommitMaxStageBytes = 32768;  // bulk-staged slice, bytes
 cudaError_t launch_append(const AppendArgs &a, bool vec_ok, cudaStream_t s);
 cudaError_t launch_attn_simt(const AttnArgs &a, int dtype, cudaStream_t s);
 cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t s, char *why, size_t why_len);
@@ -87,6 +86,7 @@ constexpr int kSimtRows = 16;   // query rows per CTA, CUDA-core path
 constexpr int kSimtKeys = 32;   // keys per tile, CUDA-core path
 constexpr int kTcRows = 128;    // query rows per CTA (UMMA M), tensor-core path
 constexpr int kTcKeys = 64;     // keys per tile (UMMA N of Q.K^T), tensor-core path
+constexpr int kTcMaxSplits = 8; // CTAs per cluster sharing one row tile, tensor-core path
 
 // ---------------------------------------------------------------------------
 // Device helpers
@@ -202,6 +202,78 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
 // Generic-proxy shared-memory writes -> visible to the async proxy (UMMA reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// ----- thread-block clusters / distributed shared memory --------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Full cluster barrier (every thread of every CTA of the cluster).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// Address of the same shared variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float2 dsmem_ld_f2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 dsmem_ld_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// ----- phase tracing (compiled in only with -DD2F_TRACE; absent otherwise) ----
+// Records %globaltimer (ns) per CTA and phase into a fixed device array so a
+// development build can show where a kernel's time goes.
+#ifdef D2F_TRACE
+constexpr int kTraceSlots = 16;
+constexpr int kTraceCtas = 8192;
+extern __device__ unsigned long long g_d2f_trace[2][kTraceCtas * kTraceSlots];
+__device__ __forceinline__ void trace_mark(int kernel, int slot) {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  const unsigned cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+  if (cta < kTraceCtas) g_d2f_trace[kernel][cta * kTraceSlots + slot] = t;
+}
+#define D2F_TRACE_MARK(kernel, slot) trace_mark(kernel, slot)
+#else
+#define D2F_TRACE_MARK(kernel, slot) ((void)0)
+#endif
+
+// ----- programmatic dependent launch ----------------------------------------
+// Block until every grid this one depends on has completed and its writes are
+// visible (no-op when the launch has no programmatic dependency).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Allow the next grid in the stream to be scheduled; it still waits for this
+// grid's completion before reading anything (grid_dependency_wait).
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ----- tcgen05 / TMEM ---------------------------------------------------------

@@ -117,12 +117,17 @@ int d2f_block_attn_workspace_size(int batch, int total_q, int max_q_per_seq, int
  *   max_q_per_seq  host upper bound on n_b (rows past it are reported through
  *               err_word as D2F_ERR_INVALID_ARG and left unwritten)
  *   max_ctx     host hint used only to pick the split count
- *   dtype       D2F_BF16 (tensor-core path, head_dim 64 or 128) or D2F_F32
- *               (CUDA-core path, head_dim <= 256 and a multiple of 32)
+ *   dtype       D2F_BF16 with head_dim 64 or 128 and block_size 8, 16 or 32 takes
+ *               the tensor-core path; everything else (D2F_F32, other bf16 shapes)
+ *               takes the CUDA-core path, head_dim 32, 64 or 128, block_size 1..256
  *   softmax_scale  > 0, typically 1/sqrt(head_dim)
- *   num_splits  0 = automatic, else the number of CTAs sharing one sequence's keys
- *   block_size  8, 16 or 32 on the tensor-core path; 1..256 on the CUDA-core path
+ *   num_splits  0 = automatic, else the number of CTAs sharing one row tile's keys.
+ *               Tensor-core path: 1..8, the CTAs of one thread-block cluster, whose
+ *               partials are composed in distributed shared memory (larger requests
+ *               are clamped to 8). CUDA-core path: any count; partials go through
+ *               the workspace.
  *   workspace   device, >= d2f_block_attn_workspace_size(...) bytes, zeroed once
+ *               (0 bytes on the tensor-core path: NULL is accepted there)
  *
  * Alignment: every device buffer 16-byte aligned.
  */

@@ -51,11 +51,15 @@ def _attn_ws(**over):
     return d2f.attn_workspace_size(**kw)
 
 
-def test_attention_workspace_size(lib):
+def test_attention_workspace_size(lib, monkeypatch):
+    # tensor-core path: splits compose in distributed shared memory, no workspace
+    assert _attn_ws() == 0
+    # CUDA-core path: counters + 4 splits x (max, sum) + 4 splits x fp32 partial rows
+    monkeypatch.setenv("D2F_ATTN_PATH", "simt")
     n4 = _attn_ws()
-    # counters + 4 splits x (max,sum) + 4 splits x fp32 partial rows
     assert n4 >= 4 * 48 * 32 * (128 * 4 + 8)
     assert _attn_ws(num_splits=1) < 4096
+    assert _attn_ws(dtype=d2f.F32) == n4
 
 
 @pytest.mark.parametrize("over,status", [

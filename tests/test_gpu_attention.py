@@ -89,16 +89,24 @@ def test_many_splits_more_than_tiles():
     check_attention(out, lse, ref, ref_lse, torch.bfloat16, "splits64")
 
 
-def test_lse_optional_and_repeatable():
+@pytest.mark.parametrize("path", ["tc", "simt"])
+def test_lse_optional_and_repeatable(path, monkeypatch):
     """lse_out may be NULL; back-to-back calls with one workspace give identical
-    results (merge counters reset themselves)."""
+    results. The tensor-core path composes its splits in distributed shared
+    memory and needs no workspace; the CUDA-core path's merge counters reset
+    themselves."""
     dev = device()
+    if path == "simt":
+        monkeypatch.setenv("D2F_ATTN_PATH", "simt")
     p = synth.make_problem(synth.small("ragged"))
     g = p.to(dev)
-    ws = d2f.attn_workspace(dev, batch=p.w.batch, total_q=p.w.total_q,
-                            max_q_per_seq=p.max_q_per_seq, max_ctx=p.max_ctx,
-                            num_heads_q=p.w.num_heads_q, num_heads_kv=p.w.num_heads_kv,
-                            head_dim=p.w.head_dim, block_size=p.w.block_size, num_splits=4)
+    kw = dict(batch=p.w.batch, total_q=p.w.total_q, max_q_per_seq=p.max_q_per_seq,
+              max_ctx=p.max_ctx, num_heads_q=p.w.num_heads_q, num_heads_kv=p.w.num_heads_kv,
+              head_dim=p.w.head_dim, block_size=p.w.block_size, num_splits=4)
+    nbytes = d2f.attn_workspace_size(**kw)
+    if path == "tc":
+        assert nbytes == 0
+    ws = d2f.attn_workspace(dev, **kw)
     outs = []
     for _ in range(3):
         out, lse = d2f.block_attn(g.q, g.k_win, g.v_win, g.k_pool, g.v_pool, g.page_table,
@@ -109,12 +117,13 @@ def test_lse_optional_and_repeatable():
     torch.cuda.synchronize()
     assert lse is None
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
-    # merge counters (one per sequence x KV head x 16-row group, at offset 0) back at zero
-    n_counters = p.w.batch * p.w.num_heads_kv * -(-p.max_q_per_seq * p.w.num_heads_q
-                                                   // p.w.num_heads_kv // 16)
-    assert int(ws[:4 * n_counters].view(torch.int32).abs().sum()) == 0
+    if path == "simt":
+        # merge counters (one per sequence x KV head x 16-row group, at offset 0) back at zero
+        n_counters = p.w.batch * p.w.num_heads_kv * -(-p.max_q_per_seq * p.w.num_heads_q
+                                                       // p.w.num_heads_kv // 16)
+        assert int(ws[:4 * n_counters].view(torch.int32).abs().sum()) == 0
     ref, _ = _ref(p)
-    check_attention(outs[0], None, ref, None, torch.bfloat16, "repeat")
+    check_attention(outs[0], None, ref, None, torch.bfloat16, "repeat/" + path)
 
 
 def test_full_size_llada_layer():
