@@ -17,21 +17,26 @@
 //   warp 0       TMA producer: page ids (32 at a time, prefetched) ->
 //                cp.async.bulk.tensor loads of the K and V tiles, 128-byte
 //                swizzle, completion counted on the stage's mbarrier.
-//   warp 1       MMA issuer (one lane): S = Q K^T into TMEM (double-buffered),
-//                then O += P V into TMEM once the softmax has written P.
-//   warps 2-5    one thread per query row (= TMEM lane): load the Q row, then per
-//                tile read S from TMEM, apply the block-causal mask as a per-row
-//                key limit, online softmax in log2 units with lazy rescaling of
-//                O (only when the running max grows by more than 2^8), write bf16
-//                P to shared memory for the second MMA.
+//   warp 1       TMEM owner and MMA issuer (one lane): S = Q K^T into TMEM
+//                (double-buffered), then O += P V into TMEM once P is written.
+//   warps 2-9    softmax, two threads per query row (TMEM lane = row): both
+//                read the row's 64 scores and take the tile maximum, each
+//                exponentiates 32 of them and owns half of O. The block-causal
+//                mask is a per-row key limit; the online softmax runs in log2
+//                units with lazy rescaling of O (only when the running max grows
+//                by more than 2^8); bf16 P goes to TMEM, where the second MMA
+//                reads its A operand.
 //
-// Composition. With cs > 1 every CTA stages its unnormalised O and (max, sum)
-// in its own shared memory; after a cluster barrier CTA k composes the rows
-// r = k mod cs by reading all cs partials through distributed shared memory and
-// writes the normalised output. No partial ever goes to global memory.
+// Composition. With cs > 1 the CTAs of the cluster push their unnormalised O
+// rows and (max, sum) into the shared memory of the CTA that owns each row
+// (row r -> CTA r mod cs) with remote stores; after a cluster barrier every
+// owner composes its rows from local shared memory and writes the normalised
+// output. No partial goes to global memory.
 //
-// Every mbarrier wait is bounded; on time-out the CTA records D2F_ERR_TIMEOUT,
-// drains its own copies and MMAs, frees TMEM and returns.
+// Set-up that reads no global memory (mbarriers, TMEM) runs before the
+// grid-dependency wait, so under programmatic dependent launch it overlaps the
+// previous kernel. Every mbarrier wait is bounded; on time-out the CTA records
+// D2F_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and returns.
 #include <string.h>
 
 #include <cstdio>
@@ -42,14 +47,18 @@
 namespace d2f {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int NS = 4;                // K/V ring stages
-constexpr int M = kTcRows;           // 128 query rows per tile
-constexpr int N = kTcKeys;           // 64 keys per tile
-constexpr uint32_t kTmemCols = 256;  // S double buffer (2 x 64) + O (<= 128)
-constexpr uint32_t kTmemO = 128;     // first TMEM column of O
-constexpr int kEpiThreads = 128;
+constexpr int kSoftWarps = 8;
+constexpr int kSoftThreads = 32 * kSoftWarps;  // two per query row
+constexpr int kThreads = 64 + kSoftThreads;    // producer + MMA warps + softmax
+constexpr int NS = 4;                          // K/V ring stages
+constexpr int M = kTcRows;                     // 128 query rows per tile
+constexpr int N = kTcKeys;                     // 64 keys per tile
+constexpr int kHalfN = N / 2;                  // keys per softmax thread per tile
+constexpr uint32_t kTmemCols = 512;            // S (2 x 64) + O (<= 128) + P (2 x 32)
+constexpr uint32_t kTmemO = 128;               // first TMEM column of O
+constexpr uint32_t kTmemP = 256;               // bf16 P, two keys per column, 2 buffers
 constexpr int kMaxCluster = 8;
+constexpr int kBarSetup = 1;                   // named barrier: MMA warp + softmax warps
 
 template <int D>
 struct Layout {
@@ -59,29 +68,23 @@ struct Layout {
   static constexpr int kKVHalf = N * 128;        // 64 key rows x 128 bytes
   static constexpr int kKBytes = kHalves * kKVHalf;
   static constexpr int kStage = 2 * kKBytes;     // K tile then V tile
-  static constexpr int kPBytes = M * N * 2;      // bf16 P, 128 rows x 128 bytes
   static constexpr int kChunks = D / 4;          // 16-byte chunks of one fp32 O row
   static constexpr int kQ = 0;
-  static constexpr int kRing = kQ + kQBytes;     // also the fp32 O staging area
-  static constexpr int kP = kRing + NS * kStage;
-  static constexpr int kML = kP + 2 * kPBytes;   // float2 (max, sum) per row
-  static constexpr int kBars = kML + M * 8;
-  static constexpr int kBytes = kBars + 256;
+  static constexpr int kRing = kQ + kQBytes;     // also receives pushed O rows
+  static constexpr int kML = kRing + NS * kStage;  // pushed (max, sum): float2 [8][128]
+  static constexpr int kX = kML + kMaxCluster * M * 8;  // pair sums: float [2][128]
+  static constexpr int kBars = kX + 2 * M * 4;
+  static constexpr int kBytes = kBars + 512;
   static constexpr int kAlloc = kBytes + 1024;   // slack for 1024-byte alignment
-  static_assert(NS * kStage >= M * D * 4, "O staging must fit in the ring");
+  static_assert(NS * kStage >= (M + kMaxCluster) * D * 4, "pushed O rows must fit in the ring");
 };
 
 struct Bars {
   uint64_t full[NS], empty[NS], s_full[2], p_full[2], pv_done[2], q_full, drain;
+  uint64_t pair[4][2];  // per TMEM quadrant: the two threads of a row exchange their sums
   uint32_t tmem_base;
   int abort_flag;
 };
-
-template <int D>
-__device__ __forceinline__ uint32_t o_stage_addr(uint32_t sb, int row, int chunk) {
-  using L = Layout<D>;
-  return sb + L::kRing + row * (D * 4) + ((chunk ^ (row % L::kChunks)) << 4);
-}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -96,7 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sb = smem_u32(smem);
   Bars *bars = reinterpret_cast<Bars *>(smem + L::kBars);
   volatile int *abort_flag = &bars->abort_flag;
-  float2 *ml_s = reinterpret_cast<float2 *>(smem + L::kML);
+  float *xsum = reinterpret_cast<float *>(smem + L::kX);  // [2 half][128]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cs = gridDim.x;  // CTAs of the cluster = splits of this row tile
@@ -105,27 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = blockIdx.z / a.num_heads_kv, g = blockIdx.z % a.num_heads_kv;
 
   if (tid == 0) D2F_TRACE_MARK(0, 0);
-  grid_dependency_wait();  // inputs may come from the previous kernel in the stream
-  if (tid == 0) D2F_TRACE_MARK(0, 1);
-
-  // ---- work of this CTA (uniform across the cluster except has_work) ---------
-  int q0, n, C;
-  if (!load_seq_meta(a, b, q0, n, C)) {
-    if (tid == 0 && mt == 0 && split == 0 && g == 0) set_err(a.err, D2F_ERR_INVALID_ARG);
-    return;
-  }
-  const int G = a.group, B = a.block_size, H = a.num_heads_q;
-  const int rows_total = G * n;
-  const int r_begin = mt * M;
-  if (r_begin >= rows_total) return;
-  const int nrows = min(M, rows_total - r_begin);
-  const int Tc = (C + N - 1) / N, Tw = (n + N - 1) / N;
-  int t0 = 0, t1 = 0, s_eff = 1;
-  const bool has_work = split_range(Tc + Tw, cs, split, t0, t1, s_eff);
-  const int T = has_work ? t1 - t0 : 0;
-  grid_launch_dependents();
-
-  // ---- set-up: barriers, TMEM --------------------------------------------------
+  // ---- set-up that reads no global memory --------------------------------------
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(&bars->full[i]), 1);
@@ -133,41 +116,77 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars->s_full[i]), 1);
-      mbar_init(smem_u32(&bars->p_full[i]), kEpiThreads);
+      mbar_init(smem_u32(&bars->p_full[i]), kSoftThreads);
       mbar_init(smem_u32(&bars->pv_done[i]), 1);
     }
-    mbar_init(smem_u32(&bars->q_full), kEpiThreads);
+    for (int q = 0; q < 4; ++q)
+      for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&bars->pair[q][i]), 64);
+    mbar_init(smem_u32(&bars->q_full), kSoftThreads);
     mbar_init(smem_u32(&bars->drain), 1);
     bars->abort_flag = 0;
     mbar_fence_init();
-  }
-  if (has_work && warp == 1) {
-    tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
-    tmem_relinquish();
-  }
-  if (has_work && warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_kpool);
     tma_prefetch_desc(&tm_vpool);
     tma_prefetch_desc(&tm_kwin);
     tma_prefetch_desc(&tm_vwin);
   }
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = bars->tmem_base;
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+
+  grid_dependency_wait();  // inputs may come from the previous kernel in the stream
+  if (tid == 0) D2F_TRACE_MARK(0, 1);
+
+  // Page ids of this split's first tiles, requested before the sequence metadata
+  // arrives: the split's tile range comes from the host (tiles_per_split), so the
+  // first logical page is known up front.
+  const int ppt = N / a.block_size;  // pages (or window blocks) per tile
+  int pre_chunk = split * a.tiles_per_split * ppt;
+  int pre_ids = -1;
+  if (warp == 0 && pre_chunk + lane < a.max_pages_per_seq)
+    pre_ids = __ldg(a.page_table + (int64_t)b * a.max_pages_per_seq + pre_chunk + lane);
+
+  // ---- work of this CTA (uniform across the cluster except has_work) ---------
+  int q0 = 0, n = 0, C = 0;
+  bool active = load_seq_meta(a, b, q0, n, C);
+  if (!active && tid == 0 && mt == 0 && split == 0 && g == 0) set_err(a.err, D2F_ERR_INVALID_ARG);
+  const int G = a.group, B = a.block_size, H = a.num_heads_q;
+  const int rows_total = G * n;
+  const int r_begin = mt * M;
+  active = active && r_begin < rows_total;
+  const int nrows = active ? min(M, rows_total - r_begin) : 0;
+  const int Tc = (C + N - 1) / N, Tw = (n + N - 1) / N;
+  // Split s takes tiles [s*tps, (s+1)*tps); tps comes from the host's max_ctx and
+  // grows here only if a sequence is longer than that hint promised.
+  const int tps = max(a.tiles_per_split, (Tc + Tw + cs - 1) / cs);
+  const int t0 = split * tps, t1 = min(Tc + Tw, t0 + tps);
+  const bool has_work = active && t0 < t1;
+  const int T = has_work ? t1 - t0 : 0;
+  grid_launch_dependents();
+
+  uint32_t tmem = 0;
+  if (active && warp >= 1) {  // TMEM address, published by warp 1
+    tc_fence_before();
+    named_sync(kBarSetup, 32 + kSoftThreads);
+    tc_fence_after();
+    tmem = bars->tmem_base;
+  }
   if (tid == 0) D2F_TRACE_MARK(0, 2);
 
-  // softmax-thread identity (warps 2-5)
-  const int quad = warp & 3;         // TMEM lanes 32*quad .. 32*quad+31
-  const int row = quad * 32 + lane;  // row of the tile = TMEM lane
+  // softmax-thread identity (warps 2-9): row = TMEM lane, half = key / O half
+  const int sw = warp - 2;
+  const int quad = warp & 3;
+  const int half = (sw >> 2) & 1;
+  const int row = quad * 32 + lane;
   const bool row_valid = row < nrows;
   const int r = r_begin + row;
   const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
-  float m_ref = -INFINITY, l = 0.f;
+  float m_ref = -INFINITY, l = 0.f, l_tot = 0.f;
 
   if (has_work && warp == 0) {
     // ======================= TMA producer (whole warp) =========================
-    const int ppt = N / B;                        // pages (or window blocks) per tile
     const int n_pages = (C + B - 1) / B;          // cached pages of the sequence
     const int p_first = t0 * ppt;                 // first logical page of this CTA
     const int32_t *pt = a.page_table + (int64_t)b * a.max_pages_per_seq;
@@ -175,8 +194,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int lp = base + lane;
       return (lp < n_pages && lp < p_first + T * ppt) ? __ldg(pt + lp) : -1;
     };
-    int chunk = p_first;                          // logical page held by lane 0 of ids_cur
-    int ids_cur = fetch(chunk);
+    int chunk = pre_chunk;                        // logical page held by lane 0 of ids_cur
+    int ids_cur = pre_ids;
+    if (chunk != p_first) {                       // the host's range hint did not hold
+      chunk = p_first;
+      ids_cur = fetch(chunk);
+    }
     int ids_next = fetch(chunk + 32);
     int issued = 0;
     for (int u = 0; u < T; ++u) {
@@ -199,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ids_cur = ids_next;
           ids_next = fetch(chunk + 32);
         }
+        // (pages outside the sequence are masked out by the C check below)
         const int pg = __shfl_sync(0xffffffffu, ids_cur, (lp0 - chunk + lane) & 31);
         if (lane < ppt && (lp0 + lane) * B < C) {
           if (pg >= 0 && pg < a.num_pages)
@@ -249,13 +273,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           return false;
         tc_fence_after();
         const int stage = v % NS;
-        const uint32_t p_base = sb + L::kP + (v & 1) * L::kPBytes;
         const uint32_t v_base = sb + L::kRing + stage * L::kStage + L::kKBytes;
 #pragma unroll
-        for (int ks = 0; ks < N / 16; ++ks) {
-          const uint64_t ad = smem_desc_sw128(p_base + ks * 32, 16, 1024);
+        for (int ks = 0; ks < N / 16; ++ks) {  // 16 keys = 8 TMEM columns of P per step
           const uint64_t bd = smem_desc_sw128(v_base + ks * 2048, L::kKVHalf, 1024);
-          umma_bf16(tmem + kTmemO, ad, bd, idesc_pv, (v > 0 || ks > 0) ? 1u : 0u);
+          umma_bf16_tmem_a(tmem + kTmemO, tmem + kTmemP + (v & 1) * (N / 2) + ks * 8, bd,
+                           idesc_pv, (v > 0 || ks > 0) ? 1u : 0u);
         }
         umma_commit(smem_u32(&bars->pv_done[v & 1]));
         umma_commit(smem_u32(&bars->empty[stage]));
@@ -289,29 +312,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(smem_u32(&bars->drain), 0, &no_abort, a.err);
     }
   } else if (has_work) {
-    // ======================= softmax (128 threads, one per row) ================
+    // ======================= softmax (256 threads, two per row) ================
     {
-      // Q row into the 128-byte-swizzled K-major layout the MMA reads: 16-byte
-      // chunk c of column block h lands at
+      // This thread's half of the Q row, into the 128-byte-swizzled K-major
+      // layout the MMA reads: 16-byte chunk c of column block h lands at
       //   h*kQHalf + (row/8)*1024 + (row%8)*128 + ((c ^ (row%8)) * 16).
-      constexpr int kQc = D / 8;
+      constexpr int kQc = D / 16;
       uint4 qv[kQc];
       const uint4 *src = reinterpret_cast<const uint4 *>(
-          reinterpret_cast<const uint16_t *>(a.q) +
-          ((int64_t)(q0 + r / G) * H + g * G + r % G) * D);
+                             reinterpret_cast<const uint16_t *>(a.q) +
+                             ((int64_t)(q0 + r / G) * H + g * G + r % G) * D) +
+                         half * kQc;
 #pragma unroll
       for (int c = 0; c < kQc; ++c) qv[c] = row_valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
 #pragma unroll
       for (int c = 0; c < kQc; ++c) {
-        const uint32_t dst = sb + L::kQ + (c >> 3) * L::kQHalf + (row >> 3) * 1024 +
-                             (row & 7) * 128 + (((c & 7) ^ (row & 7)) << 4);
+        const int cc = half * kQc + c;
+        const uint32_t dst = sb + L::kQ + (cc >> 3) * L::kQHalf + (row >> 3) * 1024 +
+                             (row & 7) * 128 + (((cc & 7) ^ (row & 7)) << 4);
         asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(qv[c].x),
                      "r"(qv[c].y), "r"(qv[c].z), "r"(qv[c].w)
                      : "memory");
       }
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&bars->q_full));
-      if (tid == 64) D2F_TRACE_MARK(0, 3);
     }
     const int win_end = row_valid ? ((r / G) / B + 1) * B : 0;
     const float sl2 = a.scale_log2;
@@ -322,21 +346,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       if (tid == 64 && u == 0) D2F_TRACE_MARK(0, 4);
+      if (tid == 128 && u == 2) D2F_TRACE_MARK(0, 11);
       if (tid == 64 && u == T - 1) D2F_TRACE_MARK(0, 5);
-      uint32_t s_lo[32], s_hi[32];
-      tmem_ld32(lane_addr + (u & 1) * N, s_lo);
-      tmem_ld32(lane_addr + (u & 1) * N + 32, s_hi);
+      // Both threads of the pair read all 64 scores of the row and take the tile
+      // maximum themselves (no exchange); each then exponentiates its own 32.
+      uint32_t sv_lo[32], sv_hi[32];
+      tmem_ld32(lane_addr + (u & 1) * N, sv_lo);
+      tmem_ld32(lane_addr + (u & 1) * N + 32, sv_hi);
+      if (tid == 128 && u == 2) D2F_TRACE_MARK(0, 12);
 
       // keys c < lim of this tile are visible to this row
       const int tile_lim = t < Tc ? C - t * N : n - (t - Tc) * N;  // valid keys of the tile
       int lim = t < Tc ? tile_lim : win_end - (t - Tc) * N;
       lim = row_valid ? max(0, min(lim, N)) : 0;
-      float tmax = -INFINITY;
+      float sf[N];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        if (c < lim) tmax = fmaxf(tmax, __uint_as_float(s_lo[c]) * sl2);
-        if (c + 32 < lim) tmax = fmaxf(tmax, __uint_as_float(s_hi[c]) * sl2);
+        sf[c] = __uint_as_float(sv_lo[c]);
+        sf[32 + c] = __uint_as_float(sv_hi[c]);
       }
+      if (!__all_sync(0xffffffffu, lim >= N)) {  // ragged tile: hide masked keys
+#pragma unroll
+        for (int c = 0; c < N; ++c)
+          if (c >= lim) sf[c] = -INFINITY;
+      }
+      float tr[N / 2];  // tree maximum (scale > 0, so max(s) * scale = max(s * scale))
+#pragma unroll
+      for (int c = 0; c < N / 2; ++c) tr[c] = fmaxf(sf[2 * c], sf[2 * c + 1]);
+#pragma unroll
+      for (int w = N / 4; w >= 1; w >>= 1)
+#pragma unroll
+        for (int c = 0; c < w; ++c) tr[c] = fmaxf(tr[2 * c], tr[2 * c + 1]);
+      const float tmax = tr[0] * sl2;
+      if (tid == 128 && u == 2) D2F_TRACE_MARK(0, 13);
       // Lazy rescale: keep the reference max unless the tile max exceeds it by 2^8.
       const bool need = tmax > m_ref + 8.0f;
       if (__any_sync(0xffffffffu, need)) {
@@ -349,93 +391,97 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
-          for (int ch = 0; ch < D / 32; ++ch) {
+          for (int ch = 0; ch < D / 64; ++ch) {  // this thread's half of O
             uint32_t o[32];
-            tmem_ld32(lane_addr + kTmemO + ch * 32, o);
+            const uint32_t oa = lane_addr + kTmemO + half * (D / 2) + ch * 32;
+            tmem_ld32(oa, o);
 #pragma unroll
             for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-            tmem_st32(lane_addr + kTmemO + ch * 32, o);
+            tmem_st32(oa, o);
           }
           tmem_wait_st();
         }
         m_ref = m_new;
       }
-      // P = 2^(s - m_ref) for visible keys, 0 otherwise, rounded to bf16.
-      uint32_t pk[32];
-      float psum = 0.f;
+      // P = 2^(s*scale - m_ref) for this thread's 32 keys, rounded to bf16; masked
+      // keys are -inf -> 0. A row with no visible key so far keeps m_ref = -inf:
+      // subtract 0 instead.
+      const float mb = m_ref == -INFINITY ? 0.f : m_ref;
+      uint32_t pk[kHalfN / 2];
+      float ps[kHalfN / 2];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int c0 = 2 * j, c1 = 2 * j + 1;
-        const float p0 = c0 < lim ? fast_exp2(fmaf(__uint_as_float(s_lo[c0]), sl2, -m_ref)) : 0.f;
-        const float p1 = c1 < lim ? fast_exp2(fmaf(__uint_as_float(s_lo[c1]), sl2, -m_ref)) : 0.f;
+      for (int j = 0; j < kHalfN / 2; ++j) {
+        // select this thread's half with compile-time indices (keeps sf in registers)
+        const float s0 = half ? sf[kHalfN + 2 * j] : sf[2 * j];
+        const float s1 = half ? sf[kHalfN + 2 * j + 1] : sf[2 * j + 1];
+        const float p0 = fast_exp2(fmaf(s0, sl2, -mb));
+        const float p1 = fast_exp2(fmaf(s1, sl2, -mb));
         pk[j] = pack_bf16x2(p0, p1);
-        const float p2 =
-            c0 + 32 < lim ? fast_exp2(fmaf(__uint_as_float(s_hi[c0]), sl2, -m_ref)) : 0.f;
-        const float p3 =
-            c1 + 32 < lim ? fast_exp2(fmaf(__uint_as_float(s_hi[c1]), sl2, -m_ref)) : 0.f;
-        pk[16 + j] = pack_bf16x2(p2, p3);
+        ps[j] = __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xffff0000u);
       }
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        psum += __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xffff0000u);
-      l += psum;
+      for (int w = kHalfN / 4; w >= 1; w >>= 1)
+#pragma unroll
+        for (int c = 0; c < w; ++c) ps[c] = ps[2 * c] + ps[2 * c + 1];
+      l += ps[0];
+      if (tid == 128 && u == 2) D2F_TRACE_MARK(0, 14);
 
       // The P buffer is free once the MMA that read it two tiles ago completed.
       if (u >= 2) {
         ok = mbar_wait(smem_u32(&bars->pv_done[u & 1]), ((u - 2) >> 1) & 1, abort_flag, a.err);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
       }
-      const uint32_t p_row =
-          sb + L::kP + (u & 1) * L::kPBytes + (row >> 3) * 1024 + (row & 7) * 128;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(p_row +
-                                                                       ((c ^ (row & 7)) << 4)),
-                     "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
-                     : "memory");
-      }
+      // P into TMEM for the P.V product (A operand from TMEM): column c of the
+      // buffer holds keys 2c and 2c+1; this thread writes columns 16*half ...
+      tmem_st16(lane_addr + kTmemP + (u & 1) * (N / 2) + half * (kHalfN / 2), pk);
+      tmem_wait_st();
       // A ragged tile (partial last page or short window) may hold stale or
       // non-finite V rows past its valid keys; P is 0 there, but 0 * NaN is not
-      // 0, so clear those rows before the P.V product reads them.
-      if (row < N && row >= tile_lim) {
+      // 0, so clear those rows before the P.V product reads them (each thread of
+      // the pair clears one 64-column block when D = 128).
+      if (row < N && row >= tile_lim && half < L::kHalves) {
         const uint32_t v_row = sb + L::kRing + (u % NS) * L::kStage + L::kKBytes +
-                               (row >> 3) * 1024 + (row & 7) * 128;
+                               half * L::kKVHalf + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
-        for (int h = 0; h < L::kHalves; ++h)
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(v_row + h * L::kKVHalf +
-                                                                           (c << 4)),
-                         "r"(0u)
-                         : "memory");
+        for (int c = 0; c < 8; ++c)
+          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(v_row + (c << 4)), "r"(0u)
+                       : "memory");
+        fence_proxy_async_smem();
       }
-      fence_proxy_async_smem();
+      if (tid == 128 && u == 2) D2F_TRACE_MARK(0, 15);
       tc_fence_before();
       mbar_arrive(smem_u32(&bars->p_full[u & 1]));
+      if (tid == 128 && u == 3) D2F_TRACE_MARK(0, 3);
     }
-    // wait for the last P.V product
     if (tid == 64) D2F_TRACE_MARK(0, 6);
-    if (ok) {
+    if (ok) {  // the last P.V product
       ok = mbar_wait(smem_u32(&bars->pv_done[(T - 1) & 1]), ((T - 1) >> 1) & 1, abort_flag, a.err);
       ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {  // row sum = sum of the pair's halves
+      xsum[half * M + row] = l;
+      mbar_arrive(smem_u32(&bars->pair[quad][0]));
+      ok = mbar_wait(smem_u32(&bars->pair[quad][0]), 0, abort_flag, a.err);
+      l_tot = l + xsum[(half ^ 1) * M + row];
     }
     tc_fence_after();
   }
 
   // ---- epilogue ---------------------------------------------------------------
   __syncwarp();
-  __syncthreads();  // every role is done; the ring and P buffers are free
+  __syncthreads();  // every role is done; the ring is free
   if (tid == 0) D2F_TRACE_MARK(0, 7);
   const bool aborted = *abort_flag != 0;
   if (cs == 1) {
     if (warp >= 2 && has_work && !aborted) {
       const int64_t hr = (int64_t)(q0 + r / G) * H + g * G + r % G;
-      const float inv = 1.0f / l;
-      uint16_t *dst = reinterpret_cast<uint16_t *>(a.out) + hr * D;
+      const float inv = 1.0f / l_tot;
+      uint16_t *dst = reinterpret_cast<uint16_t *>(a.out) + hr * D + half * (D / 2);
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
+      for (int ch = 0; ch < D / 64; ++ch) {
         uint32_t o[32];
-        tmem_ld32(lane_addr + kTmemO + ch * 32, o);
+        tmem_ld32(lane_addr + kTmemO + half * (D / 2) + ch * 32, o);
         if (row_valid) {
           uint32_t w[16];
 #pragma unroll
@@ -447,39 +493,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             d4[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
         }
       }
-      if (row_valid && a.lse_out) a.lse_out[hr] = (m_ref + __log2f(l)) * 0.6931471805599453f;
+      if (row_valid && half == 0 && a.lse_out)
+        a.lse_out[hr] = (m_ref + __log2f(l_tot)) * 0.6931471805599453f;
     }
-  } else {
-    // Stage this CTA's partial: fp32 O rows (16-byte chunks XOR-swizzled by row)
-    // and (max, sum) per row; an empty or aborted CTA contributes nothing.
+  } else if (active) {
+    const int LR = (M + cs - 1) / cs;  // receive slots per source CTA (rows a CTA owns)
+    // 1) every CTA is done with its ring
+    __syncwarp();
+    cluster_sync();
+    if (tid == 0) D2F_TRACE_MARK(0, 8);
+    // 2) push this CTA's partial rows to their owners: O half -> ring slot
+    //    [split][row / cs] of CTA row % cs (16-byte chunks XOR-swizzled by the
+    //    local row), (max, sum) -> slot [split][row / cs] of the owner's ML area.
     if (warp >= 2) {
+      const int owner = row % cs, lr = row / cs;
       const bool mine = has_work && !aborted;
-      ml_s[row] = mine ? make_float2(m_ref, l) : make_float2(-INFINITY, 0.f);
       if (mine) {
 #pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
+        for (int ch = 0; ch < D / 64; ++ch) {
           uint32_t o[32];
-          tmem_ld32(lane_addr + kTmemO + ch * 32, o);
+          tmem_ld32(lane_addr + kTmemO + half * (D / 2) + ch * 32, o);
+          if (row_valid) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
-                             o_stage_addr<D>(sb, row, ch * 8 + j)),
-                         "r"(o[4 * j]), "r"(o[4 * j + 1]), "r"(o[4 * j + 2]), "r"(o[4 * j + 3])
-                         : "memory");
+            for (int j = 0; j < 8; ++j) {
+              const int c = half * (L::kChunks / 2) + ch * 8 + j;
+              const uint32_t local = sb + L::kRing + (split * LR + lr) * (D * 4) +
+                                     ((c ^ (lr % L::kChunks)) << 4);
+              dsmem_st_u4(dsmem_addr(local, owner), o[4 * j], o[4 * j + 1], o[4 * j + 2],
+                          o[4 * j + 3]);
+            }
+          }
         }
+      }
+      if (row_valid && half == 0) {
+        const uint32_t local = sb + L::kML + (split * LR + lr) * 8;
+        dsmem_st_f2(dsmem_addr(local, owner), mine ? m_ref : -INFINITY, mine ? l_tot : 0.f);
       }
     }
     __syncwarp();
     cluster_sync();
-    if (tid == 0) D2F_TRACE_MARK(0, 8);
+    if (tid == 0) D2F_TRACE_MARK(0, 9);
+    // 3) compose the rows this CTA owns from local shared memory: one warp per
+    //    row, lane c holds 16-byte chunk c.
     if (warp >= 2) {
-      // CTA `split` composes rows split, split + cs, ...: one warp per row, lane c
-      // holds 16-byte chunk c of the row.
-      for (int rr = split + cs * (warp - 2); rr < nrows; rr += cs * 4) {
-        const int r2 = r_begin + rr;
-        const uint32_t ml_local = smem_u32(ml_s + rr);
+      for (int lr = sw; lr * cs + split < nrows; lr += kSoftWarps) {
+        const int r2 = r_begin + lr * cs + split;
         float2 ml = make_float2(-INFINITY, 0.f);
-        if (lane < cs) ml = dsmem_ld_f2(dsmem_addr(ml_local, lane));
+        if (lane < cs) ml = *reinterpret_cast<const float2 *>(smem + L::kML + (lane * LR + lr) * 8);
         float mx = ml.x;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -487,18 +547,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         float ls = w * ml.y;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        const uint32_t o_local = o_stage_addr<D>(sb, rr, lane % L::kChunks);
+        float4 v[kMaxCluster];
+        float wj[kMaxCluster];
 #pragma unroll
         for (int j = 0; j < kMaxCluster; ++j) {
-          const float wj = __shfl_sync(0xffffffffu, w, j);
-          if (j < cs && wj > 0.f && lane < L::kChunks) {
-            const float4 v = dsmem_ld_f4(dsmem_addr(o_local, j));
-            acc.x = fmaf(wj, v.x, acc.x);
-            acc.y = fmaf(wj, v.y, acc.y);
-            acc.z = fmaf(wj, v.z, acc.z);
-            acc.w = fmaf(wj, v.w, acc.w);
-          }
+          wj[j] = __shfl_sync(0xffffffffu, w, j);
+          v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (j < cs && wj[j] > 0.f && lane < L::kChunks)
+            v[j] = *reinterpret_cast<const float4 *>(
+                smem + L::kRing + (j * LR + lr) * (D * 4) + ((lane ^ (lr % L::kChunks)) << 4));
+        }
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < kMaxCluster; ++j) {
+          acc.x = fmaf(wj[j], v[j].x, acc.x);
+          acc.y = fmaf(wj[j], v[j].y, acc.y);
+          acc.z = fmaf(wj[j], v[j].z, acc.z);
+          acc.w = fmaf(wj[j], v[j].w, acc.w);
         }
         if (lane < L::kChunks && !aborted) {
           const float inv = 1.0f / ls;
@@ -511,8 +576,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    __syncwarp();
-    cluster_sync();  // keep this CTA's shared memory alive until every peer has read it
   }
 
   // ---- teardown ---------------------------------------------------------------
@@ -520,8 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (has_work && warp == 1) tmem_dealloc(tmem, kTmemCols);
-  if (tid == 0) D2F_TRACE_MARK(0, 9);
+  if (warp == 1) tmem_dealloc(bars->tmem_base, kTmemCols);
 }
 
 // ---------------------------------------------------------------------------
@@ -630,5 +692,9 @@ cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t s, char *why, size_t 
   snprintf(why, why_len, "tensor-core path supports head_dim 64 or 128");
   return cudaErrorInvalidValue;
 }
+
+#ifdef D2F_TRACE
+D2F_TRACE_COPY_FN(d2f_trace_copy_attn)
+#endif
 
 }  // namespace d2f

@@ -111,11 +111,10 @@ __device__ __forceinline__ float load_scalar(const void *base, int64_t i) {
 // One warp (lane u = row u of the block) decides block jb from the composed row
 // results in shared memory.
 __device__ void decide_block(const CommitArgs &a, int jb, const float *conf_s, const int *arg_s,
-                             float t, int phase) {
+                             float t, int phase, bool m) {
   const int lane = threadIdx.x & 31;
   const int r = jb * a.block_size + lane;
   const bool in = lane < a.block_size;
-  const bool m = in && a.masked[r] != 0;
   const float c = m ? conf_s[lane] : -1.0f;
   const int am = m ? arg_s[lane] : -1;
   bool take = m && (c > t);
@@ -169,12 +168,19 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
   const int jb = r / B;
 
   if (tid == 0) D2F_TRACE_MARK(1, 0);
+  if (PATH == 2 && tid == 0) {  // set-up that reads no global memory
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    mbar_fence_init();
+  }
   grid_dependency_wait();  // logits / state may come from the previous kernel
   if (tid == 0) D2F_TRACE_MARK(1, 1);
 
-  // Decision metadata of this block, fetched now, used only by the last arriver.
+  // Decision metadata of this block, fetched now, used only by the last arriver:
+  // lane u of warp 0 holds row u's masked flag, thread 0 the block's tau and phase.
   float tau_b = 0.f;
   int phase = 0;
+  const bool blk_masked = warp == 0 && lane < B && a.masked[jb * B + lane] != 0;
   if (tid == 0) {
     int lo = 0, hi = a.batch - 1;
     const int r0 = jb * B;
@@ -208,12 +214,7 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
     if (PATH == 2) {
       // Bulk-staged slice: whole 16-byte vectors [v0, v0 + nvec*N).
       const int nvec = (v1 - v0) / N;
-      if (tid == 0) {
-        abort_flag = 0;
-        mbar_init(smem_u32(&bar), 1);
-        mbar_fence_init();
-      }
-      __syncthreads();
+      __syncthreads();  // the mbarrier is initialised
       if (row_ok && nvec > 0) {
         if (tid == 0) {
           mbar_arrive_expect_tx(smem_u32(&bar), nvec * 16u);
@@ -288,28 +289,34 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
 
   // ---- arrival on the block's counter ----------------------------------------
   if (tid == 0) D2F_TRACE_MARK(1, 5);
-  if (tid == 0) {
-    __threadfence();
-    is_last = atomicAdd(a.blk_cnt + jb, 1) == B * a.splits - 1;
-  }
+  if (tid == 0) is_last = atomic_add_acq_rel(a.blk_cnt + jb, 1) == B * a.splits - 1;
   __syncthreads();
   if (tid == 0) D2F_TRACE_MARK(1, 6);
   if (!is_last) return;
-  __threadfence();
-  // Compose the slices of every masked row of the block: one warp per row.
-  for (int u = warp; u < B; u += kThreads / 32) {
-    const int rr = jb * B + u;
-    const bool mu = a.masked[rr] != 0;  // warp-uniform
+  // Compose the slices of every masked row of the block at once: half a warp per
+  // row (lanes 0-15 row 2w, lanes 16-31 row 2w+1 of warp w), slices strided by 16.
+  for (int u0 = 2 * warp; u0 < B; u0 += 2 * (kThreads / 32)) {
+    const int u = u0 + (lane >> 4);
+    const int sub = lane & 15;
     RowState acc2 = {-INFINITY, 0x7fffffff, 0.f};
-    if (mu) {
-      for (int j = lane; j < a.splits; j += 32) {
+    if (u < B) {
+      const int rr = jb * B + u;
+      for (int j = sub; j < a.splits; j += 16) {
         const float4 p = __ldcg(a.partial + (int64_t)rr * a.splits + j);
         acc2 = combine(acc2, RowState{p.x, __float_as_int(p.y), p.z});
       }
     }
-    acc2 = warp_combine(acc2);
-    if (lane == 0) {
-      const bool ok = mu && acc2.s > 0.f;
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) {  // reduce within each 16-lane half
+      RowState w;
+      w.m = __shfl_xor_sync(0xffffffffu, acc2.m, o);
+      w.idx = __shfl_xor_sync(0xffffffffu, acc2.idx, o);
+      w.s = __shfl_xor_sync(0xffffffffu, acc2.s, o);
+      acc2 = combine(acc2, w);
+    }
+    if (sub == 0 && u < B) {
+      // rows not masked on entry have no partials (their slots are stale)
+      const bool ok = acc2.s > 0.f;
       conf_s[u] = ok ? 1.0f / acc2.s : -1.0f;
       arg_s[u] = ok ? acc2.idx : -1;
     }
@@ -318,7 +325,7 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
   if (warp == 0) {
     tau_b = __shfl_sync(0xffffffffu, tau_b, 0);
     phase = __shfl_sync(0xffffffffu, phase, 0);
-    decide_block(a, jb, conf_s, arg_s, tau_b, phase);
+    decide_block(a, jb, conf_s, arg_s, tau_b, phase, blk_masked);
     if (lane == 0) a.blk_cnt[jb] = 0;
     if (lane == 0) D2F_TRACE_MARK(1, 7);
   }
@@ -356,3 +363,9 @@ cudaError_t launch_commit(const CommitArgs &a, int dtype, int path, cudaStream_t
 }
 
 }  // namespace d2f
+
+#ifdef D2F_TRACE
+namespace d2f {
+D2F_TRACE_COPY_FN(d2f_trace_copy_commit)
+}  // namespace d2f
+#endif

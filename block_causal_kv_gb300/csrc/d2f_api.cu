@@ -52,6 +52,7 @@ struct AttnPlan {
   bool tc;        // tensor-core path
   int m_tiles;
   int splits;
+  int tiles_per_split;
   int n_counters;
   size_t off_ml, off_o, bytes;
 };
@@ -103,6 +104,7 @@ int plan_attn(int batch, int total_q, int max_q, int max_ctx, int Hq, int Hkv, i
         splits *= 2;
     }
     p->splits = min(splits, kTcMaxSplits);
+    p->tiles_per_split = cdiv(t_max, p->splits);
     p->n_counters = 0;
     p->off_ml = p->off_o = p->bytes = 0;
     return D2F_OK;
@@ -156,17 +158,24 @@ int plan_commit(int total_q, int vocab, int dtype, int B, int num_splits, Commit
   int splits = num_splits;
   int chunk;
   if (splits == 0) {
-    // about four CTAs per SM, and slices small enough to stage in shared memory
-    const int sms = num_sms_current_device();
-    const long long target = 4LL * (sms > 0 ? sms : 1);
-    const long long rows = total_q > 0 ? total_q : 1;
-    long long want = (target + rows - 1) / rows;
-    want = max(want, (long long)cdiv(vocab, max_chunk));
-    if (want < 1) want = 1;
-    if (want > kCommitMaxSplits) want = kCommitMaxSplits;
-    splits = (int)want;
-    chunk = cdiv(cdiv(vocab, splits), vec * kCommitThreads) * vec * kCommitThreads;
-    if (chunk > max_chunk) chunk = cdiv(cdiv(vocab, splits), vec) * vec;
+    // Pick the slice count that minimises the work of the busiest SM: CTAs per SM
+    // (rounded up) x (slice length + a fixed per-CTA cost of about 2048 values),
+    // over slice counts whose slices fit the shared-memory stage.
+    const int sms = max(1, num_sms_current_device());
+    const long long rows = max(total_q, 1);
+    long long best_cost = -1;
+    splits = 1;
+    for (int s = max(1, cdiv(vocab, max_chunk)); s <= kCommitMaxSplits; ++s) {
+      const int c = cdiv(cdiv(vocab, s), vec) * vec;
+      if (cdiv(vocab, c) != s) continue;
+      const long long waves = (rows * s + sms - 1) / sms;
+      const long long cost = waves * (c + 2048LL);
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        splits = s;
+      }
+    }
+    chunk = cdiv(cdiv(vocab, splits), vec) * vec;
   } else {
     chunk = cdiv(cdiv(vocab, splits), vec) * vec;
   }
@@ -188,14 +197,6 @@ int plan_commit(int total_q, int vocab, int dtype, int B, int num_splits, Commit
 
 using namespace d2f;
 
-#ifdef D2F_TRACE
-// Development builds only: the phase-trace array and its address.
-__device__ unsigned long long d2f::g_d2f_trace[2][d2f::kTraceCtas * d2f::kTraceSlots];
-extern "C" void *d2f_trace_buffer(void) {
-  void *p = nullptr;
-  return cudaGetSymbolAddress(&p, d2f::g_d2f_trace) == cudaSuccess ? p : nullptr;
-}
-#endif
 
 extern "C" {
 
@@ -281,6 +282,7 @@ int d2f_block_attn(const void *q, const void *k_win, const void *v_win, const vo
   a.group = num_heads_q / num_heads_kv;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.num_splits = p.splits;
+  a.tiles_per_split = p.tiles_per_split;
   a.m_tiles = p.m_tiles;
   a.counters = reinterpret_cast<int32_t *>(workspace);
   a.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) + p.off_ml);

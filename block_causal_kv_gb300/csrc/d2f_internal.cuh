@@ -35,6 +35,7 @@ struct AttnArgs {
   int group;             // num_heads_q / num_heads_kv
   float scale_log2;      // softmax_scale * log2(e)
   int num_splits;        // split count requested (each sequence uses <= this many)
+  int tiles_per_split;   // tensor-core path: key tiles per split from the host's max_ctx
   int m_tiles;           // grid.x: row tiles per (sequence, KV head)
   int32_t *counters;     // [batch * Hkv * m_tiles] merge arrival counters (zero at rest)
   float2 *ws_ml;         // [num_splits][total_q * Hq] (max in log2 units, sum)
@@ -252,17 +253,51 @@ __device__ __forceinline__ float4 dsmem_ld_f4(uint32_t addr) {
 #ifdef D2F_TRACE
 constexpr int kTraceSlots = 16;
 constexpr int kTraceCtas = 8192;
-extern __device__ unsigned long long g_d2f_trace[2][kTraceCtas * kTraceSlots];
-__device__ __forceinline__ void trace_mark(int kernel, int slot) {
+// One array per translation unit (each kernel file has its own copy-out hook).
+static __device__ unsigned long long g_d2f_trace[kTraceCtas * kTraceSlots];
+__device__ __forceinline__ void trace_mark(int slot) {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   const unsigned cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
-  if (cta < kTraceCtas) g_d2f_trace[kernel][cta * kTraceSlots + slot] = t;
+  if (cta < kTraceCtas) g_d2f_trace[cta * kTraceSlots + slot] = t;
 }
-#define D2F_TRACE_MARK(kernel, slot) trace_mark(kernel, slot)
+#define D2F_TRACE_MARK(kernel, slot) trace_mark(slot)
+#define D2F_TRACE_COPY_FN(name)                                                          \
+  extern "C" int name(void *host, size_t bytes, int clear) {                             \
+    if (bytes > sizeof(g_d2f_trace)) bytes = sizeof(g_d2f_trace);                         \
+    if (host && cudaMemcpyFromSymbol(host, g_d2f_trace, bytes) != cudaSuccess) return 1;  \
+    void *p = nullptr;                                                                    \
+    if (clear && (cudaGetSymbolAddress(&p, g_d2f_trace) != cudaSuccess ||                 \
+                  cudaMemset(p, 0, sizeof(g_d2f_trace)) != cudaSuccess))                  \
+      return 2;                                                                           \
+    return 0;                                                                             \
+  }
 #else
 #define D2F_TRACE_MARK(kernel, slot) ((void)0)
 #endif
+
+__device__ __forceinline__ void dsmem_st_u4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                            uint32_t d) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
+               "r"(c), "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ void dsmem_st_f2(uint32_t addr, float x, float y) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(x), "f"(y) : "memory");
+}
+// Device-scope atomic add with acquire-release semantics: the caller's earlier
+// writes are visible to whoever later acquires the counter, and the caller sees
+// the writes every earlier arriver released.
+__device__ __forceinline__ int atomic_add_acq_rel(int32_t *p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+// Named barrier among `count` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 
 // ----- programmatic dependent launch ----------------------------------------
 // Block until every grid this one depends on has completed and its writes are
@@ -305,6 +340,18 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem], bf16 inputs, f32 accumulate (A read from TMEM:
+// row i = lane i, two consecutive K elements per 32-bit column, lower K in the
+// low half).
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrive on an mbarrier once every tcgen05 operation issued so far by this thread completes.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
@@ -331,6 +378,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr)
+      : "memory");
+}
+// 16 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
       : "memory");
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
