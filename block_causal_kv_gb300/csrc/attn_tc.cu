@@ -630,6 +630,9 @@ cudaError_t ensure_smem_attr() {
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
   e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Layout<D>::kAlloc);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return e;
 }
@@ -673,7 +676,7 @@ cudaError_t launch_d(const AttnArgs &a, cudaStream_t s, char *why, size_t why_le
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
   e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<D>, a, kp, vp, kw, vw);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -16,6 +16,8 @@
 // one warp (lane = row). The decision's metadata (sequence, tau, phase) is
 // fetched while the slice streams. There is no spin-wait on another CTA: the
 // counter hands the work to whoever arrives last and is reset by it.
+#include <mutex>
+
 #include "d2f_internal.cuh"
 
 namespace d2f {
@@ -331,8 +333,28 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
   }
 }
 
+// Keep the L1 / shared-memory split at its shared-memory maximum, as the
+// attention kernel needs it: alternating kernels then never make an SM drain and
+// reconfigure between launches. Set once per device.
+template <int DT, int PATH>
+cudaError_t ensure_carveout() {
+  static std::mutex mu;
+  static bool done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(commit_kernel<DT, PATH>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+  return e;
+}
+
 template <int DT, int PATH>
 cudaError_t launch_path(const CommitArgs &a, cudaStream_t stream) {
+  cudaError_t ce = ensure_carveout<DT, PATH>();
+  if (ce != cudaSuccess) return ce;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.splits, a.total_q);
   cfg.blockDim = dim3(kThreads);
@@ -342,7 +364,7 @@ cudaError_t launch_path(const CommitArgs &a, cudaStream_t stream) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
   cudaError_t e = cudaLaunchKernelEx(&cfg, commit_kernel<DT, PATH>, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

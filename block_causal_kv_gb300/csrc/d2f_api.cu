@@ -19,6 +19,14 @@ void set_last_error(const char *fmt, ...) {
   va_end(ap);
 }
 
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char *e = getenv("D2F_PDL");
+    return !(e && strcmp(e, "0") == 0);
+  }();
+  return on;
+}
+
 int num_sms_current_device() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;

@@ -16,6 +16,9 @@ namespace d2f {
 // ---------------------------------------------------------------------------
 void set_last_error(const char *fmt, ...);
 int num_sms_current_device();
+// Programmatic dependent launch on every kernel launch unless D2F_PDL=0 (a
+// switch for comparing launch overlap; results are identical either way).
+bool pdl_enabled();
 
 // Bounded waits give up after this many SM clock cycles (about one second at
 // the GB300's clocks), set D2F_ERR_TIMEOUT in the error word and unwind.
