@@ -12,20 +12,21 @@
 // (row r = query r / G, head r % G), so every K/V byte is read once per row
 // tile. The key tiles of the row tile (64 keys = 64/B cache pages or 64/B window
 // blocks, cache first) are split among the `cs` CTAs of one thread-block
-// cluster; each CTA streams its share through a 4-stage shared-memory ring:
+// cluster. A CTA needs ~105 KB of shared memory and 256 TMEM columns, so two
+// CTAs share an SM and hide each other's latencies. Each CTA streams its share
+// through a 2-stage shared-memory ring:
 //
-//   warp 0       TMA producer: page ids (32 at a time, prefetched) ->
-//                cp.async.bulk.tensor loads of the K and V tiles, 128-byte
-//                swizzle, completion counted on the stage's mbarrier.
+//   warp 0       TMA producer: page ids (requested with the sequence metadata,
+//                32 at a time) -> cp.async.bulk.tensor loads of the K and V
+//                tiles, 128-byte swizzle, completion counted on an mbarrier.
 //   warp 1       TMEM owner and MMA issuer (one lane): S = Q K^T into TMEM
-//                (double-buffered), then O += P V into TMEM once P is written.
-//   warps 2-9    softmax, two threads per query row (TMEM lane = row): both
-//                read the row's 64 scores and take the tile maximum, each
-//                exponentiates 32 of them and owns half of O. The block-causal
-//                mask is a per-row key limit; the online softmax runs in log2
-//                units with lazy rescaling of O (only when the running max grows
-//                by more than 2^8); bf16 P goes to TMEM, where the second MMA
-//                reads its A operand.
+//                (double-buffered), then O += P V with P read from TMEM.
+//   warps 2-5    softmax, one thread per query row (TMEM lane = row): read the
+//                row's 64 scores, apply the block-causal mask as a per-row key
+//                limit, online softmax in log2 units with lazy rescaling of O
+//                (only when the running max grows by more than 2^8), write bf16 P
+//                over the scores it came from (TMEM columns 0-31 of the S buffer),
+//                where the second MMA reads its A operand.
 //
 // Composition. With cs > 1 the CTAs of the cluster push their unnormalised O
 // rows and (max, sum) into the shared memory of the CTA that owns each row
@@ -47,16 +48,14 @@
 namespace d2f {
 namespace {
 
-constexpr int kSoftWarps = 8;
-constexpr int kSoftThreads = 32 * kSoftWarps;  // two per query row
+constexpr int kSoftWarps = 4;
+constexpr int kSoftThreads = 32 * kSoftWarps;  // one per query row
 constexpr int kThreads = 64 + kSoftThreads;    // producer + MMA warps + softmax
-constexpr int NS = 4;                          // K/V ring stages
+constexpr int NS = 2;                          // K/V ring stages
 constexpr int M = kTcRows;                     // 128 query rows per tile
 constexpr int N = kTcKeys;                     // 64 keys per tile
-constexpr int kHalfN = N / 2;                  // keys per softmax thread per tile
-constexpr uint32_t kTmemCols = 512;            // S (2 x 64) + O (<= 128) + P (2 x 32)
+constexpr uint32_t kTmemCols = 256;            // S / P (2 x 64) + O (<= 128)
 constexpr uint32_t kTmemO = 128;               // first TMEM column of O
-constexpr uint32_t kTmemP = 256;               // bf16 P, two keys per column, 2 buffers
 constexpr int kMaxCluster = 8;
 constexpr int kBarSetup = 1;                   // named barrier: MMA warp + softmax warps
 
@@ -70,24 +69,24 @@ struct Layout {
   static constexpr int kStage = 2 * kKBytes;     // K tile then V tile
   static constexpr int kChunks = D / 4;          // 16-byte chunks of one fp32 O row
   static constexpr int kQ = 0;
-  static constexpr int kRing = kQ + kQBytes;     // also receives pushed O rows
+  static constexpr int kRing = kQ + kQBytes;
+  static constexpr int kRecv = kQ;               // pushed O rows land over Q + ring
   static constexpr int kML = kRing + NS * kStage;  // pushed (max, sum): float2 [8][128]
-  static constexpr int kX = kML + kMaxCluster * M * 8;  // pair sums: float [2][128]
-  static constexpr int kBars = kX + 2 * M * 4;
-  static constexpr int kBytes = kBars + 512;
+  static constexpr int kBars = kML + kMaxCluster * M * 8;
+  static constexpr int kBytes = kBars + 256;
   static constexpr int kAlloc = kBytes + 1024;   // slack for 1024-byte alignment
-  static_assert(NS * kStage >= (M + kMaxCluster) * D * 4, "pushed O rows must fit in the ring");
+  static_assert(kQBytes + NS * kStage >= (M + kMaxCluster) * D * 4,
+                "pushed O rows must fit in the Q + ring area");
 };
 
 struct Bars {
   uint64_t full[NS], empty[NS], s_full[2], p_full[2], pv_done[2], q_full, drain;
-  uint64_t pair[4][2];  // per TMEM quadrant: the two threads of a row exchange their sums
   uint32_t tmem_base;
   int abort_flag;
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_kpool,
                    const __grid_constant__ CUtensorMap tm_vpool,
                    const __grid_constant__ CUtensorMap tm_kwin,
@@ -99,7 +98,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sb = smem_u32(smem);
   Bars *bars = reinterpret_cast<Bars *>(smem + L::kBars);
   volatile int *abort_flag = &bars->abort_flag;
-  float *xsum = reinterpret_cast<float *>(smem + L::kX);  // [2 half][128]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cs = gridDim.x;  // CTAs of the cluster = splits of this row tile
@@ -119,8 +117,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bars->p_full[i]), kSoftThreads);
       mbar_init(smem_u32(&bars->pv_done[i]), 1);
     }
-    for (int q = 0; q < 4; ++q)
-      for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&bars->pair[q][i]), 64);
     mbar_init(smem_u32(&bars->q_full), kSoftThreads);
     mbar_init(smem_u32(&bars->drain), 1);
     bars->abort_flag = 0;
@@ -139,11 +135,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   grid_dependency_wait();  // inputs may come from the previous kernel in the stream
   if (tid == 0) D2F_TRACE_MARK(0, 1);
 
-  // Page ids of this split's first tiles, requested before the sequence metadata
-  // arrives: the split's tile range comes from the host (tiles_per_split), so the
-  // first logical page is known up front.
+  // Page ids of this split's first tiles, requested together with the sequence
+  // metadata: the split's tile range comes from the host (tiles_per_split), so
+  // its first logical page is known up front.
   const int ppt = N / a.block_size;  // pages (or window blocks) per tile
-  int pre_chunk = split * a.tiles_per_split * ppt;
+  const int pre_chunk = split * a.tiles_per_split * ppt;
   int pre_ids = -1;
   if (warp == 0 && pre_chunk + lane < a.max_pages_per_seq)
     pre_ids = __ldg(a.page_table + (int64_t)b * a.max_pages_per_seq + pre_chunk + lane);
@@ -175,15 +171,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (tid == 0) D2F_TRACE_MARK(0, 2);
 
-  // softmax-thread identity (warps 2-9): row = TMEM lane, half = key / O half
-  const int sw = warp - 2;
+  // softmax-thread identity (warps 2-5): row = TMEM lane
   const int quad = warp & 3;
-  const int half = (sw >> 2) & 1;
   const int row = quad * 32 + lane;
   const bool row_valid = row < nrows;
   const int r = r_begin + row;
   const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
-  float m_ref = -INFINITY, l = 0.f, l_tot = 0.f;
+  float m_ref = -INFINITY, l = 0.f;
 
   if (has_work && warp == 0) {
     // ======================= TMA producer (whole warp) =========================
@@ -222,7 +216,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           ids_cur = ids_next;
           ids_next = fetch(chunk + 32);
         }
-        // (pages outside the sequence are masked out by the C check below)
         const int pg = __shfl_sync(0xffffffffu, ids_cur, (lp0 - chunk + lane) & 31);
         if (lane < ppt && (lp0 + lane) * B < C) {
           if (pg >= 0 && pg < a.num_pages)
@@ -277,8 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int ks = 0; ks < N / 16; ++ks) {  // 16 keys = 8 TMEM columns of P per step
           const uint64_t bd = smem_desc_sw128(v_base + ks * 2048, L::kKVHalf, 1024);
-          umma_bf16_tmem_a(tmem + kTmemO, tmem + kTmemP + (v & 1) * (N / 2) + ks * 8, bd,
-                           idesc_pv, (v > 0 || ks > 0) ? 1u : 0u);
+          umma_bf16_tmem_a(tmem + kTmemO, tmem + (v & 1) * N + ks * 8, bd, idesc_pv,
+                           (v > 0 || ks > 0) ? 1u : 0u);
         }
         umma_commit(smem_u32(&bars->pv_done[v & 1]));
         umma_commit(smem_u32(&bars->empty[stage]));
@@ -292,6 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         if (u == 0) D2F_TRACE_MARK(0, 10);
+        // S_u overwrites the S/P buffer that P_{u-2} occupied: P.V_{u-2} was issued
+        // before this (MMAs of one thread execute in order).
         const uint32_t k_base = sb + L::kRing + stage * L::kStage;
 #pragma unroll
         for (int h = 0; h < L::kHalves; ++h) {
@@ -312,24 +307,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(smem_u32(&bars->drain), 0, &no_abort, a.err);
     }
   } else if (has_work) {
-    // ======================= softmax (256 threads, two per row) ================
+    // ======================= softmax (128 threads, one per row) ================
     {
-      // This thread's half of the Q row, into the 128-byte-swizzled K-major
-      // layout the MMA reads: 16-byte chunk c of column block h lands at
+      // The Q row into the 128-byte-swizzled K-major layout the MMA reads:
+      // 16-byte chunk c of column block h lands at
       //   h*kQHalf + (row/8)*1024 + (row%8)*128 + ((c ^ (row%8)) * 16).
-      constexpr int kQc = D / 16;
+      constexpr int kQc = D / 8;
       uint4 qv[kQc];
       const uint4 *src = reinterpret_cast<const uint4 *>(
-                             reinterpret_cast<const uint16_t *>(a.q) +
-                             ((int64_t)(q0 + r / G) * H + g * G + r % G) * D) +
-                         half * kQc;
+          reinterpret_cast<const uint16_t *>(a.q) + ((int64_t)(q0 + r / G) * H + g * G + r % G) * D);
 #pragma unroll
       for (int c = 0; c < kQc; ++c) qv[c] = row_valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
 #pragma unroll
       for (int c = 0; c < kQc; ++c) {
-        const int cc = half * kQc + c;
-        const uint32_t dst = sb + L::kQ + (cc >> 3) * L::kQHalf + (row >> 3) * 1024 +
-                             (row & 7) * 128 + (((cc & 7) ^ (row & 7)) << 4);
+        const uint32_t dst = sb + L::kQ + (c >> 3) * L::kQHalf + (row >> 3) * 1024 +
+                             (row & 7) * 128 + (((c & 7) ^ (row & 7)) << 4);
         asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(qv[c].x),
                      "r"(qv[c].y), "r"(qv[c].z), "r"(qv[c].w)
                      : "memory");
@@ -346,14 +338,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       if (tid == 64 && u == 0) D2F_TRACE_MARK(0, 4);
-      if (tid == 128 && u == 2) D2F_TRACE_MARK(0, 11);
       if (tid == 64 && u == T - 1) D2F_TRACE_MARK(0, 5);
-      // Both threads of the pair read all 64 scores of the row and take the tile
-      // maximum themselves (no exchange); each then exponentiates its own 32.
       uint32_t sv_lo[32], sv_hi[32];
-      tmem_ld32(lane_addr + (u & 1) * N, sv_lo);
-      tmem_ld32(lane_addr + (u & 1) * N + 32, sv_hi);
-      if (tid == 128 && u == 2) D2F_TRACE_MARK(0, 12);
+      const uint32_t s_addr = lane_addr + (u & 1) * N;
+      tmem_ld32(s_addr, sv_lo);
+      tmem_ld32(s_addr + 32, sv_hi);
 
       // keys c < lim of this tile are visible to this row
       const int tile_lim = t < Tc ? C - t * N : n - (t - Tc) * N;  // valid keys of the tile
@@ -378,7 +367,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < w; ++c) tr[c] = fmaxf(tr[2 * c], tr[2 * c + 1]);
       const float tmax = tr[0] * sl2;
-      if (tid == 128 && u == 2) D2F_TRACE_MARK(0, 13);
       // Lazy rescale: keep the reference max unless the tile max exceeds it by 2^8.
       const bool need = tmax > m_ref + 8.0f;
       if (__any_sync(0xffffffffu, need)) {
@@ -391,9 +379,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
-          for (int ch = 0; ch < D / 64; ++ch) {  // this thread's half of O
+          for (int ch = 0; ch < D / 32; ++ch) {
             uint32_t o[32];
-            const uint32_t oa = lane_addr + kTmemO + half * (D / 2) + ch * 32;
+            const uint32_t oa = lane_addr + kTmemO + ch * 32;
             tmem_ld32(oa, o);
 #pragma unroll
             for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
@@ -403,85 +391,68 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         m_ref = m_new;
       }
-      // P = 2^(s*scale - m_ref) for this thread's 32 keys, rounded to bf16; masked
-      // keys are -inf -> 0. A row with no visible key so far keeps m_ref = -inf:
-      // subtract 0 instead.
+      // P = 2^(s*scale - m_ref), rounded to bf16; masked keys are -inf -> 0. A row
+      // with no visible key so far keeps m_ref = -inf: subtract 0 instead.
       const float mb = m_ref == -INFINITY ? 0.f : m_ref;
-      uint32_t pk[kHalfN / 2];
-      float ps[kHalfN / 2];
+      uint32_t pk[N / 2];
+      float ps[N / 2];
 #pragma unroll
-      for (int j = 0; j < kHalfN / 2; ++j) {
-        // select this thread's half with compile-time indices (keeps sf in registers)
-        const float s0 = half ? sf[kHalfN + 2 * j] : sf[2 * j];
-        const float s1 = half ? sf[kHalfN + 2 * j + 1] : sf[2 * j + 1];
-        const float p0 = fast_exp2(fmaf(s0, sl2, -mb));
-        const float p1 = fast_exp2(fmaf(s1, sl2, -mb));
+      for (int j = 0; j < N / 2; ++j) {
+        const float p0 = fast_exp2(fmaf(sf[2 * j], sl2, -mb));
+        const float p1 = fast_exp2(fmaf(sf[2 * j + 1], sl2, -mb));
         pk[j] = pack_bf16x2(p0, p1);
         ps[j] = __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xffff0000u);
       }
 #pragma unroll
-      for (int w = kHalfN / 4; w >= 1; w >>= 1)
+      for (int w = N / 4; w >= 1; w >>= 1)
 #pragma unroll
         for (int c = 0; c < w; ++c) ps[c] = ps[2 * c] + ps[2 * c + 1];
       l += ps[0];
-      if (tid == 128 && u == 2) D2F_TRACE_MARK(0, 14);
-
-      // The P buffer is free once the MMA that read it two tiles ago completed.
-      if (u >= 2) {
-        ok = mbar_wait(smem_u32(&bars->pv_done[u & 1]), ((u - 2) >> 1) & 1, abort_flag, a.err);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        tc_fence_after();
-      }
-      // P into TMEM for the P.V product (A operand from TMEM): column c of the
-      // buffer holds keys 2c and 2c+1; this thread writes columns 16*half ...
-      tmem_st16(lane_addr + kTmemP + (u & 1) * (N / 2) + half * (kHalfN / 2), pk);
+      // P over the scores it came from (this thread's own lane): column c of the
+      // S/P buffer now holds keys 2c and 2c+1.
+      tmem_st32(s_addr, pk);
       tmem_wait_st();
       // A ragged tile (partial last page or short window) may hold stale or
       // non-finite V rows past its valid keys; P is 0 there, but 0 * NaN is not
-      // 0, so clear those rows before the P.V product reads them (each thread of
-      // the pair clears one 64-column block when D = 128).
-      if (row < N && row >= tile_lim && half < L::kHalves) {
+      // 0, so clear those rows before the P.V product reads them.
+      if (row < N && row >= tile_lim) {
         const uint32_t v_row = sb + L::kRing + (u % NS) * L::kStage + L::kKBytes +
-                               half * L::kKVHalf + (row >> 3) * 1024 + (row & 7) * 128;
+                               (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(v_row + (c << 4)), "r"(0u)
-                       : "memory");
+        for (int h = 0; h < L::kHalves; ++h)
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(v_row + h * L::kKVHalf +
+                                                                           (c << 4)),
+                         "r"(0u)
+                         : "memory");
         fence_proxy_async_smem();
       }
-      if (tid == 128 && u == 2) D2F_TRACE_MARK(0, 15);
       tc_fence_before();
       mbar_arrive(smem_u32(&bars->p_full[u & 1]));
-      if (tid == 128 && u == 3) D2F_TRACE_MARK(0, 3);
+      if (tid == 64 && u == T - 1) D2F_TRACE_MARK(0, 6);
     }
-    if (tid == 64) D2F_TRACE_MARK(0, 6);
     if (ok) {  // the last P.V product
       ok = mbar_wait(smem_u32(&bars->pv_done[(T - 1) & 1]), ((T - 1) >> 1) & 1, abort_flag, a.err);
       ok = __all_sync(0xffffffffu, ok);
-    }
-    if (ok) {  // row sum = sum of the pair's halves
-      xsum[half * M + row] = l;
-      mbar_arrive(smem_u32(&bars->pair[quad][0]));
-      ok = mbar_wait(smem_u32(&bars->pair[quad][0]), 0, abort_flag, a.err);
-      l_tot = l + xsum[(half ^ 1) * M + row];
     }
     tc_fence_after();
   }
 
   // ---- epilogue ---------------------------------------------------------------
   __syncwarp();
-  __syncthreads();  // every role is done; the ring is free
+  __syncthreads();  // every role is done; Q and the ring are free
   if (tid == 0) D2F_TRACE_MARK(0, 7);
   const bool aborted = *abort_flag != 0;
   if (cs == 1) {
     if (warp >= 2 && has_work && !aborted) {
       const int64_t hr = (int64_t)(q0 + r / G) * H + g * G + r % G;
-      const float inv = 1.0f / l_tot;
-      uint16_t *dst = reinterpret_cast<uint16_t *>(a.out) + hr * D + half * (D / 2);
+      const float inv = 1.0f / l;
+      uint16_t *dst = reinterpret_cast<uint16_t *>(a.out) + hr * D;
 #pragma unroll
-      for (int ch = 0; ch < D / 64; ++ch) {
+      for (int ch = 0; ch < D / 32; ++ch) {
         uint32_t o[32];
-        tmem_ld32(lane_addr + kTmemO + half * (D / 2) + ch * 32, o);
+        tmem_ld32(lane_addr + kTmemO + ch * 32, o);
         if (row_valid) {
           uint32_t w[16];
 #pragma unroll
@@ -493,31 +464,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             d4[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
         }
       }
-      if (row_valid && half == 0 && a.lse_out)
-        a.lse_out[hr] = (m_ref + __log2f(l_tot)) * 0.6931471805599453f;
+      if (row_valid && a.lse_out) a.lse_out[hr] = (m_ref + __log2f(l)) * 0.6931471805599453f;
     }
   } else if (active) {
     const int LR = (M + cs - 1) / cs;  // receive slots per source CTA (rows a CTA owns)
-    // 1) every CTA is done with its ring
+    // 1) every CTA of the cluster is done with its Q and ring buffers
     __syncwarp();
     cluster_sync();
     if (tid == 0) D2F_TRACE_MARK(0, 8);
-    // 2) push this CTA's partial rows to their owners: O half -> ring slot
+    // 2) push this CTA's partial rows to their owners: O row -> slot
     //    [split][row / cs] of CTA row % cs (16-byte chunks XOR-swizzled by the
-    //    local row), (max, sum) -> slot [split][row / cs] of the owner's ML area.
+    //    local row), (max, sum) -> slot [split][row / cs] of its ML area.
     if (warp >= 2) {
       const int owner = row % cs, lr = row / cs;
       const bool mine = has_work && !aborted;
       if (mine) {
 #pragma unroll
-        for (int ch = 0; ch < D / 64; ++ch) {
+        for (int ch = 0; ch < D / 32; ++ch) {
           uint32_t o[32];
-          tmem_ld32(lane_addr + kTmemO + half * (D / 2) + ch * 32, o);
+          tmem_ld32(lane_addr + kTmemO + ch * 32, o);
           if (row_valid) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              const int c = half * (L::kChunks / 2) + ch * 8 + j;
-              const uint32_t local = sb + L::kRing + (split * LR + lr) * (D * 4) +
+              const int c = ch * 8 + j;
+              const uint32_t local = sb + L::kRecv + (split * LR + lr) * (D * 4) +
                                      ((c ^ (lr % L::kChunks)) << 4);
               dsmem_st_u4(dsmem_addr(local, owner), o[4 * j], o[4 * j + 1], o[4 * j + 2],
                           o[4 * j + 3]);
@@ -525,9 +495,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (row_valid && half == 0) {
+      if (row_valid) {
         const uint32_t local = sb + L::kML + (split * LR + lr) * 8;
-        dsmem_st_f2(dsmem_addr(local, owner), mine ? m_ref : -INFINITY, mine ? l_tot : 0.f);
+        dsmem_st_f2(dsmem_addr(local, owner), mine ? m_ref : -INFINITY, mine ? l : 0.f);
       }
     }
     __syncwarp();
@@ -536,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 3) compose the rows this CTA owns from local shared memory: one warp per
     //    row, lane c holds 16-byte chunk c.
     if (warp >= 2) {
-      for (int lr = sw; lr * cs + split < nrows; lr += kSoftWarps) {
+      for (int lr = warp - 2; lr * cs + split < nrows; lr += kSoftWarps) {
         const int r2 = r_begin + lr * cs + split;
         float2 ml = make_float2(-INFINITY, 0.f);
         if (lane < cs) ml = *reinterpret_cast<const float2 *>(smem + L::kML + (lane * LR + lr) * 8);
@@ -555,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
           if (j < cs && wj[j] > 0.f && lane < L::kChunks)
             v[j] = *reinterpret_cast<const float4 *>(
-                smem + L::kRing + (j * LR + lr) * (D * 4) + ((lane ^ (lr % L::kChunks)) << 4));
+                smem + L::kRecv + (j * LR + lr) * (D * 4) + ((lane ^ (lr % L::kChunks)) << 4));
         }
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -584,6 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(bars->tmem_base, kTmemCols);
+  if (tid == 0) D2F_TRACE_MARK(0, 11);
 }
 
 // ---------------------------------------------------------------------------
@@ -618,9 +589,10 @@ bool encode(EncodeTiledFn fn, CUtensorMap *map, const void *base, int rank, cons
   return r == CUDA_SUCCESS;
 }
 
-// The shared-memory opt-in is a per-device function attribute; set it once per device.
+// Function attributes (shared-memory opt-in and carveout) are per device; set
+// them once per device.
 template <int D>
-cudaError_t ensure_smem_attr() {
+cudaError_t ensure_attrs() {
   static std::mutex mu;
   static bool done[64] = {};
   int dev = 0;
@@ -660,7 +632,7 @@ cudaError_t launch_d(const AttnArgs &a, cudaStream_t s, char *why, size_t why_le
     snprintf(why, why_len, "cuTensorMapEncodeTiled rejected a K/V tensor (alignment or size)");
     return cudaErrorInvalidValue;
   }
-  cudaError_t e = ensure_smem_attr<D>();
+  cudaError_t e = ensure_attrs<D>();
   if (e != cudaSuccess) return e;
   const int cs = a.num_splits;
   cudaLaunchConfig_t cfg = {};

@@ -360,11 +360,11 @@ cudaError_t launch_path(const CommitArgs &a, cudaStream_t stream) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = PATH == 2 ? (size_t)a.chunk * (DT == D2F_BF16 ? 2 : 4) : 0;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  // No programmatic early launch for the commit: measured on GB300, its CTAs
+  // scheduled during the previous kernel's tail cost more than they saved. The
+  // kernel still waits on its dependencies (a no-op without the attribute).
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
   cudaError_t e = cudaLaunchKernelEx(&cfg, commit_kernel<DT, PATH>, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

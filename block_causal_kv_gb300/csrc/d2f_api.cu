@@ -106,9 +106,10 @@ int plan_attn(int batch, int total_q, int max_q, int max_ctx, int Hq, int Hkv, i
     // The splits of one row tile form a thread-block cluster (at most 8 CTAs)
     // and compose their partials in distributed shared memory: no workspace.
     if (splits == 0) {
-      const int sms = num_sms_current_device();
+      // two CTAs fit on an SM: fill the 2 x SM slots with power-of-two clusters
+      const int slots = 2 * num_sms_current_device();
       splits = 1;
-      while (splits * 2 <= kTcMaxSplits && splits * 2 <= t_max && base * splits * 2 <= sms)
+      while (splits * 2 <= kTcMaxSplits && splits * 2 <= t_max && base * splits * 2 <= slots)
         splits *= 2;
     }
     p->splits = min(splits, kTcMaxSplits);
