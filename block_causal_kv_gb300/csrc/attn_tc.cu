@@ -7,14 +7,16 @@
 // several active blocks decoded together); "확산 언어 모델(Diffusion LLM)이란
 // 무엇인가", §FlashBlock (attention parts recombined in log space).
 //
-// Work decomposition. A row tile is <= 128 query rows of one (sequence, KV
+// Work decomposition. A row tile is <= QR query rows of one (sequence, KV
 // head): the G = Hq/Hkv query heads of the group are packed into the rows
 // (row r = query r / G, head r % G), so every K/V byte is read once per row
-// tile. The key tiles of the row tile (64 keys = 64/B cache pages or 64/B window
-// blocks, cache first) are split among the `cs` CTAs of one thread-block
-// cluster. A CTA needs ~105 KB of shared memory and 256 TMEM columns, so two
-// CTAs share an SM and hide each other's latencies. Each CTA streams its share
-// through a 2-stage shared-memory ring:
+// tile. QR is 128, or 64 when every sequence has at most 64 rows (the Q tile
+// then takes half the shared memory and the ring gets a third stage). The key
+// tiles of the row tile (64 keys = 64/B cache pages or 64/B window blocks, cache
+// first) are split among the `cs` CTAs of one thread-block cluster. A CTA needs
+// at most ~113 KB of shared memory and 256 TMEM columns, so two CTAs share an SM
+// and hide each other's latencies. Each CTA streams its share through an
+// NS-stage shared-memory ring:
 //
 //   warp 0       TMA producer: page ids (requested with the sequence metadata,
 //                32 at a time) -> cp.async.bulk.tensor loads of the K and V
@@ -28,11 +30,17 @@
 //                over the scores it came from (TMEM columns 0-31 of the S buffer),
 //                where the second MMA reads its A operand.
 //
-// Composition. With cs > 1 the CTAs of the cluster push their unnormalised O
-// rows and (max, sum) into the shared memory of the CTA that owns each row
-// (row r -> CTA r mod cs) with remote stores; after a cluster barrier every
-// owner composes its rows from local shared memory and writes the normalised
-// output. No partial goes to global memory.
+// The MMA always has M = 128: with a 64-row Q tile, A rows 64-127 read whatever
+// shared memory follows the tile. Those rows of S are never used (their softmax
+// threads mask every key, so their P rows are exactly 0 and their O rows stay 0).
+//
+// Composition. With cs > 1 every CTA writes its rows, normalised (O / l, bf16)
+// with their (max, sum), into a staging block per owning CTA (row r -> CTA
+// r mod cs). After one cluster barrier (every CTA done with its ring, which the
+// blocks overlay) each CTA sends block j to CTA j with one shared-to-shared bulk
+// copy; the owner waits on an mbarrier for the cs blocks it receives, composes
+// its rows in log space and writes the output. No partial goes to global
+// memory.
 //
 // Set-up that reads no global memory (mbarriers, TMEM) runs before the
 // grid-dependency wait, so under programmatic dependent launch it overlaps the
@@ -49,50 +57,75 @@ namespace d2f {
 namespace {
 
 constexpr int kSoftWarps = 4;
-constexpr int kSoftThreads = 32 * kSoftWarps;  // one per query row
+constexpr int kSoftThreads = 32 * kSoftWarps;  // one per TMEM lane
 constexpr int kThreads = 64 + kSoftThreads;    // producer + MMA warps + softmax
-constexpr int NS = 2;                          // K/V ring stages
-constexpr int M = kTcRows;                     // 128 query rows per tile
+constexpr int M = kTcRows;                     // UMMA M: 128 rows
 constexpr int N = kTcKeys;                     // 64 keys per tile
 constexpr uint32_t kTmemCols = 256;            // S / P (2 x 64) + O (<= 128)
 constexpr uint32_t kTmemO = 128;               // first TMEM column of O
 constexpr int kMaxCluster = 8;
 constexpr int kBarSetup = 1;                   // named barrier: MMA warp + softmax warps
+constexpr int kSmemTwoPerSm = 115712;          // dynamic bytes that still let 2 CTAs share an SM
 
-template <int D>
+template <int D, int NS, int QR>
 struct Layout {
   static constexpr int kHalves = D / 64;         // 64-element (128-byte) swizzle columns
-  static constexpr int kQHalf = M * 128;         // one 64-wide column block of Q
+  static constexpr int kQHalf = QR * 128;        // one 64-wide column block of Q
   static constexpr int kQBytes = kHalves * kQHalf;
   static constexpr int kKVHalf = N * 128;        // 64 key rows x 128 bytes
   static constexpr int kKBytes = kHalves * kKVHalf;
   static constexpr int kStage = 2 * kKBytes;     // K tile then V tile
-  static constexpr int kChunks = D / 4;          // 16-byte chunks of one fp32 O row
   static constexpr int kQ = 0;
   static constexpr int kRing = kQ + kQBytes;
-  static constexpr int kRecv = kQ;               // pushed O rows land over Q + ring
-  static constexpr int kML = kRing + NS * kStage;  // pushed (max, sum): float2 [8][128]
-  static constexpr int kBars = kML + kMaxCluster * M * 8;
+  static constexpr int kBars = kRing + NS * kStage;
   static constexpr int kBytes = kBars + 256;
-  static constexpr int kAlloc = kBytes + 1024;   // slack for 1024-byte alignment
-  static_assert(kQBytes + NS * kStage >= (M + kMaxCluster) * D * 4,
-                "pushed O rows must fit in the Q + ring area");
+  // 1024 bytes of slack to align the base by hand, unless that would cost the
+  // second CTA per SM; then the kernel checks the base it was given instead.
+  static constexpr int kAlloc =
+      (kBytes + 1024 <= kSmemTwoPerSm || kBytes > kSmemTwoPerSm) ? kBytes + 1024 : kBytes;
+  static constexpr int kCtasPerSm = kAlloc <= kSmemTwoPerSm ? 2 : 1;
+  // Composition blocks (overlay Q and the ring): per owner, LR rows of D bf16
+  // then LR (max, sum) pairs.
+  static constexpr int kRowBytes = 2 * D;
+  __host__ __device__ static constexpr int rows_per_owner(int cs) { return (QR + cs - 1) / cs; }
+  __host__ __device__ static constexpr int block_bytes(int cs) {
+    return (rows_per_owner(cs) * (kRowBytes + 8) + 15) & ~15;
+  }
+  __host__ __device__ static constexpr int staging(int cs) {  // after the receive blocks
+    return (cs * block_bytes(cs) + 127) & ~127;
+  }
+  static_assert(2 * ((QR + kMaxCluster - 1) * (kRowBytes + 8) + 16 * kMaxCluster) + 128 <= kBars,
+                "receive and staging blocks must fit in the Q + ring area");
 };
 
 struct Bars {
-  uint64_t full[NS], empty[NS], s_full[2], p_full[2], pv_done[2], q_full, drain;
+  uint64_t full[4], empty[4], s_full[2], p_full[2], pv_done[2], q_full, drain, recv;
   uint32_t tmem_base;
   int abort_flag;
 };
+static_assert(sizeof(Bars) <= 256, "barrier block");
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 2)
+template <int D, int NS, int QR>
+__global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR>::kCtasPerSm))
     attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_kpool,
                    const __grid_constant__ CUtensorMap tm_vpool,
                    const __grid_constant__ CUtensorMap tm_kwin,
                    const __grid_constant__ CUtensorMap tm_vwin) {
-  using L = Layout<D>;
+  using L = Layout<D, NS, QR>;
+  static_assert(NS >= 2 && NS <= 4, "ring depth");
   extern __shared__ uint8_t smem_raw[];
+  {
+    // The swizzled tiles need a 1024-byte aligned base. Every CTA of the grid
+    // sees the same placement, so a misfit returns from all of them together.
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    uint32_t dyn;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+    if (pad + L::kBytes > dyn) {
+      if (threadIdx.x == 0) set_err(a.err, D2F_ERR_UNSUPPORTED);
+      return;
+    }
+  }
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sb = smem_u32(smem);
@@ -119,8 +152,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     mbar_init(smem_u32(&bars->q_full), kSoftThreads);
     mbar_init(smem_u32(&bars->drain), 1);
+    mbar_init(smem_u32(&bars->recv), 1);
     bars->abort_flag = 0;
-    mbar_fence_init();
+    mbar_fence_init();  // cluster scope: other CTAs complete bytes on `recv`
     tma_prefetch_desc(&tm_kpool);
     tma_prefetch_desc(&tm_vpool);
     tma_prefetch_desc(&tm_kwin);
@@ -150,9 +184,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (!active && tid == 0 && mt == 0 && split == 0 && g == 0) set_err(a.err, D2F_ERR_INVALID_ARG);
   const int G = a.group, B = a.block_size, H = a.num_heads_q;
   const int rows_total = G * n;
-  const int r_begin = mt * M;
+  const int r_begin = mt * QR;
   active = active && r_begin < rows_total;
-  const int nrows = active ? min(M, rows_total - r_begin) : 0;
+  const int nrows = active ? min(QR, rows_total - r_begin) : 0;
   const int Tc = (C + N - 1) / N, Tw = (n + N - 1) / N;
   // Split s takes tiles [s*tps, (s+1)*tps); tps comes from the host's max_ctx and
   // grows here only if a sequence is longer than that hint promised.
@@ -307,26 +341,29 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_wait(smem_u32(&bars->drain), 0, &no_abort, a.err);
     }
   } else if (has_work) {
-    // ======================= softmax (128 threads, one per row) ================
+    // ======================= softmax (128 threads, one per TMEM lane) ==========
     {
       // The Q row into the 128-byte-swizzled K-major layout the MMA reads:
       // 16-byte chunk c of column block h lands at
       //   h*kQHalf + (row/8)*1024 + (row%8)*128 + ((c ^ (row%8)) * 16).
       constexpr int kQc = D / 8;
-      uint4 qv[kQc];
-      const uint4 *src = reinterpret_cast<const uint4 *>(
-          reinterpret_cast<const uint16_t *>(a.q) + ((int64_t)(q0 + r / G) * H + g * G + r % G) * D);
+      if (row < QR) {  // warp-uniform
+        uint4 qv[kQc];
+        const uint4 *src = reinterpret_cast<const uint4 *>(
+            reinterpret_cast<const uint16_t *>(a.q) +
+            ((int64_t)(q0 + r / G) * H + g * G + r % G) * D);
 #pragma unroll
-      for (int c = 0; c < kQc; ++c) qv[c] = row_valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+        for (int c = 0; c < kQc; ++c) qv[c] = row_valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int c = 0; c < kQc; ++c) {
-        const uint32_t dst = sb + L::kQ + (c >> 3) * L::kQHalf + (row >> 3) * 1024 +
-                             (row & 7) * 128 + (((c & 7) ^ (row & 7)) << 4);
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(qv[c].x),
-                     "r"(qv[c].y), "r"(qv[c].z), "r"(qv[c].w)
-                     : "memory");
+        for (int c = 0; c < kQc; ++c) {
+          const uint32_t dst = sb + L::kQ + (c >> 3) * L::kQHalf + (row >> 3) * 1024 +
+                               (row & 7) * 128 + (((c & 7) ^ (row & 7)) << 4);
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(qv[c].x),
+                       "r"(qv[c].y), "r"(qv[c].z), "r"(qv[c].w)
+                       : "memory");
+        }
+        fence_proxy_async_smem();
       }
-      fence_proxy_async_smem();
       mbar_arrive(smem_u32(&bars->q_full));
     }
     const int win_end = row_valid ? ((r / G) / B + 1) * B : 0;
@@ -445,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (tid == 0) D2F_TRACE_MARK(0, 7);
   const bool aborted = *abort_flag != 0;
   if (cs == 1) {
-    if (warp >= 2 && has_work && !aborted) {
+    if (warp >= 2 && has_work && !aborted && __any_sync(0xffffffffu, row_valid)) {
       const int64_t hr = (int64_t)(q0 + r / G) * H + g * G + r % G;
       const float inv = 1.0f / l;
       uint16_t *dst = reinterpret_cast<uint16_t *>(a.out) + hr * D;
@@ -467,85 +504,110 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (row_valid && a.lse_out) a.lse_out[hr] = (m_ref + __log2f(l)) * 0.6931471805599453f;
     }
   } else if (active) {
-    const int LR = (M + cs - 1) / cs;  // receive slots per source CTA (rows a CTA owns)
-    // 1) every CTA of the cluster is done with its Q and ring buffers
-    __syncwarp();
-    cluster_sync();
-    if (tid == 0) D2F_TRACE_MARK(0, 8);
-    // 2) push this CTA's partial rows to their owners: O row -> slot
-    //    [split][row / cs] of CTA row % cs (16-byte chunks XOR-swizzled by the
-    //    local row), (max, sum) -> slot [split][row / cs] of its ML area.
-    if (warp >= 2) {
-      const int owner = row % cs, lr = row / cs;
-      const bool mine = has_work && !aborted;
+    const int LR = L::rows_per_owner(cs);  // rows a CTA owns (at most)
+    const int BS = L::block_bytes(cs);     // one owner's block: LR rows + LR (max, sum)
+    const uint32_t recv = sb + L::kQ;      // [source split][BS], filled by the bulk copies
+    const uint32_t stg = sb + L::staging(cs);  // [owner][BS], this CTA's rows
+    const uint32_t recv_bar = smem_u32(&bars->recv);
+    // 1) stage this CTA's rows: local row -> owner row % cs, slot row / cs; the
+    //    16-byte chunks of a row are XOR-swizzled by (row % 8).
+    if (warp >= 2 && __any_sync(0xffffffffu, row_valid)) {
+      const int owner = row % cs, lr = row / cs, key = row & 7;
+      const uint32_t blk = stg + owner * BS;
+      const bool mine = has_work && !aborted;  // CTA-uniform
+      const bool keep = mine && row_valid && l > 0.f;
       if (mine) {
+        const float inv = keep ? 1.0f / l : 0.f;
 #pragma unroll
         for (int ch = 0; ch < D / 32; ++ch) {
           uint32_t o[32];
           tmem_ld32(lane_addr + kTmemO + ch * 32, o);
-          if (row_valid) {
+          if (keep) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int c = ch * 8 + j;
-              const uint32_t local = sb + L::kRecv + (split * LR + lr) * (D * 4) +
-                                     ((c ^ (lr % L::kChunks)) << 4);
-              dsmem_st_u4(dsmem_addr(local, owner), o[4 * j], o[4 * j + 1], o[4 * j + 2],
-                          o[4 * j + 3]);
+            for (int j = 0; j < 4; ++j) {
+              const int c = ch * 4 + j;  // 8 bf16 per 16-byte chunk
+              const uint32_t dst = blk + lr * L::kRowBytes + ((c ^ key) << 4);
+              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
+                           "r"(pack_bf16x2(__uint_as_float(o[8 * j]) * inv,
+                                           __uint_as_float(o[8 * j + 1]) * inv)),
+                           "r"(pack_bf16x2(__uint_as_float(o[8 * j + 2]) * inv,
+                                           __uint_as_float(o[8 * j + 3]) * inv)),
+                           "r"(pack_bf16x2(__uint_as_float(o[8 * j + 4]) * inv,
+                                           __uint_as_float(o[8 * j + 5]) * inv)),
+                           "r"(pack_bf16x2(__uint_as_float(o[8 * j + 6]) * inv,
+                                           __uint_as_float(o[8 * j + 7]) * inv))
+                           : "memory");
             }
           }
         }
       }
       if (row_valid) {
-        const uint32_t local = sb + L::kML + (split * LR + lr) * 8;
-        dsmem_st_f2(dsmem_addr(local, owner), mine ? m_ref : -INFINITY, mine ? l : 0.f);
+        const float mx = keep ? m_ref : -INFINITY, sm = keep ? l : 0.f;
+        asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(blk + LR * L::kRowBytes + lr * 8),
+                     "f"(mx), "f"(sm)
+                     : "memory");
       }
+      fence_proxy_async_smem();  // the bulk copies read these blocks
     }
+    // 2) each owner expects cs blocks; the cluster barrier publishes the staged
+    //    blocks and frees every receive area (each CTA is past its ring).
+    if (tid == 0) mbar_arrive_expect_tx(recv_bar, (uint32_t)(cs * BS));
     __syncwarp();
     cluster_sync();
-    if (tid == 0) D2F_TRACE_MARK(0, 9);
-    // 3) compose the rows this CTA owns from local shared memory: one warp per
-    //    row, lane c holds 16-byte chunk c.
+    if (tid == 0) D2F_TRACE_MARK(0, 8);
+    // 3) block j of this CTA -> receive slot [split] of CTA j
+    if (warp == 0 && lane < cs)
+      bulk_copy_to_cluster(dsmem_addr(recv + split * BS, lane), stg + lane * BS, BS,
+                           dsmem_addr(recv_bar, lane));
+    // 4) wait for the cs blocks this CTA owns, then arrive on the closing
+    //    cluster barrier: once every CTA has arrived, every copy has landed and
+    //    no staging block is still being read.
+    bool got = true;
+    if (warp >= 2) got = __all_sync(0xffffffffu, mbar_wait(recv_bar, 0, abort_flag, a.err));
+    if (tid == 64) D2F_TRACE_MARK(0, 9);
+    __syncwarp();
+    cluster_arrive();
+    // 5) compose the rows this CTA owns: one warp per row, lane c holds 4 columns.
     if (warp >= 2) {
-      for (int lr = warp - 2; lr * cs + split < nrows; lr += kSoftWarps) {
-        const int r2 = r_begin + lr * cs + split;
+      for (int lr = warp - 2; got && lr * cs + split < nrows; lr += kSoftWarps) {
+        const int lrow = lr * cs + split;  // local row
+        const int r2 = r_begin + lrow, key = lrow & 7;
         float2 ml = make_float2(-INFINITY, 0.f);
-        if (lane < cs) ml = *reinterpret_cast<const float2 *>(smem + L::kML + (lane * LR + lr) * 8);
+        if (lane < cs)
+          ml = *reinterpret_cast<const float2 *>(smem + lane * BS + LR * L::kRowBytes + lr * 8);
         float mx = ml.x;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        const float w = (lane < cs && ml.y > 0.f) ? fast_exp2(ml.x - mx) : 0.f;
-        float ls = w * ml.y;
+        // weight of a normalised part: 2^(m_j - M) * l_j
+        const float w = (lane < cs && ml.y > 0.f) ? fast_exp2(ml.x - mx) * ml.y : 0.f;
+        float ws = w;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-        float4 v[kMaxCluster];
-        float wj[kMaxCluster];
-#pragma unroll
-        for (int j = 0; j < kMaxCluster; ++j) {
-          wj[j] = __shfl_sync(0xffffffffu, w, j);
-          v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (j < cs && wj[j] > 0.f && lane < L::kChunks)
-            v[j] = *reinterpret_cast<const float4 *>(
-                smem + L::kRecv + (j * LR + lr) * (D * 4) + ((lane ^ (lr % L::kChunks)) << 4));
-        }
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t off = lr * L::kRowBytes + ((((lane >> 1) ^ key)) << 4) + (lane & 1) * 8;
 #pragma unroll
         for (int j = 0; j < kMaxCluster; ++j) {
-          acc.x = fmaf(wj[j], v[j].x, acc.x);
-          acc.y = fmaf(wj[j], v[j].y, acc.y);
-          acc.z = fmaf(wj[j], v[j].z, acc.z);
-          acc.w = fmaf(wj[j], v[j].w, acc.w);
+          const float wj = __shfl_sync(0xffffffffu, w, j);
+          if (j < cs && wj > 0.f && lane < D / 4) {
+            const uint2 v = *reinterpret_cast<const uint2 *>(smem + j * BS + off);
+            acc[0] = fmaf(wj, bf16_bits_to_float(v.x & 0xffffu), acc[0]);
+            acc[1] = fmaf(wj, bf16_bits_to_float(v.x >> 16), acc[1]);
+            acc[2] = fmaf(wj, bf16_bits_to_float(v.y & 0xffffu), acc[2]);
+            acc[3] = fmaf(wj, bf16_bits_to_float(v.y >> 16), acc[3]);
+          }
         }
-        if (lane < L::kChunks && !aborted) {
-          const float inv = 1.0f / ls;
+        if (lane < D / 4 && !aborted) {
+          const float inv = ws > 0.f ? 1.0f / ws : 0.f;
           const int64_t hr2 = (int64_t)(q0 + r2 / G) * H + g * G + r2 % G;
-          const uint2 packed = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv),
-                                          pack_bf16x2(acc.z * inv, acc.w * inv));
           *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(a.out) + hr2 * D + lane * 4) =
-              packed;
-          if (lane == 0 && a.lse_out) a.lse_out[hr2] = (mx + __log2f(ls)) * 0.6931471805599453f;
+              make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv),
+                         pack_bf16x2(acc[2] * inv, acc[3] * inv));
+          if (lane == 0 && a.lse_out) a.lse_out[hr2] = (mx + __log2f(ws)) * 0.6931471805599453f;
         }
       }
     }
+    __syncwarp();
+    cluster_wait();
   }
 
   // ---- teardown ---------------------------------------------------------------
@@ -590,8 +652,8 @@ bool encode(EncodeTiledFn fn, CUtensorMap *map, const void *base, int rank, cons
 }
 
 // Function attributes (shared-memory opt-in and carveout) are per device; set
-// them once per device.
-template <int D>
+// them once per device and kernel variant.
+template <int D, int NS, int QR>
 cudaError_t ensure_attrs() {
   static std::mutex mu;
   static bool done[64] = {};
@@ -600,16 +662,16 @@ cudaError_t ensure_attrs() {
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Layout<D>::kAlloc);
+  e = cudaFuncSetAttribute(attn_tc_kernel<D, NS, QR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Layout<D, NS, QR>::kAlloc);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(attn_tc_kernel<D, NS, QR>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return e;
 }
 
-template <int D>
+template <int D, int NS, int QR>
 cudaError_t launch_d(const AttnArgs &a, cudaStream_t s, char *why, size_t why_len) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) {
@@ -632,13 +694,13 @@ cudaError_t launch_d(const AttnArgs &a, cudaStream_t s, char *why, size_t why_le
     snprintf(why, why_len, "cuTensorMapEncodeTiled rejected a K/V tensor (alignment or size)");
     return cudaErrorInvalidValue;
   }
-  cudaError_t e = ensure_attrs<D>();
+  cudaError_t e = ensure_attrs<D, NS, QR>();
   if (e != cudaSuccess) return e;
   const int cs = a.num_splits;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cs, a.m_tiles, a.batch * a.num_heads_kv);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Layout<D>::kAlloc;
+  cfg.dynamicSmemBytes = Layout<D, NS, QR>::kAlloc;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -649,7 +711,7 @@ cudaError_t launch_d(const AttnArgs &a, cudaStream_t s, char *why, size_t why_le
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_enabled() ? 2 : 1;
-  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<D>, a, kp, vp, kw, vw);
+  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<D, NS, QR>, a, kp, vp, kw, vw);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -662,8 +724,16 @@ cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t s, char *why, size_t 
     snprintf(why, why_len, "tensor-core path takes 1..%d splits", kMaxCluster);
     return cudaErrorInvalidValue;
   }
-  if (a.head_dim == 128) return launch_d<128>(a, s, why, why_len);
-  if (a.head_dim == 64) return launch_d<64>(a, s, why, why_len);
+  // 64-row tiles: three ring stages in the shared memory half a Q tile frees.
+  const bool half = a.tc_rows == 64;
+  if (!half && a.tc_rows != kTcRows) {
+    snprintf(why, why_len, "tensor-core path takes 64- or 128-row tiles");
+    return cudaErrorInvalidValue;
+  }
+  if (a.head_dim == 128)
+    return half ? launch_d<128, 3, 64>(a, s, why, why_len) : launch_d<128, 2, 128>(a, s, why, why_len);
+  if (a.head_dim == 64)
+    return half ? launch_d<64, 3, 64>(a, s, why, why_len) : launch_d<64, 2, 128>(a, s, why, why_len);
   snprintf(why, why_len, "tensor-core path supports head_dim 64 or 128");
   return cudaErrorInvalidValue;
 }

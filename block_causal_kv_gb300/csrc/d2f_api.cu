@@ -59,6 +59,7 @@ int cuda_fail(cudaError_t e, const char *what) {
 struct AttnPlan {
   bool tc;        // tensor-core path
   int m_tiles;
+  int rows;       // rows per tile: 64 or 128 on the tensor-core path
   int splits;
   int tiles_per_split;
   int n_counters;
@@ -68,6 +69,14 @@ struct AttnPlan {
 bool force_simt() {
   const char *e = getenv("D2F_ATTN_PATH");
   return e && strcmp(e, "simt") == 0;
+}
+
+// D2F_TC_ROWS=128 keeps the tensor-core path on 128-row tiles even where every
+// sequence fits a 64-row tile (for comparing the two; results agree within
+// rounding).
+bool force_full_rows() {
+  const char *e = getenv("D2F_TC_ROWS");
+  return e && strcmp(e, "128") == 0;
 }
 
 int plan_attn(int batch, int total_q, int max_q, int max_ctx, int Hq, int Hkv, int D, int B,
@@ -94,10 +103,13 @@ int plan_attn(int batch, int total_q, int max_q, int max_ctx, int Hq, int Hkv, i
                   "and 32, 64, 128 (CUDA-core path)", D);
     if (B > 256) return fail(D2F_ERR_UNSUPPORTED, "block_size %d > 256", B);
   }
-  const int rows = tc ? kTcRows : kSimtRows;
-  const int keys = tc ? kTcKeys : kSimtKeys;
   const int G = Hq / Hkv;
+  // tensor-core tiles hold 64 rows when every sequence's G * max_q rows fit
+  const int rows = !tc ? kSimtRows
+                       : ((long long)G * max_q <= 64 && !force_full_rows() ? 64 : kTcRows);
+  const int keys = tc ? kTcKeys : kSimtKeys;
   p->tc = tc;
+  p->rows = rows;
   p->m_tiles = max(1, cdiv((long long)G * max_q, rows));
   const int t_max = max(1, cdiv(max_ctx, keys) + cdiv(max_q, keys));
   int splits = num_splits;
@@ -106,11 +118,13 @@ int plan_attn(int batch, int total_q, int max_q, int max_ctx, int Hq, int Hkv, i
     // The splits of one row tile form a thread-block cluster (at most 8 CTAs)
     // and compose their partials in distributed shared memory: no workspace.
     if (splits == 0) {
-      // two CTAs fit on an SM: fill the 2 x SM slots with power-of-two clusters
-      const int slots = 2 * num_sms_current_device();
-      splits = 1;
-      while (splits * 2 <= kTcMaxSplits && splits * 2 <= t_max && base * splits * 2 <= slots)
-        splits *= 2;
+      // Two CTAs fit on an SM: take as many splits as the 2 x SM slots hold,
+      // then the fewest that keep the longest split's tile count.
+      const long long slots = 2LL * num_sms_current_device();
+      long long most = slots / base;
+      if (most > min(kTcMaxSplits, t_max)) most = min(kTcMaxSplits, t_max);
+      if (most < 1) most = 1;
+      splits = cdiv(t_max, cdiv(t_max, most));
     }
     p->splits = min(splits, kTcMaxSplits);
     p->tiles_per_split = cdiv(t_max, p->splits);
@@ -293,6 +307,7 @@ int d2f_block_attn(const void *q, const void *k_win, const void *v_win, const vo
   a.num_splits = p.splits;
   a.tiles_per_split = p.tiles_per_split;
   a.m_tiles = p.m_tiles;
+  a.tc_rows = p.rows;
   a.counters = reinterpret_cast<int32_t *>(workspace);
   a.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) + p.off_ml);
   a.ws_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + p.off_o);

@@ -40,6 +40,7 @@ struct AttnArgs {
   int num_splits;        // split count requested (each sequence uses <= this many)
   int tiles_per_split;   // tensor-core path: key tiles per split from the host's max_ctx
   int m_tiles;           // grid.x: row tiles per (sequence, KV head)
+  int tc_rows;           // tensor-core path: rows a tile holds (64 or 128)
   int32_t *counters;     // [batch * Hkv * m_tiles] merge arrival counters (zero at rest)
   float2 *ws_ml;         // [num_splits][total_q * Hq] (max in log2 units, sum)
   float *ws_o;           // [num_splits][total_q * Hq][head_dim] unnormalised partial output
@@ -228,6 +229,25 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
+}
+// The two halves of cluster_sync(), for work placed between them.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// 1-D bulk copy from this CTA's shared memory into another CTA of the cluster
+// (dst and bar are shared::cluster addresses in the destination CTA; 16-byte
+// aligned addresses, size a multiple of 16). Completion is counted on the
+// destination's mbarrier.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                     uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst),
+      "r"(src), "r"(bytes), "r"(bar)
+      : "memory");
 }
 // Address of the same shared variable in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t dsmem_addr(uint32_t local, uint32_t rank) {

@@ -43,7 +43,7 @@ SMALL = ["tiny", "llada", "ragged", "dream", "long_b8", "long_b16", "long_b32"]
 
 
 @pytest.mark.parametrize("name", SMALL)
-@pytest.mark.parametrize("splits", [0, 1, 3])
+@pytest.mark.parametrize("splits", [0, 1, 3, 6, 8])
 def test_small_workloads(name, splits):
     dev = device()
     w = synth.workload("tiny") if name == "tiny" else synth.small(name)
@@ -51,6 +51,21 @@ def test_small_workloads(name, splits):
     out, lse = _run(p, dev, splits)
     ref, ref_lse = _ref(p)
     check_attention(out, lse, ref, ref_lse, w.dtype, "%s/s%d" % (name, splits))
+
+
+@pytest.mark.parametrize("name", ["llada", "ragged", "long_b8", "long_b16"])
+@pytest.mark.parametrize("splits", [0, 1, 5])
+def test_full_row_tiles_where_half_tiles_fit(name, splits, monkeypatch):
+    """Workloads with at most 64 rows per sequence run on 64-row tiles (three
+    ring stages); D2F_TC_ROWS=128 forces the 128-row tile. Both agree with the
+    oracle."""
+    dev = device()
+    monkeypatch.setenv("D2F_TC_ROWS", "128")
+    p = synth.make_problem(synth.small(name))
+    assert p.max_q_per_seq * p.w.num_heads_q // p.w.num_heads_kv <= 64
+    out, lse = _run(p, dev, splits)
+    ref, ref_lse = _ref(p)
+    check_attention(out, lse, ref, ref_lse, torch.bfloat16, "rows128/%s/s%d" % (name, splits))
 
 
 @pytest.mark.parametrize("name", ["llada", "ragged", "dream", "long_b16"])
