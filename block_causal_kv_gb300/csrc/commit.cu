@@ -8,9 +8,10 @@
 //
 // Grid (slices, rows): CTA (s, r) reduces vocabulary slice s of row r to
 // (max, first argmax, sum of exp(l - max)). On the staged path one thread issues
-// a single 1-D bulk copy (TMA) of the whole slice into shared memory, so every
-// byte of the slice is in flight at once, and the CTA then folds it from shared
-// memory; the direct path (unaligned rows) folds 128-bit or scalar global loads.
+// the whole slice as up to four 1-D bulk copies (TMA) into shared memory, so every
+// byte of the slice is in flight at once, and the CTA folds each piece from
+// shared memory as soon as it lands; the direct path (unaligned rows) folds
+// 128-bit or scalar global loads.
 // Every CTA of a window block then bumps one arrival counter; the last one to
 // arrive composes the slices of all rows of the block and decides the block with
 // one warp (lane = row). The decision's metadata (sequence, tau, phase) is
@@ -25,6 +26,8 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
+constexpr int kParts = 4;            // staged slice: bulk copies folded as each lands
+constexpr int kMinPartVecs = 256;    // ... of at least 4 KB each
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct RowState {
@@ -158,7 +161,7 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
   __shared__ RowState red[kThreads / 32];
   __shared__ float conf_s[32];
   __shared__ int arg_s[32];
-  __shared__ uint64_t bar;
+  __shared__ uint64_t bar[kParts];
   __shared__ int is_last;
   __shared__ int abort_flag;
 
@@ -172,7 +175,7 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
   if (tid == 0) D2F_TRACE_MARK(1, 0);
   if (PATH == 2 && tid == 0) {  // set-up that reads no global memory
     abort_flag = 0;
-    mbar_init(smem_u32(&bar), 1);
+    for (int i = 0; i < kParts; ++i) mbar_init(smem_u32(&bar[i]), 1);
     mbar_fence_init();
   }
   grid_dependency_wait();  // logits / state may come from the previous kernel
@@ -214,23 +217,37 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
     int v_tail = v0;  // first index left for the scalar loop
 
     if (PATH == 2) {
-      // Bulk-staged slice: whole 16-byte vectors [v0, v0 + nvec*N).
+      // Bulk-staged slice: whole 16-byte vectors [v0, v0 + nvec*N), copied in up
+      // to kParts pieces with one mbarrier each, so folding the first piece
+      // overlaps the transfer of the rest. Each thread still visits its indices
+      // in increasing order (first-argmax rule).
       const int nvec = (v1 - v0) / N;
-      __syncthreads();  // the mbarrier is initialised
+      const int parts = max(1, min(kParts, nvec / kMinPartVecs));
+      const int per = (nvec + parts - 1) / parts;
+      __syncthreads();  // the mbarriers are initialised
       if (row_ok && nvec > 0) {
         if (tid == 0) {
-          mbar_arrive_expect_tx(smem_u32(&bar), nvec * 16u);
-          bulk_load(smem_u32(stage), row + (int64_t)v0 * (DT == D2F_BF16 ? 2 : 4), nvec * 16u,
-                    smem_u32(&bar));
+          for (int i = 0; i < parts; ++i) {
+            const int k0 = i * per, k1 = min(nvec, k0 + per);
+            if (k0 >= k1) break;
+            mbar_arrive_expect_tx(smem_u32(&bar[i]), (k1 - k0) * 16u);
+            bulk_load(smem_u32(stage) + k0 * 16u,
+                      row + (int64_t)(v0 + k0 * N) * (DT == D2F_BF16 ? 2 : 4), (k1 - k0) * 16u,
+                      smem_u32(&bar[i]));
+          }
         }
         if (tid == 0) D2F_TRACE_MARK(1, 2);
-        mbar_wait(smem_u32(&bar), 0, &abort_flag, a.err);
-        if (tid == 0) D2F_TRACE_MARK(1, 3);
         const uint4 *sv = reinterpret_cast<const uint4 *>(stage);
-        for (int k = tid; k < nvec; k += kThreads) {
-          float x[N];
-          unpack<DT>(sv[k], x);
-          fold<N>(x, v0 + k * N, m, idx, acc);
+        for (int i = 0; i < parts; ++i) {
+          const int k0 = i * per, k1 = min(nvec, k0 + per);
+          if (k0 >= k1) break;
+          if (!mbar_wait(smem_u32(&bar[i]), 0, &abort_flag, a.err)) break;
+          if (tid == 0 && i == 0) D2F_TRACE_MARK(1, 3);
+          for (int k = k0 + tid; k < k1; k += kThreads) {
+            float x[N];
+            unpack<DT>(sv[k], x);
+            fold<N>(x, v0 + k * N, m, idx, acc);
+          }
         }
         v_tail = v0 + nvec * N;
       }
