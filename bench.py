@@ -418,16 +418,8 @@ def run_ours(args, world, rank, local):
                 append(s)
     stream.synchronize()
 
-    try:
-        ev_kw = dict(enable_timing=True, external=True)
-        torch.cuda.Event(**ev_kw)
-        have_ext = True
-    except TypeError:
-        have_ext = False
-
-    def capture(indices, with_events):
+    def capture(indices):
         g = torch.cuda.CUDAGraph()
-        evs = []
         with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
             if len(indices) == n_sets:
                 reset_all()
@@ -435,25 +427,14 @@ def run_ours(args, world, rank, local):
                 s = sets[i]
                 if len(indices) != n_sets:
                     reset(s)
-                e = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)] \
-                    if with_events else None
-                if e:
-                    e[0].record()
                 attn(s)
-                if e:
-                    e[1].record()
                 commit(s)
-                if e:
-                    e[2].record()
                 if appends:
                     append(s)
-                if e:
-                    evs.append(e)
-        return g, evs
+        return g
 
-    g_all, _ = capture(range(n_sets), False)
-    singles = [capture([i], False)[0] for i in range(n_sets)]
-    g_ev, evs_all = capture(range(n_sets), have_ext)
+    g_all = capture(range(n_sets))
+    singles = [capture([i]) for i in range(n_sets)]
 
     K, W = args.steps, args.warmup
     full, rest = divmod(K, n_sets)
@@ -490,34 +471,32 @@ def run_ours(args, world, rank, local):
     if int(err.item()) != 0:
         raise RuntimeError("device error word %d after the timed region" % int(err.item()))
 
-    # Per-kernel durations: the same graph with CUDA events between the kernels
-    # (events between kernels stop one kernel's launch from overlapping the
-    # previous one's tail, so this pass is kept out of the headline timing).
-    attn_us, commit_us = [], []
-    if have_ext:
-        with torch.cuda.stream(stream):
-            for _ in range(max(3, min(full, 20))):
-                g_ev.replay()
-        torch.cuda.synchronize()
-        for e in evs_all:
-            attn_us.append(e[0].elapsed_time(e[1]) * 1000.0)
-            commit_us.append(e[1].elapsed_time(e[2]) * 1000.0)
-    else:
-        # fall back: time attention-only and commit-only graphs over the same sets
-        for which, acc in (("attn", attn_us), ("commit", commit_us)):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+    # Per-kernel durations: a graph of one kernel only, launched back to back over
+    # the same rotating input sets (programmatic dependent launch between
+    # consecutive launches, as in the step), timed with CUDA events around whole
+    # replays: the average launch duration including the gap to the next launch.
+    # (Events between kernels would add their own latency to every bracket.)
+    per_kernel = {}
+    for which, fn in (("attn", attn), ("commit", commit)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+            if which == "commit":
                 reset_all()
-                for i in range(n_sets):
-                    (attn if which == "attn" else commit)(sets[i])
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(stream):
-                a.record(stream)
-                for _ in range(20):
-                    g.replay()
-                b.record(stream)
-            torch.cuda.synchronize()
-            acc.append(a.elapsed_time(b) * 1000.0 / (20 * n_sets))
+            for i in range(n_sets):
+                fn(sets[i])
+        reps = max(3, min(50, 20000 // n_sets))
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for _ in range(reps):
+                g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        per_kernel[which] = a.elapsed_time(b) * 1000.0 / (reps * n_sets)
+    attn_us, commit_us = [per_kernel["attn"]], [per_kernel["commit"]]
 
     steps_total = K * world
     value = steps_total / (elapsed_ms / 1000.0)
@@ -536,7 +515,10 @@ def run_ours(args, world, rank, local):
                              "frac": commit_b / t_commit / 1e3 / hbm}
     dom = "block_attn" if (t_attn or 0) >= (t_commit or 0) else "commit"
     dk = kernels.get(dom, {})
-    roofline = {"bound": "hbm", "kernel": dom, "achieved": dk.get("GB/s"), "peak": hbm,
+    roofline = {"bound": "hbm", "kernel": dom,
+                "duration": "average launch of a %s-only CUDA graph over the rotating input "
+                            "sets, CUDA events around whole replays" % dom,
+                "achieved": dk.get("GB/s"), "peak": hbm,
                 "unit": "GB/s", "frac": dk.get("frac"), "peak_kind": peak_kind,
                 "traffic": recorded_traffic("attn" if dom == "block_attn" else "commit", w.name)}
 

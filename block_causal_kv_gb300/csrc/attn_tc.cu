@@ -319,6 +319,7 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR>::kCtasPerSm))
         }
         tc_fence_after();
         if (u == 0) D2F_TRACE_MARK(0, 10);
+        if (u == T - 1) D2F_TRACE_MARK(0, 3);
         // S_u overwrites the S/P buffer that P_{u-2} occupied: P.V_{u-2} was issued
         // before this (MMAs of one thread execute in order).
         const uint32_t k_base = sb + L::kRing + stage * L::kStage;
@@ -374,8 +375,10 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR>::kCtasPerSm))
       ok = mbar_wait(smem_u32(&bars->s_full[u & 1]), (u >> 1) & 1, abort_flag, a.err);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      if (tid == 64 && u == 0) D2F_TRACE_MARK(0, 4);
-      if (tid == 64 && u == T - 1) D2F_TRACE_MARK(0, 5);
+      if (tid == 128 && u == 0) D2F_TRACE_MARK(0, 4);
+      if (tid == 128 && u == 1) D2F_TRACE_MARK(0, 14);
+      if (tid == 128 && u == 2) D2F_TRACE_MARK(0, 15);
+      if (tid == 128 && u == T - 1) D2F_TRACE_MARK(0, 5);
       uint32_t sv_lo[32], sv_hi[32];
       const uint32_t s_addr = lane_addr + (u & 1) * N;
       tmem_ld32(s_addr, sv_lo);
@@ -467,7 +470,8 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR>::kCtasPerSm))
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&bars->p_full[u & 1]));
-      if (tid == 64 && u == T - 1) D2F_TRACE_MARK(0, 6);
+      if (tid == 128 && u == 0) D2F_TRACE_MARK(0, 13);
+      if (tid == 128 && u == T - 1) D2F_TRACE_MARK(0, 6);
     }
     if (ok) {  // the last P.V product
       ok = mbar_wait(smem_u32(&bars->pv_done[(T - 1) & 1]), ((T - 1) >> 1) & 1, abort_flag, a.err);
@@ -481,6 +485,7 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR>::kCtasPerSm))
   __syncthreads();  // every role is done; Q and the ring are free
   if (tid == 0) D2F_TRACE_MARK(0, 7);
   const bool aborted = *abort_flag != 0;
+  bool tmem_freed = false;
   if (cs == 1) {
     if (warp >= 2 && has_work && !aborted && __any_sync(0xffffffffu, row_valid)) {
       const int64_t hr = (int64_t)(q0 + r / G) * H + g * G + r % G;
@@ -553,8 +558,14 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR>::kCtasPerSm))
     //    blocks and frees every receive area (each CTA is past its ring).
     if (tid == 0) mbar_arrive_expect_tx(recv_bar, (uint32_t)(cs * BS));
     __syncwarp();
+    tc_fence_before();
     cluster_sync();
     if (tid == 0) D2F_TRACE_MARK(0, 8);
+    if (warp == 1) {  // every O row is staged: TMEM is free for the next grid's CTAs
+      tc_fence_after();
+      tmem_dealloc(bars->tmem_base, kTmemCols);
+      tmem_freed = true;
+    }
     // 3) block j of this CTA -> receive slot [split] of CTA j
     if (warp == 0 && lane < cs)
       bulk_copy_to_cluster(dsmem_addr(recv + split * BS, lane), stg + lane * BS, BS,
@@ -567,45 +578,70 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR>::kCtasPerSm))
     if (tid == 64) D2F_TRACE_MARK(0, 9);
     __syncwarp();
     cluster_arrive();
-    // 5) compose the rows this CTA owns: one warp per row, lane c holds 4 columns.
+    // 5) compose the rows this CTA owns: half a warp per row, lane c of the half
+    //    holds columns [c * D/16, (c + 1) * D/16).
     if (warp >= 2) {
-      for (int lr = warp - 2; got && lr * cs + split < nrows; lr += kSoftWarps) {
-        const int lrow = lr * cs + split;  // local row
-        const int r2 = r_begin + lrow, key = lrow & 7;
+      constexpr int kCols = D / 16;
+      const int hw = lane >> 4, sub = lane & 15;
+      for (int lr0 = (warp - 2) * 2; got && lr0 * cs + split < nrows; lr0 += 2 * kSoftWarps) {
+        const int lr = lr0 + hw;
+        const int lrow = lr * cs + split;  // local row of this half-warp
+        const bool valid = lrow < nrows;
+        const int key = lrow & 7;
         float2 ml = make_float2(-INFINITY, 0.f);
-        if (lane < cs)
-          ml = *reinterpret_cast<const float2 *>(smem + lane * BS + LR * L::kRowBytes + lr * 8);
+        if (valid && sub < cs)
+          ml = *reinterpret_cast<const float2 *>(smem + sub * BS + LR * L::kRowBytes + lr * 8);
         float mx = ml.x;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         // weight of a normalised part: 2^(m_j - M) * l_j
-        const float w = (lane < cs && ml.y > 0.f) ? fast_exp2(ml.x - mx) * ml.y : 0.f;
+        const float w = (sub < cs && ml.y > 0.f) ? fast_exp2(ml.x - mx) * ml.y : 0.f;
         float ws = w;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint32_t off = lr * L::kRowBytes + ((((lane >> 1) ^ key)) << 4) + (lane & 1) * 8;
+        for (int o = 8; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+        float acc[kCols];
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) acc[c] = 0.f;
+        const uint32_t off = lr * L::kRowBytes + (D == 128 ? ((sub ^ key) << 4)
+                                                            : (((sub >> 1) ^ key) << 4) + (sub & 1) * 8);
 #pragma unroll
         for (int j = 0; j < kMaxCluster; ++j) {
-          const float wj = __shfl_sync(0xffffffffu, w, j);
-          if (j < cs && wj > 0.f && lane < D / 4) {
-            const uint2 v = *reinterpret_cast<const uint2 *>(smem + j * BS + off);
-            acc[0] = fmaf(wj, bf16_bits_to_float(v.x & 0xffffu), acc[0]);
-            acc[1] = fmaf(wj, bf16_bits_to_float(v.x >> 16), acc[1]);
-            acc[2] = fmaf(wj, bf16_bits_to_float(v.y & 0xffffu), acc[2]);
-            acc[3] = fmaf(wj, bf16_bits_to_float(v.y >> 16), acc[3]);
+          const float wj = __shfl_sync(0xffffffffu, w, (hw << 4) + j);
+          if (j < cs && wj > 0.f) {
+            uint32_t v[kCols / 2];
+            if (D == 128) {
+              const uint4 q = *reinterpret_cast<const uint4 *>(smem + j * BS + off);
+              v[0] = q.x; v[1] = q.y; v[2 % (kCols / 2)] = q.z; v[3 % (kCols / 2)] = q.w;
+            } else {
+              const uint2 q = *reinterpret_cast<const uint2 *>(smem + j * BS + off);
+              v[0] = q.x; v[1 % (kCols / 2)] = q.y;
+            }
+#pragma unroll
+            for (int c = 0; c < kCols / 2; ++c) {
+              acc[2 * c] = fmaf(wj, bf16_bits_to_float(v[c] & 0xffffu), acc[2 * c]);
+              acc[2 * c + 1] = fmaf(wj, bf16_bits_to_float(v[c] >> 16), acc[2 * c + 1]);
+            }
           }
         }
-        if (lane < D / 4 && !aborted) {
+        if (valid && !aborted) {
           const float inv = ws > 0.f ? 1.0f / ws : 0.f;
+          const int r2 = r_begin + lrow;
           const int64_t hr2 = (int64_t)(q0 + r2 / G) * H + g * G + r2 % G;
-          *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(a.out) + hr2 * D + lane * 4) =
-              make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv),
-                         pack_bf16x2(acc[2] * inv, acc[3] * inv));
-          if (lane == 0 && a.lse_out) a.lse_out[hr2] = (mx + __log2f(ws)) * 0.6931471805599453f;
+          uint32_t pk[kCols / 2];
+#pragma unroll
+          for (int c = 0; c < kCols / 2; ++c)
+            pk[c] = pack_bf16x2(acc[2 * c] * inv, acc[2 * c + 1] * inv);
+          uint16_t *dst = reinterpret_cast<uint16_t *>(a.out) + hr2 * D + sub * kCols;
+          if (D == 128)
+            *reinterpret_cast<uint4 *>(dst) =
+                make_uint4(pk[0], pk[1], pk[2 % (kCols / 2)], pk[3 % (kCols / 2)]);
+          else
+            *reinterpret_cast<uint2 *>(dst) = make_uint2(pk[0], pk[1 % (kCols / 2)]);
+          if (sub == 0 && a.lse_out) a.lse_out[hr2] = (mx + __log2f(ws)) * 0.6931471805599453f;
         }
       }
     }
+    if (tid == 64) D2F_TRACE_MARK(0, 12);
     __syncwarp();
     cluster_wait();
   }
@@ -615,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR>::kCtasPerSm))
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(bars->tmem_base, kTmemCols);
+  if (warp == 1 && !tmem_freed) tmem_dealloc(bars->tmem_base, kTmemCols);
   if (tid == 0) D2F_TRACE_MARK(0, 11);
 }
 
