@@ -166,6 +166,27 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR>::kCtasPerSm))
     tmem_relinquish();
   }
 
+  // L2 prefetch of this split's first cached pages while the previous kernel in
+  // the stream finishes. The ids and the context length read here are hints only
+  // (L2-only loads, nothing cached in L1; ids clamped to the pool): if the
+  // previous kernel changes them, a prefetch is wasted, and every value the
+  // attention uses is read again after the dependency wait. L2 is the point of
+  // coherence, so a prefetched line never hides a later write.
+  if (warp == 0 && a.page_table != nullptr) {
+    const int ppt0 = N / a.block_size;
+    const int lp = split * a.tiles_per_split * ppt0 + lane;
+    const int hint_c = __ldcg(a.ctx_len + b);
+    const int pg = lp < a.max_pages_per_seq
+                       ? __ldcg(a.page_table + (int64_t)b * a.max_pages_per_seq + lp) : -1;
+    if (lp * a.block_size < hint_c && lp < (split + 1) * a.tiles_per_split * ppt0 && pg >= 0 &&
+        pg < a.num_pages) {
+      const uint32_t page_bytes = (uint32_t)a.block_size * D * 2;
+      const int64_t off = ((int64_t)pg * a.num_heads_kv + g) * page_bytes;
+      prefetch_l2(static_cast<const char *>(a.k_pool) + off, page_bytes);
+      prefetch_l2(static_cast<const char *>(a.v_pool) + off, page_bytes);
+    }
+  }
+
   grid_dependency_wait();  // inputs may come from the previous kernel in the stream
   if (tid == 0) D2F_TRACE_MARK(0, 1);
 
@@ -577,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR>::kCtasPerSm))
     if (warp >= 2) got = __all_sync(0xffffffffu, mbar_wait(recv_bar, 0, abort_flag, a.err));
     if (tid == 64) D2F_TRACE_MARK(0, 9);
     __syncwarp();
-    cluster_arrive();
+    cluster_arrive_relaxed();
     // 5) compose the rows this CTA owns: half a warp per row, lane c of the half
     //    holds columns [c * D/16, (c + 1) * D/16).
     if (warp >= 2) {

@@ -178,6 +178,10 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
     for (int i = 0; i < kParts; ++i) mbar_init(smem_u32(&bar[i]), 1);
     mbar_fence_init();
   }
+  // The next kernel in the stream may be scheduled from here on (it waits for
+  // this grid before reading anything); triggering first gives it the most time
+  // to become resident.
+  grid_launch_dependents();
   grid_dependency_wait();  // logits / state may come from the previous kernel
   if (tid == 0) D2F_TRACE_MARK(1, 1);
 
@@ -197,7 +201,6 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
     phase = __ldg(a.block_phase + jb);
   }
   const bool is_masked = a.masked[r] != 0;
-  grid_launch_dependents();
 
   if (is_masked) {
     int lr = a.logit_row ? a.logit_row[r] : r;

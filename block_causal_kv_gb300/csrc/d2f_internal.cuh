@@ -209,6 +209,13 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// L2 prefetch hint for [src, src + bytes) (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
+               "r"(bytes)
+               : "memory");
+}
+
 // 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
                                           uint32_t bar) {
@@ -233,6 +240,10 @@ __device__ __forceinline__ void cluster_sync() {
 // The two halves of cluster_sync(), for work placed between them.
 __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+// Arrival that orders no memory access (for a barrier that only marks progress).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -274,7 +285,7 @@ __device__ __forceinline__ float4 dsmem_ld_f4(uint32_t addr) {
 // Records %globaltimer (ns) per CTA and phase into a fixed device array so a
 // development build can show where a kernel's time goes.
 #ifdef D2F_TRACE
-constexpr int kTraceSlots = 16;
+constexpr int kTraceSlots = 20;
 constexpr int kTraceCtas = 8192;
 // One array per translation unit (each kernel file has its own copy-out hook).
 static __device__ unsigned long long g_d2f_trace[kTraceCtas * kTraceSlots];
