@@ -400,10 +400,9 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR>::kCtasPerSm))
       if (tid == 128 && u == 1) D2F_TRACE_MARK(0, 14);
       if (tid == 128 && u == 2) D2F_TRACE_MARK(0, 15);
       if (tid == 128 && u == T - 1) D2F_TRACE_MARK(0, 5);
-      uint32_t sv_lo[32], sv_hi[32];
+      uint32_t sv[N];
       const uint32_t s_addr = lane_addr + (u & 1) * N;
-      tmem_ld32(s_addr, sv_lo);
-      tmem_ld32(s_addr + 32, sv_hi);
+      tmem_ld64(s_addr, sv);
 
       // keys c < lim of this tile are visible to this row
       const int tile_lim = t < Tc ? C - t * N : n - (t - Tc) * N;  // valid keys of the tile
@@ -411,10 +410,7 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR>::kCtasPerSm))
       lim = row_valid ? max(0, min(lim, N)) : 0;
       float sf[N];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        sf[c] = __uint_as_float(sv_lo[c]);
-        sf[32 + c] = __uint_as_float(sv_hi[c]);
-      }
+      for (int c = 0; c < N; ++c) sf[c] = __uint_as_float(sv[c]);
       if (!__all_sync(0xffffffffu, lim >= N)) {  // ragged tile: hide masked keys
 #pragma unroll
         for (int c = 0; c < N; ++c)
@@ -452,23 +448,31 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR>::kCtasPerSm))
         }
         m_ref = m_new;
       }
-      // P = 2^(s*scale - m_ref), rounded to bf16; masked keys are -inf -> 0. A row
-      // with no visible key so far keeps m_ref = -inf: subtract 0 instead.
+      // P = 2^(s*scale - m_ref) in bf16: the exponent argument is formed in float
+      // for a pair of keys at once, rounded to bf16 and exponentiated as a packed
+      // pair (P is a bf16 MMA operand, so it carries bf16 precision either way).
+      // Masked keys are -inf -> 0. A row with no visible key so far keeps
+      // m_ref = -inf: subtract 0 instead.
       const float mb = m_ref == -INFINITY ? 0.f : m_ref;
       uint32_t pk[N / 2];
-      float ps[N / 2];
 #pragma unroll
       for (int j = 0; j < N / 2; ++j) {
-        const float p0 = fast_exp2(fmaf(sf[2 * j], sl2, -mb));
-        const float p1 = fast_exp2(fmaf(sf[2 * j + 1], sl2, -mb));
-        pk[j] = pack_bf16x2(p0, p1);
-        ps[j] = __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xffff0000u);
+        float x0, x1;
+        fma2_bc(x0, x1, sf[2 * j], sf[2 * j + 1], sl2, -mb);
+        pk[j] = ex2_bf16x2(pack_bf16x2(x0, x1));
       }
+      // row sum of the P actually used (the rounded values), in float pairs
+      float ps0[N / 4], ps1[N / 4];
 #pragma unroll
-      for (int w = N / 4; w >= 1; w >>= 1)
+      for (int j = 0; j < N / 4; ++j)
+        add2(ps0[j], ps1[j], __uint_as_float(pk[2 * j] << 16),
+             __uint_as_float(pk[2 * j] & 0xffff0000u), __uint_as_float(pk[2 * j + 1] << 16),
+             __uint_as_float(pk[2 * j + 1] & 0xffff0000u));
 #pragma unroll
-        for (int c = 0; c < w; ++c) ps[c] = ps[2 * c] + ps[2 * c + 1];
-      l += ps[0];
+      for (int w = N / 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int c = 0; c < w; ++c) add2(ps0[c], ps1[c], ps0[2 * c], ps1[2 * c], ps0[2 * c + 1], ps1[2 * c + 1]);
+      l += ps0[0] + ps1[0];
       // P over the scores it came from (this thread's own lane): column c of the
       // S/P buffer now holds keys 2c and 2c+1.
       tmem_st32(s_addr, pk);
