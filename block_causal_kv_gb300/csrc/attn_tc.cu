@@ -98,8 +98,11 @@ struct Layout {
                 "receive and staging blocks must fit in the Q + ring area");
 };
 
+constexpr int kMaxStages = 6;
+
 struct Bars {
-  uint64_t full[4], empty[4], s_full[2], p_full[2], pv_done[2], q_full, drain, recv;
+  uint64_t full[kMaxStages], empty[kMaxStages], s_full[2], p_full[2], pv_done[2], q_full, drain,
+      recv;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -112,7 +115,7 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR>::kCtasPerSm))
                    const __grid_constant__ CUtensorMap tm_kwin,
                    const __grid_constant__ CUtensorMap tm_vwin) {
   using L = Layout<D, NS, QR>;
-  static_assert(NS >= 2 && NS <= 4, "ring depth");
+  static_assert(NS >= 2 && NS <= kMaxStages, "ring depth");
   extern __shared__ uint8_t smem_raw[];
   {
     // The swizzled tiles need a 1024-byte aligned base. Every CTA of the grid
@@ -779,22 +782,61 @@ cudaError_t launch_d(const AttnArgs &a, cudaStream_t s, char *why, size_t why_le
 
 }  // namespace
 
+// CTAs of the one-CTA-per-SM variant (head_dim 128, 128-row tiles, 6 stages) that
+// can be resident at once in clusters of cs: clusters are placed within one GPC,
+// so this is below the SM count for most cs. 0 when the query fails. Cached per
+// device.
+int attn_tc_deep_slots(int cs) {
+  static std::mutex mu;
+  static int cache[64][kMaxCluster + 1] = {};
+  if (cs < 1 || cs > kMaxCluster) return 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev][cs] == 0) {
+    if (ensure_attrs<128, 6, 128>() != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs, 1, 1);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Layout<128, 6, 128>::kAlloc;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<128, 6, 128>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    cache[dev][cs] = n * cs;
+  }
+  return cache[dev][cs];
+}
+
 cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t s, char *why, size_t why_len) {
   if (a.batch == 0 || a.total_q == 0) return cudaSuccess;
   if (a.num_splits < 1 || a.num_splits > kMaxCluster) {
     snprintf(why, why_len, "tensor-core path takes 1..%d splits", kMaxCluster);
     return cudaErrorInvalidValue;
   }
-  // 64-row tiles: three ring stages in the shared memory half a Q tile frees.
-  const bool half = a.tc_rows == 64;
-  if (!half && a.tc_rows != kTcRows) {
-    snprintf(why, why_len, "tensor-core path takes 64- or 128-row tiles");
-    return cudaErrorInvalidValue;
+  // Ring depth by shared-memory budget: two CTAs per SM hold Q + NS stages in
+  // ~113 KB (head_dim 64: 6 stages; head_dim 128: 3 stages with 64-row tiles, 2
+  // with 128-row tiles); the 6-stage head_dim-128 variant takes a whole SM.
+  const int rows = a.tc_rows, ns = a.tc_stages;
+  if (a.head_dim == 128) {
+    if (rows == 64 && ns == 3) return launch_d<128, 3, 64>(a, s, why, why_len);
+    if (rows == 128 && ns == 2) return launch_d<128, 2, 128>(a, s, why, why_len);
+    if (rows == 128 && ns == 6) return launch_d<128, 6, 128>(a, s, why, why_len);
+  } else if (a.head_dim == 64) {
+    if (rows == 64 && ns == 6) return launch_d<64, 6, 64>(a, s, why, why_len);
+    if (rows == 128 && ns == 6) return launch_d<64, 6, 128>(a, s, why, why_len);
   }
-  if (a.head_dim == 128)
-    return half ? launch_d<128, 3, 64>(a, s, why, why_len) : launch_d<128, 2, 128>(a, s, why, why_len);
-  if (a.head_dim == 64)
-    return half ? launch_d<64, 3, 64>(a, s, why, why_len) : launch_d<64, 2, 128>(a, s, why, why_len);
+  snprintf(why, why_len, "no tensor-core variant for head_dim %d, %d-row tiles, %d stages",
+           a.head_dim, rows, ns);
+  return cudaErrorInvalidValue;
   snprintf(why, why_len, "tensor-core path supports head_dim 64 or 128");
   return cudaErrorInvalidValue;
 }

@@ -60,6 +60,7 @@ struct AttnPlan {
   bool tc;        // tensor-core path
   int m_tiles;
   int rows;       // rows per tile: 64 or 128 on the tensor-core path
+  int stages;     // tensor-core K/V ring depth
   int splits;
   int tiles_per_split;
   int n_counters;
@@ -77,6 +78,14 @@ bool force_simt() {
 bool force_full_rows() {
   const char *e = getenv("D2F_TC_ROWS");
   return e && strcmp(e, "128") == 0;
+}
+
+// D2F_TC_DEEP=1 / 0 forces / forbids the one-CTA-per-SM 6-stage variant for
+// head_dim 128 with 128-row tiles (for comparisons and tests); unset = planner.
+int force_deep() {
+  const char *e = getenv("D2F_TC_DEEP");
+  if (!e || !e[0]) return -1;
+  return e[0] == '1' ? 1 : 0;
 }
 
 int plan_attn(int batch, int total_q, int max_q, int max_ctx, int Hq, int Hkv, int D, int B,
@@ -117,14 +126,39 @@ int plan_attn(int batch, int total_q, int max_q, int max_ctx, int Hq, int Hkv, i
   if (tc) {
     // The splits of one row tile form a thread-block cluster (at most 8 CTAs)
     // and compose their partials in distributed shared memory: no workspace.
-    if (splits == 0) {
-      // Two CTAs fit on an SM: take as many splits as the 2 x SM slots hold,
-      // then the fewest that keep the longest split's tile count.
-      const long long slots = 2LL * num_sms_current_device();
-      long long most = slots / base;
-      if (most > min(kTcMaxSplits, t_max)) most = min(kTcMaxSplits, t_max);
-      if (most < 1) most = 1;
-      splits = cdiv(t_max, cdiv(t_max, most));
+    // Split count: as many splits as one wave of resident CTAs holds, then the
+    // fewest splits that keep the longest split's tile count. (Several waves of
+    // shorter splits measured slower: every wave pays the ramp-up and the
+    // composition again.)
+    const int sms = max(1, num_sms_current_device());
+    auto pick = [&](bool deep_variant) {
+      int most = 1;
+      for (int cs = 2; cs <= min(kTcMaxSplits, t_max); ++cs) {
+        const long long slots = deep_variant ? attn_tc_deep_slots(cs) : 2LL * sms;
+        if (base * cs <= slots) most = cs;
+      }
+      return cdiv(t_max, cdiv(t_max, most));
+    };
+    p->stages = D == 64 ? 6 : (rows == 64 ? 3 : 2);
+    const int two = splits ? splits : pick(false);  // two CTAs per SM
+    splits = two;
+    if (D == 128 && rows == 128) {
+      // 2 ring stages at two CTAs per SM, or 6 stages at one: per streamed tile a
+      // CTA takes ~2.2 us in the first (the ring waits on the load latency) and
+      // ~0.9 us in the second (measured on GB300); take the deeper ring when its
+      // one wave finishes first and the splits are long enough for the steady
+      // state to matter.
+      const int one = num_splits ? num_splits : pick(true);
+      const int tps2 = cdiv(t_max, two), tps1 = cdiv(t_max, one);
+      const long long w2 = cdiv(base * two, 2LL * sms);
+      const long long slots1 = attn_tc_deep_slots(one);
+      const long long w1 = slots1 > 0 ? cdiv(base * one, slots1) : -1;
+      bool deep = tps2 >= 8 && w1 > 0 && w1 * tps1 * 9 < w2 * tps2 * 22;
+      if (force_deep() >= 0) deep = force_deep() == 1;
+      if (deep) {
+        p->stages = 6;
+        splits = one;
+      }
     }
     p->splits = min(splits, kTcMaxSplits);
     p->tiles_per_split = cdiv(t_max, p->splits);
@@ -308,6 +342,7 @@ int d2f_block_attn(const void *q, const void *k_win, const void *v_win, const vo
   a.tiles_per_split = p.tiles_per_split;
   a.m_tiles = p.m_tiles;
   a.tc_rows = p.rows;
+  a.tc_stages = p.stages;
   a.counters = reinterpret_cast<int32_t *>(workspace);
   a.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) + p.off_ml);
   a.ws_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + p.off_o);

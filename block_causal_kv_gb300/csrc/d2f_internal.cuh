@@ -41,6 +41,7 @@ struct AttnArgs {
   int tiles_per_split;   // tensor-core path: key tiles per split from the host's max_ctx
   int m_tiles;           // grid.x: row tiles per (sequence, KV head)
   int tc_rows;           // tensor-core path: rows a tile holds (64 or 128)
+  int tc_stages;         // tensor-core path: K/V ring depth (2, 3 or 6)
   int32_t *counters;     // [batch * Hkv * m_tiles] merge arrival counters (zero at rest)
   float2 *ws_ml;         // [num_splits][total_q * Hq] (max in log2 units, sum)
   float *ws_o;           // [num_splits][total_q * Hq][head_dim] unnormalised partial output
@@ -85,6 +86,7 @@ constexpr int kCommitMaxStageBytes = 32768;  // bulk-staged slice, bytes
 cudaError_t launch_append(const AppendArgs &a, bool vec_ok, cudaStream_t s);
 cudaError_t launch_attn_simt(const AttnArgs &a, int dtype, cudaStream_t s);
 cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t s, char *why, size_t why_len);
+int attn_tc_deep_slots(int cs);  // resident CTAs of the 6-stage head_dim-128 variant
 
 // Tile and row sizes of the two attention paths (also used for workspace sizing).
 constexpr int kSimtRows = 16;   // query rows per CTA, CUDA-core path

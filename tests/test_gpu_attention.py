@@ -68,6 +68,21 @@ def test_full_row_tiles_where_half_tiles_fit(name, splits, monkeypatch):
     check_attention(out, lse, ref, ref_lse, torch.bfloat16, "rows128/%s/s%d" % (name, splits))
 
 
+@pytest.mark.parametrize("name", ["dream", "long_b32"])
+@pytest.mark.parametrize("splits", [0, 1, 3, 8])
+@pytest.mark.parametrize("deep", ["1", "0"])
+def test_ring_depth_variants_for_full_row_tiles(name, splits, deep, monkeypatch):
+    """head_dim 128 with 128-row tiles runs either a 6-stage ring at one CTA per SM
+    (D2F_TC_DEEP=1) or a 2-stage ring at two CTAs per SM (D2F_TC_DEEP=0); both
+    agree with the oracle."""
+    dev = device()
+    monkeypatch.setenv("D2F_TC_DEEP", deep)
+    p = synth.make_problem(synth.small(name))
+    out, lse = _run(p, dev, splits)
+    ref, ref_lse = _ref(p)
+    check_attention(out, lse, ref, ref_lse, torch.bfloat16, "deep%s/%s/s%d" % (deep, name, splits))
+
+
 @pytest.mark.parametrize("name", ["llada", "ragged", "dream", "long_b16"])
 def test_cuda_core_path_bf16(name, monkeypatch):
     """The CUDA-core kernel on bf16 operands, cross-checked like the main path."""
