@@ -471,13 +471,19 @@ def run_ours(args, world, rank, local):
     if int(err.item()) != 0:
         raise RuntimeError("device error word %d after the timed region" % int(err.item()))
 
-    # Per-kernel durations: a graph of one kernel only, launched back to back over
-    # the same rotating input sets (programmatic dependent launch between
-    # consecutive launches, as in the step), timed with CUDA events around whole
+    # Per-kernel durations. The commit (and the append) run as graphs of that
+    # kernel only over the same rotating input sets, launched back to back as in
+    # the step (no programmatic early launch), timed with CUDA events around whole
     # replays: the average launch duration including the gap to the next launch.
-    # (Events between kernels would add their own latency to every bracket.)
+    # The attention's duration is the step time less those: its share of the
+    # step. (An attention-only graph chains attention launches through
+    # programmatic dependent launch, which the step never does: for grids that
+    # fill the GPU the next launch's early CTAs take slots from the current one,
+    # so that number is reported for reference only. Events between kernels
+    # would add their own latency to every bracket.)
     per_kernel = {}
-    for which, fn in (("attn", attn), ("commit", commit)):
+    kernel_fns = [("attn", attn), ("commit", commit)] + ([("append", append)] if appends else [])
+    for which, fn in kernel_fns:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
             if which == "commit":
@@ -496,7 +502,9 @@ def run_ours(args, world, rank, local):
             b.record(stream)
         torch.cuda.synchronize()
         per_kernel[which] = a.elapsed_time(b) * 1000.0 / (reps * n_sets)
-    attn_us, commit_us = [per_kernel["attn"]], [per_kernel["commit"]]
+    step_us = elapsed_ms * 1000.0 / K
+    attn_in_step = step_us - per_kernel["commit"] - per_kernel.get("append", 0.0)
+    attn_us, commit_us = [attn_in_step], [per_kernel["commit"]]
 
     steps_total = K * world
     value = steps_total / (elapsed_ms / 1000.0)
@@ -509,15 +517,24 @@ def run_ours(args, world, rank, local):
     if t_attn:
         kernels["block_attn"] = {"us": t_attn, "bytes": attn_b, "GB/s": attn_b / t_attn / 1e3,
                                  "frac": attn_b / t_attn / 1e3 / hbm,
-                                 "TFLOP/s": flops(p) / t_attn / 1e6}
+                                 "TFLOP/s": flops(p) / t_attn / 1e6,
+                                 "us_attention_only_graph": per_kernel["attn"]}
     if t_commit:
         kernels["commit"] = {"us": t_commit, "bytes": commit_b, "GB/s": commit_b / t_commit / 1e3,
                              "frac": commit_b / t_commit / 1e3 / hbm}
+    if appends:
+        t_app = per_kernel["append"]
+        kernels["kv_append"] = {"us": t_app, "bytes": append_b, "GB/s": append_b / t_app / 1e3,
+                                "frac": append_b / t_app / 1e3 / hbm}
     dom = "block_attn" if (t_attn or 0) >= (t_commit or 0) else "commit"
     dk = kernels.get(dom, {})
     roofline = {"bound": "hbm", "kernel": dom,
-                "duration": "average launch of a %s-only CUDA graph over the rotating input "
-                            "sets, CUDA events around whole replays" % dom,
+                "duration": ("step time less the commit%s: commit-only%s graphs over the "
+                             "rotating input sets, CUDA events around whole replays" % (
+                                 " and append" if appends else "", " and append-only" if appends
+                                 else "")) if dom == "block_attn" else
+                            "average launch of a commit-only CUDA graph over the rotating input "
+                            "sets, CUDA events around whole replays",
                 "achieved": dk.get("GB/s"), "peak": hbm,
                 "unit": "GB/s", "frac": dk.get("frac"), "peak_kind": peak_kind,
                 "traffic": recorded_traffic("attn" if dom == "block_attn" else "commit", w.name)}
