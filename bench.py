@@ -359,11 +359,12 @@ def run_ours(args, world, rank, local):
         st.tokens, st.masked = tokens_all[i], masked_all[i]
     appends = len(p.src_row) > 0
 
-    ws_attn = d2f.attn_workspace(dev, batch=w.batch, total_q=w.total_q,
+    dcode = d2f.F32 if w.dtype == torch.float32 else d2f.BF16
+    ws_attn = d2f.attn_workspace(dev, batch=w.batch, total_q=w.total_q, dtype=dcode,
                                  max_q_per_seq=p.max_q_per_seq, max_ctx=p.max_ctx,
                                  num_heads_q=w.num_heads_q, num_heads_kv=w.num_heads_kv,
                                  head_dim=w.head_dim, block_size=B, num_splits=args.num_splits)
-    ws_commit = d2f.commit_workspace(dev, total_q=w.total_q, vocab=w.vocab, block_size=B,
+    ws_commit = d2f.commit_workspace(dev, total_q=w.total_q, vocab=w.vocab, block_size=B, dtype=dcode,
                                      num_splits=args.commit_splits)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     conf = torch.empty(w.total_q, dtype=torch.float32, device=dev)
