@@ -7,11 +7,12 @@
 // §쉽게 이해하기 (conservative threshold commit, aggressive top-1, remask).
 //
 // Grid (slices, rows): CTA (s, r) reduces vocabulary slice s of row r to
-// (max, first argmax, sum of exp(l - max)). On the staged path one thread issues
-// the whole slice as up to four 1-D bulk copies (TMA) into shared memory, so every
-// byte of the slice is in flight at once, and the CTA folds each piece from
-// shared memory as soon as it lands; the direct path (unaligned rows) folds
-// 128-bit or scalar global loads.
+// (max, first argmax, sum of exp(l - max)) with 128-bit streaming loads, four
+// in flight per thread (scalar loads where rows are not 16-byte aligned). The
+// slices are long (a few CTAs per SM over the whole grid): measured on GB300,
+// staging slices in shared memory with bulk copies, or persistent CTAs streaming
+// many slices through a ring of bulk copies, were slower (Dream-shaped layer:
+// 42.8 and 39-42 us against 34.5 us for this form).
 // Every CTA of a window block then bumps one arrival counter; the last one to
 // arrive composes the slices of all rows of the block and decides the block with
 // one warp (lane = row). The decision's metadata (sequence, tau, phase) is
@@ -26,8 +27,6 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
-constexpr int kParts = 4;            // staged slice: bulk copies folded as each lands
-constexpr int kMinPartVecs = 256;    // ... of at least 4 KB each
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct RowState {
@@ -154,16 +153,13 @@ __device__ void decide_block(const CommitArgs &a, int jb, const float *conf_s, c
   if (lane == 0 && a.block_remaining) a.block_remaining[jb] = __popc(left);
 }
 
-template <int DT, int PATH>  // PATH 0: scalar loads, 1: 128-bit loads, 2: bulk-staged
+template <int DT, int PATH>  // PATH 0: scalar loads, 1: 128-bit loads
 __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
   constexpr int N = (DT == D2F_BF16) ? 8 : 4;  // values per 16-byte vector
-  extern __shared__ __align__(128) uint8_t stage[];
   __shared__ RowState red[kThreads / 32];
   __shared__ float conf_s[32];
   __shared__ int arg_s[32];
-  __shared__ uint64_t bar[kParts];
   __shared__ int is_last;
-  __shared__ int abort_flag;
 
   const int s = blockIdx.x;
   const int r = blockIdx.y;
@@ -173,11 +169,6 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
   const int jb = r / B;
 
   if (tid == 0) D2F_TRACE_MARK(1, 0);
-  if (PATH == 2 && tid == 0) {  // set-up that reads no global memory
-    abort_flag = 0;
-    for (int i = 0; i < kParts; ++i) mbar_init(smem_u32(&bar[i]), 1);
-    mbar_fence_init();
-  }
   // The next kernel in the stream may be scheduled from here on (it waits for
   // this grid before reading anything); triggering first gives it the most time
   // to become resident.
@@ -219,42 +210,7 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
     for (int j = 0; j < N; ++j) acc[j] = 0.f;
     int v_tail = v0;  // first index left for the scalar loop
 
-    if (PATH == 2) {
-      // Bulk-staged slice: whole 16-byte vectors [v0, v0 + nvec*N), copied in up
-      // to kParts pieces with one mbarrier each, so folding the first piece
-      // overlaps the transfer of the rest. Each thread still visits its indices
-      // in increasing order (first-argmax rule).
-      const int nvec = (v1 - v0) / N;
-      const int parts = max(1, min(kParts, nvec / kMinPartVecs));
-      const int per = (nvec + parts - 1) / parts;
-      __syncthreads();  // the mbarriers are initialised
-      if (row_ok && nvec > 0) {
-        if (tid == 0) {
-          for (int i = 0; i < parts; ++i) {
-            const int k0 = i * per, k1 = min(nvec, k0 + per);
-            if (k0 >= k1) break;
-            mbar_arrive_expect_tx(smem_u32(&bar[i]), (k1 - k0) * 16u);
-            bulk_load(smem_u32(stage) + k0 * 16u,
-                      row + (int64_t)(v0 + k0 * N) * (DT == D2F_BF16 ? 2 : 4), (k1 - k0) * 16u,
-                      smem_u32(&bar[i]));
-          }
-        }
-        if (tid == 0) D2F_TRACE_MARK(1, 2);
-        const uint4 *sv = reinterpret_cast<const uint4 *>(stage);
-        for (int i = 0; i < parts; ++i) {
-          const int k0 = i * per, k1 = min(nvec, k0 + per);
-          if (k0 >= k1) break;
-          if (!mbar_wait(smem_u32(&bar[i]), 0, &abort_flag, a.err)) break;
-          if (tid == 0 && i == 0) D2F_TRACE_MARK(1, 3);
-          for (int k = k0 + tid; k < k1; k += kThreads) {
-            float x[N];
-            unpack<DT>(sv[k], x);
-            fold<N>(x, v0 + k * N, m, idx, acc);
-          }
-        }
-        v_tail = v0 + nvec * N;
-      }
-    } else if (PATH == 1 && row_ok) {
+    if (PATH == 1 && row_ok) {
       // v0 and chunk are multiples of N and the row start is 16-byte aligned.
       const uint4 *vec = reinterpret_cast<const uint4 *>(row);
       const int nvec_end = v1 / N;  // vectors fully inside [v0, v1)
@@ -378,7 +334,7 @@ cudaError_t launch_path(const CommitArgs &a, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.splits, a.total_q);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = PATH == 2 ? (size_t)a.chunk * (DT == D2F_BF16 ? 2 : 4) : 0;
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   // No programmatic early launch for the commit: measured on GB300, its CTAs
   // scheduled during the previous kernel's tail cost more than they saved. The
@@ -395,11 +351,9 @@ cudaError_t launch_path(const CommitArgs &a, cudaStream_t stream) {
 cudaError_t launch_commit(const CommitArgs &a, int dtype, int path, cudaStream_t stream) {
   if (a.total_q == 0) return cudaSuccess;
   if (dtype == D2F_BF16) {
-    if (path == 2) return launch_path<D2F_BF16, 2>(a, stream);
     if (path == 1) return launch_path<D2F_BF16, 1>(a, stream);
     return launch_path<D2F_BF16, 0>(a, stream);
   }
-  if (path == 2) return launch_path<D2F_F32, 2>(a, stream);
   if (path == 1) return launch_path<D2F_F32, 1>(a, stream);
   return launch_path<D2F_F32, 0>(a, stream);
 }

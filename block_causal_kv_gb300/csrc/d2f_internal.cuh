@@ -80,9 +80,8 @@ struct AppendArgs {
 };
 
 // Launchers (one per translation unit). Return cudaSuccess or the launch error.
-// path: 0 scalar loads, 1 128-bit loads, 2 bulk-staged slices (see commit.cu)
+// path: 0 scalar loads, 1 128-bit loads (see commit.cu)
 cudaError_t launch_commit(const CommitArgs &a, int dtype, int path, cudaStream_t s);
-constexpr int kCommitMaxStageBytes = 32768;  // bulk-staged slice, bytes
 cudaError_t launch_append(const AppendArgs &a, bool vec_ok, cudaStream_t s);
 cudaError_t launch_attn_simt(const AttnArgs &a, int dtype, cudaStream_t s);
 cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t s, char *why, size_t why_len);
