@@ -66,6 +66,7 @@ constexpr uint32_t kTmemO = 128;               // first TMEM column of O
 constexpr int kMaxCluster = 8;
 constexpr int kBarSetup = 1;                   // named barrier: MMA warp + softmax warps
 constexpr int kSmemTwoPerSm = 115712;          // dynamic bytes that still let 2 CTAs share an SM
+static_assert(kMaxLongestFirstBatch * 4 + 4 <= 2 * 64 * 64 * 2, "ordering scratch fits a ring stage");
 
 template <int D, int NS, int QR>
 struct Layout {
@@ -139,7 +140,8 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR>::kCtasPerSm))
   const int cs = gridDim.x;  // CTAs of the cluster = splits of this row tile
   const int split = blockIdx.x;
   const int mt = blockIdx.y;
-  const int b = blockIdx.z / a.num_heads_kv, g = blockIdx.z % a.num_heads_kv;
+  int b = blockIdx.z / a.num_heads_kv;  // sequence (remapped longest-first below)
+  const int g = blockIdx.z % a.num_heads_kv;
 
   if (tid == 0) D2F_TRACE_MARK(0, 0);
   // ---- set-up that reads no global memory --------------------------------------
@@ -175,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR>::kCtasPerSm))
   // previous kernel changes them, a prefetch is wasted, and every value the
   // attention uses is read again after the dependency wait. L2 is the point of
   // coherence, so a prefetched line never hides a later write.
-  if (warp == 0 && a.page_table != nullptr) {
+  if (warp == 0 && a.page_table != nullptr && !a.longest_first) {
     const int ppt0 = N / a.block_size;
     const int lp = split * a.tiles_per_split * ppt0 + lane;
     const int hint_c = __ldcg(a.ctx_len + b);
@@ -192,6 +194,30 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR>::kCtasPerSm))
 
   grid_dependency_wait();  // inputs may come from the previous kernel in the stream
   if (tid == 0) D2F_TRACE_MARK(0, 1);
+
+  if (a.longest_first) {
+    // More CTAs than resident slots and sequences of different lengths: take the
+    // sequences longest context first (ties by index), so the long CTAs start in
+    // the first wave and the short ones fill in after them. Every CTA derives the
+    // same permutation from the same ctx_len values. Scratch: ring stage 0, which
+    // no copy has touched yet.
+    int *scr = reinterpret_cast<int *>(smem + L::kRing);
+    for (int j = tid; j < a.batch; j += kThreads) scr[j] = __ldg(a.ctx_len + j);
+    __syncthreads();
+    const int want = b;  // this CTA takes the sequence of rank `want`
+    for (int j = tid; j < a.batch; j += kThreads) {
+      const int cj = scr[j];
+      int rank = 0;
+      for (int i = 0; i < a.batch; ++i) {
+        const int ci = scr[i];
+        rank += (ci > cj || (ci == cj && i < j)) ? 1 : 0;
+      }
+      if (rank == want) scr[kMaxLongestFirstBatch] = j;
+    }
+    __syncthreads();
+    b = scr[kMaxLongestFirstBatch];
+    __syncthreads();  // stage 0 is free for the copies again
+  }
 
   // Page ids of this split's first tiles, requested together with the sequence
   // metadata: the split's tile range comes from the host (tiles_per_split), so

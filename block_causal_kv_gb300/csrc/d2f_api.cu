@@ -61,6 +61,7 @@ struct AttnPlan {
   int m_tiles;
   int rows;       // rows per tile: 64 or 128 on the tensor-core path
   int stages;     // tensor-core K/V ring depth
+  bool longest_first;  // more CTAs than one wave: longest sequences first
   int splits;
   int tiles_per_split;
   int n_counters;
@@ -161,6 +162,13 @@ int plan_attn(int batch, int total_q, int max_q, int max_ctx, int Hq, int Hkv, i
       }
     }
     p->splits = min(splits, kTcMaxSplits);
+    {
+      const long long ctas = base * p->splits;
+      const long long slots = p->stages == 6 && D == 128 ? attn_tc_deep_slots(p->splits) : 2LL * sms;
+      const char *ev = getenv("D2F_LONGEST_FIRST");  // 1 / 0: force on / off (tests)
+      const bool want = (ev && ev[0]) ? ev[0] == '1' : ctas > slots;
+      p->longest_first = batch > 1 && batch <= kMaxLongestFirstBatch && want;
+    }
     p->tiles_per_split = cdiv(t_max, p->splits);
     p->n_counters = 0;
     p->off_ml = p->off_o = p->bytes = 0;
@@ -331,6 +339,7 @@ int d2f_block_attn(const void *q, const void *k_win, const void *v_win, const vo
   a.m_tiles = p.m_tiles;
   a.tc_rows = p.rows;
   a.tc_stages = p.stages;
+  a.longest_first = p.longest_first ? 1 : 0;
   a.counters = reinterpret_cast<int32_t *>(workspace);
   a.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) + p.off_ml);
   a.ws_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + p.off_o);

@@ -42,6 +42,7 @@ struct AttnArgs {
   int m_tiles;           // grid.x: row tiles per (sequence, KV head)
   int tc_rows;           // tensor-core path: rows a tile holds (64 or 128)
   int tc_stages;         // tensor-core path: K/V ring depth (2, 3 or 6)
+  int longest_first;     // tensor-core path: map blockIdx.z to sequences longest context first
   int32_t *counters;     // [batch * Hkv * m_tiles] merge arrival counters (zero at rest)
   float2 *ws_ml;         // [num_splits][total_q * Hq] (max in log2 units, sum)
   float *ws_o;           // [num_splits][total_q * Hq][head_dim] unnormalised partial output
@@ -93,6 +94,7 @@ constexpr int kSimtKeys = 32;   // keys per tile, CUDA-core path
 constexpr int kTcRows = 128;    // query rows per CTA (UMMA M), tensor-core path
 constexpr int kTcKeys = 64;     // keys per tile (UMMA N of Q.K^T), tensor-core path
 constexpr int kTcMaxSplits = 8; // CTAs per cluster sharing one row tile, tensor-core path
+constexpr int kMaxLongestFirstBatch = 256;  // largest batch the longest-first order covers
 
 // ---------------------------------------------------------------------------
 // Device helpers

@@ -83,6 +83,20 @@ def test_ring_depth_variants_for_full_row_tiles(name, splits, deep, monkeypatch)
     check_attention(out, lse, ref, ref_lse, torch.bfloat16, "deep%s/%s/s%d" % (deep, name, splits))
 
 
+@pytest.mark.parametrize("name", ["ragged", "dream", "long_b32"])
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_longest_first_sequence_order(name, splits, monkeypatch):
+    """CTAs mapped to sequences longest context first (D2F_LONGEST_FIRST=1, the
+    order taken when the grid exceeds one wave): same result as the oracle."""
+    dev = device()
+    monkeypatch.setenv("D2F_LONGEST_FIRST", "1")
+    w = synth.small(name)
+    p = synth.make_problem(w)
+    out, lse = _run(p, dev, splits)
+    ref, ref_lse = _ref(p)
+    check_attention(out, lse, ref, ref_lse, torch.bfloat16, "lf/%s/s%d" % (name, splits))
+
+
 @pytest.mark.parametrize("name", ["llada", "ragged", "dream", "long_b16"])
 def test_cuda_core_path_bf16(name, monkeypatch):
     """The CUDA-core kernel on bf16 operands, cross-checked like the main path."""
