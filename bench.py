@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="oracle time budget of the reference arm")
     ap.add_argument("--profile-steps", type=int, default=0,
                     help="run this many eager steps and exit (for ncu captures)")
     return ap.parse_args()
@@ -280,8 +282,8 @@ def run_reference(args, world, rank):
     w = synth.workload(args.workload)
     p = synth.make_problem(w)
     nthreads = oracle_threads()
-    # bounded: the whole run takes about a minute regardless of K
-    budget = 60.0
+    # bounded: the whole run takes about --ref-seconds regardless of K
+    budget = args.ref_seconds
     for _ in range(max(0, min(args.warmup, 1))):
         time_oracle(p, 0.1, nthreads)
     value, sample = time_oracle(p, budget, nthreads)
