@@ -61,18 +61,20 @@ constexpr int kSoftThreads = 32 * kSoftWarps;  // one per TMEM lane
 constexpr int kThreads = 64 + kSoftThreads;    // producer + MMA warps + softmax
 constexpr int M = kTcRows;                     // UMMA M: 128 rows
 constexpr int N = kTcKeys;                     // 64 keys per tile
-constexpr uint32_t kTmemCols = 256;            // S / P (2 x 64) + O (<= 128)
-constexpr uint32_t kTmemO = 128;               // first TMEM column of O
+constexpr uint32_t kTmemO = 128;               // first TMEM column of O (S / P: 2 x 64 before it)
 constexpr int kMaxCluster = 8;
 constexpr int kBarSetup = 1;                   // named barrier: MMA warp + softmax warps
 constexpr int kSmemTwoPerSm = 115712;          // dynamic bytes that still let 2 CTAs share an SM
 static_assert(kMaxLongestFirstBatch * 4 + 4 <= 2 * 64 * 64 * 2, "ordering scratch fits a ring stage");
 
-template <int D, int NS, int QR>
+template <int D, int NS, int QR, int MT>
 struct Layout {
   static constexpr int kHalves = D / 64;         // 64-element (128-byte) swizzle columns
-  static constexpr int kQHalf = QR * 128;        // one 64-wide column block of Q
-  static constexpr int kQBytes = kHalves * kQHalf;
+  static constexpr int kQHalf = QR * 128;        // one 64-wide column block of one Q tile
+  static constexpr int kTileQBytes = kHalves * kQHalf;
+  static constexpr int kQBytes = MT * kTileQBytes;  // MT row tiles of Q
+  // TMEM: S / P buffers (2 x 64 columns), then MT accumulators of D columns
+  static constexpr uint32_t kTmemCols = 128 + MT * D <= 256 ? 256 : 512;
   static constexpr int kKVHalf = N * 128;        // 64 key rows x 128 bytes
   static constexpr int kKBytes = kHalves * kKVHalf;
   static constexpr int kStage = 2 * kKBytes;     // K tile then V tile
@@ -88,15 +90,17 @@ struct Layout {
   // Composition blocks (overlay Q and the ring): per owner, LR rows of D bf16
   // then LR (max, sum) pairs.
   static constexpr int kRowBytes = 2 * D;
-  __host__ __device__ static constexpr int rows_per_owner(int cs) { return (QR + cs - 1) / cs; }
+  __host__ __device__ static constexpr int rows_per_owner(int cs) { return (MT * QR + cs - 1) / cs; }
   __host__ __device__ static constexpr int block_bytes(int cs) {
     return (rows_per_owner(cs) * (kRowBytes + 8) + 15) & ~15;
   }
   __host__ __device__ static constexpr int staging(int cs) {  // after the receive blocks
     return (cs * block_bytes(cs) + 127) & ~127;
   }
-  static_assert(2 * ((QR + kMaxCluster - 1) * (kRowBytes + 8) + 16 * kMaxCluster) + 128 <= kBars,
+  static_assert(2 * ((MT * QR + kMaxCluster - 1) * (kRowBytes + 8) + 16 * kMaxCluster) + 128 <=
+                    kBars,
                 "receive and staging blocks must fit in the Q + ring area");
+  static_assert(128 + MT * D <= 512, "accumulators fit TMEM");
 };
 
 constexpr int kMaxStages = 6;
@@ -109,13 +113,13 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
-template <int D, int NS, int QR>
-__global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR>::kCtasPerSm))
+template <int D, int NS, int QR, int MT>
+__global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR, MT>::kCtasPerSm))
     attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_kpool,
                    const __grid_constant__ CUtensorMap tm_vpool,
                    const __grid_constant__ CUtensorMap tm_kwin,
                    const __grid_constant__ CUtensorMap tm_vwin) {
-  using L = Layout<D, NS, QR>;
+  using L = Layout<D, NS, QR, MT>;
   static_assert(NS >= 2 && NS <= kMaxStages, "ring depth");
   extern __shared__ uint8_t smem_raw[];
   {
@@ -167,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR>::kCtasPerSm))
   }
   __syncthreads();
   if (warp == 1) {
-    tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
+    tmem_alloc(smem_u32(&bars->tmem_base), L::kTmemCols);
     tmem_relinquish();
   }
 
@@ -234,9 +238,9 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR>::kCtasPerSm))
   if (!active && tid == 0 && mt == 0 && split == 0 && g == 0) set_err(a.err, D2F_ERR_INVALID_ARG);
   const int G = a.group, B = a.block_size, H = a.num_heads_q;
   const int rows_total = G * n;
-  const int r_begin = mt * QR;
+  const int r_begin = mt * MT * QR;  // first of the MT row tiles of this CTA
   active = active && r_begin < rows_total;
-  const int nrows = active ? min(QR, rows_total - r_begin) : 0;
+  const int nrows = active ? min(MT * QR, rows_total - r_begin) : 0;  // valid rows, all tiles
   const int Tc = (C + N - 1) / N, Tw = (n + N - 1) / N;
   // Split s takes tiles [s*tps, (s+1)*tps); tps comes from the host's max_ctx and
   // grows here only if a sequence is longer than that hint promised.
@@ -258,10 +262,14 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR>::kCtasPerSm))
   // softmax-thread identity (warps 2-5): row = TMEM lane
   const int quad = warp & 3;
   const int row = quad * 32 + lane;
-  const bool row_valid = row < nrows;
   const int r = r_begin + row;
   const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
-  float m_ref = -INFINITY, l = 0.f;
+  float m_ref[MT], l[MT];
+#pragma unroll
+  for (int i = 0; i < MT; ++i) {
+    m_ref[i] = -INFINITY;
+    l[i] = 0.f;
+  }
 
   if (has_work && warp == 0) {
     // ======================= TMA producer (whole warp) =========================
@@ -345,47 +353,55 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR>::kCtasPerSm))
       constexpr uint32_t idesc_pv = idesc_bf16_f32(M, D, 0, 1);
       const uint32_t q_base = sb + L::kQ;
       bool ok = mbar_wait(smem_u32(&bars->q_full), 0, abort_flag, a.err);
-      auto issue_pv = [&](int v) -> bool {
-        if (!mbar_wait(smem_u32(&bars->p_full[v & 1]), (v >> 1) & 1, abort_flag, a.err))
+      // Sub-tile v = u*MT + i: key tile u against row tile i. S_v goes to S/P
+      // buffer v % 2; P_v.V_u accumulates into row tile i's O.
+      auto issue_pv = [&](int w) -> bool {
+        if (!mbar_wait(smem_u32(&bars->p_full[w & 1]), (w >> 1) & 1, abort_flag, a.err))
           return false;
         tc_fence_after();
-        const int stage = v % NS;
+        const int uw = w / MT, iw = w % MT;
+        const int stage = uw % NS;
         const uint32_t v_base = sb + L::kRing + stage * L::kStage + L::kKBytes;
 #pragma unroll
         for (int ks = 0; ks < N / 16; ++ks) {  // 16 keys = 8 TMEM columns of P per step
           const uint64_t bd = smem_desc_sw128(v_base + ks * 2048, L::kKVHalf, 1024);
-          umma_bf16_tmem_a(tmem + kTmemO, tmem + (v & 1) * N + ks * 8, bd, idesc_pv,
-                           (v > 0 || ks > 0) ? 1u : 0u);
+          umma_bf16_tmem_a(tmem + kTmemO + iw * D, tmem + (w & 1) * N + ks * 8, bd, idesc_pv,
+                           (uw > 0 || ks > 0) ? 1u : 0u);
         }
-        umma_commit(smem_u32(&bars->pv_done[v & 1]));
-        umma_commit(smem_u32(&bars->empty[stage]));
+        umma_commit(smem_u32(&bars->pv_done[w & 1]));
+        if (iw == MT - 1) umma_commit(smem_u32(&bars->empty[stage]));  // key tile done
         return true;
       };
-      for (int u = 0; u < T && ok; ++u) {
+      const int V = T * MT;
+      for (int v = 0; v < V && ok; ++v) {
+        const int u = v / MT, i = v % MT;
         const int stage = u % NS;
-        if (!mbar_wait(smem_u32(&bars->full[stage]), (u / NS) & 1, abort_flag, a.err)) {
-          ok = false;
-          break;
+        if (i == 0) {
+          if (!mbar_wait(smem_u32(&bars->full[stage]), (u / NS) & 1, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (u == 0) D2F_TRACE_MARK(0, 10);
+          if (u == T - 1) D2F_TRACE_MARK(0, 3);
         }
-        tc_fence_after();
-        if (u == 0) D2F_TRACE_MARK(0, 10);
-        if (u == T - 1) D2F_TRACE_MARK(0, 3);
-        // S_u overwrites the S/P buffer that P_{u-2} occupied: P.V_{u-2} was issued
+        // S_v overwrites the S/P buffer that P_{v-2} occupied: P.V_{v-2} was issued
         // before this (MMAs of one thread execute in order).
         const uint32_t k_base = sb + L::kRing + stage * L::kStage;
+        const uint32_t qi_base = q_base + i * L::kTileQBytes;
 #pragma unroll
         for (int h = 0; h < L::kHalves; ++h) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = smem_desc_sw128(q_base + h * L::kQHalf + kk * 32, 16, 1024);
+            const uint64_t ad = smem_desc_sw128(qi_base + h * L::kQHalf + kk * 32, 16, 1024);
             const uint64_t bd = smem_desc_sw128(k_base + h * L::kKVHalf + kk * 32, 16, 1024);
-            umma_bf16(tmem + (u & 1) * N, ad, bd, idesc_qk, (h | kk) ? 1u : 0u);
+            umma_bf16(tmem + (v & 1) * N, ad, bd, idesc_qk, (h | kk) ? 1u : 0u);
           }
         }
-        umma_commit(smem_u32(&bars->s_full[u & 1]));
-        if (u >= 1) ok = issue_pv(u - 1);
+        umma_commit(smem_u32(&bars->s_full[v & 1]));
+        if (v >= 1) ok = issue_pv(v - 1);
       }
-      if (ok) issue_pv(T - 1);
+      if (ok) issue_pv(V - 1);
       // Drain: wait until every MMA issued above has completed.
       umma_commit(smem_u32(&bars->drain));
       volatile int no_abort = 0;
@@ -394,141 +410,159 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR>::kCtasPerSm))
   } else if (has_work) {
     // ======================= softmax (128 threads, one per TMEM lane) ==========
     {
-      // The Q row into the 128-byte-swizzled K-major layout the MMA reads:
-      // 16-byte chunk c of column block h lands at
-      //   h*kQHalf + (row/8)*1024 + (row%8)*128 + ((c ^ (row%8)) * 16).
+      // The Q rows into the 128-byte-swizzled K-major layout the MMA reads: in
+      // row tile i, 16-byte chunk c of column block h lands at
+      //   i*kTileQBytes + h*kQHalf + (row/8)*1024 + (row%8)*128 + ((c ^ (row%8)) * 16).
       constexpr int kQc = D / 8;
       if (row < QR) {  // warp-uniform
-        uint4 qv[kQc];
-        const uint4 *src = reinterpret_cast<const uint4 *>(
-            reinterpret_cast<const uint16_t *>(a.q) +
-            ((int64_t)(q0 + r / G) * H + g * G + r % G) * D);
 #pragma unroll
-        for (int c = 0; c < kQc; ++c) qv[c] = row_valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < MT; ++i) {
+          const int ri = r + i * QR;
+          const bool vi = i * QR + row < nrows;
+          uint4 qv[kQc];
+          const uint4 *src = reinterpret_cast<const uint4 *>(
+              reinterpret_cast<const uint16_t *>(a.q) +
+              ((int64_t)(q0 + ri / G) * H + g * G + ri % G) * D);
 #pragma unroll
-        for (int c = 0; c < kQc; ++c) {
-          const uint32_t dst = sb + L::kQ + (c >> 3) * L::kQHalf + (row >> 3) * 1024 +
-                               (row & 7) * 128 + (((c & 7) ^ (row & 7)) << 4);
-          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(qv[c].x),
-                       "r"(qv[c].y), "r"(qv[c].z), "r"(qv[c].w)
-                       : "memory");
+          for (int c = 0; c < kQc; ++c) qv[c] = vi ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int c = 0; c < kQc; ++c) {
+            const uint32_t dst = sb + L::kQ + i * L::kTileQBytes + (c >> 3) * L::kQHalf +
+                                 (row >> 3) * 1024 + (row & 7) * 128 + (((c & 7) ^ (row & 7)) << 4);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(qv[c].x),
+                         "r"(qv[c].y), "r"(qv[c].z), "r"(qv[c].w)
+                         : "memory");
+          }
         }
         fence_proxy_async_smem();
       }
       mbar_arrive(smem_u32(&bars->q_full));
     }
-    const int win_end = row_valid ? ((r / G) / B + 1) * B : 0;
+    int win_end[MT];
+#pragma unroll
+    for (int i = 0; i < MT; ++i)
+      win_end[i] = i * QR + row < nrows ? (((r + i * QR) / G) / B + 1) * B : 0;
     const float sl2 = a.scale_log2;
     bool ok = true;
-    for (int u = 0; u < T; ++u) {
+    // Sub-tile v = u*MT + i: key tile u against row tile i (S/P buffer v % 2).
+    for (int u = 0; u < T && ok; ++u) {
       const int t = t0 + u;
-      ok = mbar_wait(smem_u32(&bars->s_full[u & 1]), (u >> 1) & 1, abort_flag, a.err);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      tc_fence_after();
-      if (tid == 128 && u == 0) D2F_TRACE_MARK(0, 4);
-      if (tid == 128 && u == 1) D2F_TRACE_MARK(0, 14);
-      if (tid == 128 && u == 2) D2F_TRACE_MARK(0, 15);
-      if (tid == 128 && u == T - 1) D2F_TRACE_MARK(0, 5);
-      uint32_t sv[N];
-      const uint32_t s_addr = lane_addr + (u & 1) * N;
-      tmem_ld64(s_addr, sv);
-
-      // keys c < lim of this tile are visible to this row
       const int tile_lim = t < Tc ? C - t * N : n - (t - Tc) * N;  // valid keys of the tile
-      int lim = t < Tc ? tile_lim : win_end - (t - Tc) * N;
-      lim = row_valid ? max(0, min(lim, N)) : 0;
-      float sf[N];
 #pragma unroll
-      for (int c = 0; c < N; ++c) sf[c] = __uint_as_float(sv[c]);
-      if (!__all_sync(0xffffffffu, lim >= N)) {  // ragged tile: hide masked keys
+      for (int i = 0; i < MT; ++i) {
+        const int v = u * MT + i;
+        const bool rv = i * QR + row < nrows;
+        ok = mbar_wait(smem_u32(&bars->s_full[v & 1]), (v >> 1) & 1, abort_flag, a.err);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        if (tid == 128 && i == 0 && u == 0) D2F_TRACE_MARK(0, 4);
+        if (tid == 128 && i == 0 && u == 1) D2F_TRACE_MARK(0, 14);
+        if (tid == 128 && i == 0 && u == 2) D2F_TRACE_MARK(0, 15);
+        if (tid == 128 && i == 0 && u == T - 1) D2F_TRACE_MARK(0, 5);
+        uint32_t sv[N];
+        const uint32_t s_addr = lane_addr + (v & 1) * N;
+        tmem_ld64(s_addr, sv);
+
+        // keys c < lim of this tile are visible to this row
+        int lim = t < Tc ? tile_lim : win_end[i] - (t - Tc) * N;
+        lim = rv ? max(0, min(lim, N)) : 0;
+        float sf[N];
 #pragma unroll
-        for (int c = 0; c < N; ++c)
-          if (c >= lim) sf[c] = -INFINITY;
-      }
-      float tr[N / 2];  // tree maximum (scale > 0, so max(s) * scale = max(s * scale))
+        for (int c = 0; c < N; ++c) sf[c] = __uint_as_float(sv[c]);
+        if (!__all_sync(0xffffffffu, lim >= N)) {  // ragged tile: hide masked keys
 #pragma unroll
-      for (int c = 0; c < N / 2; ++c) tr[c] = fmaxf(sf[2 * c], sf[2 * c + 1]);
-#pragma unroll
-      for (int w = N / 4; w >= 1; w >>= 1)
-#pragma unroll
-        for (int c = 0; c < w; ++c) tr[c] = fmaxf(tr[2 * c], tr[2 * c + 1]);
-      const float tmax = tr[0] * sl2;
-      // Lazy rescale: keep the reference max unless the tile max exceeds it by 2^8.
-      const bool need = tmax > m_ref + 8.0f;
-      if (__any_sync(0xffffffffu, need)) {
-        const float m_new = need ? tmax : m_ref;
-        const float alpha = need ? fast_exp2(m_ref - m_new) : 1.0f;
-        l *= alpha;
-        if (u > 0) {
-          ok = mbar_wait(smem_u32(&bars->pv_done[(u - 1) & 1]), ((u - 1) >> 1) & 1, abort_flag,
-                         a.err);
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t o[32];
-            const uint32_t oa = lane_addr + kTmemO + ch * 32;
-            tmem_ld32(oa, o);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-            tmem_st32(oa, o);
-          }
-          tmem_wait_st();
+          for (int c = 0; c < N; ++c)
+            if (c >= lim) sf[c] = -INFINITY;
         }
-        m_ref = m_new;
+        float tr[N / 2];  // tree maximum (scale > 0, so max(s) * scale = max(s * scale))
+#pragma unroll
+        for (int c = 0; c < N / 2; ++c) tr[c] = fmaxf(sf[2 * c], sf[2 * c + 1]);
+#pragma unroll
+        for (int w = N / 4; w >= 1; w >>= 1)
+#pragma unroll
+          for (int c = 0; c < w; ++c) tr[c] = fmaxf(tr[2 * c], tr[2 * c + 1]);
+        const float tmax = tr[0] * sl2;
+        // Lazy rescale: keep the reference max unless the tile max exceeds it by 2^8.
+        const bool need = tmax > m_ref[i] + 8.0f;
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_new = need ? tmax : m_ref[i];
+          const float alpha = need ? fast_exp2(m_ref[i] - m_new) : 1.0f;
+          l[i] *= alpha;
+          if (u > 0) {
+            // every earlier P.V (MMAs complete in order) has landed in this row
+            // tile's accumulator
+            ok = mbar_wait(smem_u32(&bars->pv_done[(v - 1) & 1]), ((v - 1) >> 1) & 1, abort_flag,
+                           a.err);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) {
+              uint32_t o[32];
+              const uint32_t oa = lane_addr + kTmemO + i * D + ch * 32;
+              tmem_ld32(oa, o);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+              tmem_st32(oa, o);
+            }
+            tmem_wait_st();
+          }
+          m_ref[i] = m_new;
+        }
+        // P = 2^(s*scale - m_ref) in bf16: the exponent argument is formed in float
+        // for a pair of keys at once, rounded to bf16 and exponentiated as a packed
+        // pair (P is a bf16 MMA operand, so it carries bf16 precision either way).
+        // Masked keys are -inf -> 0. A row with no visible key so far keeps
+        // m_ref = -inf: subtract 0 instead.
+        const float mb = m_ref[i] == -INFINITY ? 0.f : m_ref[i];
+        uint32_t pk[N / 2];
+#pragma unroll
+        for (int j = 0; j < N / 2; ++j) {
+          float x0, x1;
+          fma2_bc(x0, x1, sf[2 * j], sf[2 * j + 1], sl2, -mb);
+          pk[j] = ex2_bf16x2(pack_bf16x2(x0, x1));
+        }
+        // row sum of the P actually used (the rounded values), in float pairs
+        float ps0[N / 4], ps1[N / 4];
+#pragma unroll
+        for (int j = 0; j < N / 4; ++j)
+          add2(ps0[j], ps1[j], __uint_as_float(pk[2 * j] << 16),
+               __uint_as_float(pk[2 * j] & 0xffff0000u), __uint_as_float(pk[2 * j + 1] << 16),
+               __uint_as_float(pk[2 * j + 1] & 0xffff0000u));
+#pragma unroll
+        for (int w = N / 8; w >= 1; w >>= 1)
+#pragma unroll
+          for (int c = 0; c < w; ++c)
+            add2(ps0[c], ps1[c], ps0[2 * c], ps1[2 * c], ps0[2 * c + 1], ps1[2 * c + 1]);
+        l[i] += ps0[0] + ps1[0];
+        // P over the scores it came from (this thread's own lane): column c of the
+        // S/P buffer now holds keys 2c and 2c+1.
+        tmem_st32(s_addr, pk);
+        tmem_wait_st();
+        // A ragged tile (partial last page or short window) may hold stale or
+        // non-finite V rows past its valid keys; P is 0 there, but 0 * NaN is not
+        // 0, so clear those rows before the first P.V product reads them.
+        if (i == 0 && row < N && row >= tile_lim) {
+          const uint32_t v_row = sb + L::kRing + (u % NS) * L::kStage + L::kKBytes +
+                                 (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+          for (int h = 0; h < L::kHalves; ++h)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(v_row + h * L::kKVHalf +
+                                                                             (c << 4)),
+                           "r"(0u)
+                           : "memory");
+          fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars->p_full[v & 1]));
+        if (tid == 128 && i == 0 && u == 0) D2F_TRACE_MARK(0, 13);
+        if (tid == 128 && i == MT - 1 && u == T - 1) D2F_TRACE_MARK(0, 6);
       }
-      // P = 2^(s*scale - m_ref) in bf16: the exponent argument is formed in float
-      // for a pair of keys at once, rounded to bf16 and exponentiated as a packed
-      // pair (P is a bf16 MMA operand, so it carries bf16 precision either way).
-      // Masked keys are -inf -> 0. A row with no visible key so far keeps
-      // m_ref = -inf: subtract 0 instead.
-      const float mb = m_ref == -INFINITY ? 0.f : m_ref;
-      uint32_t pk[N / 2];
-#pragma unroll
-      for (int j = 0; j < N / 2; ++j) {
-        float x0, x1;
-        fma2_bc(x0, x1, sf[2 * j], sf[2 * j + 1], sl2, -mb);
-        pk[j] = ex2_bf16x2(pack_bf16x2(x0, x1));
-      }
-      // row sum of the P actually used (the rounded values), in float pairs
-      float ps0[N / 4], ps1[N / 4];
-#pragma unroll
-      for (int j = 0; j < N / 4; ++j)
-        add2(ps0[j], ps1[j], __uint_as_float(pk[2 * j] << 16),
-             __uint_as_float(pk[2 * j] & 0xffff0000u), __uint_as_float(pk[2 * j + 1] << 16),
-             __uint_as_float(pk[2 * j + 1] & 0xffff0000u));
-#pragma unroll
-      for (int w = N / 8; w >= 1; w >>= 1)
-#pragma unroll
-        for (int c = 0; c < w; ++c) add2(ps0[c], ps1[c], ps0[2 * c], ps1[2 * c], ps0[2 * c + 1], ps1[2 * c + 1]);
-      l += ps0[0] + ps1[0];
-      // P over the scores it came from (this thread's own lane): column c of the
-      // S/P buffer now holds keys 2c and 2c+1.
-      tmem_st32(s_addr, pk);
-      tmem_wait_st();
-      // A ragged tile (partial last page or short window) may hold stale or
-      // non-finite V rows past its valid keys; P is 0 there, but 0 * NaN is not
-      // 0, so clear those rows before the P.V product reads them.
-      if (row < N && row >= tile_lim) {
-        const uint32_t v_row = sb + L::kRing + (u % NS) * L::kStage + L::kKBytes +
-                               (row >> 3) * 1024 + (row & 7) * 128;
-#pragma unroll
-        for (int h = 0; h < L::kHalves; ++h)
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(v_row + h * L::kKVHalf +
-                                                                           (c << 4)),
-                         "r"(0u)
-                         : "memory");
-        fence_proxy_async_smem();
-      }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bars->p_full[u & 1]));
-      if (tid == 128 && u == 0) D2F_TRACE_MARK(0, 13);
-      if (tid == 128 && u == T - 1) D2F_TRACE_MARK(0, 6);
     }
     if (ok) {  // the last P.V product
-      ok = mbar_wait(smem_u32(&bars->pv_done[(T - 1) & 1]), ((T - 1) >> 1) & 1, abort_flag, a.err);
+      const int last = T * MT - 1;
+      ok = mbar_wait(smem_u32(&bars->pv_done[last & 1]), (last >> 1) & 1, abort_flag, a.err);
       ok = __all_sync(0xffffffffu, ok);
     }
     tc_fence_after();
@@ -541,26 +575,32 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR>::kCtasPerSm))
   const bool aborted = *abort_flag != 0;
   bool tmem_freed = false;
   if (cs == 1) {
-    if (warp >= 2 && has_work && !aborted && __any_sync(0xffffffffu, row_valid)) {
-      const int64_t hr = (int64_t)(q0 + r / G) * H + g * G + r % G;
-      const float inv = 1.0f / l;
-      uint16_t *dst = reinterpret_cast<uint16_t *>(a.out) + hr * D;
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t o[32];
-        tmem_ld32(lane_addr + kTmemO + ch * 32, o);
-        if (row_valid) {
-          uint32_t w[16];
+    for (int i = 0; i < MT; ++i) {
+      const bool rv = i * QR + row < nrows;
+      if (warp >= 2 && has_work && !aborted && __any_sync(0xffffffffu, rv)) {
+        const int ri = r + i * QR;
+        const int64_t hr = (int64_t)(q0 + ri / G) * H + g * G + ri % G;
+        const float inv = 1.0f / l[i];
+        uint16_t *dst = reinterpret_cast<uint16_t *>(a.out) + hr * D;
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            w[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
-          uint4 *d4 = reinterpret_cast<uint4 *>(dst + ch * 32);
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t o[32];
+          tmem_ld32(lane_addr + kTmemO + i * D + ch * 32, o);
+          if (rv) {
+            uint32_t w[16];
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            d4[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+            for (int j = 0; j < 16; ++j)
+              w[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv,
+                                 __uint_as_float(o[2 * j + 1]) * inv);
+            uint4 *d4 = reinterpret_cast<uint4 *>(dst + ch * 32);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              d4[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+          }
         }
+        if (rv && a.lse_out) a.lse_out[hr] = (m_ref[i] + __log2f(l[i])) * 0.6931471805599453f;
       }
-      if (row_valid && a.lse_out) a.lse_out[hr] = (m_ref + __log2f(l)) * 0.6931471805599453f;
     }
   } else if (active) {
     const int LR = L::rows_per_owner(cs);  // rows a CTA owns (at most)
@@ -568,45 +608,51 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR>::kCtasPerSm))
     const uint32_t recv = sb + L::kQ;      // [source split][BS], filled by the bulk copies
     const uint32_t stg = sb + L::staging(cs);  // [owner][BS], this CTA's rows
     const uint32_t recv_bar = smem_u32(&bars->recv);
-    // 1) stage this CTA's rows: local row -> owner row % cs, slot row / cs; the
-    //    16-byte chunks of a row are XOR-swizzled by (row % 8).
-    if (warp >= 2 && __any_sync(0xffffffffu, row_valid)) {
-      const int owner = row % cs, lr = row / cs, key = row & 7;
-      const uint32_t blk = stg + owner * BS;
-      const bool mine = has_work && !aborted;  // CTA-uniform
-      const bool keep = mine && row_valid && l > 0.f;
-      if (mine) {
-        const float inv = keep ? 1.0f / l : 0.f;
+    // 1) stage this CTA's rows: local row (i*QR + lane row of row tile i) ->
+    //    owner lrow % cs, slot lrow / cs; the 16-byte chunks of a row are
+    //    XOR-swizzled by (lrow % 8).
 #pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t o[32];
-          tmem_ld32(lane_addr + kTmemO + ch * 32, o);
-          if (keep) {
+    for (int i = 0; i < MT; ++i) {
+      const int lrow = i * QR + row;
+      const bool rv = lrow < nrows;
+      if (warp >= 2 && __any_sync(0xffffffffu, rv)) {
+        const int owner = lrow % cs, lr = lrow / cs, key = lrow & 7;
+        const uint32_t blk = stg + owner * BS;
+        const bool mine = has_work && !aborted;  // CTA-uniform
+        const bool keep = mine && rv && l[i] > 0.f;
+        if (mine) {
+          const float inv = keep ? 1.0f / l[i] : 0.f;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int c = ch * 4 + j;  // 8 bf16 per 16-byte chunk
-              const uint32_t dst = blk + lr * L::kRowBytes + ((c ^ key) << 4);
-              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
-                           "r"(pack_bf16x2(__uint_as_float(o[8 * j]) * inv,
-                                           __uint_as_float(o[8 * j + 1]) * inv)),
-                           "r"(pack_bf16x2(__uint_as_float(o[8 * j + 2]) * inv,
-                                           __uint_as_float(o[8 * j + 3]) * inv)),
-                           "r"(pack_bf16x2(__uint_as_float(o[8 * j + 4]) * inv,
-                                           __uint_as_float(o[8 * j + 5]) * inv)),
-                           "r"(pack_bf16x2(__uint_as_float(o[8 * j + 6]) * inv,
-                                           __uint_as_float(o[8 * j + 7]) * inv))
-                           : "memory");
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t o[32];
+            tmem_ld32(lane_addr + kTmemO + i * D + ch * 32, o);
+            if (keep) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int c = ch * 4 + j;  // 8 bf16 per 16-byte chunk
+                const uint32_t dst = blk + lr * L::kRowBytes + ((c ^ key) << 4);
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
+                             "r"(pack_bf16x2(__uint_as_float(o[8 * j]) * inv,
+                                             __uint_as_float(o[8 * j + 1]) * inv)),
+                             "r"(pack_bf16x2(__uint_as_float(o[8 * j + 2]) * inv,
+                                             __uint_as_float(o[8 * j + 3]) * inv)),
+                             "r"(pack_bf16x2(__uint_as_float(o[8 * j + 4]) * inv,
+                                             __uint_as_float(o[8 * j + 5]) * inv)),
+                             "r"(pack_bf16x2(__uint_as_float(o[8 * j + 6]) * inv,
+                                             __uint_as_float(o[8 * j + 7]) * inv))
+                             : "memory");
+              }
             }
           }
         }
+        if (rv) {
+          const float mx = keep ? m_ref[i] : -INFINITY, sm = keep ? l[i] : 0.f;
+          asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(blk + LR * L::kRowBytes + lr * 8),
+                       "f"(mx), "f"(sm)
+                       : "memory");
+        }
+        fence_proxy_async_smem();  // the bulk copies read these blocks
       }
-      if (row_valid) {
-        const float mx = keep ? m_ref : -INFINITY, sm = keep ? l : 0.f;
-        asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(blk + LR * L::kRowBytes + lr * 8),
-                     "f"(mx), "f"(sm)
-                     : "memory");
-      }
-      fence_proxy_async_smem();  // the bulk copies read these blocks
     }
     // 2) each owner expects cs blocks; the cluster barrier publishes the staged
     //    blocks and frees every receive area (each CTA is past its ring).
@@ -617,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR>::kCtasPerSm))
     if (tid == 0) D2F_TRACE_MARK(0, 8);
     if (warp == 1) {  // every O row is staged: TMEM is free for the next grid's CTAs
       tc_fence_after();
-      tmem_dealloc(bars->tmem_base, kTmemCols);
+      tmem_dealloc(bars->tmem_base, L::kTmemCols);
       tmem_freed = true;
     }
     // 3) block j of this CTA -> receive slot [split] of CTA j
@@ -705,7 +751,7 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR>::kCtasPerSm))
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1 && !tmem_freed) tmem_dealloc(bars->tmem_base, kTmemCols);
+  if (warp == 1 && !tmem_freed) tmem_dealloc(bars->tmem_base, L::kTmemCols);
   if (tid == 0) D2F_TRACE_MARK(0, 11);
 }
 
@@ -743,7 +789,7 @@ bool encode(EncodeTiledFn fn, CUtensorMap *map, const void *base, int rank, cons
 
 // Function attributes (shared-memory opt-in and carveout) are per device; set
 // them once per device and kernel variant.
-template <int D, int NS, int QR>
+template <int D, int NS, int QR, int MT>
 cudaError_t ensure_attrs() {
   static std::mutex mu;
   static bool done[64] = {};
@@ -752,16 +798,16 @@ cudaError_t ensure_attrs() {
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(attn_tc_kernel<D, NS, QR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Layout<D, NS, QR>::kAlloc);
+  e = cudaFuncSetAttribute(attn_tc_kernel<D, NS, QR, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Layout<D, NS, QR, MT>::kAlloc);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_tc_kernel<D, NS, QR>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(attn_tc_kernel<D, NS, QR, MT>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return e;
 }
 
-template <int D, int NS, int QR>
+template <int D, int NS, int QR, int MT>
 cudaError_t launch_d(const AttnArgs &a, cudaStream_t s, char *why, size_t why_len) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) {
@@ -784,13 +830,13 @@ cudaError_t launch_d(const AttnArgs &a, cudaStream_t s, char *why, size_t why_le
     snprintf(why, why_len, "cuTensorMapEncodeTiled rejected a K/V tensor (alignment or size)");
     return cudaErrorInvalidValue;
   }
-  cudaError_t e = ensure_attrs<D, NS, QR>();
+  cudaError_t e = ensure_attrs<D, NS, QR, MT>();
   if (e != cudaSuccess) return e;
   const int cs = a.num_splits;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cs, a.m_tiles, a.batch * a.num_heads_kv);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Layout<D, NS, QR>::kAlloc;
+  cfg.dynamicSmemBytes = Layout<D, NS, QR, MT>::kAlloc;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -801,7 +847,7 @@ cudaError_t launch_d(const AttnArgs &a, cudaStream_t s, char *why, size_t why_le
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_enabled() ? 2 : 1;
-  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<D, NS, QR>, a, kp, vp, kw, vw);
+  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<D, NS, QR, MT>, a, kp, vp, kw, vw);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -820,11 +866,11 @@ int attn_tc_deep_slots(int cs) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
   if (cache[dev][cs] == 0) {
-    if (ensure_attrs<128, 6, 128>() != cudaSuccess) return 0;
+    if (ensure_attrs<128, 6, 128, 1>() != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cs, 1, 1);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = Layout<128, 6, 128>::kAlloc;
+    cfg.dynamicSmemBytes = Layout<128, 6, 128, 1>::kAlloc;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = cs;
@@ -833,7 +879,7 @@ int attn_tc_deep_slots(int cs) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<128, 6, 128>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<128, 6, 128, 1>, &cfg) != cudaSuccess) {
       cudaGetLastError();
       return 0;
     }
@@ -851,17 +897,23 @@ cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t s, char *why, size_t 
   // Ring depth by shared-memory budget: two CTAs per SM hold Q + NS stages in
   // ~113 KB (head_dim 64: 6 stages; head_dim 128: 3 stages with 64-row tiles, 2
   // with 128-row tiles); the 6-stage head_dim-128 variant takes a whole SM.
-  const int rows = a.tc_rows, ns = a.tc_stages;
+  // The MT > 1 variants hold MT 128-row tiles of one (sequence, KV head) in one
+  // CTA (GQA groups of 129..384 rows): every K/V tile is loaded once for all of
+  // them, and the CTA takes a whole SM.
+  const int rows = a.tc_rows, ns = a.tc_stages, mt = a.tc_mt;
   if (a.head_dim == 128) {
-    if (rows == 64 && ns == 3) return launch_d<128, 3, 64>(a, s, why, why_len);
-    if (rows == 128 && ns == 2) return launch_d<128, 2, 128>(a, s, why, why_len);
-    if (rows == 128 && ns == 6) return launch_d<128, 6, 128>(a, s, why, why_len);
+    if (rows == 64 && ns == 3 && mt == 1) return launch_d<128, 3, 64, 1>(a, s, why, why_len);
+    if (rows == 128 && ns == 2 && mt == 1) return launch_d<128, 2, 128, 1>(a, s, why, why_len);
+    if (rows == 128 && ns == 6 && mt == 1) return launch_d<128, 6, 128, 1>(a, s, why, why_len);
+    if (rows == 128 && ns == 5 && mt == 2) return launch_d<128, 5, 128, 2>(a, s, why, why_len);
+    if (rows == 128 && ns == 4 && mt == 3) return launch_d<128, 4, 128, 3>(a, s, why, why_len);
   } else if (a.head_dim == 64) {
-    if (rows == 64 && ns == 6) return launch_d<64, 6, 64>(a, s, why, why_len);
-    if (rows == 128 && ns == 6) return launch_d<64, 6, 128>(a, s, why, why_len);
+    if (rows == 64 && ns == 6 && mt == 1) return launch_d<64, 6, 64, 1>(a, s, why, why_len);
+    if (rows == 128 && ns == 6 && mt == 1) return launch_d<64, 6, 128, 1>(a, s, why, why_len);
   }
-  snprintf(why, why_len, "no tensor-core variant for head_dim %d, %d-row tiles, %d stages",
-           a.head_dim, rows, ns);
+  snprintf(why, why_len,
+           "no tensor-core variant for head_dim %d, %d-row tiles x %d, %d stages", a.head_dim,
+           rows, mt, ns);
   return cudaErrorInvalidValue;
   snprintf(why, why_len, "tensor-core path supports head_dim 64 or 128");
   return cudaErrorInvalidValue;

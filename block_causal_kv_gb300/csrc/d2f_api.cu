@@ -61,6 +61,7 @@ struct AttnPlan {
   int m_tiles;
   int rows;       // rows per tile: 64 or 128 on the tensor-core path
   int stages;     // tensor-core K/V ring depth
+  int mt;         // tensor-core 128-row tiles per CTA
   bool longest_first;  // more CTAs than one wave: longest sequences first
   int splits;
   int tiles_per_split;
@@ -83,6 +84,14 @@ bool force_full_rows() {
 
 // D2F_TC_DEEP=1 / 0 forces / forbids the one-CTA-per-SM 6-stage variant for
 // head_dim 128 with 128-row tiles (for comparisons and tests); unset = planner.
+// D2F_TC_MT=1 / 0 forces / forbids one CTA for all the 128-row tiles (2 or 3) of a
+// (sequence, KV head) for head_dim 128 (tests); unset = planner.
+int force_mt() {
+  const char *e = getenv("D2F_TC_MT");
+  if (!e || !e[0]) return -1;
+  return e[0] == '1' ? 1 : 0;
+}
+
 int force_deep() {
   const char *e = getenv("D2F_TC_DEEP");
   if (!e || !e[0]) return -1;
@@ -141,9 +150,32 @@ int plan_attn(int batch, int total_q, int max_q, int max_ctx, int Hq, int Hkv, i
       return cdiv(t_max, cdiv(t_max, most));
     };
     p->stages = D == 64 ? 6 : (rows == 64 ? 3 : 2);
+    p->mt = 1;
     const int two = splits ? splits : pick(false);  // two CTAs per SM
     splits = two;
-    if (D == 128 && rows == 128) {
+    if (D == 128 && rows == 128 && (p->m_tiles == 2 || p->m_tiles == 3)) {
+      // GQA groups of 129..384 rows: one CTA for all the row tiles of a (sequence,
+      // KV head) reads each K/V tile once instead of m_tiles times, through a
+      // deeper ring, at one CTA per SM. It serialises the row tiles' softmax per
+      // key tile, so it pays only once splits are long.
+      const long long base_mt = (long long)max(batch, 1) * Hkv;
+      int one = splits ? splits : 1;
+      if (!num_splits) {
+        int most = 1;
+        for (int cs = 2; cs <= min(kTcMaxSplits, t_max); ++cs)
+          if (attn_tc_deep_slots(cs) > 0 && base_mt * cs <= attn_tc_deep_slots(cs)) most = cs;
+        one = cdiv(t_max, cdiv(t_max, most));
+      }
+      bool use = cdiv(t_max, two) >= 8 && attn_tc_deep_slots(one) > 0;
+      if (force_mt() >= 0) use = force_mt() == 1;
+      if (use) {
+        p->mt = p->m_tiles;
+        p->stages = p->mt == 3 ? 4 : 5;
+        p->m_tiles = 1;
+        splits = one;
+      }
+    }
+    if (p->mt == 1 && D == 128 && rows == 128) {
       // 2 ring stages at two CTAs per SM, or 6 stages at one: per streamed tile a
       // CTA takes ~2.2 us in the first (the ring waits on the load latency) and
       // ~0.9 us in the second (measured on GB300); take the deeper ring when its
@@ -163,8 +195,9 @@ int plan_attn(int batch, int total_q, int max_q, int max_ctx, int Hq, int Hkv, i
     }
     p->splits = min(splits, kTcMaxSplits);
     {
-      const long long ctas = base * p->splits;
-      const long long slots = p->stages == 6 && D == 128 ? attn_tc_deep_slots(p->splits) : 2LL * sms;
+      const long long ctas = (long long)max(batch, 1) * Hkv * p->m_tiles * p->splits;
+      const bool whole_sm = D == 128 && (p->stages == 6 || p->mt > 1);
+      const long long slots = whole_sm ? attn_tc_deep_slots(p->splits) : 2LL * sms;
       const char *ev = getenv("D2F_LONGEST_FIRST");  // 1 / 0: force on / off (tests)
       const bool want = (ev && ev[0]) ? ev[0] == '1' : ctas > slots;
       p->longest_first = batch > 1 && batch <= kMaxLongestFirstBatch && want;
@@ -339,6 +372,7 @@ int d2f_block_attn(const void *q, const void *k_win, const void *v_win, const vo
   a.m_tiles = p.m_tiles;
   a.tc_rows = p.rows;
   a.tc_stages = p.stages;
+  a.tc_mt = p.mt > 0 ? p.mt : 1;
   a.longest_first = p.longest_first ? 1 : 0;
   a.counters = reinterpret_cast<int32_t *>(workspace);
   a.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) + p.off_ml);

@@ -83,6 +83,26 @@ def test_ring_depth_variants_for_full_row_tiles(name, splits, deep, monkeypatch)
     check_attention(out, lse, ref, ref_lse, torch.bfloat16, "deep%s/%s/s%d" % (deep, name, splits))
 
 
+def _gqa_two_tiles():
+    # G = 4, windows of 3 and 2 blocks of 16: 192 and 128 packed rows
+    return synth.Workload("gqa2", 2, 16, 4, 128, 16, torch.bfloat16, [700, 333], [3, 2], 64,
+                          permute_pages=True, extra_pages=3, seed=515)
+
+
+@pytest.mark.parametrize("name", ["dream", "gqa2"])
+@pytest.mark.parametrize("splits", [0, 1, 3, 8])
+def test_all_row_tiles_of_a_kv_head_in_one_cta(name, splits, monkeypatch):
+    """GQA groups of 2 or 3 row tiles in one CTA (D2F_TC_MT=1): one K/V stream,
+    one accumulator per row tile; same result as the oracle."""
+    dev = device()
+    monkeypatch.setenv("D2F_TC_MT", "1")
+    w = _gqa_two_tiles() if name == "gqa2" else synth.small(name)
+    p = synth.make_problem(w)
+    out, lse = _run(p, dev, splits)
+    ref, ref_lse = _ref(p)
+    check_attention(out, lse, ref, ref_lse, torch.bfloat16, "mt/%s/s%d" % (name, splits))
+
+
 @pytest.mark.parametrize("name", ["ragged", "dream", "long_b32"])
 @pytest.mark.parametrize("splits", [0, 1, 3])
 def test_longest_first_sequence_order(name, splits, monkeypatch):
