@@ -474,14 +474,18 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR, MT>::kCtasPerSm))
           for (int c = 0; c < N; ++c)
             if (c >= lim) sf[c] = -INFINITY;
         }
-        float tr[N / 2];  // tree maximum (scale > 0, so max(s) * scale = max(s * scale))
+        // tree maximum of the 64 scores with three-input maxima (scale > 0, so
+        // max(s) * scale = max(s * scale)): 64 -> 22 -> 8 -> 3 -> 1
+        static_assert(N == 64, "maximum tree shape");
+        float t1[22], t2[8];
 #pragma unroll
-        for (int c = 0; c < N / 2; ++c) tr[c] = fmaxf(sf[2 * c], sf[2 * c + 1]);
+        for (int c = 0; c < 21; ++c) t1[c] = fmax3(sf[3 * c], sf[3 * c + 1], sf[3 * c + 2]);
+        t1[21] = sf[63];
 #pragma unroll
-        for (int w = N / 4; w >= 1; w >>= 1)
-#pragma unroll
-          for (int c = 0; c < w; ++c) tr[c] = fmaxf(tr[2 * c], tr[2 * c + 1]);
-        const float tmax = tr[0] * sl2;
+        for (int c = 0; c < 7; ++c) t2[c] = fmax3(t1[3 * c], t1[3 * c + 1], t1[3 * c + 2]);
+        t2[7] = t1[21];
+        const float tmax = fmax3(fmax3(t2[0], t2[1], t2[2]), fmax3(t2[3], t2[4], t2[5]),
+                                 fmaxf(t2[6], t2[7])) * sl2;
         // Lazy rescale: keep the reference max unless the tile max exceeds it by 2^8.
         const bool need = tmax > m_ref[i] + 8.0f;
         if (__any_sync(0xffffffffu, need)) {

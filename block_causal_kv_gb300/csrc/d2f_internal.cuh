@@ -457,6 +457,12 @@ __device__ __forceinline__ void add2(float &d0, float &d1, float a0, float a1, f
       : "=f"(d0), "=f"(d1)
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
+// Largest of three floats, one instruction (NaN operands are ignored, as fmaxf).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 // 2^x for both bf16 halves of a packed pair (flush-to-zero; 2^-inf = 0).
 __device__ __forceinline__ uint32_t ex2_bf16x2(uint32_t x) {
   uint32_t y;
