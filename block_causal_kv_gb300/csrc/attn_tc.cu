@@ -11,28 +11,40 @@
 // head): the G = Hq/Hkv query heads of the group are packed into the rows
 // (row r = query r / G, head r % G), so every K/V byte is read once per row
 // tile. QR is 128, or 64 when every sequence has at most 64 rows (the Q tile
-// then takes half the shared memory and the ring gets a third stage). The key
-// tiles of the row tile (64 keys = 64/B cache pages or 64/B window blocks, cache
-// first) are split among the `cs` CTAs of one thread-block cluster. A CTA needs
-// at most ~113 KB of shared memory and 256 TMEM columns, so two CTAs share an SM
-// and hide each other's latencies. Each CTA streams its share through an
-// NS-stage shared-memory ring:
+// then takes half the shared memory and the ring gets a third stage). A CTA
+// holds MT row tiles (1, or 2 for GQA groups of 129..384 rows) of one
+// (sequence, KV head), each with its own softmax warpgroup, so one K/V tile
+// read serves both. The key tiles (64 keys = 64/B cache pages or 64/B window
+// blocks, cache first) are split among the `cs` CTAs of one thread-block
+// cluster. With MT = 1 a CTA needs at most ~113 KB of shared memory and 256 TMEM
+// columns, so two CTAs share an SM and hide each other's latencies. Each CTA
+// streams its share through an NS-stage shared-memory ring:
 //
-//   warp 0       TMA producer: page ids (requested with the sequence metadata,
-//                32 at a time) -> cp.async.bulk.tensor loads of the K and V
-//                tiles, 128-byte swizzle, completion counted on an mbarrier.
-//   warp 1       TMEM owner and MMA issuer (one lane): S = Q K^T into TMEM
-//                (double-buffered), then O += P V with P read from TMEM.
-//   warps 2-5    softmax, one thread per query row (TMEM lane = row): read the
-//                row's 64 scores, apply the block-causal mask as a per-row key
-//                limit, online softmax in log2 units with lazy rescaling of O
-//                (only when the running max grows by more than 2^8), write bf16 P
-//                over the scores it came from (TMEM columns 0-31 of the S buffer),
-//                where the second MMA reads its A operand.
+//   producers    page ids (requested with the sequence metadata, 32 at a time)
+//                -> cp.async.bulk.tensor loads of the K and V tiles, 128-byte
+//                swizzle, completion counted on an mbarrier. Warp 0; with two
+//                row tiles a second warp; with 64-row tiles also the two softmax
+//                warps whose TMEM lanes hold no rows. A tile's boxes are spread
+//                over lanes and warps: one thread issues a copy only every ~170
+//                cycles.
+//   warps 1..MT  MMA issuers, one lane per row tile (warp 1 also owns TMEM):
+//                S = Q K^T into TMEM (double-buffered), then O += P V with P read
+//                from TMEM. One thread issues a tcgen05.mma only every ~100
+//                cycles whatever its N, so each row tile has its own issuer.
+//   softmax      one warpgroup per row tile, one thread per query row
+//                (TMEM lane = row): read the row's 64 scores, apply the
+//                block-causal mask as a per-row key limit, online softmax in log2
+//                units with lazy rescaling of O (only when the running max grows
+//                by more than 2^8), write bf16 P over the scores it came from
+//                (TMEM columns 0-31 of the S buffer), where the second MMA reads
+//                its A operand.
+//
+// TMEM columns of warpgroup w: [w*(128+D), +64) and [+64, +128) the two S/P
+// buffers, then D columns of O.
 //
 // The MMA always has M = 128: with a 64-row Q tile, A rows 64-127 read whatever
-// shared memory follows the tile. Those rows of S are never used (their softmax
-// threads mask every key, so their P rows are exactly 0 and their O rows stay 0).
+// shared memory follows the tile. Rows 64-127 of S, P and O are never read back
+// (their TMEM lanes belong to warps that load K/V instead).
 //
 // Composition. With cs > 1 every CTA writes its rows, normalised (O / l, bf16)
 // with their (max, sum), into a staging block per owning CTA (row r -> CTA
@@ -56,12 +68,10 @@
 namespace d2f {
 namespace {
 
-constexpr int kSoftWarps = 4;
-constexpr int kSoftThreads = 32 * kSoftWarps;  // one per TMEM lane
-constexpr int kThreads = 64 + kSoftThreads;    // producer + MMA warps + softmax
+constexpr int kWgThreads = 128;                // one softmax warpgroup: a thread per TMEM lane
 constexpr int M = kTcRows;                     // UMMA M: 128 rows
 constexpr int N = kTcKeys;                     // 64 keys per tile
-constexpr uint32_t kTmemO = 128;               // first TMEM column of O (S / P: 2 x 64 before it)
+constexpr uint32_t kTmemO = 128;               // O within a warpgroup's columns (S / P: 2 x 64 before it)
 constexpr int kMaxCluster = 8;
 constexpr int kBarSetup = 1;                   // named barrier: MMA warp + softmax warps
 constexpr int kSmemTwoPerSm = 115712;          // dynamic bytes that still let 2 CTAs share an SM
@@ -70,11 +80,20 @@ static_assert(kMaxLongestFirstBatch * 4 + 4 <= 2 * 64 * 64 * 2, "ordering scratc
 template <int D, int NS, int QR, int MT>
 struct Layout {
   static constexpr int kHalves = D / 64;         // 64-element (128-byte) swizzle columns
+  // warp 0 producer, warps 1..MT MMA issuers (one per row tile), with MT = 2 a
+  // second producer warp, then MT softmax warpgroups. With QR = 64 the two
+  // softmax warps whose TMEM lanes (64-127) hold no rows load K/V as well.
+  static constexpr int kFirstSoft = 1 + MT + (MT == 2 ? 1 : 0);
+  static constexpr int kThreads = 32 * kFirstSoft + kWgThreads * MT;
+  static constexpr int kSoftWarps = 4 * MT;
+  static constexpr int kProducers = 1 + (MT == 2 ? 1 : 0) + (QR == 64 ? 2 : 0);
+  static constexpr int kGroups = 2 * kHalves;  // TMA box groups of a tile: (K | V) x column half
   static constexpr int kQHalf = QR * 128;        // one 64-wide column block of one Q tile
   static constexpr int kTileQBytes = kHalves * kQHalf;
   static constexpr int kQBytes = MT * kTileQBytes;  // MT row tiles of Q
-  // TMEM: S / P buffers (2 x 64 columns), then MT accumulators of D columns
-  static constexpr uint32_t kTmemCols = 128 + MT * D <= 256 ? 256 : 512;
+  // TMEM: per warpgroup, two S / P buffers of 64 columns, then D columns of O
+  static constexpr uint32_t kWgCols = 128 + D;
+  static constexpr uint32_t kTmemCols = MT * kWgCols <= 256 ? 256 : 512;
   static constexpr int kKVHalf = N * 128;        // 64 key rows x 128 bytes
   static constexpr int kKBytes = kHalves * kKVHalf;
   static constexpr int kStage = 2 * kKBytes;     // K tile then V tile
@@ -100,21 +119,38 @@ struct Layout {
   static_assert(2 * ((MT * QR + kMaxCluster - 1) * (kRowBytes + 8) + 16 * kMaxCluster) + 128 <=
                     kBars,
                 "receive and staging blocks must fit in the Q + ring area");
-  static_assert(128 + MT * D <= 512, "accumulators fit TMEM");
+  static_assert(MT == 1 || MT == 2, "one or two softmax warpgroups");
+  static_assert(MT * kWgCols <= 512, "S / P buffers and accumulators fit TMEM");
+  static_assert(kAlloc <= 232448, "shared memory per CTA");
 };
 
 constexpr int kMaxStages = 6;
 
+#ifdef D2F_TRACE
+// Development build only: SM clock at points of the first 64 key tiles of CTA
+// (0, 0, 0), per actor (0/1: first thread of softmax warpgroup 0/1, 2: MMA).
+static __device__ long long g_d2f_pass[3][8][64];
+#define D2F_PASS_MARK(actor, point, u)                                                   \
+  do {                                                                                   \
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (u) < 64)               \
+      g_d2f_pass[actor][point][u] = clock64();                                           \
+  } while (0)
+#else
+#define D2F_PASS_MARK(actor, point, u) ((void)0)
+#endif
+
 struct Bars {
-  uint64_t full[kMaxStages], empty[kMaxStages], s_full[2], p_full[2], pv_done[2], q_full, drain,
-      recv;
+  // s_full / p_full / pv_done: [warpgroup][S/P buffer]
+  uint64_t full[kMaxStages], empty[kMaxStages], s_full[2][2], p_full[2][2], pv_done[2][2], q_full,
+      drain, recv;
   uint32_t tmem_base;
   int abort_flag;
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
 template <int D, int NS, int QR, int MT>
-__global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR, MT>::kCtasPerSm))
+__global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
+                                  (Layout<D, NS, QR, MT>::kCtasPerSm))
     attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_kpool,
                    const __grid_constant__ CUtensorMap tm_vpool,
                    const __grid_constant__ CUtensorMap tm_kwin,
@@ -151,16 +187,17 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR, MT>::kCtasPerSm))
   // ---- set-up that reads no global memory --------------------------------------
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
-      mbar_init(smem_u32(&bars->full[i]), 1);
-      mbar_init(smem_u32(&bars->empty[i]), 1);
+      mbar_init(smem_u32(&bars->full[i]), L::kProducers);
+      mbar_init(smem_u32(&bars->empty[i]), MT);  // one release per MMA issuer
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&bars->s_full[i]), 1);
-      mbar_init(smem_u32(&bars->p_full[i]), kSoftThreads);
-      mbar_init(smem_u32(&bars->pv_done[i]), 1);
-    }
-    mbar_init(smem_u32(&bars->q_full), kSoftThreads);
-    mbar_init(smem_u32(&bars->drain), 1);
+    for (int w = 0; w < MT; ++w)
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(smem_u32(&bars->s_full[w][i]), 1);
+        mbar_init(smem_u32(&bars->p_full[w][i]), QR);  // the threads of rows < QR
+        mbar_init(smem_u32(&bars->pv_done[w][i]), 1);
+      }
+    mbar_init(smem_u32(&bars->q_full), QR * MT);
+    mbar_init(smem_u32(&bars->drain), MT);
     mbar_init(smem_u32(&bars->recv), 1);
     bars->abort_flag = 0;
     mbar_fence_init();  // cluster scope: other CTAs complete bytes on `recv`
@@ -206,10 +243,10 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR, MT>::kCtasPerSm))
     // same permutation from the same ctx_len values. Scratch: ring stage 0, which
     // no copy has touched yet.
     int *scr = reinterpret_cast<int *>(smem + L::kRing);
-    for (int j = tid; j < a.batch; j += kThreads) scr[j] = __ldg(a.ctx_len + j);
+    for (int j = tid; j < a.batch; j += L::kThreads) scr[j] = __ldg(a.ctx_len + j);
     __syncthreads();
     const int want = b;  // this CTA takes the sequence of rank `want`
-    for (int j = tid; j < a.batch; j += kThreads) {
+    for (int j = tid; j < a.batch; j += L::kThreads) {
       const int cj = scr[j];
       int rank = 0;
       for (int i = 0; i < a.batch; ++i) {
@@ -228,8 +265,13 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR, MT>::kCtasPerSm))
   // its first logical page is known up front.
   const int ppt = N / a.block_size;  // pages (or window blocks) per tile
   const int pre_chunk = split * a.tiles_per_split * ppt;
+  // producer index of this warp (-1: not a producer)
+  const int prod = warp == 0 ? 0
+                   : (MT == 2 && warp == 1 + MT) ? 1
+                   : (QR == 64 && warp >= L::kFirstSoft && (warp & 3) >= 2) ? 1 + (MT == 2) + ((warp & 3) - 2)
+                   : -1;
   int pre_ids = -1;
-  if (warp == 0 && pre_chunk + lane < a.max_pages_per_seq)
+  if (prod >= 0 && pre_chunk + lane < a.max_pages_per_seq)
     pre_ids = __ldg(a.page_table + (int64_t)b * a.max_pages_per_seq + pre_chunk + lane);
 
   // ---- work of this CTA (uniform across the cluster except has_work) ---------
@@ -241,6 +283,7 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR, MT>::kCtasPerSm))
   const int r_begin = mt * MT * QR;  // first of the MT row tiles of this CTA
   active = active && r_begin < rows_total;
   const int nrows = active ? min(MT * QR, rows_total - r_begin) : 0;  // valid rows, all tiles
+  const int mt_live = (nrows + QR - 1) / QR;  // row tiles of this CTA that hold rows
   const int Tc = (C + N - 1) / N, Tw = (n + N - 1) / N;
   // Split s takes tiles [s*tps, (s+1)*tps); tps comes from the host's max_ctx and
   // grows here only if a sequence is longer than that hint promised.
@@ -253,26 +296,36 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR, MT>::kCtasPerSm))
   uint32_t tmem = 0;
   if (active && warp >= 1) {  // TMEM address, published by warp 1
     tc_fence_before();
-    named_sync(kBarSetup, 32 + kSoftThreads);
+    named_sync(kBarSetup, L::kThreads - 32);
     tc_fence_after();
     tmem = bars->tmem_base;
   }
   if (tid == 0) D2F_TRACE_MARK(0, 2);
 
-  // softmax-thread identity (warps 2-5): row = TMEM lane
+  // softmax-thread identity (warps 1+MT..): warpgroup wg takes row tile wg of the
+  // CTA; row = TMEM lane (a warp reaches lanes 32 * (warp % 4) .. + 31)
+  const int wg = warp >= L::kFirstSoft ? (warp - L::kFirstSoft) >> 2 : 0;
   const int quad = warp & 3;
   const int row = quad * 32 + lane;
-  const int r = r_begin + row;
-  const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
-  float m_ref[MT], l[MT];
-#pragma unroll
-  for (int i = 0; i < MT; ++i) {
-    m_ref[i] = -INFINITY;
-    l[i] = 0.f;
-  }
+  const int lrow = wg * QR + row;  // row of the CTA's MT row tiles
+  const int r = r_begin + lrow;
+  const bool rv = row < QR && lrow < nrows;
+  const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16) + wg * L::kWgCols;
+  float m_ref = -INFINITY, l = 0.f;
 
-  if (has_work && warp == 0) {
-    // ======================= TMA producer (whole warp) =========================
+  if (has_work && prod >= 0) {
+    // ======================= TMA producers (whole warps) ========================
+    // A tile is kGroups x ppt boxes of B rows x 128 bytes. Producer `prod` takes
+    // the groups c = prod, prod + kProducers, ...; lane = slot + ppt * (its j-th
+    // group), one box per lane. A thread's bulk-tensor copies issue one after
+    // another (~170 cycles each, measured on GB300), so the boxes of a tile are
+    // spread over lanes and warps.
+    constexpr int NP = L::kProducers;
+    const int ng = (L::kGroups - prod + NP - 1) / NP;  // groups of this producer
+    const int slot = lane % ppt, jg = lane / ppt;
+    const int grp = prod + jg * NP;                     // group of this lane
+    const bool lane_on = jg < ng;
+    const int tensor = grp / L::kHalves, half = grp % L::kHalves;  // 0 = K, 1 = V
     const int n_pages = (C + B - 1) / B;          // cached pages of the sequence
     const int p_first = t0 * ppt;                 // first logical page of this CTA
     const int32_t *pt = a.page_table + (int64_t)b * a.max_pages_per_seq;
@@ -297,9 +350,9 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR, MT>::kCtasPerSm))
           ok = mbar_wait(smem_u32(&bars->empty[stage]), ((u / NS) - 1) & 1, abort_flag, a.err);
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       }
-      // Source of slot p (lane p < ppt): a physical page or a window row; -1 =
-      // nothing to load (past the sequence, or a bad page id). Skipped slots keep
-      // stale shared memory: their keys are masked and their V rows cleared.
+      // Source of this lane's slot: a physical page or a window row; -1 = nothing
+      // to load (past the sequence, or a bad page id). Skipped slots keep stale
+      // shared memory: their keys are masked and their V rows cleared.
       int src = -1;
       if (t < Tc) {
         const int lp0 = t * ppt;
@@ -308,36 +361,32 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR, MT>::kCtasPerSm))
           ids_cur = ids_next;
           ids_next = fetch(chunk + 32);
         }
-        const int pg = __shfl_sync(0xffffffffu, ids_cur, (lp0 - chunk + lane) & 31);
-        if (lane < ppt && (lp0 + lane) * B < C) {
+        const int pg = __shfl_sync(0xffffffffu, ids_cur, (lp0 - chunk + slot) & 31);
+        if (lane_on && (lp0 + slot) * B < C) {
           if (pg >= 0 && pg < a.num_pages)
             src = pg;
           else
             set_err(a.err, D2F_ERR_BAD_INDEX);
         }
-      } else if (lane < ppt) {
-        const int w0 = (t - Tc) * N + lane * B;   // first window row of this block
+      } else if (lane_on) {
+        const int w0 = (t - Tc) * N + slot * B;   // first window row of this block
         if (w0 < n) src = q0 + w0;
       }
+      if (lane == 0 && prod == 0) D2F_PASS_MARK(2, 6, u);
       const unsigned have = __ballot_sync(0xffffffffu, src >= 0);
       const uint32_t full = smem_u32(&bars->full[stage]);
-      if (lane == 0) mbar_arrive_expect_tx(full, __popc(have) * 2u * L::kHalves * B * 128);
+      if (lane == 0) mbar_arrive_expect_tx(full, __popc(have) * (uint32_t)B * 128u);
       __syncwarp();
       if (src >= 0) {
-        const uint32_t kdst = sb + L::kRing + stage * L::kStage + lane * B * 128;
-        const uint32_t vdst = kdst + L::kKBytes;
-#pragma unroll
-        for (int h = 0; h < L::kHalves; ++h) {
-          if (t < Tc) {
-            tma_load_4d(kdst + h * L::kKVHalf, &tm_kpool, full, h * 64, 0, g, src);
-            tma_load_4d(vdst + h * L::kKVHalf, &tm_vpool, full, h * 64, 0, g, src);
-          } else {
-            tma_load_3d(kdst + h * L::kKVHalf, &tm_kwin, full, h * 64, g, src);
-            tma_load_3d(vdst + h * L::kKVHalf, &tm_vwin, full, h * 64, g, src);
-          }
-        }
+        const uint32_t dst = sb + L::kRing + stage * L::kStage + tensor * L::kKBytes +
+                             half * L::kKVHalf + slot * B * 128;
+        if (t < Tc)
+          tma_load_4d(dst, tensor ? &tm_vpool : &tm_kpool, full, half * 64, 0, g, src);
+        else
+          tma_load_3d(dst, tensor ? &tm_vwin : &tm_kwin, full, half * 64, g, src);
       }
       issued = u + 1;
+      if (lane == 0 && prod == 0) D2F_PASS_MARK(2, 7, u);
     }
     // Drain: every issued stage must have landed before the CTA moves on.
     if (lane == 0) {
@@ -346,227 +395,234 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR, MT>::kCtasPerSm))
         mbar_wait(smem_u32(&bars->full[u % NS]), (u / NS) & 1, &no_abort, a.err);
       }
     }
-  } else if (has_work && warp == 1) {
-    // ======================= MMA issuer ========================================
+  } else if (has_work && warp <= MT) {
+    // ============ MMA issuer of row tile wi (one lane) ===========================
+    // A thread's tcgen05.mma instructions issue one after another, each taking
+    // ~100 cycles to issue whatever its N (measured on GB300), so each row tile
+    // gets its own issuing warp; the tensor pipe interleaves their MMAs.
+    const int wi = warp - 1;
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(M, N, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(M, D, 0, 1);
       const uint32_t q_base = sb + L::kQ;
       bool ok = mbar_wait(smem_u32(&bars->q_full), 0, abort_flag, a.err);
-      // Sub-tile v = u*MT + i: key tile u against row tile i. S_v goes to S/P
-      // buffer v % 2; P_v.V_u accumulates into row tile i's O.
-      auto issue_pv = [&](int w) -> bool {
-        if (!mbar_wait(smem_u32(&bars->p_full[w & 1]), (w >> 1) & 1, abort_flag, a.err))
+      // Key tile u: S goes to S/P buffer u % 2 of warpgroup wi; P.V_u accumulates
+      // into warpgroup wi's O.
+      auto issue_pv = [&](int u, int i) -> bool {
+        if (!mbar_wait(smem_u32(&bars->p_full[i][u & 1]), (u >> 1) & 1, abort_flag, a.err))
           return false;
         tc_fence_after();
-        const int uw = w / MT, iw = w % MT;
-        const int stage = uw % NS;
-        const uint32_t v_base = sb + L::kRing + stage * L::kStage + L::kKBytes;
+        D2F_PASS_MARK(2, 3 + i, u);
+        const uint32_t v_base = sb + L::kRing + (u % NS) * L::kStage + L::kKBytes;
+        const uint32_t tw = tmem + i * L::kWgCols;
 #pragma unroll
         for (int ks = 0; ks < N / 16; ++ks) {  // 16 keys = 8 TMEM columns of P per step
           const uint64_t bd = smem_desc_sw128(v_base + ks * 2048, L::kKVHalf, 1024);
-          umma_bf16_tmem_a(tmem + kTmemO + iw * D, tmem + (w & 1) * N + ks * 8, bd, idesc_pv,
-                           (uw > 0 || ks > 0) ? 1u : 0u);
+          umma_bf16_tmem_a(tw + kTmemO, tw + (u & 1) * N + ks * 8, bd, idesc_pv,
+                           (u > 0 || ks > 0) ? 1u : 0u);
         }
-        umma_commit(smem_u32(&bars->pv_done[w & 1]));
-        if (iw == MT - 1) umma_commit(smem_u32(&bars->empty[stage]));  // key tile done
+        umma_commit(smem_u32(&bars->pv_done[i][u & 1]));
         return true;
       };
-      const int V = T * MT;
-      for (int v = 0; v < V && ok; ++v) {
-        const int u = v / MT, i = v % MT;
+      // P.V of the previous key tile, then release its stage (the stage is free
+      // once every issuer has released it)
+      auto finish = [&](int u) -> bool {
+        if (!issue_pv(u, wi)) return false;
+        umma_commit(smem_u32(&bars->empty[u % NS]));
+        return true;
+      };
+      const bool idle = wi >= mt_live;  // a row tile without rows: only release stages
+      for (int u = 0; u < T && ok; ++u) {
         const int stage = u % NS;
-        if (i == 0) {
-          if (!mbar_wait(smem_u32(&bars->full[stage]), (u / NS) & 1, abort_flag, a.err)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          if (u == 0) D2F_TRACE_MARK(0, 10);
-          if (u == T - 1) D2F_TRACE_MARK(0, 3);
+        if (!mbar_wait(smem_u32(&bars->full[stage]), (u / NS) & 1, abort_flag, a.err)) {
+          ok = false;
+          break;
         }
-        // S_v overwrites the S/P buffer that P_{v-2} occupied: P.V_{v-2} was issued
+        if (idle) {
+          mbar_arrive(smem_u32(&bars->empty[stage]));
+          continue;
+        }
+        tc_fence_after();
+        if (wi == 0) D2F_PASS_MARK(2, 0, u);
+        if (u == 0) D2F_TRACE_MARK(0, 10);
+        if (u == T - 1) D2F_TRACE_MARK(0, 3);
+        // S_u overwrites the S/P buffer that P_{u-2} occupied: P.V_{u-2} was issued
         // before this (MMAs of one thread execute in order).
         const uint32_t k_base = sb + L::kRing + stage * L::kStage;
-        const uint32_t qi_base = q_base + i * L::kTileQBytes;
+        const uint32_t qi_base = q_base + wi * L::kTileQBytes;
 #pragma unroll
         for (int h = 0; h < L::kHalves; ++h) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t ad = smem_desc_sw128(qi_base + h * L::kQHalf + kk * 32, 16, 1024);
             const uint64_t bd = smem_desc_sw128(k_base + h * L::kKVHalf + kk * 32, 16, 1024);
-            umma_bf16(tmem + (v & 1) * N, ad, bd, idesc_qk, (h | kk) ? 1u : 0u);
+            umma_bf16(tmem + wi * L::kWgCols + (u & 1) * N, ad, bd, idesc_qk, (h | kk) ? 1u : 0u);
           }
         }
-        umma_commit(smem_u32(&bars->s_full[v & 1]));
-        if (v >= 1) ok = issue_pv(v - 1);
+        umma_commit(smem_u32(&bars->s_full[wi][u & 1]));
+        if (wi == 0) D2F_PASS_MARK(2, 1, u);
+        if (u >= 1) ok = finish(u - 1);
+        if (u >= 1 && wi == 0) D2F_PASS_MARK(2, 2, u - 1);
       }
-      if (ok) issue_pv(V - 1);
+      if (ok && !idle) finish(T - 1);
       // Drain: wait until every MMA issued above has completed.
       umma_commit(smem_u32(&bars->drain));
       volatile int no_abort = 0;
       mbar_wait(smem_u32(&bars->drain), 0, &no_abort, a.err);
     }
   } else if (has_work) {
-    // ======================= softmax (128 threads, one per TMEM lane) ==========
+    // ============ softmax (a warpgroup per row tile, a thread per TMEM lane) =====
+    const bool live = wg < mt_live;  // warpgroup-uniform
     {
       // The Q rows into the 128-byte-swizzled K-major layout the MMA reads: in
-      // row tile i, 16-byte chunk c of column block h lands at
-      //   i*kTileQBytes + h*kQHalf + (row/8)*1024 + (row%8)*128 + ((c ^ (row%8)) * 16).
+      // row tile wg, 16-byte chunk c of column block h lands at
+      //   wg*kTileQBytes + h*kQHalf + (row/8)*1024 + (row%8)*128 + ((c ^ (row%8)) * 16).
       constexpr int kQc = D / 8;
-      if (row < QR) {  // warp-uniform
+      if (live && row < QR) {  // warp-uniform
+        uint4 qv[kQc];
+        const uint4 *src = reinterpret_cast<const uint4 *>(
+            reinterpret_cast<const uint16_t *>(a.q) + ((int64_t)(q0 + r / G) * H + g * G + r % G) * D);
 #pragma unroll
-        for (int i = 0; i < MT; ++i) {
-          const int ri = r + i * QR;
-          const bool vi = i * QR + row < nrows;
-          uint4 qv[kQc];
-          const uint4 *src = reinterpret_cast<const uint4 *>(
-              reinterpret_cast<const uint16_t *>(a.q) +
-              ((int64_t)(q0 + ri / G) * H + g * G + ri % G) * D);
+        for (int c = 0; c < kQc; ++c) qv[c] = rv ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-          for (int c = 0; c < kQc; ++c) qv[c] = vi ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-          for (int c = 0; c < kQc; ++c) {
-            const uint32_t dst = sb + L::kQ + i * L::kTileQBytes + (c >> 3) * L::kQHalf +
-                                 (row >> 3) * 1024 + (row & 7) * 128 + (((c & 7) ^ (row & 7)) << 4);
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(qv[c].x),
-                         "r"(qv[c].y), "r"(qv[c].z), "r"(qv[c].w)
-                         : "memory");
-          }
+        for (int c = 0; c < kQc; ++c) {
+          const uint32_t dst = sb + L::kQ + wg * L::kTileQBytes + (c >> 3) * L::kQHalf +
+                               (row >> 3) * 1024 + (row & 7) * 128 + (((c & 7) ^ (row & 7)) << 4);
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(qv[c].x),
+                       "r"(qv[c].y), "r"(qv[c].z), "r"(qv[c].w)
+                       : "memory");
         }
         fence_proxy_async_smem();
       }
       mbar_arrive(smem_u32(&bars->q_full));
     }
-    int win_end[MT];
-#pragma unroll
-    for (int i = 0; i < MT; ++i)
-      win_end[i] = i * QR + row < nrows ? (((r + i * QR) / G) / B + 1) * B : 0;
+    const int win_end = rv ? ((r / G) / B + 1) * B : 0;
     const float sl2 = a.scale_log2;
     bool ok = true;
-    // Sub-tile v = u*MT + i: key tile u against row tile i (S/P buffer v % 2).
-    for (int u = 0; u < T && ok; ++u) {
+    for (int u = 0; u < T && ok && live; ++u) {
       const int t = t0 + u;
       const int tile_lim = t < Tc ? C - t * N : n - (t - Tc) * N;  // valid keys of the tile
-#pragma unroll
-      for (int i = 0; i < MT; ++i) {
-        const int v = u * MT + i;
-        const bool rv = i * QR + row < nrows;
-        ok = mbar_wait(smem_u32(&bars->s_full[v & 1]), (v >> 1) & 1, abort_flag, a.err);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        tc_fence_after();
-        if (tid == 128 && i == 0 && u == 0) D2F_TRACE_MARK(0, 4);
-        if (tid == 128 && i == 0 && u == 1) D2F_TRACE_MARK(0, 14);
-        if (tid == 128 && i == 0 && u == 2) D2F_TRACE_MARK(0, 15);
-        if (tid == 128 && i == 0 && u == T - 1) D2F_TRACE_MARK(0, 5);
-        uint32_t sv[N];
-        const uint32_t s_addr = lane_addr + (v & 1) * N;
-        tmem_ld64(s_addr, sv);
+      ok = mbar_wait(smem_u32(&bars->s_full[wg][u & 1]), (u >> 1) & 1, abort_flag, a.err);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      const bool pm = lane == 0 && warp == L::kFirstSoft + 4 * wg;  // first thread of the warpgroup
+      if (pm) D2F_PASS_MARK(wg, 0, u);
+      if (tid == 128 && u == 0) D2F_TRACE_MARK(0, 4);
+      if (tid == 128 && u == 1) D2F_TRACE_MARK(0, 14);
+      if (tid == 128 && u == 2) D2F_TRACE_MARK(0, 15);
+      if (tid == 128 && u == T - 1) D2F_TRACE_MARK(0, 5);
+      uint32_t sv[N];
+      const uint32_t s_addr = lane_addr + (u & 1) * N;
+      tmem_ld64(s_addr, sv);
+      if (pm) D2F_PASS_MARK(wg, 1, u);
 
-        // keys c < lim of this tile are visible to this row
-        int lim = t < Tc ? tile_lim : win_end[i] - (t - Tc) * N;
-        lim = rv ? max(0, min(lim, N)) : 0;
-        float sf[N];
+      // keys c < lim of this tile are visible to this row
+      int lim = t < Tc ? tile_lim : win_end - (t - Tc) * N;
+      lim = rv ? max(0, min(lim, N)) : 0;
+      float sf[N];
 #pragma unroll
-        for (int c = 0; c < N; ++c) sf[c] = __uint_as_float(sv[c]);
-        if (!__all_sync(0xffffffffu, lim >= N)) {  // ragged tile: hide masked keys
+      for (int c = 0; c < N; ++c) sf[c] = __uint_as_float(sv[c]);
+      if (!__all_sync(0xffffffffu, lim >= N)) {  // ragged tile: hide masked keys
 #pragma unroll
-          for (int c = 0; c < N; ++c)
-            if (c >= lim) sf[c] = -INFINITY;
-        }
-        // tree maximum of the 64 scores with three-input maxima (scale > 0, so
-        // max(s) * scale = max(s * scale)): 64 -> 22 -> 8 -> 3 -> 1
-        static_assert(N == 64, "maximum tree shape");
-        float t1[22], t2[8];
-#pragma unroll
-        for (int c = 0; c < 21; ++c) t1[c] = fmax3(sf[3 * c], sf[3 * c + 1], sf[3 * c + 2]);
-        t1[21] = sf[63];
-#pragma unroll
-        for (int c = 0; c < 7; ++c) t2[c] = fmax3(t1[3 * c], t1[3 * c + 1], t1[3 * c + 2]);
-        t2[7] = t1[21];
-        const float tmax = fmax3(fmax3(t2[0], t2[1], t2[2]), fmax3(t2[3], t2[4], t2[5]),
-                                 fmaxf(t2[6], t2[7])) * sl2;
-        // Lazy rescale: keep the reference max unless the tile max exceeds it by 2^8.
-        const bool need = tmax > m_ref[i] + 8.0f;
-        if (__any_sync(0xffffffffu, need)) {
-          const float m_new = need ? tmax : m_ref[i];
-          const float alpha = need ? fast_exp2(m_ref[i] - m_new) : 1.0f;
-          l[i] *= alpha;
-          if (u > 0) {
-            // every earlier P.V (MMAs complete in order) has landed in this row
-            // tile's accumulator
-            ok = mbar_wait(smem_u32(&bars->pv_done[(v - 1) & 1]), ((v - 1) >> 1) & 1, abort_flag,
-                           a.err);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            tc_fence_after();
-#pragma unroll
-            for (int ch = 0; ch < D / 32; ++ch) {
-              uint32_t o[32];
-              const uint32_t oa = lane_addr + kTmemO + i * D + ch * 32;
-              tmem_ld32(oa, o);
-#pragma unroll
-              for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-              tmem_st32(oa, o);
-            }
-            tmem_wait_st();
-          }
-          m_ref[i] = m_new;
-        }
-        // P = 2^(s*scale - m_ref) in bf16: the exponent argument is formed in float
-        // for a pair of keys at once, rounded to bf16 and exponentiated as a packed
-        // pair (P is a bf16 MMA operand, so it carries bf16 precision either way).
-        // Masked keys are -inf -> 0. A row with no visible key so far keeps
-        // m_ref = -inf: subtract 0 instead.
-        const float mb = m_ref[i] == -INFINITY ? 0.f : m_ref[i];
-        uint32_t pk[N / 2];
-#pragma unroll
-        for (int j = 0; j < N / 2; ++j) {
-          float x0, x1;
-          fma2_bc(x0, x1, sf[2 * j], sf[2 * j + 1], sl2, -mb);
-          pk[j] = ex2_bf16x2(pack_bf16x2(x0, x1));
-        }
-        // row sum of the P actually used (the rounded values), in float pairs
-        float ps0[N / 4], ps1[N / 4];
-#pragma unroll
-        for (int j = 0; j < N / 4; ++j)
-          add2(ps0[j], ps1[j], __uint_as_float(pk[2 * j] << 16),
-               __uint_as_float(pk[2 * j] & 0xffff0000u), __uint_as_float(pk[2 * j + 1] << 16),
-               __uint_as_float(pk[2 * j + 1] & 0xffff0000u));
-#pragma unroll
-        for (int w = N / 8; w >= 1; w >>= 1)
-#pragma unroll
-          for (int c = 0; c < w; ++c)
-            add2(ps0[c], ps1[c], ps0[2 * c], ps1[2 * c], ps0[2 * c + 1], ps1[2 * c + 1]);
-        l[i] += ps0[0] + ps1[0];
-        // P over the scores it came from (this thread's own lane): column c of the
-        // S/P buffer now holds keys 2c and 2c+1.
-        tmem_st32(s_addr, pk);
-        tmem_wait_st();
-        // A ragged tile (partial last page or short window) may hold stale or
-        // non-finite V rows past its valid keys; P is 0 there, but 0 * NaN is not
-        // 0, so clear those rows before the first P.V product reads them.
-        if (i == 0 && row < N && row >= tile_lim) {
-          const uint32_t v_row = sb + L::kRing + (u % NS) * L::kStage + L::kKBytes +
-                                 (row >> 3) * 1024 + (row & 7) * 128;
-#pragma unroll
-          for (int h = 0; h < L::kHalves; ++h)
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-              asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(v_row + h * L::kKVHalf +
-                                                                             (c << 4)),
-                           "r"(0u)
-                           : "memory");
-          fence_proxy_async_smem();
-        }
-        tc_fence_before();
-        mbar_arrive(smem_u32(&bars->p_full[v & 1]));
-        if (tid == 128 && i == 0 && u == 0) D2F_TRACE_MARK(0, 13);
-        if (tid == 128 && i == MT - 1 && u == T - 1) D2F_TRACE_MARK(0, 6);
+        for (int c = 0; c < N; ++c)
+          if (c >= lim) sf[c] = -INFINITY;
       }
+      // tree maximum of the 64 scores with three-input maxima (scale > 0, so
+      // max(s) * scale = max(s * scale)): 64 -> 22 -> 8 -> 3 -> 1
+      static_assert(N == 64, "maximum tree shape");
+      float t1[22], t2[8];
+#pragma unroll
+      for (int c = 0; c < 21; ++c) t1[c] = fmax3(sf[3 * c], sf[3 * c + 1], sf[3 * c + 2]);
+      t1[21] = sf[63];
+#pragma unroll
+      for (int c = 0; c < 7; ++c) t2[c] = fmax3(t1[3 * c], t1[3 * c + 1], t1[3 * c + 2]);
+      t2[7] = t1[21];
+      const float tmax = fmax3(fmax3(t2[0], t2[1], t2[2]), fmax3(t2[3], t2[4], t2[5]),
+                               fmaxf(t2[6], t2[7])) * sl2;
+      // Lazy rescale: keep the reference max unless the tile max exceeds it by 2^8.
+      const bool need = tmax > m_ref + 8.0f;
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_new = need ? tmax : m_ref;
+        const float alpha = need ? fast_exp2(m_ref - m_new) : 1.0f;
+        l *= alpha;
+        if (u > 0) {
+          // every earlier P.V (MMAs complete in order) has landed in O
+          ok = mbar_wait(smem_u32(&bars->pv_done[wg][(u - 1) & 1]), ((u - 1) >> 1) & 1, abort_flag,
+                         a.err);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t o[32];
+            const uint32_t oa = lane_addr + kTmemO + ch * 32;
+            tmem_ld32(oa, o);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+            tmem_st32(oa, o);
+          }
+          tmem_wait_st();
+        }
+        m_ref = m_new;
+      }
+      // P = 2^(s*scale - m_ref) in bf16: the exponent argument is formed in float
+      // for a pair of keys at once, rounded to bf16 and exponentiated as a packed
+      // pair (P is a bf16 MMA operand, so it carries bf16 precision either way).
+      // Masked keys are -inf -> 0. A row with no visible key so far keeps
+      // m_ref = -inf: subtract 0 instead.
+      if (pm) D2F_PASS_MARK(wg, 2, u);
+      const float mb = m_ref == -INFINITY ? 0.f : m_ref;
+      uint32_t pk[N / 2];
+#pragma unroll
+      for (int j = 0; j < N / 2; ++j) {
+        float x0, x1;
+        fma2_bc(x0, x1, sf[2 * j], sf[2 * j + 1], sl2, -mb);
+        pk[j] = ex2_bf16x2(pack_bf16x2(x0, x1));
+      }
+      // row sum of the P actually used (the rounded values), in float pairs
+      float ps0[N / 4], ps1[N / 4];
+#pragma unroll
+      for (int j = 0; j < N / 4; ++j)
+        add2(ps0[j], ps1[j], __uint_as_float(pk[2 * j] << 16),
+             __uint_as_float(pk[2 * j] & 0xffff0000u), __uint_as_float(pk[2 * j + 1] << 16),
+             __uint_as_float(pk[2 * j + 1] & 0xffff0000u));
+#pragma unroll
+      for (int w = N / 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int c = 0; c < w; ++c)
+          add2(ps0[c], ps1[c], ps0[2 * c], ps1[2 * c], ps0[2 * c + 1], ps1[2 * c + 1]);
+      l += ps0[0] + ps1[0];
+      if (pm) D2F_PASS_MARK(wg, 3, u);
+      // P over the scores it came from (this thread's own lane): column c of the
+      // S/P buffer now holds keys 2c and 2c+1.
+      tmem_st32(s_addr, pk);
+      tmem_wait_st();
+      if (pm) D2F_PASS_MARK(wg, 4, u);
+      // A ragged tile (partial last page or short window) may hold stale or
+      // non-finite V rows past its valid keys; P is 0 there, but 0 * NaN is not
+      // 0, so clear those rows before the P.V product reads them. Every
+      // warpgroup clears them (the same zeros) before its own P.V is issued.
+      if (row < N && row >= tile_lim) {
+        const uint32_t v_row = sb + L::kRing + (u % NS) * L::kStage + L::kKBytes +
+                               (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+        for (int h = 0; h < L::kHalves; ++h)
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(v_row + h * L::kKVHalf +
+                                                                           (c << 4)),
+                         "r"(0u)
+                         : "memory");
+        fence_proxy_async_smem();
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars->p_full[wg][u & 1]));
+      if (pm) D2F_PASS_MARK(wg, 5, u);
+      if (tid == 128 && u == 0) D2F_TRACE_MARK(0, 13);
+      if (tid == 128 && u == T - 1) D2F_TRACE_MARK(0, 6);
     }
-    if (ok) {  // the last P.V product
-      const int last = T * MT - 1;
-      ok = mbar_wait(smem_u32(&bars->pv_done[last & 1]), (last >> 1) & 1, abort_flag, a.err);
+    if (ok && live) {  // the last P.V product
+      const int last = T - 1;
+      ok = mbar_wait(smem_u32(&bars->pv_done[wg][last & 1]), (last >> 1) & 1, abort_flag, a.err);
       ok = __all_sync(0xffffffffu, ok);
     }
     tc_fence_after();
@@ -579,32 +635,26 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR, MT>::kCtasPerSm))
   const bool aborted = *abort_flag != 0;
   bool tmem_freed = false;
   if (cs == 1) {
+    if (warp >= L::kFirstSoft && has_work && !aborted && __any_sync(0xffffffffu, rv)) {
+      const int64_t hr = (int64_t)(q0 + r / G) * H + g * G + r % G;
+      const float inv = 1.0f / l;
+      uint16_t *dst = reinterpret_cast<uint16_t *>(a.out) + hr * D;
 #pragma unroll
-    for (int i = 0; i < MT; ++i) {
-      const bool rv = i * QR + row < nrows;
-      if (warp >= 2 && has_work && !aborted && __any_sync(0xffffffffu, rv)) {
-        const int ri = r + i * QR;
-        const int64_t hr = (int64_t)(q0 + ri / G) * H + g * G + ri % G;
-        const float inv = 1.0f / l[i];
-        uint16_t *dst = reinterpret_cast<uint16_t *>(a.out) + hr * D;
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t o[32];
+        tmem_ld32(lane_addr + kTmemO + ch * 32, o);
+        if (rv) {
+          uint32_t w[16];
 #pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t o[32];
-          tmem_ld32(lane_addr + kTmemO + i * D + ch * 32, o);
-          if (rv) {
-            uint32_t w[16];
+          for (int j = 0; j < 16; ++j)
+            w[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
+          uint4 *d4 = reinterpret_cast<uint4 *>(dst + ch * 32);
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              w[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv,
-                                 __uint_as_float(o[2 * j + 1]) * inv);
-            uint4 *d4 = reinterpret_cast<uint4 *>(dst + ch * 32);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              d4[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-          }
+          for (int j = 0; j < 4; ++j)
+            d4[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
         }
-        if (rv && a.lse_out) a.lse_out[hr] = (m_ref[i] + __log2f(l[i])) * 0.6931471805599453f;
       }
+      if (rv && a.lse_out) a.lse_out[hr] = (m_ref + __log2f(l)) * 0.6931471805599453f;
     }
   } else if (active) {
     const int LR = L::rows_per_owner(cs);  // rows a CTA owns (at most)
@@ -612,51 +662,46 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR, MT>::kCtasPerSm))
     const uint32_t recv = sb + L::kQ;      // [source split][BS], filled by the bulk copies
     const uint32_t stg = sb + L::staging(cs);  // [owner][BS], this CTA's rows
     const uint32_t recv_bar = smem_u32(&bars->recv);
-    // 1) stage this CTA's rows: local row (i*QR + lane row of row tile i) ->
-    //    owner lrow % cs, slot lrow / cs; the 16-byte chunks of a row are
-    //    XOR-swizzled by (lrow % 8).
+    // 1) stage this CTA's rows: local row lrow (wg*QR + lane row) -> owner
+    //    lrow % cs, slot lrow / cs; the 16-byte chunks of a row are XOR-swizzled
+    //    by (lrow % 8).
+    if (warp >= L::kFirstSoft && __any_sync(0xffffffffu, rv)) {
+      const int owner = lrow % cs, lr = lrow / cs, key = lrow & 7;
+      const uint32_t blk = stg + owner * BS;
+      const bool mine = has_work && !aborted;  // CTA-uniform
+      const bool keep = mine && rv && l > 0.f;
+      if (mine) {
+        const float inv = keep ? 1.0f / l : 0.f;
 #pragma unroll
-    for (int i = 0; i < MT; ++i) {
-      const int lrow = i * QR + row;
-      const bool rv = lrow < nrows;
-      if (warp >= 2 && __any_sync(0xffffffffu, rv)) {
-        const int owner = lrow % cs, lr = lrow / cs, key = lrow & 7;
-        const uint32_t blk = stg + owner * BS;
-        const bool mine = has_work && !aborted;  // CTA-uniform
-        const bool keep = mine && rv && l[i] > 0.f;
-        if (mine) {
-          const float inv = keep ? 1.0f / l[i] : 0.f;
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t o[32];
+          tmem_ld32(lane_addr + kTmemO + ch * 32, o);
+          if (keep) {
 #pragma unroll
-          for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t o[32];
-            tmem_ld32(lane_addr + kTmemO + i * D + ch * 32, o);
-            if (keep) {
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int c = ch * 4 + j;  // 8 bf16 per 16-byte chunk
-                const uint32_t dst = blk + lr * L::kRowBytes + ((c ^ key) << 4);
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
-                             "r"(pack_bf16x2(__uint_as_float(o[8 * j]) * inv,
-                                             __uint_as_float(o[8 * j + 1]) * inv)),
-                             "r"(pack_bf16x2(__uint_as_float(o[8 * j + 2]) * inv,
-                                             __uint_as_float(o[8 * j + 3]) * inv)),
-                             "r"(pack_bf16x2(__uint_as_float(o[8 * j + 4]) * inv,
-                                             __uint_as_float(o[8 * j + 5]) * inv)),
-                             "r"(pack_bf16x2(__uint_as_float(o[8 * j + 6]) * inv,
-                                             __uint_as_float(o[8 * j + 7]) * inv))
-                             : "memory");
-              }
+            for (int j = 0; j < 4; ++j) {
+              const int c = ch * 4 + j;  // 8 bf16 per 16-byte chunk
+              const uint32_t dst = blk + lr * L::kRowBytes + ((c ^ key) << 4);
+              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
+                           "r"(pack_bf16x2(__uint_as_float(o[8 * j]) * inv,
+                                           __uint_as_float(o[8 * j + 1]) * inv)),
+                           "r"(pack_bf16x2(__uint_as_float(o[8 * j + 2]) * inv,
+                                           __uint_as_float(o[8 * j + 3]) * inv)),
+                           "r"(pack_bf16x2(__uint_as_float(o[8 * j + 4]) * inv,
+                                           __uint_as_float(o[8 * j + 5]) * inv)),
+                           "r"(pack_bf16x2(__uint_as_float(o[8 * j + 6]) * inv,
+                                           __uint_as_float(o[8 * j + 7]) * inv))
+                           : "memory");
             }
           }
         }
-        if (rv) {
-          const float mx = keep ? m_ref[i] : -INFINITY, sm = keep ? l[i] : 0.f;
-          asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(blk + LR * L::kRowBytes + lr * 8),
-                       "f"(mx), "f"(sm)
-                       : "memory");
-        }
-        fence_proxy_async_smem();  // the bulk copies read these blocks
       }
+      if (rv) {
+        const float mx = keep ? m_ref : -INFINITY, sm = keep ? l : 0.f;
+        asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(blk + LR * L::kRowBytes + lr * 8),
+                     "f"(mx), "f"(sm)
+                     : "memory");
+      }
+      fence_proxy_async_smem();  // the bulk copies read these blocks
     }
     // 2) each owner expects cs blocks; the cluster barrier publishes the staged
     //    blocks and frees every receive area (each CTA is past its ring).
@@ -678,20 +723,20 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR, MT>::kCtasPerSm))
     //    cluster barrier: once every CTA has arrived, every copy has landed and
     //    no staging block is still being read.
     bool got = true;
-    if (warp >= 2) got = __all_sync(0xffffffffu, mbar_wait(recv_bar, 0, abort_flag, a.err));
+    if (warp >= L::kFirstSoft) got = __all_sync(0xffffffffu, mbar_wait(recv_bar, 0, abort_flag, a.err));
     if (tid == 64) D2F_TRACE_MARK(0, 9);
     __syncwarp();
     cluster_arrive_relaxed();
     // 5) compose the rows this CTA owns: half a warp per row, lane c of the half
     //    holds columns [c * D/16, (c + 1) * D/16).
-    if (warp >= 2) {
+    if (warp >= L::kFirstSoft) {
       constexpr int kCols = D / 16;
       const int hw = lane >> 4, sub = lane & 15;
-      for (int lr0 = (warp - 2) * 2; got && lr0 * cs + split < nrows; lr0 += 2 * kSoftWarps) {
+      for (int lr0 = (warp - L::kFirstSoft) * 2; got && lr0 * cs + split < nrows; lr0 += 2 * L::kSoftWarps) {
         const int lr = lr0 + hw;
-        const int lrow = lr * cs + split;  // local row of this half-warp
-        const bool valid = lrow < nrows;
-        const int key = lrow & 7;
+        const int crow = lr * cs + split;  // CTA row of this half-warp
+        const bool valid = crow < nrows;
+        const int key = crow & 7;
         float2 ml = make_float2(-INFINITY, 0.f);
         if (valid && sub < cs)
           ml = *reinterpret_cast<const float2 *>(smem + sub * BS + LR * L::kRowBytes + lr * 8);
@@ -729,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, (Layout<D, NS, QR, MT>::kCtasPerSm))
         }
         if (valid && !aborted) {
           const float inv = ws > 0.f ? 1.0f / ws : 0.f;
-          const int r2 = r_begin + lrow;
+          const int r2 = r_begin + crow;
           const int64_t hr2 = (int64_t)(q0 + r2 / G) * H + g * G + r2 % G;
           uint32_t pk[kCols / 2];
 #pragma unroll
@@ -839,7 +884,7 @@ cudaError_t launch_d(const AttnArgs &a, cudaStream_t s, char *why, size_t why_le
   const int cs = a.num_splits;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cs, a.m_tiles, a.batch * a.num_heads_kv);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(Layout<D, NS, QR, MT>::kThreads);
   cfg.dynamicSmemBytes = Layout<D, NS, QR, MT>::kAlloc;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -873,7 +918,7 @@ int attn_tc_deep_slots(int cs) {
     if (ensure_attrs<128, 6, 128, 1>() != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cs, 1, 1);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(Layout<128, 6, 128, 1>::kThreads);
     cfg.dynamicSmemBytes = Layout<128, 6, 128, 1>::kAlloc;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -901,16 +946,15 @@ cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t s, char *why, size_t 
   // Ring depth by shared-memory budget: two CTAs per SM hold Q + NS stages in
   // ~113 KB (head_dim 64: 6 stages; head_dim 128: 3 stages with 64-row tiles, 2
   // with 128-row tiles); the 6-stage head_dim-128 variant takes a whole SM.
-  // The MT > 1 variants hold MT 128-row tiles of one (sequence, KV head) in one
-  // CTA (GQA groups of 129..384 rows): every K/V tile is loaded once for all of
-  // them, and the CTA takes a whole SM.
+  // The MT = 2 variant holds two 128-row tiles of one (sequence, KV head) with a
+  // softmax warpgroup each (GQA groups of 129..384 rows): every K/V tile is
+  // loaded once for both, and the CTA takes a whole SM.
   const int rows = a.tc_rows, ns = a.tc_stages, mt = a.tc_mt;
   if (a.head_dim == 128) {
     if (rows == 64 && ns == 3 && mt == 1) return launch_d<128, 3, 64, 1>(a, s, why, why_len);
     if (rows == 128 && ns == 2 && mt == 1) return launch_d<128, 2, 128, 1>(a, s, why, why_len);
     if (rows == 128 && ns == 6 && mt == 1) return launch_d<128, 6, 128, 1>(a, s, why, why_len);
     if (rows == 128 && ns == 5 && mt == 2) return launch_d<128, 5, 128, 2>(a, s, why, why_len);
-    if (rows == 128 && ns == 4 && mt == 3) return launch_d<128, 4, 128, 3>(a, s, why, why_len);
   } else if (a.head_dim == 64) {
     if (rows == 64 && ns == 6 && mt == 1) return launch_d<64, 6, 64, 1>(a, s, why, why_len);
     if (rows == 128 && ns == 6 && mt == 1) return launch_d<64, 6, 128, 1>(a, s, why, why_len);
@@ -919,12 +963,14 @@ cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t s, char *why, size_t 
            "no tensor-core variant for head_dim %d, %d-row tiles x %d, %d stages", a.head_dim,
            rows, mt, ns);
   return cudaErrorInvalidValue;
-  snprintf(why, why_len, "tensor-core path supports head_dim 64 or 128");
-  return cudaErrorInvalidValue;
 }
 
 #ifdef D2F_TRACE
 D2F_TRACE_COPY_FN(d2f_trace_copy_attn)
+extern "C" int d2f_trace_copy_pass(void *host, size_t bytes) {
+  if (bytes > sizeof(g_d2f_pass)) bytes = sizeof(g_d2f_pass);
+  return cudaMemcpyFromSymbol(host, g_d2f_pass, bytes) == cudaSuccess ? 0 : 1;
+}
 #endif
 
 }  // namespace d2f

@@ -84,8 +84,8 @@ bool force_full_rows() {
 
 // D2F_TC_DEEP=1 / 0 forces / forbids the one-CTA-per-SM 6-stage variant for
 // head_dim 128 with 128-row tiles (for comparisons and tests); unset = planner.
-// D2F_TC_MT=1 / 0 forces / forbids one CTA for all the 128-row tiles (2 or 3) of a
-// (sequence, KV head) for head_dim 128 (tests); unset = planner.
+// D2F_TC_MT=1 / 0 forces / forbids CTAs of two 128-row tiles (two softmax
+// warpgroups) for head_dim 128 groups of 2 or 3 row tiles (tests); unset = planner.
 int force_mt() {
   const char *e = getenv("D2F_TC_MT");
   if (!e || !e[0]) return -1;
@@ -154,11 +154,12 @@ int plan_attn(int batch, int total_q, int max_q, int max_ctx, int Hq, int Hkv, i
     const int two = splits ? splits : pick(false);  // two CTAs per SM
     splits = two;
     if (D == 128 && rows == 128 && (p->m_tiles == 2 || p->m_tiles == 3)) {
-      // GQA groups of 129..384 rows: one CTA for all the row tiles of a (sequence,
-      // KV head) reads each K/V tile once instead of m_tiles times, through a
-      // deeper ring, at one CTA per SM. It serialises the row tiles' softmax per
-      // key tile, so it pays only once splits are long.
-      const long long base_mt = (long long)max(batch, 1) * Hkv;
+      // GQA groups of 129..384 rows: a CTA with two softmax warpgroups takes two
+      // row tiles of a (sequence, KV head) and reads each K/V tile once for both,
+      // through a deeper ring, at one CTA per SM (three row tiles: two CTAs, the
+      // second with one row tile). It pays only once splits are long.
+      const int groups = cdiv(p->m_tiles, 2);
+      const long long base_mt = (long long)max(batch, 1) * Hkv * groups;
       int one = splits ? splits : 1;
       if (!num_splits) {
         int most = 1;
@@ -169,9 +170,9 @@ int plan_attn(int batch, int total_q, int max_q, int max_ctx, int Hq, int Hkv, i
       bool use = cdiv(t_max, two) >= 8 && attn_tc_deep_slots(one) > 0;
       if (force_mt() >= 0) use = force_mt() == 1;
       if (use) {
-        p->mt = p->m_tiles;
-        p->stages = p->mt == 3 ? 4 : 5;
-        p->m_tiles = 1;
+        p->mt = 2;
+        p->stages = 5;
+        p->m_tiles = groups;
         splits = one;
       }
     }

@@ -42,7 +42,7 @@ struct AttnArgs {
   int m_tiles;           // grid.x: row tiles per (sequence, KV head)
   int tc_rows;           // tensor-core path: rows a tile holds (64 or 128)
   int tc_stages;         // tensor-core path: K/V ring depth (2 .. 6)
-  int tc_mt;             // tensor-core path: 128-row tiles per CTA (1 .. 3)
+  int tc_mt;             // tensor-core path: row tiles per CTA, a softmax warpgroup each (1, 2)
   int longest_first;     // tensor-core path: map blockIdx.z to sequences longest context first
   int32_t *counters;     // [batch * Hkv * m_tiles] merge arrival counters (zero at rest)
   float2 *ws_ml;         // [num_splits][total_q * Hq] (max in log2 units, sum)

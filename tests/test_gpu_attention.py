@@ -91,9 +91,11 @@ def _gqa_two_tiles():
 
 @pytest.mark.parametrize("name", ["dream", "gqa2"])
 @pytest.mark.parametrize("splits", [0, 1, 3, 8])
-def test_all_row_tiles_of_a_kv_head_in_one_cta(name, splits, monkeypatch):
-    """GQA groups of 2 or 3 row tiles in one CTA (D2F_TC_MT=1): one K/V stream,
-    one accumulator per row tile; same result as the oracle."""
+def test_two_row_tiles_per_cta(name, splits, monkeypatch):
+    """GQA groups of 2 or 3 row tiles on CTAs of two row tiles with a softmax
+    warpgroup each (D2F_TC_MT=1): one K/V stream for both, one accumulator per
+    row tile; three tiles leave the second CTA one tile, and a 128-row sequence
+    one idle warpgroup. Same result as the oracle."""
     dev = device()
     monkeypatch.setenv("D2F_TC_MT", "1")
     w = _gqa_two_tiles() if name == "gqa2" else synth.small(name)
