@@ -80,14 +80,6 @@ static_assert(kMaxLongestFirstBatch * 4 + 4 <= 2 * 64 * 64 * 2, "ordering scratc
 template <int D, int NS, int QR, int MT>
 struct Layout {
   static constexpr int kHalves = D / 64;         // 64-element (128-byte) swizzle columns
-  // warp 0 producer, warps 1..MT MMA issuers (one per row tile), with MT = 2 a
-  // second producer warp, then MT softmax warpgroups. With QR = 64 the two
-  // softmax warps whose TMEM lanes (64-127) hold no rows load K/V as well.
-  static constexpr int kFirstSoft = 1 + MT + (MT == 2 ? 1 : 0);
-  static constexpr int kThreads = 32 * kFirstSoft + kWgThreads * MT;
-  static constexpr int kSoftWarps = 4 * MT;
-  static constexpr int kProducers = 1 + (MT == 2 ? 1 : 0) + (QR == 64 ? 2 : 0);
-  static constexpr int kGroups = 2 * kHalves;  // TMA box groups of a tile: (K | V) x column half
   static constexpr int kQHalf = QR * 128;        // one 64-wide column block of one Q tile
   static constexpr int kTileQBytes = kHalves * kQHalf;
   static constexpr int kQBytes = MT * kTileQBytes;  // MT row tiles of Q
@@ -106,6 +98,18 @@ struct Layout {
   static constexpr int kAlloc =
       (kBytes + 1024 <= kSmemTwoPerSm || kBytes > kSmemTwoPerSm) ? kBytes + 1024 : kBytes;
   static constexpr int kCtasPerSm = kAlloc <= kSmemTwoPerSm ? 2 : 1;
+  // Warp roles: warp 0 producer; then the MMA issuers: one per row tile, or,
+  // for one row tile at one CTA per SM, one for S and one for P.V (kSplit);
+  // with MT = 2 a second producer warp; then MT softmax warpgroups. With
+  // QR = 64 the two softmax warps whose TMEM lanes (64-127) hold no rows load
+  // K/V as well.
+  static constexpr bool kSplit = MT == 1 && kCtasPerSm == 1;
+  static constexpr int kIssuers = kSplit ? 2 : MT;
+  static constexpr int kFirstSoft = 1 + kIssuers + (MT == 2 ? 1 : 0);
+  static constexpr int kThreads = 32 * kFirstSoft + kWgThreads * MT;
+  static constexpr int kSoftWarps = 4 * MT;
+  static constexpr int kProducers = 1 + (MT == 2 ? 1 : 0) + (QR == 64 ? 2 : 0);
+  static constexpr int kGroups = 2 * kHalves;  // TMA box groups of a tile: (K | V) x column half
   // Composition blocks (overlay Q and the ring): per owner, LR rows of D bf16
   // then LR (max, sum) pairs.
   static constexpr int kRowBytes = 2 * D;
@@ -197,7 +201,7 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
         mbar_init(smem_u32(&bars->pv_done[w][i]), 1);
       }
     mbar_init(smem_u32(&bars->q_full), QR * MT);
-    mbar_init(smem_u32(&bars->drain), MT);
+    mbar_init(smem_u32(&bars->drain), L::kIssuers);
     mbar_init(smem_u32(&bars->recv), 1);
     bars->abort_flag = 0;
     mbar_fence_init();  // cluster scope: other CTAs complete bytes on `recv`
@@ -395,7 +399,57 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
         mbar_wait(smem_u32(&bars->full[u % NS]), (u / NS) & 1, &no_abort, a.err);
       }
     }
-  } else if (has_work && warp <= MT) {
+  } else if (has_work && L::kSplit && warp <= 2) {
+    // ============ MMA issuers of the one row tile: warp 1 S, warp 2 P.V =========
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(M, N, 0, 0);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(M, D, 0, 1);
+      bool ok = mbar_wait(smem_u32(&bars->q_full), 0, abort_flag, a.err);
+      for (int u = 0; u < T && ok; ++u) {
+        const int stage = u % NS;
+        ok = mbar_wait(smem_u32(&bars->full[stage]), (u / NS) & 1, abort_flag, a.err);
+        if (!ok) break;
+        if (warp == 1) {
+          // S_u overwrites the S/P buffer of P_{u-2}: its P.V must be complete
+          if (u >= 2 && !mbar_wait(smem_u32(&bars->pv_done[0][u & 1]), ((u - 2) >> 1) & 1,
+                                   abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t k_base = sb + L::kRing + stage * L::kStage;
+#pragma unroll
+          for (int h = 0; h < L::kHalves; ++h) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = smem_desc_sw128(sb + L::kQ + h * L::kQHalf + kk * 32, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(k_base + h * L::kKVHalf + kk * 32, 16, 1024);
+              umma_bf16(tmem + (u & 1) * N, ad, bd, idesc_qk, (h | kk) ? 1u : 0u);
+            }
+          }
+          umma_commit(smem_u32(&bars->s_full[0][u & 1]));
+        } else {
+          if (!mbar_wait(smem_u32(&bars->p_full[0][u & 1]), (u >> 1) & 1, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t v_base = sb + L::kRing + stage * L::kStage + L::kKBytes;
+#pragma unroll
+          for (int ks = 0; ks < N / 16; ++ks) {
+            const uint64_t bd = smem_desc_sw128(v_base + ks * 2048, L::kKVHalf, 1024);
+            umma_bf16_tmem_a(tmem + kTmemO, tmem + (u & 1) * N + ks * 8, bd, idesc_pv,
+                             (u > 0 || ks > 0) ? 1u : 0u);
+          }
+          umma_commit(smem_u32(&bars->pv_done[0][u & 1]));
+          umma_commit(smem_u32(&bars->empty[stage]));
+        }
+      }
+      umma_commit(smem_u32(&bars->drain));
+      volatile int no_abort = 0;
+      mbar_wait(smem_u32(&bars->drain), 0, &no_abort, a.err);
+    }
+  } else if (has_work && !L::kSplit && warp <= MT) {
     // ============ MMA issuer of row tile wi (one lane) ===========================
     // A thread's tcgen05.mma instructions issue one after another, each taking
     // ~100 cycles to issue whatever its N (measured on GB300), so each row tile
