@@ -21,12 +21,12 @@
 // streams its share through an NS-stage shared-memory ring:
 //
 //   producers    page ids (requested with the sequence metadata, 32 at a time)
-//                -> cp.async.bulk.tensor loads of the K and V tiles, 128-byte
-//                swizzle, completion counted on an mbarrier. Warp 0; with two
-//                row tiles a second warp; with 64-row tiles also the two softmax
-//                warps whose TMEM lanes hold no rows. A tile's boxes are spread
-//                over lanes and warps: one thread issues a copy only every ~170
-//                cycles.
+//                -> cp.async.bulk.tensor loads of the K and V tiles, one box per
+//                page (or window block) and tensor, 128-byte swizzle, completion
+//                counted on an mbarrier. Warp 0; with two row tiles a second
+//                warp; with 64-row tiles also the two softmax warps whose TMEM
+//                lanes hold no rows. A tile's boxes are spread over lanes and
+//                warps: one thread issues a copy only every ~170 cycles.
 //   warps 1..MT  MMA issuers, one lane per row tile (warp 1 also owns TMEM):
 //                S = Q K^T into TMEM (double-buffered), then O += P V with P read
 //                from TMEM. One thread issues a tcgen05.mma only every ~100
@@ -86,8 +86,12 @@ struct Layout {
   // TMEM: per warpgroup, two S / P buffers of 64 columns, then D columns of O
   static constexpr uint32_t kWgCols = 128 + D;
   static constexpr uint32_t kTmemCols = MT * kWgCols <= 256 ? 256 : 512;
-  static constexpr int kKVHalf = N * 128;        // 64 key rows x 128 bytes
-  static constexpr int kKBytes = kHalves * kKVHalf;
+  // A K or V tile of 64 keys: eight 8-key groups, each kHalves blocks of 8 rows x
+  // 128 bytes (one 64-column half), group-major. A page (B / 8 groups, both
+  // halves) is then contiguous, one TMA box, and the MMA reads half h of all 64
+  // keys at a uniform 8-row stride.
+  static constexpr int kGroupBytes = kHalves * 1024;
+  static constexpr int kKBytes = 8 * kGroupBytes;
   static constexpr int kStage = 2 * kKBytes;     // K tile then V tile
   static constexpr int kQ = 0;
   static constexpr int kRing = kQ + kQBytes;
@@ -109,7 +113,6 @@ struct Layout {
   static constexpr int kThreads = 32 * kFirstSoft + kWgThreads * MT;
   static constexpr int kSoftWarps = 4 * MT;
   static constexpr int kProducers = 1 + (MT == 2 ? 1 : 0) + (QR == 64 ? 2 : 0);
-  static constexpr int kGroups = 2 * kHalves;  // TMA box groups of a tile: (K | V) x column half
   // Composition blocks (overlay Q and the ring): per owner, LR rows of D bf16
   // then LR (max, sum) pairs.
   static constexpr int kRowBytes = 2 * D;
@@ -319,17 +322,15 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
 
   if (has_work && prod >= 0) {
     // ======================= TMA producers (whole warps) ========================
-    // A tile is kGroups x ppt boxes of B rows x 128 bytes. Producer `prod` takes
-    // the groups c = prod, prod + kProducers, ...; lane = slot + ppt * (its j-th
-    // group), one box per lane. A thread's bulk-tensor copies issue one after
-    // another (~170 cycles each, measured on GB300), so the boxes of a tile are
-    // spread over lanes and warps.
+    // A tile is 2 x ppt boxes, box i = (tensor i / ppt: 0 = K, 1 = V; slot
+    // i % ppt: page or window block), B rows x D columns each. Producer `prod`
+    // takes boxes prod, prod + kProducers, ..., one per lane. A thread's
+    // bulk-tensor copies issue one after another (~170 cycles each, measured on
+    // GB300), so the boxes of a tile are spread over lanes and warps.
     constexpr int NP = L::kProducers;
-    const int ng = (L::kGroups - prod + NP - 1) / NP;  // groups of this producer
-    const int slot = lane % ppt, jg = lane / ppt;
-    const int grp = prod + jg * NP;                     // group of this lane
-    const bool lane_on = jg < ng;
-    const int tensor = grp / L::kHalves, half = grp % L::kHalves;  // 0 = K, 1 = V
+    const int box = prod + NP * lane;
+    const bool lane_on = box < 2 * ppt;
+    const int tensor = lane_on ? box / ppt : 0, slot = lane_on ? box % ppt : 0;
     const int n_pages = (C + B - 1) / B;          // cached pages of the sequence
     const int p_first = t0 * ppt;                 // first logical page of this CTA
     const int32_t *pt = a.page_table + (int64_t)b * a.max_pages_per_seq;
@@ -379,15 +380,15 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
       if (lane == 0 && prod == 0) D2F_PASS_MARK(2, 6, u);
       const unsigned have = __ballot_sync(0xffffffffu, src >= 0);
       const uint32_t full = smem_u32(&bars->full[stage]);
-      if (lane == 0) mbar_arrive_expect_tx(full, __popc(have) * (uint32_t)B * 128u);
+      if (lane == 0) mbar_arrive_expect_tx(full, __popc(have) * (uint32_t)B * D * 2u);
       __syncwarp();
       if (src >= 0) {
-        const uint32_t dst = sb + L::kRing + stage * L::kStage + tensor * L::kKBytes +
-                             half * L::kKVHalf + slot * B * 128;
-        if (t < Tc)
-          tma_load_4d(dst, tensor ? &tm_vpool : &tm_kpool, full, half * 64, 0, g, src);
-        else
-          tma_load_3d(dst, tensor ? &tm_vwin : &tm_kwin, full, half * 64, g, src);
+        const uint32_t dst =
+            sb + L::kRing + stage * L::kStage + tensor * L::kKBytes + slot * (B / 8) * L::kGroupBytes;
+        if (t < Tc)  // page src of KV head g: (page, head) row src * Hkv + g of the pool map
+          tma_load_5d(dst, tensor ? &tm_vpool : &tm_kpool, full, 0, 0, 0, 0, src * a.num_heads_kv + g);
+        else         // window rows src .. src + B - 1 (src is a multiple of 8)
+          tma_load_5d(dst, tensor ? &tm_vwin : &tm_kwin, full, 0, 0, 0, src >> 3, g);
       }
       issued = u + 1;
       if (lane == 0 && prod == 0) D2F_PASS_MARK(2, 7, u);
@@ -423,7 +424,7 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t ad = smem_desc_sw128(sb + L::kQ + h * L::kQHalf + kk * 32, 16, 1024);
-              const uint64_t bd = smem_desc_sw128(k_base + h * L::kKVHalf + kk * 32, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(k_base + h * 1024 + kk * 32, 16, L::kGroupBytes);
               umma_bf16(tmem + (u & 1) * N, ad, bd, idesc_qk, (h | kk) ? 1u : 0u);
             }
           }
@@ -437,7 +438,7 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
           const uint32_t v_base = sb + L::kRing + stage * L::kStage + L::kKBytes;
 #pragma unroll
           for (int ks = 0; ks < N / 16; ++ks) {
-            const uint64_t bd = smem_desc_sw128(v_base + ks * 2048, L::kKVHalf, 1024);
+            const uint64_t bd = smem_desc_sw128(v_base + ks * 2 * L::kGroupBytes, 1024, L::kGroupBytes);
             umma_bf16_tmem_a(tmem + kTmemO, tmem + (u & 1) * N + ks * 8, bd, idesc_pv,
                              (u > 0 || ks > 0) ? 1u : 0u);
           }
@@ -471,7 +472,7 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
         const uint32_t tw = tmem + i * L::kWgCols;
 #pragma unroll
         for (int ks = 0; ks < N / 16; ++ks) {  // 16 keys = 8 TMEM columns of P per step
-          const uint64_t bd = smem_desc_sw128(v_base + ks * 2048, L::kKVHalf, 1024);
+          const uint64_t bd = smem_desc_sw128(v_base + ks * 2 * L::kGroupBytes, 1024, L::kGroupBytes);
           umma_bf16_tmem_a(tw + kTmemO, tw + (u & 1) * N + ks * 8, bd, idesc_pv,
                            (u > 0 || ks > 0) ? 1u : 0u);
         }
@@ -509,7 +510,7 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t ad = smem_desc_sw128(qi_base + h * L::kQHalf + kk * 32, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(k_base + h * L::kKVHalf + kk * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(k_base + h * 1024 + kk * 32, 16, L::kGroupBytes);
             umma_bf16(tmem + wi * L::kWgCols + (u & 1) * N, ad, bd, idesc_qk, (h | kk) ? 1u : 0u);
           }
         }
@@ -657,12 +658,12 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
       // warpgroup clears them (the same zeros) before its own P.V is issued.
       if (row < N && row >= tile_lim) {
         const uint32_t v_row = sb + L::kRing + (u % NS) * L::kStage + L::kKBytes +
-                               (row >> 3) * 1024 + (row & 7) * 128;
+                               (row >> 3) * L::kGroupBytes + (row & 7) * 128;
 #pragma unroll
         for (int h = 0; h < L::kHalves; ++h)
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(v_row + h * L::kKVHalf +
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(v_row + h * 1024 +
                                                                            (c << 4)),
                          "r"(0u)
                          : "memory");
@@ -882,7 +883,7 @@ EncodeTiledFn get_encode_fn() {
 
 bool encode(EncodeTiledFn fn, CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims,
             const cuuint64_t *strides, const cuuint32_t *box) {
-  const cuuint32_t elem_strides[4] = {1, 1, 1, 1};
+  const cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims,
                         strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -918,18 +919,23 @@ cudaError_t launch_d(const AttnArgs &a, cudaStream_t s, char *why, size_t why_le
     return cudaErrorNotSupported;
   }
   CUtensorMap kp, vp, kw, vw;
-  const cuuint64_t pool_dims[4] = {(cuuint64_t)D, (cuuint64_t)a.block_size,
-                                   (cuuint64_t)a.num_heads_kv, (cuuint64_t)a.num_pages};
-  const cuuint64_t pool_strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)a.block_size * D * 2,
-                                      (cuuint64_t)a.num_heads_kv * a.block_size * D * 2};
-  const cuuint32_t pool_box[4] = {64, (cuuint32_t)a.block_size, 1, 1};
-  const cuuint64_t win_dims[3] = {(cuuint64_t)D, (cuuint64_t)a.num_heads_kv, (cuuint64_t)a.total_q};
-  const cuuint64_t win_strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.num_heads_kv * D * 2};
-  const cuuint32_t win_box[3] = {64, 1, (cuuint32_t)a.block_size};
-  if (!encode(fn, &kp, a.k_pool, 4, pool_dims, pool_strides, pool_box) ||
-      !encode(fn, &vp, a.v_pool, 4, pool_dims, pool_strides, pool_box) ||
-      !encode(fn, &kw, a.k_win, 3, win_dims, win_strides, win_box) ||
-      !encode(fn, &vw, a.v_win, 3, win_dims, win_strides, win_box)) {
+  // 5-D views whose box is one page (or window block) of one KV head, both
+  // column halves, landing group-major in shared memory (see Layout):
+  // (64 columns, 8 rows, column half, 8-row group, page x head | token group x head).
+  constexpr int H2 = D / 64;
+  const cuuint64_t B8 = (cuuint64_t)a.block_size / 8, rowb = (cuuint64_t)D * 2;
+  const cuuint64_t pool_dims[5] = {64, 8, (cuuint64_t)H2, B8,
+                                   (cuuint64_t)a.num_pages * a.num_heads_kv};
+  const cuuint64_t pool_strides[4] = {rowb, 128, 8 * rowb, (cuuint64_t)a.block_size * rowb};
+  const cuuint64_t tok = (cuuint64_t)a.num_heads_kv * rowb;  // window row stride
+  const cuuint64_t win_dims[5] = {64, 8, (cuuint64_t)H2, (cuuint64_t)a.total_q / 8,
+                                  (cuuint64_t)a.num_heads_kv};
+  const cuuint64_t win_strides[4] = {tok, 128, 8 * tok, rowb};
+  const cuuint32_t box[5] = {64, 8, (cuuint32_t)H2, (cuuint32_t)(a.block_size / 8), 1};
+  if (!encode(fn, &kp, a.k_pool, 5, pool_dims, pool_strides, box) ||
+      !encode(fn, &vp, a.v_pool, 5, pool_dims, pool_strides, box) ||
+      !encode(fn, &kw, a.k_win, 5, win_dims, win_strides, box) ||
+      !encode(fn, &vw, a.v_win, 5, win_dims, win_strides, box)) {
     snprintf(why, why_len, "cuTensorMapEncodeTiled rejected a K/V tensor (alignment or size)");
     return cudaErrorInvalidValue;
   }
