@@ -89,20 +89,39 @@ def _gqa_two_tiles():
                           permute_pages=True, extra_pages=3, seed=515)
 
 
-@pytest.mark.parametrize("name", ["dream", "gqa2"])
+def _gqa_mixed_rows():
+    # G = 7, windows of 3, 1 and 2 blocks of 16: 336, 112 and 224 packed rows, so
+    # the second CTA of a row-tile group holds one row tile, or none
+    return synth.Workload("gqa3r", 3, 28, 4, 128, 16, torch.bfloat16, [700, 333, 1500], [3, 1, 2], 64,
+                          permute_pages=True, extra_pages=5, seed=516)
+
+
+@pytest.mark.parametrize("name", ["dream", "gqa2", "gqa3r"])
 @pytest.mark.parametrize("splits", [0, 1, 3, 8])
 def test_two_row_tiles_per_cta(name, splits, monkeypatch):
     """GQA groups of 2 or 3 row tiles on CTAs of two row tiles with a softmax
     warpgroup each (D2F_TC_MT=1): one K/V stream for both, one accumulator per
-    row tile; three tiles leave the second CTA one tile, and a 128-row sequence
-    one idle warpgroup. Same result as the oracle."""
+    row tile; three tiles leave the second CTA one tile, and shorter sequences
+    one idle warpgroup or a CTA without rows. Same result as the oracle."""
     dev = device()
     monkeypatch.setenv("D2F_TC_MT", "1")
-    w = _gqa_two_tiles() if name == "gqa2" else synth.small(name)
+    w = {"gqa2": _gqa_two_tiles, "gqa3r": _gqa_mixed_rows}.get(name, lambda: synth.small(name))()
     p = synth.make_problem(w)
     out, lse = _run(p, dev, splits)
     ref, ref_lse = _ref(p)
     check_attention(out, lse, ref, ref_lse, torch.bfloat16, "mt/%s/s%d" % (name, splits))
+
+
+@pytest.mark.parametrize("splits", [0, 2])
+def test_two_row_tiles_longest_first(splits, monkeypatch):
+    """Two-row-tile CTAs with the sequences taken longest context first."""
+    dev = device()
+    monkeypatch.setenv("D2F_TC_MT", "1")
+    monkeypatch.setenv("D2F_LONGEST_FIRST", "1")
+    p = synth.make_problem(_gqa_mixed_rows())
+    out, lse = _run(p, dev, splits)
+    ref, ref_lse = _ref(p)
+    check_attention(out, lse, ref, ref_lse, torch.bfloat16, "mt-lf/s%d" % splits)
 
 
 @pytest.mark.parametrize("name", ["ragged", "dream", "long_b32"])
