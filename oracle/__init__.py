@@ -42,6 +42,11 @@ def _load():
             _P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P,
             _P, _P, _P, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int32,
             _P, _P, _P, ctypes.c_int]
+        lib.d2f_oracle_commit_metric.restype = ctypes.c_int
+        lib.d2f_oracle_commit_metric.argtypes = [
+            _P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P,
+            _P, _P, _P, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int32,
+            _P, _P, _P, ctypes.c_int, ctypes.c_int]
         lib.d2f_oracle_kv_append.restype = ctypes.c_int
         lib.d2f_oracle_kv_append.argtypes = [
             _P, _P, _P, _P, ctypes.c_int, ctypes.c_int, _P, _P,
@@ -113,11 +118,17 @@ def block_attn(q, k_win, v_win, k_pool, v_pool, page_table, ctx_len, q_start,
     return out, lse
 
 
+# confidence metrics of commit(): largest probability, negative entropy,
+# top-1 - top-2 probability margin, top-1 - top-2 logit gap
+CONF_PMAX, CONF_NEG_ENTROPY, CONF_MARGIN, CONF_LOGIT_GAP = 0, 1, 2, 3
+
+
 def commit(logits, tokens, masked, q_start, block_phase, tau, block_size, mask_id,
-           logit_row=None, row_stride=None, nthreads=None):
+           logit_row=None, row_stride=None, nthreads=None, metric=CONF_PMAX):
     """Confidence commit + remask. Returns a dict of new CPU tensors:
     tokens (int32), masked (uint8), conf (float32), argmax (int32),
-    block_remaining (int32). Inputs are not modified."""
+    block_remaining (int32). Inputs are not modified. `metric` picks the
+    confidence (tau in its units)."""
     lib = _load()
     logits = _cpu(logits)
     dt = _dt(logits)
@@ -138,11 +149,18 @@ def commit(logits, tokens, masked, q_start, block_phase, tau, block_size, mask_i
     conf = torch.empty(total_q, dtype=torch.float32)
     amax = torch.empty(total_q, dtype=torch.int32)
     rem = torch.empty(max(total_q // block_size, 0), dtype=torch.int32)
-    rc = lib.d2f_oracle_commit(
-        _ptr(logits), int(row_stride), dt, vocab, n_rows, _ptr(logit_row), _ptr(tokens),
-        _ptr(masked), _ptr(q_start), _ptr(block_phase), _ptr(tau), batch, total_q,
-        block_size, int(mask_id), _ptr(conf), _ptr(amax), _ptr(rem),
-        nthreads or default_threads())
+    if metric == CONF_PMAX:
+        rc = lib.d2f_oracle_commit(
+            _ptr(logits), int(row_stride), dt, vocab, n_rows, _ptr(logit_row), _ptr(tokens),
+            _ptr(masked), _ptr(q_start), _ptr(block_phase), _ptr(tau), batch, total_q,
+            block_size, int(mask_id), _ptr(conf), _ptr(amax), _ptr(rem),
+            nthreads or default_threads())
+    else:
+        rc = lib.d2f_oracle_commit_metric(
+            _ptr(logits), int(row_stride), dt, vocab, n_rows, _ptr(logit_row), _ptr(tokens),
+            _ptr(masked), _ptr(q_start), _ptr(block_phase), _ptr(tau), batch, total_q,
+            block_size, int(mask_id), _ptr(conf), _ptr(amax), _ptr(rem), int(metric),
+            nthreads or default_threads())
     if rc != 0:
         raise ValueError("oracle commit rejected its input (code %d)" % rc)
     return {"tokens": tokens, "masked": masked, "conf": conf, "argmax": amax,

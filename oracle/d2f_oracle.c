@@ -206,7 +206,66 @@ static void row_confidence(const void *logits, int64_t row_off, int dtype,
 }
 
 /*
+ * Alternative confidences of a still-masked position (same logit row).
+ *
+ * [P3] §토큰 순서의 이론: Dream ranks positions by negative entropy instead of the
+ * largest probability, and the top-probability-margin ordering ranks them by the
+ * difference between the largest and the second largest probability. [P3] §답을
+ * 미리 안다: 조기 확정 디코딩(Prophet): the confidence gap is the difference
+ * between the largest and the second largest logit.
+ *
+ * With m the largest logit, l2 the second largest (counted with multiplicity, so
+ * l2 = m when the maximum occurs twice; -inf for a one-token vocabulary),
+ * S = sum_v exp(l_v - m) and E = sum_v exp(l_v - m) (l_v - m):
+ *   metric 1, negative entropy:  sum_v p_v log p_v = E / S - log S
+ *   metric 2, probability margin: p_1 - p_2 = (1 - exp(l2 - m)) / S
+ *   metric 3, logit gap:          m - l2
+ * (p_v = exp(l_v - m) / S). Sums in double, each result rounded to float once;
+ * the gap of two floats widened from bf16 is exact. A logit of -inf has
+ * probability 0 and adds nothing to E. The greedy token is the lowest v with
+ * l_v = m, as for metric 0.
+ */
+static void row_metric(const void *logits, int64_t row_off, int dtype, int vocab,
+                       int metric, float *c_out, int32_t *a_out) {
+  float m = -INFINITY, l2 = -INFINITY;
+  int32_t a = -1;
+  for (int v = 0; v < vocab; ++v) {
+    const float x = load_elem_f32(logits, row_off + v, dtype);
+    if (a < 0) {
+      m = x;
+      a = v;
+    } else if (x > m) {
+      l2 = m;
+      m = x;
+      a = v;
+    } else if (x > l2) {
+      l2 = x;
+    }
+  }
+  double S = 0.0, E = 0.0;
+  for (int v = 0; v < vocab; ++v) {
+    const double x = (double)load_elem_f32(logits, row_off + v, dtype);
+    if (x == -INFINITY) continue;
+    const double t = exp(x - (double)m);
+    S += t;
+    E += t * (x - (double)m);
+  }
+  double c;
+  if (metric == 1)
+    c = E / S - log(S);
+  else if (metric == 2)
+    c = (1.0 - exp((double)l2 - (double)m)) / S;
+  else
+    c = (double)m - (double)l2;
+  *c_out = (float)c;
+  *a_out = a;
+}
+
+/*
  * Confidence commit with conservative / aggressive phases, then remasking.
+ * `metric` picks the confidence: 0 the largest softmax probability (below), 1-3
+ * the alternatives of row_metric (negative entropy, probability margin, logit
+ * gap); tau is in the metric's own units.
  *
  * [P2] §쉽게 이해하기 (pipelined decoding): a block that has just entered the
  * window is conservative and fixes only the tokens whose confidence is above
@@ -234,13 +293,14 @@ static void row_confidence(const void *logits, int64_t row_off, int dtype,
  *
  * Returns 0, or -1 bad sizes, -2 inconsistent q_start, -3 logit row out of range.
  */
-int d2f_oracle_commit(const void *logits, int64_t row_stride, int dtype,
-                      int vocab, int num_logit_rows, const int32_t *logit_row,
-                      int32_t *tokens, uint8_t *masked, const int32_t *q_start,
-                      const uint8_t *block_phase, const float *tau, int batch,
-                      int total_q, int block_size, int32_t mask_id,
-                      float *conf_out, int32_t *argmax_out,
-                      int32_t *block_remaining, int nthreads) {
+int d2f_oracle_commit_metric(const void *logits, int64_t row_stride, int dtype,
+                             int vocab, int num_logit_rows, const int32_t *logit_row,
+                             int32_t *tokens, uint8_t *masked, const int32_t *q_start,
+                             const uint8_t *block_phase, const float *tau, int batch,
+                             int total_q, int block_size, int32_t mask_id,
+                             float *conf_out, int32_t *argmax_out,
+                             int32_t *block_remaining, int metric, int nthreads) {
+  if (metric < 0 || metric > 3) return -1;
   if (batch < 0 || total_q < 0 || vocab <= 0 || block_size <= 0 ||
       block_size > 1024 || total_q % block_size != 0 || row_stride < vocab)
     return -1;
@@ -265,7 +325,10 @@ int d2f_oracle_commit(const void *logits, int64_t row_stride, int dtype,
   for (int r = 0; r < total_q; ++r) {
     if (masked[r]) {
       int lr = logit_row ? logit_row[r] : r;
-      row_confidence(logits, (int64_t)lr * row_stride, dtype, vocab, &conf[r], &amax[r]);
+      if (metric == 0)
+        row_confidence(logits, (int64_t)lr * row_stride, dtype, vocab, &conf[r], &amax[r]);
+      else
+        row_metric(logits, (int64_t)lr * row_stride, dtype, vocab, metric, &conf[r], &amax[r]);
     } else {
       conf[r] = -1.0f;
       amax[r] = -1;
@@ -318,6 +381,20 @@ int d2f_oracle_commit(const void *logits, int64_t row_stride, int dtype,
   free(conf);
   free(amax);
   return 0;
+}
+
+/* The commit with the largest softmax probability as confidence (metric 0). */
+int d2f_oracle_commit(const void *logits, int64_t row_stride, int dtype,
+                      int vocab, int num_logit_rows, const int32_t *logit_row,
+                      int32_t *tokens, uint8_t *masked, const int32_t *q_start,
+                      const uint8_t *block_phase, const float *tau, int batch,
+                      int total_q, int block_size, int32_t mask_id,
+                      float *conf_out, int32_t *argmax_out,
+                      int32_t *block_remaining, int nthreads) {
+  return d2f_oracle_commit_metric(logits, row_stride, dtype, vocab, num_logit_rows, logit_row,
+                                  tokens, masked, q_start, block_phase, tau, batch, total_q,
+                                  block_size, mask_id, conf_out, argmax_out, block_remaining,
+                                  0, nthreads);
 }
 
 /*
