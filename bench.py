@@ -44,6 +44,9 @@ def parse():
     ap.add_argument("--workload", default="llada")
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--commit-splits", type=int, default=0)
+    ap.add_argument("--conf-metric", default="pmax", choices=list(CONF_METRICS),
+                    help="confidence of the commit: largest probability (d2f_commit), negative "
+                         "entropy, probability margin or logit gap (d2f_commit_metric)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -221,10 +224,11 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # CPU oracle timing (reference arm and cpu_baseline)
 # ---------------------------------------------------------------------------
-def time_oracle(p, seconds, nthreads):
+def time_oracle(p, seconds, nthreads, metric=0):
     """Time the CPU oracle on a bounded sample of one step and extrapolate to
     full steps: attention over a subset of KV heads (its cost is linear in heads)
-    and the commit over a subset of rows (linear in rows)."""
+    and the commit over a subset of rows (linear in rows), with the commit's
+    confidence `metric`."""
     import oracle
     w = p.w
     Hk, G = w.num_heads_kv, w.num_heads_q // w.num_heads_kv
@@ -244,7 +248,8 @@ def time_oracle(p, seconds, nthreads):
         qs = torch.tensor([0, rows], dtype=torch.int32)
         t0 = time.perf_counter()
         oracle.commit(p.logits[:rows], p.tokens[:rows], p.masked[:rows], qs,
-                      p.block_phase[:nb], p.tau[:1], B, p.mask_id, nthreads=nthreads)
+                      p.block_phase[:nb], p.tau[:1], B, p.mask_id, nthreads=nthreads,
+                      metric=metric)
         return time.perf_counter() - t0
 
     ta1 = attn_sample(1)
@@ -285,8 +290,8 @@ def run_reference(args, world, rank):
     # bounded: the whole run takes about --ref-seconds regardless of K
     budget = args.ref_seconds
     for _ in range(max(0, min(args.warmup, 1))):
-        time_oracle(p, 0.1, nthreads)
-    value, sample = time_oracle(p, budget, nthreads)
+        time_oracle(p, 0.1, nthreads, CONF_METRICS[args.conf_metric])
+    value, sample = time_oracle(p, budget, nthreads, CONF_METRICS[args.conf_metric])
     ms = 1000.0 / value
     cfg = workload_config(p, args)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s",
@@ -300,9 +305,15 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+# confidence metric -> D2F_CONF_* value
+CONF_METRICS = {"pmax": 0, "negent": 1, "margin": 2, "gap": 3}
+
+
 def workload_config(p, args):
     w = p.w
-    return {"workload": "%s: batch %d, Hq %d / Hkv %d, head_dim %d, block %d, context %s, "
+    extra = {} if args.conf_metric == "pmax" else {
+        "confidence": "%s (d2f_commit_metric; tau as drawn for the workload)" % args.conf_metric}
+    return {**extra,"workload": "%s: batch %d, Hq %d / Hkv %d, head_dim %d, block %d, context %s, "
                         "window %s blocks, vocab %d" % (
                             w.name, w.batch, w.num_heads_q, w.num_heads_kv, w.head_dim,
                             w.block_size, "/".join(str(c) for c in sorted(set(w.ctx_lens))),
@@ -382,7 +393,8 @@ def run_ours(args, world, rank, local):
     def commit(s):
         d2f.commit(s.logits, s.tokens, s.masked, s.q_start, s.block_phase, s.tau, block_size=B,
                    mask_id=p.mask_id, num_splits=args.commit_splits, conf=conf, argmax=amax,
-                   block_remaining=rem, workspace=ws_commit, err=err)
+                   block_remaining=rem, workspace=ws_commit, err=err,
+                   metric=CONF_METRICS[args.conf_metric])
 
     def append(s):
         d2f.kv_append(s.k_win, s.v_win, s.src_row, s.dst_page, s.k_pool, s.v_pool, block_size=B,
@@ -565,7 +577,8 @@ def run_ours(args, world, rank, local):
             "clocks": clocks, "e2e": e2e}
     if rank == 0 and not args.no_cpu_baseline:
         value_cpu, sample = time_oracle(p if p.q.device.type == "cpu" else p.to("cpu"),
-                                        args.cpu_seconds, oracle_threads())
+                                        args.cpu_seconds, oracle_threads(),
+                                        CONF_METRICS[args.conf_metric])
         line["cpu_baseline"] = {"value": value_cpu, "unit": "steps/s", "cores": oracle_threads(),
                                 "kind": "oracle", "sample": sample}
     if rank == 0:

@@ -29,13 +29,29 @@ constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Per-row terms beyond (max, argmax, sum) by metric kind: MK 0 none (largest
+// probability), MK 1 e = sum of exp(l - m) (l - m) (negative entropy), MK 2
+// e = the second largest logit, counted with multiplicity (margin, logit gap).
+constexpr int kMkNone = 0, kMkEntropy = 1, kMkTop2 = 2;
+__host__ __device__ constexpr int metric_kind(int metric) {
+  return metric == D2F_CONF_NEG_ENTROPY ? kMkEntropy
+         : (metric == D2F_CONF_MARGIN || metric == D2F_CONF_LOGIT_GAP) ? kMkTop2 : kMkNone;
+}
+
 struct RowState {
   float m;    // running maximum
   int idx;    // lowest index attaining m
   float s;    // sum of exp(l - m)
+  float e;    // metric term (see metric_kind)
 };
 
+template <int MK>
 __device__ __forceinline__ RowState combine(RowState a, RowState b) {
+  if (MK == kMkTop2) {  // second largest of the union (before a state is dropped as empty)
+    const float e = fmaxf(fminf(a.m, b.m), fmaxf(a.e, b.e));
+    a.e = e;
+    b.e = e;
+  }
   if (b.m == -INFINITY) return a;
   if (a.m == -INFINITY) return b;
   RowState r;
@@ -49,10 +65,14 @@ __device__ __forceinline__ RowState combine(RowState a, RowState b) {
     r.m = a.m;
     r.idx = min(a.idx, b.idx);
   }
-  r.s = a.s * fast_exp2((a.m - r.m) * kLog2e) + b.s * fast_exp2((b.m - r.m) * kLog2e);
+  const float wa = fast_exp2((a.m - r.m) * kLog2e), wb = fast_exp2((b.m - r.m) * kLog2e);
+  r.s = a.s * wa + b.s * wb;
+  // sum exp(l - M)(l - M) = w (E + (m - M) S) for each part
+  r.e = MK == kMkEntropy ? wa * (a.e + (a.m - r.m) * a.s) + wb * (b.e + (b.m - r.m) * b.s) : a.e;
   return r;
 }
 
+template <int MK>
 __device__ __forceinline__ RowState warp_combine(RowState v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -60,16 +80,35 @@ __device__ __forceinline__ RowState warp_combine(RowState v) {
     w.m = __shfl_xor_sync(0xffffffffu, v.m, o);
     w.idx = __shfl_xor_sync(0xffffffffu, v.idx, o);
     w.s = __shfl_xor_sync(0xffffffffu, v.s, o);
-    v = combine(v, w);
+    w.e = MK != kMkNone ? __shfl_xor_sync(0xffffffffu, v.e, o) : 0.f;
+    v = combine<MK>(v, w);
   }
   return v;
 }
 
+// Confidence of a composed row state.
+__device__ __forceinline__ float row_conf(const RowState &r, int metric) {
+  if (metric == D2F_CONF_NEG_ENTROPY) return r.e / r.s - __logf(r.s);
+  if (metric == D2F_CONF_MARGIN) return (1.0f - fast_exp2((r.e - r.m) * kLog2e)) / r.s;
+  if (metric == D2F_CONF_LOGIT_GAP) return r.m - r.e;
+  return 1.0f / r.s;
+}
+
 // Fold N consecutive values starting at index v0 into the thread state. The
-// per-lane sums keep N independent accumulation chains.
-template <int N>
+// per-lane sums keep N independent accumulation chains; MK adds the entropy
+// numerator (one accumulator, rescaled with the sums) or the second largest value.
+template <int N, int MK>
 __device__ __forceinline__ void fold(const float (&x)[N], int v0, float &m, int &idx,
-                                     float (&acc)[N]) {
+                                     float (&acc)[N], float &acc_e, float &m2) {
+  if (MK == kMkTop2) {  // top two with multiplicity, before m takes this vector in
+    float t1 = m, t2 = m2;
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      t2 = fmaxf(t2, fminf(t1, x[j]));
+      t1 = fmaxf(t1, x[j]);
+    }
+    m2 = t2;
+  }
   float vm = x[0];
 #pragma unroll
   for (int j = 1; j < N; ++j) vm = fmaxf(vm, x[j]);
@@ -79,6 +118,13 @@ __device__ __forceinline__ void fold(const float (&x)[N], int v0, float &m, int 
     for (int j = N - 1; j >= 0; --j)
       if (x[j] == vm) first = j;
     const float alpha = fast_exp2((m - vm) * kLog2e);
+    if (MK == kMkEntropy) {
+      // sum exp(l - vm)(l - vm) = alpha (E + (m - vm) S); nothing to carry from m = -inf
+      float S = 0.f;
+#pragma unroll
+      for (int j = 0; j < N; ++j) S += acc[j];
+      acc_e = m == -INFINITY ? 0.f : alpha * (acc_e + (m - vm) * S);
+    }
 #pragma unroll
     for (int j = 0; j < N; ++j) acc[j] *= alpha;
     m = vm;
@@ -86,7 +132,16 @@ __device__ __forceinline__ void fold(const float (&x)[N], int v0, float &m, int 
   }
   // x - m is exact in float for bf16 inputs; one rounding in the scale.
 #pragma unroll
-  for (int j = 0; j < N; ++j) acc[j] += fast_exp2((x[j] - m) * kLog2e);
+  for (int j = 0; j < N; ++j) {
+    if (MK == kMkEntropy) {
+      const float d = fmaxf(x[j] - m, -1e30f);  // a -inf logit adds 0 (not 0 * inf)
+      const float t = fast_exp2(d * kLog2e);
+      acc[j] += t;
+      acc_e = fmaf(t, d, acc_e);
+    } else {
+      acc[j] += fast_exp2((x[j] - m) * kLog2e);
+    }
+  }
 }
 
 template <int DT>
@@ -153,7 +208,7 @@ __device__ void decide_block(const CommitArgs &a, int jb, const float *conf_s, c
   if (lane == 0 && a.block_remaining) a.block_remaining[jb] = __popc(left);
 }
 
-template <int DT, int PATH>  // PATH 0: scalar loads, 1: 128-bit loads
+template <int DT, int PATH, int MK>  // PATH 0: scalar loads, 1: 128-bit loads; MK: metric_kind
 __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
   constexpr int N = (DT == D2F_BF16) ? 8 : 4;  // values per 16-byte vector
   __shared__ RowState red[kThreads / 32];
@@ -203,9 +258,9 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
     const int v0 = s * a.chunk;
     const int v1 = min(a.vocab, v0 + a.chunk);
     const char *row = (const char *)a.logits + (int64_t)lr * a.row_stride * (DT == D2F_BF16 ? 2 : 4);
-    float m = -INFINITY;
+    float m = -INFINITY, m2 = -INFINITY;
     int idx = 0x7fffffff;
-    float acc[N];
+    float acc[N], acc_e = 0.f;
 #pragma unroll
     for (int j = 0; j < N; ++j) acc[j] = 0.f;
     int v_tail = v0;  // first index left for the scalar loop
@@ -223,13 +278,13 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
         for (int u = 0; u < kUnroll; ++u) {
           float x[N];
           unpack<DT>(raw[u], x);
-          fold<N>(x, (k + u * kThreads) * N, m, idx, acc);
+          fold<N, MK>(x, (k + u * kThreads) * N, m, idx, acc, acc_e, m2);
         }
       }
       for (; k < nvec_end; k += kThreads) {
         float x[N];
         unpack<DT>(__ldcs(vec + k), x);
-        fold<N>(x, k * N, m, idx, acc);
+        fold<N, MK>(x, k * N, m, idx, acc, acc_e, m2);
       }
       v_tail = max(v0, nvec_end * N);
     }
@@ -237,30 +292,45 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
     if (row_ok) {
       for (int e = v_tail + tid; e < v1; e += kThreads) {
         const float x = load_scalar<DT>(row, e);
+        if (MK == kMkTop2) m2 = fmaxf(m2, fminf(m, x));
         if (x > m) {  // new maximum: rescale every lane accumulator
           const float alpha = fast_exp2((m - x) * kLog2e);
+          if (MK == kMkEntropy) {
+            float S = 0.f;
+#pragma unroll
+            for (int j = 0; j < N; ++j) S += acc[j];
+            acc_e = m == -INFINITY ? 0.f : alpha * (acc_e + (m - x) * S);
+          }
 #pragma unroll
           for (int j = 0; j < N; ++j) acc[j] *= alpha;
           m = x;
           idx = e;
         }
-        acc[0] += fast_exp2((x - m) * kLog2e);
+        if (MK == kMkEntropy) {
+          const float d = fmaxf(x - m, -1e30f);
+          const float t = fast_exp2(d * kLog2e);
+          acc[0] += t;
+          acc_e = fmaf(t, d, acc_e);
+        } else {
+          acc[0] += fast_exp2((x - m) * kLog2e);
+        }
       }
     }
     float tot = 0.f;
 #pragma unroll
     for (int j = 0; j < N; ++j) tot += acc[j];
     if (tid == 0) D2F_TRACE_MARK(1, 4);
-    RowState st = {m, idx, tot};
-    st = warp_combine(st);
+    RowState st = {m, idx, tot, MK == kMkEntropy ? acc_e : MK == kMkTop2 ? m2 : 0.f};
+    const RowState empty = {-INFINITY, 0x7fffffff, 0.f, MK == kMkTop2 ? -INFINITY : 0.f};
+    st = warp_combine<MK>(st);
     if (lane == 0) red[warp] = st;
     __syncthreads();
     if (warp == 0) {
-      st = lane < kThreads / 32 ? red[lane] : RowState{-INFINITY, 0x7fffffff, 0.f};
-      st = warp_combine(st);
+      st = lane < kThreads / 32 ? red[lane] : empty;
+      st = warp_combine<MK>(st);
       if (lane == 0) {
-        if (!row_ok) st = RowState{-INFINITY, 0x7fffffff, 0.f};
-        a.partial[(int64_t)r * a.splits + s] = make_float4(st.m, __int_as_float(st.idx), st.s, 0.f);
+        if (!row_ok) st = empty;
+        a.partial[(int64_t)r * a.splits + s] = make_float4(st.m, __int_as_float(st.idx), st.s, st.e);
       }
     }
   }
@@ -276,12 +346,12 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
   for (int u0 = 2 * warp; u0 < B; u0 += 2 * (kThreads / 32)) {
     const int u = u0 + (lane >> 4);
     const int sub = lane & 15;
-    RowState acc2 = {-INFINITY, 0x7fffffff, 0.f};
+    RowState acc2 = {-INFINITY, 0x7fffffff, 0.f, MK == kMkTop2 ? -INFINITY : 0.f};
     if (u < B) {
       const int rr = jb * B + u;
       for (int j = sub; j < a.splits; j += 16) {
         const float4 p = __ldcg(a.partial + (int64_t)rr * a.splits + j);
-        acc2 = combine(acc2, RowState{p.x, __float_as_int(p.y), p.z});
+        acc2 = combine<MK>(acc2, RowState{p.x, __float_as_int(p.y), p.z, p.w});
       }
     }
 #pragma unroll
@@ -290,12 +360,13 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
       w.m = __shfl_xor_sync(0xffffffffu, acc2.m, o);
       w.idx = __shfl_xor_sync(0xffffffffu, acc2.idx, o);
       w.s = __shfl_xor_sync(0xffffffffu, acc2.s, o);
-      acc2 = combine(acc2, w);
+      w.e = __shfl_xor_sync(0xffffffffu, acc2.e, o);
+      acc2 = combine<MK>(acc2, w);
     }
     if (sub == 0 && u < B) {
       // rows not masked on entry have no partials (their slots are stale)
       const bool ok = acc2.s > 0.f;
-      conf_s[u] = ok ? 1.0f / acc2.s : -1.0f;
+      conf_s[u] = ok ? row_conf(acc2, a.metric) : -1.0f;
       arg_s[u] = ok ? acc2.idx : -1;
     }
   }
@@ -312,7 +383,7 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
 // Keep the L1 / shared-memory split at its shared-memory maximum, as the
 // attention kernel needs it: alternating kernels then never make an SM drain and
 // reconfigure between launches. Set once per device.
-template <int DT, int PATH>
+template <int DT, int PATH, int MK>
 cudaError_t ensure_carveout() {
   static std::mutex mu;
   static bool done[64] = {};
@@ -321,15 +392,15 @@ cudaError_t ensure_carveout() {
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(commit_kernel<DT, PATH>, cudaFuncAttributePreferredSharedMemoryCarveout,
+  e = cudaFuncSetAttribute(commit_kernel<DT, PATH, MK>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return e;
 }
 
-template <int DT, int PATH>
+template <int DT, int PATH, int MK>
 cudaError_t launch_path(const CommitArgs &a, cudaStream_t stream) {
-  cudaError_t ce = ensure_carveout<DT, PATH>();
+  cudaError_t ce = ensure_carveout<DT, PATH, MK>();
   if (ce != cudaSuccess) return ce;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.splits, a.total_q);
@@ -341,21 +412,30 @@ cudaError_t launch_path(const CommitArgs &a, cudaStream_t stream) {
   // kernel still waits on its dependencies (a no-op without the attribute).
   cfg.attrs = nullptr;
   cfg.numAttrs = 0;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, commit_kernel<DT, PATH>, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, commit_kernel<DT, PATH, MK>, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+template <int MK>
+cudaError_t launch_kind(const CommitArgs &a, int dtype, int path, cudaStream_t stream) {
+  if (dtype == D2F_BF16) {
+    if (path == 1) return launch_path<D2F_BF16, 1, MK>(a, stream);
+    return launch_path<D2F_BF16, 0, MK>(a, stream);
+  }
+  if (path == 1) return launch_path<D2F_F32, 1, MK>(a, stream);
+  return launch_path<D2F_F32, 0, MK>(a, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_commit(const CommitArgs &a, int dtype, int path, cudaStream_t stream) {
   if (a.total_q == 0) return cudaSuccess;
-  if (dtype == D2F_BF16) {
-    if (path == 1) return launch_path<D2F_BF16, 1>(a, stream);
-    return launch_path<D2F_BF16, 0>(a, stream);
+  switch (metric_kind(a.metric)) {
+    case kMkEntropy: return launch_kind<kMkEntropy>(a, dtype, path, stream);
+    case kMkTop2: return launch_kind<kMkTop2>(a, dtype, path, stream);
+    default: return launch_kind<kMkNone>(a, dtype, path, stream);
   }
-  if (path == 1) return launch_path<D2F_F32, 1>(a, stream);
-  return launch_path<D2F_F32, 0>(a, stream);
 }
 
 }  // namespace d2f

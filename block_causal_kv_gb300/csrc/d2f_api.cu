@@ -406,12 +406,15 @@ int d2f_commit_workspace_size(int total_q, int vocab, int dtype, int block_size,
   return D2F_OK;
 }
 
-int d2f_commit(const void *logits, int64_t row_stride, int dtype, int vocab, int num_logit_rows,
-               const int32_t *logit_row, int32_t *tokens, uint8_t *masked,
-               const int32_t *q_start, const uint8_t *block_phase, const float *tau, int batch,
-               int total_q, int block_size, int32_t mask_id, float *conf_out,
-               int32_t *argmax_out, int32_t *block_remaining, int num_splits, void *workspace,
-               size_t workspace_bytes, int32_t *err_word, void *stream) {
+int d2f_commit_metric(const void *logits, int64_t row_stride, int dtype, int vocab,
+                      int num_logit_rows, const int32_t *logit_row, int32_t *tokens,
+                      uint8_t *masked, const int32_t *q_start, const uint8_t *block_phase,
+                      const float *tau, int batch, int total_q, int block_size, int32_t mask_id,
+                      int metric, float *conf_out, int32_t *argmax_out, int32_t *block_remaining,
+                      int num_splits, void *workspace, size_t workspace_bytes, int32_t *err_word,
+                      void *stream) {
+  if (metric < D2F_CONF_PMAX || metric > D2F_CONF_LOGIT_GAP)
+    return fail(D2F_ERR_INVALID_ARG, "metric %d is not a D2F_CONF_* value", metric);
   CommitPlan p{};
   int st = plan_commit(total_q, vocab, dtype, block_size, num_splits, &p);
   if (st != D2F_OK) return st;
@@ -451,9 +454,22 @@ int d2f_commit(const void *logits, int64_t row_stride, int dtype, int vocab, int
   a.partial = reinterpret_cast<float4 *>(ws + p.off_partial);
   a.blk_cnt = reinterpret_cast<int32_t *>(ws + p.off_blkcnt);
   a.err = err_word;
+  a.metric = metric;
   const cudaError_t e = launch_commit(a, dtype, path, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "commit launch");
   return D2F_OK;
+}
+
+int d2f_commit(const void *logits, int64_t row_stride, int dtype, int vocab, int num_logit_rows,
+               const int32_t *logit_row, int32_t *tokens, uint8_t *masked,
+               const int32_t *q_start, const uint8_t *block_phase, const float *tau, int batch,
+               int total_q, int block_size, int32_t mask_id, float *conf_out,
+               int32_t *argmax_out, int32_t *block_remaining, int num_splits, void *workspace,
+               size_t workspace_bytes, int32_t *err_word, void *stream) {
+  return d2f_commit_metric(logits, row_stride, dtype, vocab, num_logit_rows, logit_row, tokens,
+                           masked, q_start, block_phase, tau, batch, total_q, block_size, mask_id,
+                           D2F_CONF_PMAX, conf_out, argmax_out, block_remaining, num_splits,
+                           workspace, workspace_bytes, err_word, stream);
 }
 
 int d2f_kv_append(const void *k_win, const void *v_win, const int32_t *src_row,

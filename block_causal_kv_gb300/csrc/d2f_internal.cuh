@@ -66,7 +66,8 @@ struct CommitArgs {
   int32_t *argmax_out, *block_remaining;
   int splits;            // CTAs per row
   int chunk;             // vocabulary entries per CTA
-  float4 *partial;       // [total_q][splits] (max, argmax bits, sum, unused)
+  float4 *partial;       // [total_q][splits] (max, argmax bits, sum, metric term)
+  int metric;            // D2F_CONF_*: confidence compared with tau
   int32_t *blk_cnt;      // [total_q / block_size] arrivals per block (zero at rest)
   int32_t *err;
 };

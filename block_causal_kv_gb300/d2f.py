@@ -32,7 +32,10 @@ STATUS = {0: "D2F_OK", 1: "D2F_ERR_INVALID_ARG", 2: "D2F_ERR_UNSUPPORTED", 3: "D
 # Every symbol include/d2f.h declares.
 EXPORTS = ("d2f_version", "d2f_status_string", "d2f_last_error_string",
            "d2f_block_attn_workspace_size", "d2f_block_attn", "d2f_commit_workspace_size",
-           "d2f_commit", "d2f_commit_noalloc", "d2f_kv_append")
+           "d2f_commit", "d2f_commit_metric", "d2f_commit_noalloc", "d2f_kv_append")
+
+# confidence metrics of commit(metric=...) (include/d2f.h D2F_CONF_*)
+CONF_PMAX, CONF_NEG_ENTROPY, CONF_MARGIN, CONF_LOGIT_GAP = 0, 1, 2, 3
 
 
 class D2FError(RuntimeError):
@@ -69,6 +72,9 @@ def load(path=LIB_PATH):
     lib.d2f_commit.restype = _I
     lib.d2f_commit.argtypes = ([_P, ctypes.c_int64, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I,
                                 ctypes.c_int32, _P, _P, _P, _I, _P, _SZ, _P, _P])
+    lib.d2f_commit_metric.restype = _I
+    lib.d2f_commit_metric.argtypes = ([_P, ctypes.c_int64, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I,
+                                       _I, _I, ctypes.c_int32, _I, _P, _P, _P, _I, _P, _SZ, _P, _P])
     lib.d2f_commit_noalloc.restype = _I
     lib.d2f_commit_noalloc.argtypes = ([_P, ctypes.c_int64, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I,
                                         _I, _I, ctypes.c_int32, _P, _P, _P, _I, _P, _P])
@@ -193,11 +199,13 @@ def commit_workspace(device, **kw):
 
 def commit(logits, tokens, masked, q_start, block_phase, tau, *, block_size, mask_id,
            logit_row=None, num_splits=0, conf=None, argmax=None, block_remaining=None,
-           want_outputs=True, workspace=None, err=None, stream=None):
+           want_outputs=True, workspace=None, err=None, stream=None, metric=CONF_PMAX):
     """Confidence commit + remask, in place on tokens / masked.
 
     logits may be a row-strided view ([rows, vocab] with stride(1) == 1).
-    Returns dict(conf, argmax, block_remaining) (device tensors, or None)."""
+    metric: CONF_PMAX (d2f_commit) or another CONF_* (d2f_commit_metric; tau in
+    the metric's units). Returns dict(conf, argmax, block_remaining) (device
+    tensors, or None)."""
     lib = load()
     if not logits.is_cuda or logits.stride(-1) != 1:
         raise ValueError("logits must be a CUDA tensor with unit stride along the vocabulary")
@@ -222,12 +230,20 @@ def commit(logits, tokens, masked, q_start, block_phase, tau, *, block_size, mas
     if workspace is None:
         workspace = commit_workspace(dev, total_q=total_q, vocab=vocab, block_size=block_size,
                                      dtype=dt, num_splits=num_splits)
-    _check(lib.d2f_commit(
-        _ptr(logits), logits.stride(0), dt, vocab, rows, _ptr(logit_row), _ptr(tokens),
-        _ptr(masked), _ptr(q_start), _ptr(block_phase), _ptr(tau), q_start.shape[0] - 1, total_q,
-        block_size, int(mask_id), _ptr(conf), _ptr(argmax), _ptr(block_remaining), num_splits,
-        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err),
-        _stream(stream)))
+    if metric == CONF_PMAX:
+        _check(lib.d2f_commit(
+            _ptr(logits), logits.stride(0), dt, vocab, rows, _ptr(logit_row), _ptr(tokens),
+            _ptr(masked), _ptr(q_start), _ptr(block_phase), _ptr(tau), q_start.shape[0] - 1,
+            total_q, block_size, int(mask_id), _ptr(conf), _ptr(argmax), _ptr(block_remaining),
+            num_splits, _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err),
+            _stream(stream)))
+    else:
+        _check(lib.d2f_commit_metric(
+            _ptr(logits), logits.stride(0), dt, vocab, rows, _ptr(logit_row), _ptr(tokens),
+            _ptr(masked), _ptr(q_start), _ptr(block_phase), _ptr(tau), q_start.shape[0] - 1,
+            total_q, block_size, int(mask_id), int(metric), _ptr(conf), _ptr(argmax),
+            _ptr(block_remaining), num_splits, _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream)))
     return {"conf": conf, "argmax": argmax, "block_remaining": block_remaining}
 
 

@@ -65,6 +65,13 @@ typedef enum d2f_dtype { D2F_BF16 = 0, D2F_F32 = 1 } d2f_dtype;
 
 /* Block phases ([P2] §쉽게 이해하기). */
 enum { D2F_PHASE_CONSERVATIVE = 0, D2F_PHASE_AGGRESSIVE = 1 };
+/* Confidence metrics of d2f_commit_metric (d2f_commit uses D2F_CONF_PMAX). */
+enum {
+  D2F_CONF_PMAX = 0,         /* largest softmax probability */
+  D2F_CONF_NEG_ENTROPY = 1,  /* sum_v p_v ln p_v */
+  D2F_CONF_MARGIN = 2,       /* largest minus second largest probability */
+  D2F_CONF_LOGIT_GAP = 3     /* largest minus second largest logit */
+};
 
 /* Library version, e.g. 100 for 0.1.0. */
 int d2f_version(void);
@@ -186,6 +193,39 @@ int d2f_commit(const void *logits, int64_t row_stride, int dtype, int vocab, int
                int total_q, int block_size, int32_t mask_id, float *conf_out,
                int32_t *argmax_out, int32_t *block_remaining, int num_splits, void *workspace,
                size_t workspace_bytes, int32_t *err_word, void *stream);
+
+/*
+ * d2f_commit_metric -- d2f_commit with another confidence, in the same single
+ * pass over each masked position's logits.
+ *
+ * "확산 언어 모델(Diffusion LLM)이란 무엇인가", §토큰 순서의 이론: Dream ranks
+ * positions by negative entropy rather than the largest probability, and the
+ * top-probability-margin ordering ranks them by the difference between the
+ * largest and the second largest probability; §답을 미리 안다: 조기 확정
+ * 디코딩(Prophet): the confidence gap is the largest logit minus the second
+ * largest. With m, a and S = sum_v exp(l_v - m) as for d2f_commit,
+ * E = sum_v exp(l_v - m) (l_v - m) and l2 the second largest logit counted with
+ * multiplicity (l2 = m when the maximum occurs twice):
+ *   D2F_CONF_PMAX         c = 1 / S                   (d2f_commit)
+ *   D2F_CONF_NEG_ENTROPY  c = E / S - ln S  (= sum_v p_v ln p_v, <= 0)
+ *   D2F_CONF_MARGIN       c = (1 - exp(l2 - m)) / S  (= p_1 - p_2)
+ *   D2F_CONF_LOGIT_GAP    c = m - l2
+ * in float arithmetic (the gap is exact for bf16 logits). The commit rule is
+ * d2f_commit's with c in place of p: conservative blocks commit c > tau[b]
+ * (tau in the metric's units), aggressive blocks also their largest c;
+ * conf_out receives c. A logit of -inf adds nothing to S or E.
+ *
+ * Arguments as d2f_commit, plus metric (D2F_CONF_*; other values return
+ * D2F_ERR_INVALID_ARG). The workspace is d2f_commit_workspace_size's for the
+ * same sizes.
+ */
+int d2f_commit_metric(const void *logits, int64_t row_stride, int dtype, int vocab,
+                      int num_logit_rows, const int32_t *logit_row, int32_t *tokens,
+                      uint8_t *masked, const int32_t *q_start, const uint8_t *block_phase,
+                      const float *tau, int batch, int total_q, int block_size, int32_t mask_id,
+                      int metric, float *conf_out, int32_t *argmax_out, int32_t *block_remaining,
+                      int num_splits, void *workspace, size_t workspace_bytes, int32_t *err_word,
+                      void *stream);
 
 /*
  * d2f_commit_noalloc -- d2f_commit without a caller workspace, for callers that

@@ -45,9 +45,13 @@ def check_attention(out, lse, ref, ref_lse, dtype, label=""):
     return mx, mean
 
 
-def commit_compare(p, gpu_tokens, gpu_masked, gpu_conf, gpu_arg, gpu_rem, phase, tau, ref):
+def commit_compare(p, gpu_tokens, gpu_masked, gpu_conf, gpu_arg, gpu_rem, phase, tau, ref,
+                   band=None, atol=0.0):
     """Compare a GPU commit with the oracle's. Returns (n_band, n_tie) positions
-    excluded from the bit-exact check."""
+    excluded from the bit-exact check. band: the |c - tau| (and top-two) band
+    excluded from it (default BAND); atol: absolute slack on the confidence
+    besides CONF_RTOL (for metrics that can be near 0)."""
+    BAND_ = BAND if band is None else band
     m0 = p.masked.cpu().bool()
     conf = gpu_conf.cpu()
     arg = gpu_arg.cpu()
@@ -55,14 +59,15 @@ def commit_compare(p, gpu_tokens, gpu_masked, gpu_conf, gpu_arg, gpu_rem, phase,
     assert torch.equal(arg[m0], ref["argmax"][m0]), "argmax mismatch"
     assert torch.equal(arg[~m0], torch.full_like(arg[~m0], -1))
     rc = ref["conf"][m0].double()
-    rel = ((conf[m0].double() - rc).abs() / rc).max().item() if m0.any() else 0.0
+    err = ((conf[m0].double() - rc).abs() - atol).clamp(min=0.0)
+    rel = (err / (rc.abs() + 1e-30)).max().item() if m0.any() else 0.0
     assert rel <= CONF_RTOL, "conf rel err %.3g" % rel
     # excluded positions
     B = p.w.block_size
     q_start = p.q_start.cpu()
     seq = torch.searchsorted(q_start, torch.arange(len(m0), dtype=torch.int32), right=True) - 1
     t_row = tau.cpu()[seq]
-    band = m0 & ((ref["conf"] - t_row).abs() < BAND)
+    band = m0 & ((ref["conf"] - t_row).abs() < BAND_)
     tie_rows = torch.zeros_like(m0)
     nb = len(m0) // B
     ph = phase.cpu()
@@ -70,9 +75,9 @@ def commit_compare(p, gpu_tokens, gpu_masked, gpu_conf, gpu_arg, gpu_rem, phase,
         if ph[jb] != 1:
             continue
         sl = slice(jb * B, (jb + 1) * B)
-        c = torch.where(m0[sl], ref["conf"][sl], torch.tensor(-1.0))
+        c = torch.where(m0[sl], ref["conf"][sl], torch.tensor(float("-inf")))
         top = torch.sort(c, descending=True).values
-        if m0[sl].sum() >= 2 and float(top[0] - top[1]) < BAND:
+        if m0[sl].sum() >= 2 and float(top[0] - top[1]) < BAND_:
             tie_rows[sl] = True
     excl = band | tie_rows
     tok = gpu_tokens.cpu()

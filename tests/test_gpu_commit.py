@@ -16,25 +16,32 @@ from gpu_common import commit_compare, device
 pytestmark = pytest.mark.gpu
 
 
-def _gpu_commit(p, dev, phase=None, tau=None, num_splits=0, logit_row=None, logits=None):
+def _gpu_commit(p, dev, phase=None, tau=None, num_splits=0, logit_row=None, logits=None,
+                metric=0):
     g = p.to(dev)
     phase = g.block_phase if phase is None else phase.to(dev)
     tau = g.tau if tau is None else tau.to(dev)
     lg = g.logits if logits is None else logits.to(dev)
     lr = None if logit_row is None else logit_row.to(dev)
     res = d2f.commit(lg, g.tokens, g.masked, g.q_start, phase, tau, block_size=p.w.block_size,
-                     mask_id=p.mask_id, logit_row=lr, num_splits=num_splits)
+                     mask_id=p.mask_id, logit_row=lr, num_splits=num_splits, metric=metric)
     torch.cuda.synchronize()
     return g, res, phase, tau
 
 
-def _check(p, dev, phase=None, tau=None, num_splits=0, logit_row=None, logits=None):
-    g, res, phase, tau = _gpu_commit(p, dev, phase, tau, num_splits, logit_row, logits)
+# per metric: (absolute slack on the confidence, |c - tau| band excluded from
+# the bit-exact decisions); the logit gap is exact
+METRIC_TOL = {0: (0.0, None), 1: (2e-5, 1e-4), 2: (2e-6, 1e-5), 3: (0.0, 1e-6)}
+
+
+def _check(p, dev, phase=None, tau=None, num_splits=0, logit_row=None, logits=None, metric=0):
+    g, res, phase, tau = _gpu_commit(p, dev, phase, tau, num_splits, logit_row, logits, metric)
     ref = oracle.commit(p.logits if logits is None else logits, p.tokens, p.masked, p.q_start,
                         phase.cpu(), tau.cpu(), p.w.block_size, p.mask_id,
-                        logit_row=logit_row)
+                        logit_row=logit_row, metric=metric)
+    atol, band = METRIC_TOL[metric]
     return commit_compare(p, g.tokens, g.masked, res["conf"], res["argmax"],
-                          res["block_remaining"], phase, tau, ref)
+                          res["block_remaining"], phase, tau, ref, band=band, atol=atol)
 
 
 @pytest.mark.parametrize("name", ["tiny", "llada", "ragged", "dream", "long_b8", "long_b32"])
@@ -143,3 +150,51 @@ def test_nothing_masked_and_repeated_calls():
     torch.cuda.synchronize()
     assert int(res["block_remaining"].sum()) == 0
     assert torch.all(res["conf"] == -1)
+
+
+# tau in each metric's units, near the middle of its range on these logits
+METRIC_TAU = {1: (-2.5, -0.5, -0.05), 2: (0.3, 0.6, 0.9), 3: (1.0, 3.0, 6.0)}
+
+
+@pytest.mark.parametrize("metric", [1, 2, 3])
+@pytest.mark.parametrize("name", ["tiny", "llada", "ragged", "dream"])
+@pytest.mark.parametrize("splits", [0, 5])
+def test_confidence_metrics(metric, name, splits):
+    """Negative entropy, probability margin and logit gap in the same streaming
+    pass (d2f_commit_metric): confidence, greedy token and commit decisions match
+    the oracle's on every workload shape (float32 Tiny on the scalar path),
+    with tau drawn in the metric's own units and random phases."""
+    dev = device()
+    w = synth.workload("tiny") if name == "tiny" else synth.small(name)
+    p = synth.make_problem(w)
+    g = torch.Generator().manual_seed(100 + metric)
+    taus = torch.tensor(METRIC_TAU[metric], dtype=torch.float32)
+    tau = taus[torch.randint(0, len(taus), (p.w.batch,), generator=g)]
+    phase = torch.randint(0, 2, p.block_phase.shape, generator=g, dtype=torch.uint8)
+    lr = None
+    if name == "dream":  # Dream's one-position shift of the logit rows
+        lr = torch.clamp(torch.arange(p.w.total_q, dtype=torch.int32) - 1, min=0)
+    nb, nt = _check(p, dev, phase=phase, tau=tau, num_splits=splits, logit_row=lr, metric=metric)
+    print("%s m%d s%d: band %d tie %d" % (name, metric, splits, nb, nt))
+
+
+@pytest.mark.parametrize("metric", [1, 2, 3])
+def test_confidence_metrics_ties_and_unaligned_rows(metric):
+    """Tie-heavy logits (repeated maxima: margin and gap 0) and rows that are not
+    16-byte aligned (scalar path)."""
+    dev = device()
+    p = _tiny_vocab(3, vocab=4096)
+    g = torch.Generator().manual_seed(7)
+    tied = (torch.randint(0, 3, p.logits.shape, generator=g).float() * 0.5).to(torch.bfloat16)
+    _check(p, dev, logits=tied, num_splits=5, metric=metric,
+           tau=torch.full_like(p.tau, METRIC_TAU[metric][1]))
+    w = synth.Workload("u", 1, 1, 1, 8, 8, torch.bfloat16, [0], [2], 999, logit_row_pad=2, seed=23)
+    _check(synth.make_problem(w), dev, num_splits=3, metric=metric,
+           tau=torch.full((1,), METRIC_TAU[metric][0]))
+
+
+def test_unknown_metric_is_rejected():
+    dev = device()
+    p = _tiny_vocab(2)
+    with pytest.raises(d2f.D2FError):
+        _gpu_commit(p, dev, metric=7)
