@@ -46,7 +46,7 @@ def _load():
         lib.d2f_oracle_commit_metric.argtypes = [
             _P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P,
             _P, _P, _P, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int32,
-            _P, _P, _P, ctypes.c_int, ctypes.c_int]
+            _P, _P, _P, ctypes.c_int, _P, _P, ctypes.c_int]
         lib.d2f_oracle_kv_append.restype = ctypes.c_int
         lib.d2f_oracle_kv_append.argtypes = [
             _P, _P, _P, _P, ctypes.c_int, ctypes.c_int, _P, _P,
@@ -124,11 +124,12 @@ CONF_PMAX, CONF_NEG_ENTROPY, CONF_MARGIN, CONF_LOGIT_GAP = 0, 1, 2, 3
 
 
 def commit(logits, tokens, masked, q_start, block_phase, tau, block_size, mask_id,
-           logit_row=None, row_stride=None, nthreads=None, metric=CONF_PMAX):
+           logit_row=None, row_stride=None, nthreads=None, metric=CONF_PMAX, early_gap=None):
     """Confidence commit + remask. Returns a dict of new CPU tensors:
     tokens (int32), masked (uint8), conf (float32), argmax (int32),
-    block_remaining (int32). Inputs are not modified. `metric` picks the
-    confidence (tau in its units)."""
+    block_remaining (int32), stopped (uint8 per sequence). Inputs are not
+    modified. `metric` picks the confidence (tau in its units); early_gap (per
+    sequence) turns on the early commit of whole sequences."""
     lib = _load()
     logits = _cpu(logits)
     dt = _dt(logits)
@@ -149,7 +150,9 @@ def commit(logits, tokens, masked, q_start, block_phase, tau, block_size, mask_i
     conf = torch.empty(total_q, dtype=torch.float32)
     amax = torch.empty(total_q, dtype=torch.int32)
     rem = torch.empty(max(total_q // block_size, 0), dtype=torch.int32)
-    if metric == CONF_PMAX:
+    early_gap = _cpu(early_gap, torch.float32)
+    stopped = torch.zeros(max(batch, 1), dtype=torch.uint8)
+    if metric == CONF_PMAX and early_gap is None:
         rc = lib.d2f_oracle_commit(
             _ptr(logits), int(row_stride), dt, vocab, n_rows, _ptr(logit_row), _ptr(tokens),
             _ptr(masked), _ptr(q_start), _ptr(block_phase), _ptr(tau), batch, total_q,
@@ -160,11 +163,11 @@ def commit(logits, tokens, masked, q_start, block_phase, tau, block_size, mask_i
             _ptr(logits), int(row_stride), dt, vocab, n_rows, _ptr(logit_row), _ptr(tokens),
             _ptr(masked), _ptr(q_start), _ptr(block_phase), _ptr(tau), batch, total_q,
             block_size, int(mask_id), _ptr(conf), _ptr(amax), _ptr(rem), int(metric),
-            nthreads or default_threads())
+            _ptr(early_gap), _ptr(stopped), nthreads or default_threads())
     if rc != 0:
         raise ValueError("oracle commit rejected its input (code %d)" % rc)
     return {"tokens": tokens, "masked": masked, "conf": conf, "argmax": amax,
-            "block_remaining": rem}
+            "block_remaining": rem, "stopped": stopped[:batch]}
 
 
 def kv_append(k_win, v_win, src_row, dst_page, k_pool, v_pool, block_size):

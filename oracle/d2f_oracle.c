@@ -267,6 +267,18 @@ static void row_metric(const void *logits, int64_t row_off, int dtype, int vocab
  * the alternatives of row_metric (negative entropy, probability margin, logit
  * gap); tau is in the metric's own units.
  *
+ * Early commit ([P3] §답을 미리 안다: 조기 확정 디코딩(Prophet): when the
+ * confidence gap -- largest minus second largest logit -- over the answer region
+ * exceeds a threshold, every remaining mask is filled with its argmax at once;
+ * the threshold is lowered in stages (7.5, 5.0, 2.5) as decoding progresses).
+ * With early_gap (per sequence, the caller's current threshold; NULL = off):
+ * reading taken, the region is the sequence's window and its gap is the
+ * smallest logit gap over the positions masked on entry; if that exceeds
+ * early_gap[b] (strict), every masked position of b is committed with its
+ * greedy token, its blocks' block_remaining become 0 and stopped[b] = 1; else
+ * the block rules apply and stopped[b] = 0 (a sequence with nothing masked does
+ * not stop). stopped may be NULL.
+ *
  * [P2] §쉽게 이해하기 (pipelined decoding): a block that has just entered the
  * window is conservative and fixes only the tokens whose confidence is above
  * the threshold; once its predecessor has progressed enough it turns
@@ -299,7 +311,8 @@ int d2f_oracle_commit_metric(const void *logits, int64_t row_stride, int dtype,
                              const uint8_t *block_phase, const float *tau, int batch,
                              int total_q, int block_size, int32_t mask_id,
                              float *conf_out, int32_t *argmax_out,
-                             int32_t *block_remaining, int metric, int nthreads) {
+                             int32_t *block_remaining, int metric, const float *early_gap,
+                             uint8_t *stopped, int nthreads) {
   if (metric < 0 || metric > 3) return -1;
   if (batch < 0 || total_q < 0 || vocab <= 0 || block_size <= 0 ||
       block_size > 1024 || total_q % block_size != 0 || row_stride < vocab)
@@ -314,9 +327,11 @@ int d2f_oracle_commit_metric(const void *logits, int64_t row_stride, int dtype,
 
   float *conf = (float *)malloc(sizeof(float) * (size_t)(total_q > 0 ? total_q : 1));
   int32_t *amax = (int32_t *)malloc(sizeof(int32_t) * (size_t)(total_q > 0 ? total_q : 1));
-  if (!conf || !amax) {
+  float *gap = (float *)malloc(sizeof(float) * (size_t)(total_q > 0 ? total_q : 1));
+  if (!conf || !amax || !gap) {
     free(conf);
     free(amax);
+    free(gap);
     return -4;
   }
 
@@ -329,6 +344,10 @@ int d2f_oracle_commit_metric(const void *logits, int64_t row_stride, int dtype,
         row_confidence(logits, (int64_t)lr * row_stride, dtype, vocab, &conf[r], &amax[r]);
       else
         row_metric(logits, (int64_t)lr * row_stride, dtype, vocab, metric, &conf[r], &amax[r]);
+      if (early_gap) {
+        int32_t a2;
+        row_metric(logits, (int64_t)lr * row_stride, dtype, vocab, 3, &gap[r], &a2);
+      }
     } else {
       conf[r] = -1.0f;
       amax[r] = -1;
@@ -374,12 +393,35 @@ int d2f_oracle_commit_metric(const void *logits, int64_t row_stride, int dtype,
     }
     if (block_remaining) block_remaining[jb] = remaining;
   }
+  /* Early commit of a whole sequence (only with early_gap). */
+  for (int b = 0; early_gap && b < batch; ++b) {
+    float gmin = INFINITY;
+    int any = 0;
+    for (int r = q_start[b]; r < q_start[b + 1]; ++r)
+      if (amax[r] >= 0) {  /* masked on entry */
+        any = 1;
+        if (gap[r] < gmin) gmin = gap[r];
+      }
+    const int stop = any && gmin > early_gap[b];
+    if (stopped) stopped[b] = (uint8_t)stop;
+    if (!stop) continue;
+    for (int r = q_start[b]; r < q_start[b + 1]; ++r)
+      if (masked[r]) {
+        tokens[r] = amax[r];
+        masked[r] = 0;
+      }
+    for (int jb = q_start[b] / block_size; jb < q_start[b + 1] / block_size; ++jb)
+      if (block_remaining) block_remaining[jb] = 0;
+  }
+  if (!early_gap && stopped)
+    for (int b = 0; b < batch; ++b) stopped[b] = 0;
   for (int r = 0; r < total_q; ++r) {
     if (conf_out) conf_out[r] = conf[r];
     if (argmax_out) argmax_out[r] = amax[r];
   }
   free(conf);
   free(amax);
+  free(gap);
   return 0;
 }
 
@@ -394,7 +436,7 @@ int d2f_oracle_commit(const void *logits, int64_t row_stride, int dtype,
   return d2f_oracle_commit_metric(logits, row_stride, dtype, vocab, num_logit_rows, logit_row,
                                   tokens, masked, q_start, block_phase, tau, batch, total_q,
                                   block_size, mask_id, conf_out, argmax_out, block_remaining,
-                                  0, nthreads);
+                                  0, NULL, NULL, nthreads);
 }
 
 /*

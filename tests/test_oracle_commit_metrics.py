@@ -110,3 +110,59 @@ def test_threshold_in_metric_units_is_strict(oracle, metric):
                             torch.tensor([0, 1], dtype=torch.int32), torch.zeros(1, dtype=torch.uint8),
                             torch.tensor([tau]), 1, 3, metric=metric)
         assert res["masked"].item() == (0 if committed else 1)
+
+
+def _early_problem():
+    """Two sequences of two blocks of 2 (vocab 4, float32 logits). Sequence 0:
+    masked rows with logit gaps 3, 5 and 4 (row 1 committed earlier); sequence 1:
+    gaps 6, 6, 0.5 and 7."""
+    rows = [[3, 0, 0, 0], [0, 0, 0, 0], [0, 5, 0, 0], [0, 0, 4, -1],
+            [6, 0, 0, 0], [0, 6, 0, 0], [0.5, 0, 0, 0], [0, 0, 0, 7]]
+    logits = torch.tensor(rows, dtype=torch.float32)
+    tokens = torch.full((8,), 4, dtype=torch.int32)
+    tokens[1] = 2
+    masked = torch.ones(8, dtype=torch.uint8)
+    masked[1] = 0
+    q_start = torch.tensor([0, 4, 8], dtype=torch.int32)
+    return logits, tokens, masked, q_start
+
+
+@pytest.mark.parametrize("metric", [0, 2, 3])
+def test_early_commit_of_whole_sequences(oracle, metric):
+    """Prophet's early commit: a sequence whose smallest logit gap over its masked
+    positions exceeds its threshold commits them all with their greedy tokens
+    (stopped = 1, block_remaining = 0); a sequence with one position at or below
+    the threshold keeps the block rule (here: nothing passes tau)."""
+    logits, tokens, masked, q_start = _early_problem()
+    phase = torch.zeros(4, dtype=torch.uint8)
+    tau = torch.tensor([1e9, 1e9])
+    for gap0, gap1, stop in ((2.5, 0.4, (1, 1)), (3.0, 0.5, (0, 0)), (2.9, 5.0, (1, 0))):
+        res = oracle.commit(logits, tokens, masked, q_start, phase, tau, 2, 4, metric=metric,
+                            early_gap=torch.tensor([gap0, gap1]))
+        assert res["stopped"].tolist() == list(stop), (gap0, gap1, res["stopped"])
+        want_tok = [0, 2, 1, 2] if stop[0] else [4, 2, 4, 4]
+        want_tok += [0, 1, 0, 3] if stop[1] else [4, 4, 4, 4]
+        assert res["tokens"].tolist() == want_tok
+        assert res["masked"].tolist() == ([0, 0, 0, 0] if stop[0] else [1, 0, 1, 1]) + \
+            ([0, 0, 0, 0] if stop[1] else [1, 1, 1, 1])
+        assert res["block_remaining"].tolist() == ([0, 0] if stop[0] else [1, 2]) + \
+            ([0, 0] if stop[1] else [2, 2])
+
+
+def test_early_commit_leaves_the_block_rule_otherwise(oracle):
+    """Without early_gap the result equals the plain commit; a sequence with
+    nothing masked never stops."""
+    logits, tokens, masked, q_start = _early_problem()
+    phase = torch.tensor([1, 0, 1, 0], dtype=torch.uint8)
+    tau = torch.tensor([4.5, 6.5])
+    plain = oracle.commit(logits, tokens, masked, q_start, phase, tau, 2, 4, metric=3)
+    off = oracle.commit(logits, tokens, masked, q_start, phase, tau, 2, 4, metric=3,
+                        early_gap=torch.tensor([1e9, 1e9]))
+    for k in ("tokens", "masked", "block_remaining", "conf", "argmax"):
+        assert torch.equal(plain[k], off[k]), k
+    assert off["stopped"].tolist() == [0, 0]
+    none = torch.zeros(8, dtype=torch.uint8)
+    res = oracle.commit(logits, tokens, none, q_start, phase, tau, 2, 4, metric=3,
+                        early_gap=torch.tensor([-1.0, -1.0]))
+    assert res["stopped"].tolist() == [0, 0]
+    assert torch.equal(res["tokens"], tokens)
