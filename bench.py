@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--conf-metric", default="pmax", choices=list(CONF_METRICS),
                     help="confidence of the commit: largest probability (d2f_commit), negative "
                          "entropy, probability margin or logit gap (d2f_commit_metric)")
+    ap.add_argument("--early-gap", type=float, default=None,
+                    help="early commit of whole sequences at this logit-gap threshold "
+                         "(d2f_commit_metric; every sequence)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -313,6 +316,8 @@ def workload_config(p, args):
     w = p.w
     extra = {} if args.conf_metric == "pmax" else {
         "confidence": "%s (d2f_commit_metric; tau as drawn for the workload)" % args.conf_metric}
+    if args.early_gap is not None:
+        extra["early_commit_gap"] = args.early_gap
     return {**extra,"workload": "%s: batch %d, Hq %d / Hkv %d, head_dim %d, block %d, context %s, "
                         "window %s blocks, vocab %d" % (
                             w.name, w.batch, w.num_heads_q, w.num_heads_kv, w.head_dim,
@@ -390,11 +395,16 @@ def run_ours(args, world, rank, local):
                        num_splits=args.num_splits, out=s.out, want_lse=False, workspace=ws_attn,
                        err=err)
 
+    early_gap = stopped = None
+    if args.early_gap is not None:
+        early_gap = torch.full((w.batch,), args.early_gap, dtype=torch.float32, device=dev)
+        stopped = torch.zeros(w.batch, dtype=torch.uint8, device=dev)
+
     def commit(s):
         d2f.commit(s.logits, s.tokens, s.masked, s.q_start, s.block_phase, s.tau, block_size=B,
                    mask_id=p.mask_id, num_splits=args.commit_splits, conf=conf, argmax=amax,
                    block_remaining=rem, workspace=ws_commit, err=err,
-                   metric=CONF_METRICS[args.conf_metric])
+                   metric=CONF_METRICS[args.conf_metric], early_gap=early_gap, stopped=stopped)
 
     def append(s):
         d2f.kv_append(s.k_win, s.v_win, s.src_row, s.dst_page, s.k_pool, s.v_pool, block_size=B,

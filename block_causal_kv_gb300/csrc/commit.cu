@@ -208,11 +208,61 @@ __device__ void decide_block(const CommitArgs &a, int jb, const float *conf_s, c
   if (lane == 0 && a.block_remaining) a.block_remaining[jb] = __popc(left);
 }
 
+// Early commit of whole sequences ("확산 언어 모델(Diffusion LLM)이란 무엇인가",
+// §답을 미리 안다: 조기 확정 디코딩(Prophet): once the gap between the largest and
+// the second largest logit over the answer region exceeds a threshold, every
+// remaining mask is filled with its argmax). Reading: the region is the
+// sequence's window and its gap the smallest over the rows masked on entry. One
+// warp, after decide_block for block jb of sequence b: record the block's
+// smallest gap and its rows' greedy tokens, arrive on the sequence's counter
+// (at its first block); the last block of the sequence to arrive decides it and
+// commits the rows still masked in every block of it.
+__device__ void early_commit(const CommitArgs &a, int jb, int b, const float *gap_s,
+                             const int *arg_s, bool m) {
+  const int lane = threadIdx.x & 31;
+  const int B = a.block_size;
+  const int r = jb * B + lane;
+  float g = m ? gap_s[lane] : INFINITY;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) g = fminf(g, __shfl_xor_sync(0xffffffffu, g, o));
+  if (m) a.row_arg[r] = arg_s[lane];
+  if (lane == 0) a.blk_gap[jb] = g;
+  const int q0 = __ldg(a.q_start + b), q1 = __ldg(a.q_start + b + 1);
+  const int jb0 = q0 / B, nblk = (q1 - q0) / B;
+  __threadfence();  // this block's decision, gap and tokens before the arrival
+  __syncwarp();
+  int last = 0;
+  if (lane == 0) last = atomic_add_acq_rel(a.seq_cnt + jb0, 1) == nblk - 1;
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return;
+  __threadfence();
+  float gs = INFINITY;
+  for (int j = jb0 + lane; j < jb0 + nblk; j += 32) gs = fminf(gs, __ldcg(a.blk_gap + j));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) gs = fminf(gs, __shfl_xor_sync(0xffffffffu, gs, o));
+  const bool stop = gs < INFINITY && gs > __ldg(a.early_gap + b);  // strict, in float
+  if (stop) {
+    for (int rr = q0 + lane; rr < q1; rr += 32) {
+      if (__ldcg(a.masked + rr)) {
+        a.tokens[rr] = __ldcg(a.row_arg + rr);
+        a.masked[rr] = 0;
+      }
+    }
+    if (a.block_remaining)
+      for (int j = jb0 + lane; j < jb0 + nblk; j += 32) a.block_remaining[j] = 0;
+  }
+  if (lane == 0) {
+    if (a.stopped) a.stopped[b] = stop ? 1 : 0;
+    a.seq_cnt[jb0] = 0;
+  }
+}
+
 template <int DT, int PATH, int MK>  // PATH 0: scalar loads, 1: 128-bit loads; MK: metric_kind
 __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
   constexpr int N = (DT == D2F_BF16) ? 8 : 4;  // values per 16-byte vector
   __shared__ RowState red[kThreads / 32];
   __shared__ float conf_s[32];
+  __shared__ float gap_s[32];  // logit gap of each row (top-two state only)
   __shared__ int arg_s[32];
   __shared__ int is_last;
 
@@ -234,7 +284,7 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
   // Decision metadata of this block, fetched now, used only by the last arriver:
   // lane u of warp 0 holds row u's masked flag, thread 0 the block's tau and phase.
   float tau_b = 0.f;
-  int phase = 0;
+  int phase = 0, seq_b = 0;
   const bool blk_masked = warp == 0 && lane < B && a.masked[jb * B + lane] != 0;
   if (tid == 0) {
     int lo = 0, hi = a.batch - 1;
@@ -245,6 +295,7 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
     }
     tau_b = __ldg(a.tau + lo);
     phase = __ldg(a.block_phase + jb);
+    seq_b = lo;
   }
   const bool is_masked = a.masked[r] != 0;
 
@@ -367,6 +418,7 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
       // rows not masked on entry have no partials (their slots are stale)
       const bool ok = acc2.s > 0.f;
       conf_s[u] = ok ? row_conf(acc2, a.metric) : -1.0f;
+      gap_s[u] = ok && MK == kMkTop2 ? acc2.m - acc2.e : INFINITY;
       arg_s[u] = ok ? acc2.idx : -1;
     }
   }
@@ -376,6 +428,8 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
     phase = __shfl_sync(0xffffffffu, phase, 0);
     decide_block(a, jb, conf_s, arg_s, tau_b, phase, blk_masked);
     if (lane == 0) a.blk_cnt[jb] = 0;
+    if (MK == kMkTop2 && a.early_gap) early_commit(a, jb, __shfl_sync(0xffffffffu, seq_b, 0),
+                                                   gap_s, arg_s, blk_masked);
     if (lane == 0) D2F_TRACE_MARK(1, 7);
   }
 }
@@ -431,6 +485,9 @@ cudaError_t launch_kind(const CommitArgs &a, int dtype, int path, cudaStream_t s
 
 cudaError_t launch_commit(const CommitArgs &a, int dtype, int path, cudaStream_t stream) {
   if (a.total_q == 0) return cudaSuccess;
+  // the early commit needs every row's logit gap: the top-two state
+  if (a.early_gap && a.metric != D2F_CONF_NEG_ENTROPY)
+    return launch_kind<kMkTop2>(a, dtype, path, stream);
   switch (metric_kind(a.metric)) {
     case kMkEntropy: return launch_kind<kMkEntropy>(a, dtype, path, stream);
     case kMkTop2: return launch_kind<kMkTop2>(a, dtype, path, stream);

@@ -236,7 +236,7 @@ constexpr int kCommitMaxSplits = 64;
 
 struct CommitPlan {
   int splits, chunk;
-  size_t off_blkcnt, off_partial, bytes;
+  size_t off_blkcnt, off_seqcnt, off_blkgap, off_rowarg, off_partial, bytes;
 };
 
 int plan_commit(int total_q, int vocab, int dtype, int B, int num_splits, CommitPlan *p) {
@@ -274,7 +274,10 @@ int plan_commit(int total_q, int vocab, int dtype, int B, int num_splits, Commit
   // zeroed workspace stays valid across calls with different splits.
   const size_t nq = (size_t)total_q;
   p->off_blkcnt = 0;
-  p->off_partial = align_up((nq / B + 1) * sizeof(int32_t));
+  p->off_seqcnt = align_up((nq / B + 1) * sizeof(int32_t));
+  p->off_blkgap = p->off_seqcnt + align_up((nq / B + 1) * sizeof(int32_t));
+  p->off_rowarg = p->off_blkgap + align_up((nq / B + 1) * sizeof(float));
+  p->off_partial = p->off_rowarg + align_up((nq + 1) * sizeof(int32_t));
   p->bytes = p->off_partial + align_up(nq * splits * sizeof(float4));
   return D2F_OK;
 }
@@ -410,11 +413,14 @@ int d2f_commit_metric(const void *logits, int64_t row_stride, int dtype, int voc
                       int num_logit_rows, const int32_t *logit_row, int32_t *tokens,
                       uint8_t *masked, const int32_t *q_start, const uint8_t *block_phase,
                       const float *tau, int batch, int total_q, int block_size, int32_t mask_id,
-                      int metric, float *conf_out, int32_t *argmax_out, int32_t *block_remaining,
-                      int num_splits, void *workspace, size_t workspace_bytes, int32_t *err_word,
-                      void *stream) {
+                      int metric, const float *early_gap, uint8_t *stopped, float *conf_out,
+                      int32_t *argmax_out, int32_t *block_remaining, int num_splits,
+                      void *workspace, size_t workspace_bytes, int32_t *err_word, void *stream) {
   if (metric < D2F_CONF_PMAX || metric > D2F_CONF_LOGIT_GAP)
     return fail(D2F_ERR_INVALID_ARG, "metric %d is not a D2F_CONF_* value", metric);
+  if (early_gap && metric == D2F_CONF_NEG_ENTROPY)
+    return fail(D2F_ERR_UNSUPPORTED, "the early commit combines with D2F_CONF_PMAX, _MARGIN or "
+                "_LOGIT_GAP, not with D2F_CONF_NEG_ENTROPY");
   CommitPlan p{};
   int st = plan_commit(total_q, vocab, dtype, block_size, num_splits, &p);
   if (st != D2F_OK) return st;
@@ -455,6 +461,11 @@ int d2f_commit_metric(const void *logits, int64_t row_stride, int dtype, int voc
   a.blk_cnt = reinterpret_cast<int32_t *>(ws + p.off_blkcnt);
   a.err = err_word;
   a.metric = metric;
+  a.early_gap = early_gap;
+  a.stopped = stopped;
+  a.seq_cnt = reinterpret_cast<int32_t *>(ws + p.off_seqcnt);
+  a.blk_gap = reinterpret_cast<float *>(ws + p.off_blkgap);
+  a.row_arg = reinterpret_cast<int32_t *>(ws + p.off_rowarg);
   const cudaError_t e = launch_commit(a, dtype, path, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "commit launch");
   return D2F_OK;
@@ -468,8 +479,8 @@ int d2f_commit(const void *logits, int64_t row_stride, int dtype, int vocab, int
                size_t workspace_bytes, int32_t *err_word, void *stream) {
   return d2f_commit_metric(logits, row_stride, dtype, vocab, num_logit_rows, logit_row, tokens,
                            masked, q_start, block_phase, tau, batch, total_q, block_size, mask_id,
-                           D2F_CONF_PMAX, conf_out, argmax_out, block_remaining, num_splits,
-                           workspace, workspace_bytes, err_word, stream);
+                           D2F_CONF_PMAX, nullptr, nullptr, conf_out, argmax_out, block_remaining,
+                           num_splits, workspace, workspace_bytes, err_word, stream);
 }
 
 int d2f_kv_append(const void *k_win, const void *v_win, const int32_t *src_row,

@@ -68,6 +68,11 @@ struct CommitArgs {
   int chunk;             // vocabulary entries per CTA
   float4 *partial;       // [total_q][splits] (max, argmax bits, sum, metric term)
   int metric;            // D2F_CONF_*: confidence compared with tau
+  const float *early_gap;  // [batch] early-commit logit-gap thresholds, or NULL (off)
+  uint8_t *stopped;        // [batch] early-commit flags out, or NULL
+  int32_t *seq_cnt;        // [total_q / block_size] block arrivals per sequence, at its first block
+  float *blk_gap;          // [total_q / block_size] smallest logit gap over a block's masked rows
+  int32_t *row_arg;        // [total_q] greedy token of every masked row
   int32_t *blk_cnt;      // [total_q / block_size] arrivals per block (zero at rest)
   int32_t *err;
 };

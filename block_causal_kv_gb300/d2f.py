@@ -74,7 +74,8 @@ def load(path=LIB_PATH):
                                 ctypes.c_int32, _P, _P, _P, _I, _P, _SZ, _P, _P])
     lib.d2f_commit_metric.restype = _I
     lib.d2f_commit_metric.argtypes = ([_P, ctypes.c_int64, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I,
-                                       _I, _I, ctypes.c_int32, _I, _P, _P, _P, _I, _P, _SZ, _P, _P])
+                                       _I, _I, ctypes.c_int32, _I, _P, _P, _P, _P, _P, _I, _P, _SZ,
+                                       _P, _P])
     lib.d2f_commit_noalloc.restype = _I
     lib.d2f_commit_noalloc.argtypes = ([_P, ctypes.c_int64, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I,
                                         _I, _I, ctypes.c_int32, _P, _P, _P, _I, _P, _P])
@@ -199,13 +200,15 @@ def commit_workspace(device, **kw):
 
 def commit(logits, tokens, masked, q_start, block_phase, tau, *, block_size, mask_id,
            logit_row=None, num_splits=0, conf=None, argmax=None, block_remaining=None,
-           want_outputs=True, workspace=None, err=None, stream=None, metric=CONF_PMAX):
+           want_outputs=True, workspace=None, err=None, stream=None, metric=CONF_PMAX,
+           early_gap=None, stopped=None):
     """Confidence commit + remask, in place on tokens / masked.
 
     logits may be a row-strided view ([rows, vocab] with stride(1) == 1).
     metric: CONF_PMAX (d2f_commit) or another CONF_* (d2f_commit_metric; tau in
-    the metric's units). Returns dict(conf, argmax, block_remaining) (device
-    tensors, or None)."""
+    the metric's units). early_gap (float32 [batch]) turns on the early commit
+    of whole sequences; stopped (uint8 [batch]) receives its flags. Returns
+    dict(conf, argmax, block_remaining, stopped) (device tensors, or None)."""
     lib = load()
     if not logits.is_cuda or logits.stride(-1) != 1:
         raise ValueError("logits must be a CUDA tensor with unit stride along the vocabulary")
@@ -230,7 +233,9 @@ def commit(logits, tokens, masked, q_start, block_phase, tau, *, block_size, mas
     if workspace is None:
         workspace = commit_workspace(dev, total_q=total_q, vocab=vocab, block_size=block_size,
                                      dtype=dt, num_splits=num_splits)
-    if metric == CONF_PMAX:
+    _dev(early_gap, "early_gap", torch.float32)
+    _dev(stopped, "stopped", torch.uint8)
+    if metric == CONF_PMAX and early_gap is None:
         _check(lib.d2f_commit(
             _ptr(logits), logits.stride(0), dt, vocab, rows, _ptr(logit_row), _ptr(tokens),
             _ptr(masked), _ptr(q_start), _ptr(block_phase), _ptr(tau), q_start.shape[0] - 1,
@@ -241,10 +246,11 @@ def commit(logits, tokens, masked, q_start, block_phase, tau, *, block_size, mas
         _check(lib.d2f_commit_metric(
             _ptr(logits), logits.stride(0), dt, vocab, rows, _ptr(logit_row), _ptr(tokens),
             _ptr(masked), _ptr(q_start), _ptr(block_phase), _ptr(tau), q_start.shape[0] - 1,
-            total_q, block_size, int(mask_id), int(metric), _ptr(conf), _ptr(argmax),
-            _ptr(block_remaining), num_splits, _ptr(workspace),
+            total_q, block_size, int(mask_id), int(metric), _ptr(early_gap), _ptr(stopped),
+            _ptr(conf), _ptr(argmax), _ptr(block_remaining), num_splits, _ptr(workspace),
             workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream)))
-    return {"conf": conf, "argmax": argmax, "block_remaining": block_remaining}
+    return {"conf": conf, "argmax": argmax, "block_remaining": block_remaining,
+            "stopped": stopped}
 
 
 def commit_noalloc(logits, tokens, masked, q_start, block_phase, tau, *, block_size, mask_id,

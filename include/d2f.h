@@ -215,17 +215,30 @@ int d2f_commit(const void *logits, int64_t row_stride, int dtype, int vocab, int
  * (tau in the metric's units), aggressive blocks also their largest c;
  * conf_out receives c. A logit of -inf adds nothing to S or E.
  *
+ * Early commit (same passage on Prophet: once the gap between the largest and
+ * the second largest logit over the answer region exceeds a threshold, every
+ * remaining mask is filled with its argmax; the threshold is lowered in stages,
+ * 7.5 / 5.0 / 2.5, as decoding progresses): with early_gap non-NULL (device
+ * float [batch], the caller's current thresholds), sequence b -- reading taken:
+ * its window is the region, its gap the smallest m - l2 over the rows masked on
+ * entry -- stops when that gap exceeds early_gap[b] (strict): after the block
+ * rules every row of b still masked is committed with its greedy token, its
+ * blocks' block_remaining become 0 and stopped[b] = 1 (device uint8 [batch], or
+ * NULL); otherwise stopped[b] = 0, also for a sequence with nothing masked.
+ * It combines with D2F_CONF_PMAX, _MARGIN and _LOGIT_GAP (D2F_ERR_UNSUPPORTED
+ * with _NEG_ENTROPY).
+ *
  * Arguments as d2f_commit, plus metric (D2F_CONF_*; other values return
- * D2F_ERR_INVALID_ARG). The workspace is d2f_commit_workspace_size's for the
- * same sizes.
+ * D2F_ERR_INVALID_ARG), early_gap and stopped. The workspace is
+ * d2f_commit_workspace_size's for the same sizes.
  */
 int d2f_commit_metric(const void *logits, int64_t row_stride, int dtype, int vocab,
                       int num_logit_rows, const int32_t *logit_row, int32_t *tokens,
                       uint8_t *masked, const int32_t *q_start, const uint8_t *block_phase,
                       const float *tau, int batch, int total_q, int block_size, int32_t mask_id,
-                      int metric, float *conf_out, int32_t *argmax_out, int32_t *block_remaining,
-                      int num_splits, void *workspace, size_t workspace_bytes, int32_t *err_word,
-                      void *stream);
+                      int metric, const float *early_gap, uint8_t *stopped, float *conf_out,
+                      int32_t *argmax_out, int32_t *block_remaining, int num_splits,
+                      void *workspace, size_t workspace_bytes, int32_t *err_word, void *stream);
 
 /*
  * d2f_commit_noalloc -- d2f_commit without a caller workspace, for callers that

@@ -198,3 +198,81 @@ def test_unknown_metric_is_rejected():
     p = _tiny_vocab(2)
     with pytest.raises(d2f.D2FError):
         _gpu_commit(p, dev, metric=7)
+
+
+def _early_hand_problem():
+    rows = [[3, 0, 0, 0], [0, 0, 0, 0], [0, 5, 0, 0], [0, 0, 4, -1],
+            [6, 0, 0, 0], [0, 6, 0, 0], [0.5, 0, 0, 0], [0, 0, 0, 7]]
+    w = synth.Workload("e", 2, 1, 1, 8, 2, torch.float32, [0, 0], [2, 2], 4, seed=30)
+    p = synth.make_problem(w)
+    p.logits = torch.tensor(rows, dtype=torch.float32)
+    p.tokens = torch.full((8,), 4, dtype=torch.int32)
+    p.tokens[1] = 2
+    p.masked = torch.ones(8, dtype=torch.uint8)
+    p.masked[1] = 0
+    p.mask_id = 4
+    return p
+
+
+def _early_check(p, dev, metric, early_gap, phase=None, tau=None, num_splits=0):
+    g = p.to(dev)
+    phase = g.block_phase if phase is None else phase.to(dev)
+    tau = g.tau if tau is None else tau.to(dev)
+    stopped = torch.full((p.w.batch,), 9, dtype=torch.uint8, device=dev)
+    res = d2f.commit(g.logits, g.tokens, g.masked, g.q_start, phase, tau, block_size=p.w.block_size,
+                     mask_id=p.mask_id, num_splits=num_splits, metric=metric,
+                     early_gap=early_gap.to(dev), stopped=stopped)
+    torch.cuda.synchronize()
+    ref = oracle.commit(p.logits, p.tokens, p.masked, p.q_start, phase.cpu(), tau.cpu(),
+                        p.w.block_size, p.mask_id, metric=metric, early_gap=early_gap)
+    assert torch.equal(stopped.cpu(), ref["stopped"]), (stopped.cpu(), ref["stopped"])
+    atol, band = METRIC_TOL[metric]
+    commit_compare(p, g.tokens, g.masked, res["conf"], res["argmax"], res["block_remaining"],
+                   phase, tau, ref, band=band, atol=atol)
+    return ref["stopped"]
+
+
+@pytest.mark.parametrize("metric", [0, 2, 3])
+def test_early_commit_hand_sequences(metric):
+    """Prophet's early commit on hand-built sequences (gaps 3/5/4 and 6/6/0.5/7):
+    stopped flags, tokens, masks and block_remaining as the oracle's."""
+    dev = device()
+    p = _early_hand_problem()
+    tau = torch.tensor([1e9, 1e9])
+    for gaps, stop in (((2.5, 0.4), [1, 1]), ((3.0, 0.5), [0, 0]), ((2.9, 5.0), [1, 0])):
+        got = _early_check(p, dev, metric, torch.tensor(gaps), tau=tau)
+        assert got.tolist() == stop
+
+
+@pytest.mark.parametrize("metric", [0, 3])
+@pytest.mark.parametrize("name", ["llada", "ragged", "dream"])
+@pytest.mark.parametrize("splits", [0, 3])
+def test_early_commit_workloads(metric, name, splits):
+    """Thresholds just below / above each sequence's smallest logit gap (from the
+    oracle), alternating: half the sequences stop. Random phases."""
+    dev = device()
+    p = synth.make_problem(synth.small(name))
+    gaps = oracle.commit(p.logits, p.tokens, p.masked, p.q_start, p.block_phase, p.tau,
+                         p.w.block_size, p.mask_id, metric=3)["conf"]
+    m0 = p.masked.bool()
+    thr = []
+    for b in range(p.w.batch):
+        r0, r1 = int(p.q_start[b]), int(p.q_start[b + 1])
+        g = gaps[r0:r1][m0[r0:r1]]
+        gmin = float(g.min()) if len(g) else 0.0
+        thr.append(gmin - 0.25 if b % 2 == 0 else gmin + 0.25)
+    g = torch.Generator().manual_seed(41)
+    phase = torch.randint(0, 2, p.block_phase.shape, generator=g, dtype=torch.uint8)
+    stop = _early_check(p, dev, metric, torch.tensor(thr, dtype=torch.float32), phase=phase,
+                        num_splits=splits)
+    print("%s m%d s%d: stopped %s" % (name, metric, splits, stop.tolist()))
+
+
+def test_early_commit_rejects_entropy():
+    dev = device()
+    p = _tiny_vocab(2)
+    g = p.to(dev)
+    with pytest.raises(d2f.D2FError):
+        d2f.commit(g.logits, g.tokens, g.masked, g.q_start, g.block_phase, g.tau,
+                   block_size=p.w.block_size, mask_id=p.mask_id, metric=1,
+                   early_gap=torch.zeros(p.w.batch, device=dev))
