@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--conf-metric", default="pmax", choices=list(CONF_METRICS),
                     help="confidence of the commit: largest probability (d2f_commit), negative "
                          "entropy, probability margin or logit gap (d2f_commit_metric)")
+    ap.add_argument("--fused-append", action="store_true",
+                    help="append finished blocks inside the attention (d2f_block_attn_append) "
+                         "instead of d2f_kv_append after it")
     ap.add_argument("--early-gap", type=float, default=None,
                     help="early commit of whole sequences at this logit-gap threshold "
                          "(d2f_commit_metric; every sequence)")
@@ -318,6 +321,8 @@ def workload_config(p, args):
         "confidence": "%s (d2f_commit_metric; tau as drawn for the workload)" % args.conf_metric}
     if args.early_gap is not None:
         extra["early_commit_gap"] = args.early_gap
+    if args.fused_append and w.appends_per_seq:
+        extra["append"] = "fused into the attention (d2f_block_attn_append)"
     return {**extra,"workload": "%s: batch %d, Hq %d / Hkv %d, head_dim %d, block %d, context %s, "
                         "window %s blocks, vocab %d" % (
                             w.name, w.batch, w.num_heads_q, w.num_heads_kv, w.head_dim,
@@ -375,7 +380,8 @@ def run_ours(args, world, rank, local):
     tokens_all, masked_all = tokens0.clone(), masked0.clone()
     for i, st in enumerate(sets):
         st.tokens, st.masked = tokens_all[i], masked_all[i]
-    appends = len(p.src_row) > 0
+    fused = args.fused_append and len(p.src_row) > 0
+    appends = len(p.src_row) > 0 and not fused
 
     dcode = d2f.F32 if w.dtype == torch.float32 else d2f.BF16
     ws_attn = d2f.attn_workspace(dev, batch=w.batch, total_q=w.total_q, dtype=dcode,
@@ -390,10 +396,11 @@ def run_ours(args, world, rank, local):
     rem = torch.empty(w.total_q // B, dtype=torch.int32, device=dev)
 
     def attn(s):
+        kw = dict(append_src_row=s.src_row, append_dst_page=s.dst_page) if fused else {}
         d2f.block_attn(s.q, s.k_win, s.v_win, s.k_pool, s.v_pool, s.page_table, s.ctx_len,
                        s.q_start, block_size=B, max_q_per_seq=p.max_q_per_seq, max_ctx=p.max_ctx,
                        num_splits=args.num_splits, out=s.out, want_lse=False, workspace=ws_attn,
-                       err=err)
+                       err=err, **kw)
 
     early_gap = stopped = None
     if args.early_gap is not None:
@@ -535,6 +542,8 @@ def run_ours(args, world, rank, local):
     value = steps_total / (elapsed_ms / 1000.0)
     ms_per_step = elapsed_ms / K
     attn_b, commit_b, append_b = algorithmic_bytes(p)
+    if fused:  # the appended pages' writes (their window rows are read by the attention anyway)
+        attn_b += append_b // 2
     hbm, tflops, peak_kind = peaks()
     t_attn = statistics.mean(attn_us) if attn_us else None
     t_commit = statistics.mean(commit_us) if commit_us else None

@@ -382,18 +382,42 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
       const uint32_t full = smem_u32(&bars->full[stage]);
       if (lane == 0) mbar_arrive_expect_tx(full, __popc(have) * (uint32_t)B * D * 2u);
       __syncwarp();
+      const uint32_t dst = sb + L::kRing + stage * L::kStage + tensor * L::kKBytes +
+                           slot * (B / 8) * L::kGroupBytes;
       if (src >= 0) {
-        const uint32_t dst =
-            sb + L::kRing + stage * L::kStage + tensor * L::kKBytes + slot * (B / 8) * L::kGroupBytes;
         if (t < Tc)  // page src of KV head g: (page, head) row src * Hkv + g of the pool map
           tma_load_5d(dst, tensor ? &tm_vpool : &tm_kpool, full, 0, 0, 0, 0, src * a.num_heads_kv + g);
         else         // window rows src .. src + B - 1 (src is a multiple of 8)
           tma_load_5d(dst, tensor ? &tm_vwin : &tm_kwin, full, 0, 0, 0, src >> 3, g);
       }
+      // Fused append: a window block listed as an append source goes from this
+      // stage to its page once the tile has landed (row group 0 only: one CTA per
+      // sequence, KV head and window tile stores it). The store has read the
+      // stage before this thread can refill it.
+      if (a.n_append > 0 && mt == 0 && t >= Tc && src >= 0) {
+        bool landed = false;
+        for (int ap = 0; ap < a.n_append; ++ap) {
+          if (__ldg(a.app_src + ap) != src) continue;
+          const int dp = __ldg(a.app_dst + ap);
+          if (dp < 0 || dp >= a.num_pages) {
+            set_err(a.err, D2F_ERR_BAD_INDEX);
+            continue;
+          }
+          if (!landed && !mbar_wait(full, (u / NS) & 1, abort_flag, a.err)) break;
+          landed = true;
+          tma_store_5d(tensor ? &tm_vpool : &tm_kpool, dst, 0, 0, 0, 0, dp * a.num_heads_kv + g);
+        }
+        if (landed) {
+          bulk_commit_group();
+          bulk_wait_group_read0();
+        }
+      }
       issued = u + 1;
       if (lane == 0 && prod == 0) D2F_PASS_MARK(2, 7, u);
     }
-    // Drain: every issued stage must have landed before the CTA moves on.
+    // Drain: every issued stage must have landed before the CTA moves on, and
+    // every fused-append store must be complete.
+    bulk_wait_group0();
     if (lane == 0) {
       for (int u = max(0, issued - NS); u < issued; ++u) {
         volatile int no_abort = 0;

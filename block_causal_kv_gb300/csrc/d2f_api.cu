@@ -319,13 +319,18 @@ int d2f_block_attn_workspace_size(int batch, int total_q, int max_q_per_seq, int
   return D2F_OK;
 }
 
-int d2f_block_attn(const void *q, const void *k_win, const void *v_win, const void *k_pool,
-                   const void *v_pool, const int32_t *page_table, int max_pages_per_seq,
-                   const int32_t *ctx_len, const int32_t *q_start, void *out, float *lse_out,
-                   int batch, int total_q, int max_q_per_seq, int max_ctx, int num_heads_q,
-                   int num_heads_kv, int head_dim, int block_size, int num_pages, int dtype,
-                   float softmax_scale, int num_splits, void *workspace, size_t workspace_bytes,
-                   int32_t *err_word, void *stream) {
+int d2f_block_attn_append(const void *q, const void *k_win, const void *v_win, const void *k_pool,
+                          const void *v_pool, const int32_t *page_table, int max_pages_per_seq,
+                          const int32_t *ctx_len, const int32_t *q_start, void *out,
+                          float *lse_out, int batch, int total_q, int max_q_per_seq, int max_ctx,
+                          int num_heads_q, int num_heads_kv, int head_dim, int block_size,
+                          int num_pages, int dtype, float softmax_scale, int num_splits,
+                          void *workspace, size_t workspace_bytes, const int32_t *src_row,
+                          const int32_t *dst_page, int n_append, int32_t *err_word,
+                          void *stream) {
+  if (n_append < 0) return fail(D2F_ERR_INVALID_ARG, "n_append %d < 0", n_append);
+  if (n_append > 0 && (!src_row || !dst_page || !k_pool || !v_pool || num_pages <= 0))
+    return fail(D2F_ERR_INVALID_ARG, "an append needs src_row, dst_page, k_pool, v_pool and pages");
   AttnPlan p{};
   int st = plan_attn(batch, total_q, max_q_per_seq, max_ctx, num_heads_q, num_heads_kv, head_dim,
                      block_size, dtype, num_splits, &p);
@@ -382,6 +387,10 @@ int d2f_block_attn(const void *q, const void *k_win, const void *v_win, const vo
   a.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) + p.off_ml);
   a.ws_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + p.off_o);
   a.err = err_word;
+  // fused append on the tensor-core path; the CUDA-core path appends after
+  a.n_append = p.tc ? n_append : 0;
+  a.app_src = src_row;
+  a.app_dst = dst_page;
   if (num_pages <= 0 && max_ctx > 0) return fail(D2F_ERR_INVALID_ARG, "no pages");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
@@ -395,8 +404,26 @@ int d2f_block_attn(const void *q, const void *k_win, const void *v_win, const vo
   } else {
     e = launch_attn_simt(a, dtype, s);
     if (e != cudaSuccess) return cuda_fail(e, "CUDA-core attention launch");
+    if (n_append > 0)
+      return d2f_kv_append(k_win, v_win, src_row, dst_page, n_append, total_q, const_cast<void *>(k_pool),
+                           const_cast<void *>(v_pool), num_heads_kv, head_dim, block_size, num_pages,
+                           dtype, err_word, stream);
   }
   return D2F_OK;
+}
+
+int d2f_block_attn(const void *q, const void *k_win, const void *v_win, const void *k_pool,
+                   const void *v_pool, const int32_t *page_table, int max_pages_per_seq,
+                   const int32_t *ctx_len, const int32_t *q_start, void *out, float *lse_out,
+                   int batch, int total_q, int max_q_per_seq, int max_ctx, int num_heads_q,
+                   int num_heads_kv, int head_dim, int block_size, int num_pages, int dtype,
+                   float softmax_scale, int num_splits, void *workspace, size_t workspace_bytes,
+                   int32_t *err_word, void *stream) {
+  return d2f_block_attn_append(q, k_win, v_win, k_pool, v_pool, page_table, max_pages_per_seq,
+                               ctx_len, q_start, out, lse_out, batch, total_q, max_q_per_seq,
+                               max_ctx, num_heads_q, num_heads_kv, head_dim, block_size, num_pages,
+                               dtype, softmax_scale, num_splits, workspace, workspace_bytes, nullptr,
+                               nullptr, 0, err_word, stream);
 }
 
 int d2f_commit_workspace_size(int total_q, int vocab, int dtype, int block_size, int num_splits,

@@ -44,6 +44,9 @@ struct AttnArgs {
   int tc_stages;         // tensor-core path: K/V ring depth (2 .. 6)
   int tc_mt;             // tensor-core path: row tiles per CTA, a softmax warpgroup each (1, 2)
   int longest_first;     // tensor-core path: map blockIdx.z to sequences longest context first
+  const int32_t *app_src;  // tensor-core path, fused append: window rows of finished blocks
+  const int32_t *app_dst;  // ... and their pages; n_append = 0: no append
+  int n_append;
   int32_t *counters;     // [batch * Hkv * m_tiles] merge arrival counters (zero at rest)
   float2 *ws_ml;         // [num_splits][total_q * Hq] (max in log2 units, sum)
   float *ws_o;           // [num_splits][total_q * Hq][head_dim] unnormalised partial output
@@ -261,6 +264,26 @@ __device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src,
       "[%3];" ::"r"(dst),
       "r"(src), "r"(bytes), "r"(bar)
       : "memory");
+}
+// Tensor copy from shared memory to global (bulk async-group completion).
+__device__ __forceinline__ void tma_store_5d(const CUtensorMap *map, uint32_t src, int c0, int c1,
+                                             int c2, int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5, %6}], [%1];" ::
+          "l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(c4)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until this thread's committed bulk stores have read their shared memory.
+__device__ __forceinline__ void bulk_wait_group_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until this thread's committed bulk stores are complete.
+__device__ __forceinline__ void bulk_wait_group0() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 // Address of the same shared variable in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t dsmem_addr(uint32_t local, uint32_t rank) {

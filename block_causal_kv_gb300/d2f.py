@@ -31,7 +31,8 @@ STATUS = {0: "D2F_OK", 1: "D2F_ERR_INVALID_ARG", 2: "D2F_ERR_UNSUPPORTED", 3: "D
 
 # Every symbol include/d2f.h declares.
 EXPORTS = ("d2f_version", "d2f_status_string", "d2f_last_error_string",
-           "d2f_block_attn_workspace_size", "d2f_block_attn", "d2f_commit_workspace_size",
+           "d2f_block_attn_workspace_size", "d2f_block_attn", "d2f_block_attn_append",
+           "d2f_commit_workspace_size",
            "d2f_commit", "d2f_commit_metric", "d2f_commit_noalloc", "d2f_kv_append")
 
 # confidence metrics of commit(metric=...) (include/d2f.h D2F_CONF_*)
@@ -67,6 +68,9 @@ def load(path=LIB_PATH):
     lib.d2f_block_attn.restype = _I
     lib.d2f_block_attn.argtypes = ([_P] * 6 + [_I] + [_P] * 2 + [_P, _P] + [_I] * 10 +
                                    [ctypes.c_float, _I, _P, _SZ, _P, _P])
+    lib.d2f_block_attn_append.restype = _I
+    lib.d2f_block_attn_append.argtypes = ([_P] * 6 + [_I] + [_P] * 2 + [_P, _P] + [_I] * 10 +
+                                          [ctypes.c_float, _I, _P, _SZ, _P, _P, _I, _P, _P])
     lib.d2f_commit_workspace_size.restype = _I
     lib.d2f_commit_workspace_size.argtypes = [_I] * 5 + [ctypes.POINTER(_SZ)]
     lib.d2f_commit.restype = _I
@@ -147,8 +151,11 @@ def attn_workspace(device, **kw):
 
 def block_attn(q, k_win, v_win, k_pool, v_pool, page_table, ctx_len, q_start, *, block_size,
                max_q_per_seq, max_ctx, softmax_scale=None, num_splits=0, out=None, lse=None,
-               want_lse=True, workspace=None, err=None, stream=None):
+               want_lse=True, workspace=None, err=None, stream=None, append_src_row=None,
+               append_dst_page=None):
     """Block-causal attention of the window over [paged cache ; window] (one layer).
+    With append_src_row / append_dst_page (int32 [n_append]) the finished blocks
+    are appended to their pages in the same launch (d2f_block_attn_append).
 
     Returns (out [total_q, Hq, D] like q, lse [total_q, Hq] float32 or None)."""
     lib = load()
@@ -174,12 +181,18 @@ def block_attn(q, k_win, v_win, k_pool, v_pool, page_table, ctx_len, q_start, *,
                                    max_q_per_seq=max_q_per_seq, max_ctx=max_ctx,
                                    num_heads_q=hq, num_heads_kv=hkv, head_dim=d,
                                    block_size=block_size, dtype=dt, num_splits=num_splits)
-    _check(lib.d2f_block_attn(
-        _ptr(q), _ptr(k_win), _ptr(v_win), _ptr(k_pool), _ptr(v_pool), _ptr(page_table),
-        page_table.shape[1] if page_table is not None else 0, _ptr(ctx_len), _ptr(q_start),
-        _ptr(out), _ptr(lse), batch, total_q, max_q_per_seq, max_ctx, hq, hkv, d, block_size,
-        k_pool.shape[0] if k_pool is not None else 0, dt, float(softmax_scale), num_splits,
-        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream)))
+    args = (_ptr(q), _ptr(k_win), _ptr(v_win), _ptr(k_pool), _ptr(v_pool), _ptr(page_table),
+            page_table.shape[1] if page_table is not None else 0, _ptr(ctx_len), _ptr(q_start),
+            _ptr(out), _ptr(lse), batch, total_q, max_q_per_seq, max_ctx, hq, hkv, d, block_size,
+            k_pool.shape[0] if k_pool is not None else 0, dt, float(softmax_scale), num_splits,
+            _ptr(workspace), workspace.numel() * workspace.element_size())
+    if append_src_row is None:
+        _check(lib.d2f_block_attn(*args, _ptr(err), _stream(stream)))
+    else:
+        _dev(append_src_row, "append_src_row", torch.int32)
+        _dev(append_dst_page, "append_dst_page", torch.int32)
+        _check(lib.d2f_block_attn_append(*args, _ptr(append_src_row), _ptr(append_dst_page),
+                                         append_src_row.shape[0], _ptr(err), _stream(stream)))
     return out, lse
 
 

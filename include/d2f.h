@@ -146,6 +146,36 @@ int d2f_block_attn(const void *q, const void *k_win, const void *v_win, const vo
                    float softmax_scale, int num_splits, void *workspace, size_t workspace_bytes,
                    int32_t *err_word, void *stream);
 
+/*
+ * d2f_block_attn_append -- d2f_block_attn, then d2f_kv_append of finished
+ * window blocks, in one launch where the attention runs on tensor cores.
+ *
+ * [P1] §블록 단위 인과 어텐션 and §운영 관점: a completed block's K/V are final
+ * and persisted into the paged cache. The attention already streams every
+ * window block's K/V into shared memory; there the CTA that holds a block
+ * listed in src_row stores it to its page (one tensor copy per page and
+ * tensor) instead of a separate kernel reading the window again. The result is
+ * that of d2f_block_attn followed by d2f_kv_append with the same arguments.
+ *
+ * Arguments as d2f_block_attn, plus src_row / dst_page / n_append as for
+ * d2f_kv_append (src_row[a] a window row starting a block: a multiple of
+ * block_size below total_q). Additional requirement: no dst_page is a page the
+ * attention reads in this call (a cached page of any sequence); the append
+ * writes while the attention reads. Out-of-range pages set err_word =
+ * D2F_ERR_BAD_INDEX and are skipped. On the CUDA-core path (float32, or shapes
+ * outside the tensor-core variants) the append runs as its own kernel after the
+ * attention.
+ */
+int d2f_block_attn_append(const void *q, const void *k_win, const void *v_win, const void *k_pool,
+                          const void *v_pool, const int32_t *page_table, int max_pages_per_seq,
+                          const int32_t *ctx_len, const int32_t *q_start, void *out,
+                          float *lse_out, int batch, int total_q, int max_q_per_seq, int max_ctx,
+                          int num_heads_q, int num_heads_kv, int head_dim, int block_size,
+                          int num_pages, int dtype, float softmax_scale, int num_splits,
+                          void *workspace, size_t workspace_bytes, const int32_t *src_row,
+                          const int32_t *dst_page, int n_append, int32_t *err_word,
+                          void *stream);
+
 /* ------------------------------------------------------------------------- */
 /* Confidence commit over the vocabulary                                    */
 /* ------------------------------------------------------------------------- */
