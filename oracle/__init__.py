@@ -37,6 +37,12 @@ def _load():
             _P, _P, _P, _P, _P, _P, ctypes.c_int, _P, _P,
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, _P, _P, ctypes.c_int]
+        lib.d2f_oracle_block_attn_part.restype = ctypes.c_int
+        lib.d2f_oracle_block_attn_part.argtypes = [
+            _P, _P, _P, _P, _P, _P, ctypes.c_int, _P, _P,
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int, _P, _P,
+            _P, _P, ctypes.c_int]
         lib.d2f_oracle_commit.restype = ctypes.c_int
         lib.d2f_oracle_commit.argtypes = [
             _P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P,
@@ -115,6 +121,39 @@ def block_attn(q, k_win, v_win, k_pool, v_pool, page_table, ctx_len, q_start,
         _ptr(out), _ptr(lse), nthreads or default_threads())
     if rc != 0:
         raise ValueError("oracle block_attn rejected its input (code %d)" % rc)
+    return out, lse
+
+
+# attention parts of block_attn_part(): all keys, cached tokens only, window only
+ATTN_ALL, ATTN_CACHED, ATTN_WINDOW = 0, 1, 2
+
+
+def block_attn_part(q, k_win, v_win, k_pool, v_pool, page_table, ctx_len, q_start, block_size,
+                    part, prev_out=None, prev_lse=None, scale=None, nthreads=None):
+    """Attention over one part of the keys (fp64); part ATTN_WINDOW with
+    prev_out / prev_lse (a cached-part result) composes the two in log space.
+    Returns (out [total_q, Hq, D] float64, lse [total_q, Hq] float64)."""
+    lib = _load()
+    q, k_win, v_win, k_pool, v_pool = (_cpu(x) for x in (q, k_win, v_win, k_pool, v_pool))
+    dt = _dt(q)
+    page_table = _cpu(page_table, torch.int32)
+    ctx_len = _cpu(ctx_len, torch.int32)
+    q_start = _cpu(q_start, torch.int32)
+    prev_out = _cpu(prev_out, torch.float64)
+    prev_lse = _cpu(prev_lse, torch.float64)
+    total_q, hq, d = q.shape
+    if scale is None:
+        scale = 1.0 / (d ** 0.5)
+    out = torch.zeros((total_q, hq, d), dtype=torch.float64)
+    lse = torch.zeros((total_q, hq), dtype=torch.float64)
+    rc = lib.d2f_oracle_block_attn_part(
+        _ptr(q), _ptr(k_win), _ptr(v_win), _ptr(k_pool), _ptr(v_pool), _ptr(page_table),
+        page_table.shape[1] if page_table.dim() == 2 else 0, _ptr(ctx_len), _ptr(q_start),
+        ctx_len.shape[0], total_q, hq, k_win.shape[1], d, block_size, k_pool.shape[0], dt,
+        float(scale), int(part), _ptr(prev_out), _ptr(prev_lse), _ptr(out), _ptr(lse),
+        nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle attention part rejected its input (code %d)" % rc)
     return out, lse
 
 

@@ -80,14 +80,14 @@ static float load_elem_f32(const void *base, int64_t idx, int dtype) {
  * Returns 0, or a negative code: -1 bad sizes, -2 inconsistent q_start,
  * -3 page id out of range, -4 out of memory.
  */
-int d2f_oracle_block_attn(const void *q, const void *k_win, const void *v_win,
-                          const void *k_pool, const void *v_pool,
-                          const int32_t *page_table, int max_pages_per_seq,
-                          const int32_t *ctx_len, const int32_t *q_start,
-                          int batch, int total_q, int num_heads_q,
-                          int num_heads_kv, int head_dim, int block_size,
-                          int num_pages, int dtype, double scale, double *out,
-                          double *lse, int nthreads) {
+static int block_attn_keys(const void *q, const void *k_win, const void *v_win,
+                           const void *k_pool, const void *v_pool,
+                           const int32_t *page_table, int max_pages_per_seq,
+                           const int32_t *ctx_len, const int32_t *q_start,
+                           int batch, int total_q, int num_heads_q,
+                           int num_heads_kv, int head_dim, int block_size,
+                           int num_pages, int dtype, double scale, double *out,
+                           double *lse, int part, int nthreads) {
   if (batch < 0 || num_heads_q <= 0 || num_heads_kv <= 0 || head_dim <= 0 ||
       block_size <= 0 || num_heads_q % num_heads_kv != 0)
     return -1;
@@ -128,16 +128,16 @@ int d2f_oracle_block_attn(const void *q, const void *k_win, const void *v_win,
       continue;
     }
 
-    /* Build the visible key set K(i). */
+    /* Build the visible key set K(i) (part 1: cached tokens only, 2: window only). */
     int nk = 0;
-    for (int t = 0; t < C; ++t) {
+    for (int t = 0; part != 2 && t < C; ++t) {
       int32_t page = page_table[(int64_t)b * max_pages_per_seq + t / B];
       int slot = t % B;
       koff[nk] = (((int64_t)page * Hk + g) * B + slot) * D;
       kwin[nk] = 0;
       ++nk;
     }
-    for (int i2 = 0; i2 < n_b; ++i2) {
+    for (int i2 = 0; part != 1 && i2 < n_b; ++i2) {
       if (i2 / B <= i / B) {
         koff[nk] = ((int64_t)(q_start[b] + i2) * Hk + g) * D;
         kwin[nk] = 1;
@@ -162,6 +162,13 @@ int d2f_oracle_block_attn(const void *q, const void *k_win, const void *v_win,
     }
     double *o = out + qoff;
     for (int d = 0; d < D; ++d) o[d] = 0.0;
+    if (nk == 0) { /* no visible key (a cached part without cached tokens) */
+      if (lse) lse[(int64_t)R * H + h] = -INFINITY;
+      free(s);
+      free(koff);
+      free(kwin);
+      continue;
+    }
     for (int kk = 0; kk < nk; ++kk) {
       const void *vb = kwin[kk] ? v_win : v_pool;
       const double w = s[kk] / denom;
@@ -173,6 +180,69 @@ int d2f_oracle_block_attn(const void *q, const void *k_win, const void *v_win,
     free(kwin);
   }
   return err;
+}
+
+int d2f_oracle_block_attn(const void *q, const void *k_win, const void *v_win,
+                          const void *k_pool, const void *v_pool,
+                          const int32_t *page_table, int max_pages_per_seq,
+                          const int32_t *ctx_len, const int32_t *q_start,
+                          int batch, int total_q, int num_heads_q,
+                          int num_heads_kv, int head_dim, int block_size,
+                          int num_pages, int dtype, double scale, double *out,
+                          double *lse, int nthreads) {
+  return block_attn_keys(q, k_win, v_win, k_pool, v_pool, page_table, max_pages_per_seq, ctx_len,
+                         q_start, batch, total_q, num_heads_q, num_heads_kv, head_dim, block_size,
+                         num_pages, dtype, scale, out, lse, 0, nthreads);
+}
+
+/*
+ * The attention over one part of the keys, and the composition of a saved part
+ * with the window part.
+ *
+ * [P3] §FlashBlock: 블록 외부 어텐션 캐싱: the attention output and normaliser over
+ * the tokens outside the blocks being decoded are cached at one step; at the
+ * next only the attention inside is recomputed, and the two are recombined in
+ * log space as FlashAttention composes partial results.
+ *
+ * part 0: all visible keys (d2f_oracle_block_attn). part 1: the cached tokens
+ * only (a row of a sequence with no cached token gets out 0, lse -inf). part 2:
+ * the window keys only; with prev_out / prev_lse (a part-1 result, of this step
+ * or an earlier one; double, same layouts as out / lse) the output is their
+ * composition:
+ *   out = (e^{lse_p} prev_out + e^{lse_w} out_w) / (e^{lse_p} + e^{lse_w}),
+ *   lse = log(e^{lse_p} + e^{lse_w}),
+ * computed with the larger of the two normalisers factored out. lse is
+ * required for part 1 and part 2 (the composition needs it).
+ */
+int d2f_oracle_block_attn_part(const void *q, const void *k_win, const void *v_win,
+                               const void *k_pool, const void *v_pool,
+                               const int32_t *page_table, int max_pages_per_seq,
+                               const int32_t *ctx_len, const int32_t *q_start,
+                               int batch, int total_q, int num_heads_q,
+                               int num_heads_kv, int head_dim, int block_size,
+                               int num_pages, int dtype, double scale, int part,
+                               const double *prev_out, const double *prev_lse,
+                               double *out, double *lse, int nthreads) {
+  if (part < 0 || part > 2 || (part != 0 && !lse)) return -1;
+  const int rc = block_attn_keys(q, k_win, v_win, k_pool, v_pool, page_table, max_pages_per_seq,
+                                 ctx_len, q_start, batch, total_q, num_heads_q, num_heads_kv,
+                                 head_dim, block_size, num_pages, dtype, scale, out, lse, part,
+                                 nthreads);
+  if (rc != 0 || part != 2 || !prev_out || !prev_lse) return rc;
+  const int64_t n_items = (int64_t)total_q * num_heads_q;
+  const int D = head_dim;
+  for (int64_t item = 0; item < n_items; ++item) {
+    const double lp = prev_lse[item], lw = lse[item];
+    const double M = lp > lw ? lp : lw;
+    if (M == -INFINITY) continue;
+    const double wp = lp == -INFINITY ? 0.0 : exp(lp - M);
+    const double ww = lw == -INFINITY ? 0.0 : exp(lw - M);
+    double *o = out + item * D;
+    const double *po = prev_out + item * D;
+    for (int d = 0; d < D; ++d) o[d] = (wp * po[d] + ww * o[d]) / (wp + ww);
+    lse[item] = M + log(wp + ww);
+  }
+  return 0;
 }
 
 /*
