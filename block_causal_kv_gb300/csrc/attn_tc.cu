@@ -225,7 +225,7 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
   // previous kernel changes them, a prefetch is wasted, and every value the
   // attention uses is read again after the dependency wait. L2 is the point of
   // coherence, so a prefetched line never hides a later write.
-  if (warp == 0 && a.page_table != nullptr && !a.longest_first) {
+  if (warp == 0 && a.page_table != nullptr && !a.longest_first && a.part != 2) {
     const int ppt0 = N / a.block_size;
     const int lp = split * a.tiles_per_split * ppt0 + lane;
     const int hint_c = __ldcg(a.ctx_len + b);
@@ -291,7 +291,8 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
   active = active && r_begin < rows_total;
   const int nrows = active ? min(MT * QR, rows_total - r_begin) : 0;  // valid rows, all tiles
   const int mt_live = (nrows + QR - 1) / QR;  // row tiles of this CTA that hold rows
-  const int Tc = (C + N - 1) / N, Tw = (n + N - 1) / N;
+  // key tiles: the cached tokens', then the window's (one part only, if asked)
+  const int Tc = a.part == 2 ? 0 : (C + N - 1) / N, Tw = a.part == 1 ? 0 : (n + N - 1) / N;
   // Split s takes tiles [s*tps, (s+1)*tps); tps comes from the host's max_ctx and
   // grows here only if a sequence is longer than that hint promised.
   const int tps = max(a.tiles_per_split, (Tc + Tw + cs - 1) / cs);
@@ -714,26 +715,62 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
   const bool aborted = *abort_flag != 0;
   bool tmem_freed = false;
   if (cs == 1) {
-    if (warp >= L::kFirstSoft && has_work && !aborted && __any_sync(0xffffffffu, rv)) {
+    if (warp >= L::kFirstSoft && active && !aborted && __any_sync(0xffffffffu, rv)) {
       const int64_t hr = (int64_t)(q0 + r / G) * H + g * G + r % G;
-      const float inv = 1.0f / l;
+      // this part's normaliser in log2 units (l = 0: no visible key, e.g. the
+      // cached part of a sequence without cached tokens: output 0, lse -inf)
+      const bool any = has_work && l > 0.f;
+      const float lw = any ? m_ref + __log2f(l) : -INFINITY;
+      // composition with a kept cached part: weights 2^(L - M) of the two parts
+      float wv = any ? 1.f : 0.f, wp = 0.f, lse2 = lw;
+      if (a.prev_lse && rv) {
+        const float lp = a.prev_lse[hr] * 1.4426950408889634f;
+        const float M = fmaxf(lw, lp);
+        if (M > -INFINITY) {
+          wv = any ? fast_exp2(lw - M) : 0.f;
+          wp = lp > -INFINITY ? fast_exp2(lp - M) : 0.f;
+          lse2 = M + __log2f(wv + wp);
+          const float rs = 1.0f / (wv + wp);
+          wv *= rs;
+          wp *= rs;
+        }
+      }
+      const float inv = any ? wv / l : 0.f;
       uint16_t *dst = reinterpret_cast<uint16_t *>(a.out) + hr * D;
+      const uint4 *prev = reinterpret_cast<const uint4 *>(
+          reinterpret_cast<const uint16_t *>(a.prev_out) + hr * D);
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {
         uint32_t o[32];
-        tmem_ld32(lane_addr + kTmemO + ch * 32, o);
+        if (has_work) {
+          tmem_ld32(lane_addr + kTmemO + ch * 32, o);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = 0u;
+        }
         if (rv) {
+          uint32_t pv[16];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint4 q4 = wp > 0.f ? prev[ch * 4 + j] : make_uint4(0, 0, 0, 0);
+            pv[4 * j] = q4.x;
+            pv[4 * j + 1] = q4.y;
+            pv[4 * j + 2] = q4.z;
+            pv[4 * j + 3] = q4.w;
+          }
           uint32_t w[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            w[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
+            w[j] = pack_bf16x2(
+                fmaf(__uint_as_float(o[2 * j]), inv, wp * bf16_bits_to_float(pv[j] & 0xffffu)),
+                fmaf(__uint_as_float(o[2 * j + 1]), inv, wp * bf16_bits_to_float(pv[j] >> 16)));
           uint4 *d4 = reinterpret_cast<uint4 *>(dst + ch * 32);
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             d4[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
         }
       }
-      if (rv && a.lse_out) a.lse_out[hr] = (m_ref + __log2f(l)) * 0.6931471805599453f;
+      if (rv && a.lse_out) a.lse_out[hr] = lse2 * 0.6931471805599453f;
     }
   } else if (active) {
     const int LR = L::rows_per_owner(cs);  // rows a CTA owns (at most)
@@ -816,20 +853,31 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
         const int crow = lr * cs + split;  // CTA row of this half-warp
         const bool valid = crow < nrows;
         const int key = crow & 7;
+        const int r2 = r_begin + crow;
+        const int64_t hr2 = (int64_t)(q0 + r2 / G) * H + g * G + r2 % G;
         float2 ml = make_float2(-INFINITY, 0.f);
         if (valid && sub < cs)
           ml = *reinterpret_cast<const float2 *>(smem + sub * BS + LR * L::kRowBytes + lr * 8);
-        float mx = ml.x;
+        // a kept cached part is one more normalised part: (its lse in log2 units, 1)
+        const float lp = (a.prev_lse && valid) ? a.prev_lse[hr2] * 1.4426950408889634f : -INFINITY;
+        float mx = fmaxf(ml.x, lp);
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         // weight of a normalised part: 2^(m_j - M) * l_j
         const float w = (sub < cs && ml.y > 0.f) ? fast_exp2(ml.x - mx) * ml.y : 0.f;
+        const float wp = lp > -INFINITY ? fast_exp2(lp - mx) : 0.f;
         float ws = w;
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+        ws += wp;
         float acc[kCols];
 #pragma unroll
         for (int c = 0; c < kCols; ++c) acc[c] = 0.f;
+        if (wp > 0.f) {  // this lane's columns of the kept part
+          const uint16_t *pr = reinterpret_cast<const uint16_t *>(a.prev_out) + hr2 * D + sub * kCols;
+#pragma unroll
+          for (int c = 0; c < kCols; ++c) acc[c] = wp * bf16_bits_to_float(pr[c]);
+        }
         const uint32_t off = lr * L::kRowBytes + (D == 128 ? ((sub ^ key) << 4)
                                                             : (((sub >> 1) ^ key) << 4) + (sub & 1) * 8);
 #pragma unroll
@@ -853,8 +901,6 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
         }
         if (valid && !aborted) {
           const float inv = ws > 0.f ? 1.0f / ws : 0.f;
-          const int r2 = r_begin + crow;
-          const int64_t hr2 = (int64_t)(q0 + r2 / G) * H + g * G + r2 % G;
           uint32_t pk[kCols / 2];
 #pragma unroll
           for (int c = 0; c < kCols / 2; ++c)

@@ -319,16 +319,26 @@ int d2f_block_attn_workspace_size(int batch, int total_q, int max_q_per_seq, int
   return D2F_OK;
 }
 
-int d2f_block_attn_append(const void *q, const void *k_win, const void *v_win, const void *k_pool,
-                          const void *v_pool, const int32_t *page_table, int max_pages_per_seq,
-                          const int32_t *ctx_len, const int32_t *q_start, void *out,
-                          float *lse_out, int batch, int total_q, int max_q_per_seq, int max_ctx,
-                          int num_heads_q, int num_heads_kv, int head_dim, int block_size,
-                          int num_pages, int dtype, float softmax_scale, int num_splits,
-                          void *workspace, size_t workspace_bytes, const int32_t *src_row,
-                          const int32_t *dst_page, int n_append, int32_t *err_word,
-                          void *stream) {
+namespace {
+int attn_entry(const void *q, const void *k_win, const void *v_win, const void *k_pool,
+               const void *v_pool, const int32_t *page_table, int max_pages_per_seq,
+               const int32_t *ctx_len, const int32_t *q_start, void *out, float *lse_out,
+               int batch, int total_q, int max_q_per_seq, int max_ctx, int num_heads_q,
+               int num_heads_kv, int head_dim, int block_size, int num_pages, int dtype,
+               float softmax_scale, int num_splits, void *workspace, size_t workspace_bytes,
+               const int32_t *src_row, const int32_t *dst_page, int n_append, int part,
+               const void *prev_out, const float *prev_lse, int32_t *err_word, void *stream) {
   if (n_append < 0) return fail(D2F_ERR_INVALID_ARG, "n_append %d < 0", n_append);
+  if (part < D2F_ATTN_ALL || part > D2F_ATTN_WINDOW)
+    return fail(D2F_ERR_INVALID_ARG, "part %d is not a D2F_ATTN_* value", part);
+  if (part == D2F_ATTN_CACHED && !lse_out)
+    return fail(D2F_ERR_INVALID_ARG, "the cached part needs lse_out (its normaliser is kept)");
+  if ((prev_out == nullptr) != (prev_lse == nullptr) || (prev_out && part != D2F_ATTN_WINDOW))
+    return fail(D2F_ERR_INVALID_ARG, "prev_out / prev_lse go together, with D2F_ATTN_WINDOW");
+  if (prev_out && !aligned16(prev_out))
+    return fail(D2F_ERR_INVALID_ARG, "device buffers must be 16-byte aligned");
+  // the window part reads no cached page: plan it as a window-only attention
+  if (part == D2F_ATTN_WINDOW) max_ctx = 0;
   if (n_append > 0 && (!src_row || !dst_page || !k_pool || !v_pool || num_pages <= 0))
     return fail(D2F_ERR_INVALID_ARG, "an append needs src_row, dst_page, k_pool, v_pool and pages");
   AttnPlan p{};
@@ -387,6 +397,12 @@ int d2f_block_attn_append(const void *q, const void *k_win, const void *v_win, c
   a.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) + p.off_ml);
   a.ws_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + p.off_o);
   a.err = err_word;
+  if (part != D2F_ATTN_ALL && !p.tc)
+    return fail(D2F_ERR_UNSUPPORTED, "attention parts run on the tensor-core path (bf16, head_dim "
+                "64/128, block 8/16/32)");
+  a.part = part;
+  a.prev_out = prev_out;
+  a.prev_lse = prev_lse;
   // fused append on the tensor-core path; the CUDA-core path appends after
   a.n_append = p.tc ? n_append : 0;
   a.app_src = src_row;
@@ -411,6 +427,38 @@ int d2f_block_attn_append(const void *q, const void *k_win, const void *v_win, c
   }
   return D2F_OK;
 }
+}  // namespace
+
+int d2f_block_attn_append(const void *q, const void *k_win, const void *v_win, const void *k_pool,
+                          const void *v_pool, const int32_t *page_table, int max_pages_per_seq,
+                          const int32_t *ctx_len, const int32_t *q_start, void *out,
+                          float *lse_out, int batch, int total_q, int max_q_per_seq, int max_ctx,
+                          int num_heads_q, int num_heads_kv, int head_dim, int block_size,
+                          int num_pages, int dtype, float softmax_scale, int num_splits,
+                          void *workspace, size_t workspace_bytes, const int32_t *src_row,
+                          const int32_t *dst_page, int n_append, int32_t *err_word,
+                          void *stream) {
+  return attn_entry(q, k_win, v_win, k_pool, v_pool, page_table, max_pages_per_seq, ctx_len,
+                    q_start, out, lse_out, batch, total_q, max_q_per_seq, max_ctx, num_heads_q,
+                    num_heads_kv, head_dim, block_size, num_pages, dtype, softmax_scale, num_splits,
+                    workspace, workspace_bytes, src_row, dst_page, n_append, D2F_ATTN_ALL, nullptr,
+                    nullptr, err_word, stream);
+}
+
+int d2f_block_attn_part(const void *q, const void *k_win, const void *v_win, const void *k_pool,
+                        const void *v_pool, const int32_t *page_table, int max_pages_per_seq,
+                        const int32_t *ctx_len, const int32_t *q_start, void *out, float *lse_out,
+                        int batch, int total_q, int max_q_per_seq, int max_ctx, int num_heads_q,
+                        int num_heads_kv, int head_dim, int block_size, int num_pages, int dtype,
+                        float softmax_scale, int num_splits, void *workspace,
+                        size_t workspace_bytes, int part, const void *prev_out,
+                        const float *prev_lse, int32_t *err_word, void *stream) {
+  return attn_entry(q, k_win, v_win, k_pool, v_pool, page_table, max_pages_per_seq, ctx_len,
+                    q_start, out, lse_out, batch, total_q, max_q_per_seq, max_ctx, num_heads_q,
+                    num_heads_kv, head_dim, block_size, num_pages, dtype, softmax_scale, num_splits,
+                    workspace, workspace_bytes, nullptr, nullptr, 0, part, prev_out, prev_lse,
+                    err_word, stream);
+}
 
 int d2f_block_attn(const void *q, const void *k_win, const void *v_win, const void *k_pool,
                    const void *v_pool, const int32_t *page_table, int max_pages_per_seq,
@@ -419,11 +467,11 @@ int d2f_block_attn(const void *q, const void *k_win, const void *v_win, const vo
                    int num_heads_kv, int head_dim, int block_size, int num_pages, int dtype,
                    float softmax_scale, int num_splits, void *workspace, size_t workspace_bytes,
                    int32_t *err_word, void *stream) {
-  return d2f_block_attn_append(q, k_win, v_win, k_pool, v_pool, page_table, max_pages_per_seq,
-                               ctx_len, q_start, out, lse_out, batch, total_q, max_q_per_seq,
-                               max_ctx, num_heads_q, num_heads_kv, head_dim, block_size, num_pages,
-                               dtype, softmax_scale, num_splits, workspace, workspace_bytes, nullptr,
-                               nullptr, 0, err_word, stream);
+  return attn_entry(q, k_win, v_win, k_pool, v_pool, page_table, max_pages_per_seq, ctx_len,
+                    q_start, out, lse_out, batch, total_q, max_q_per_seq, max_ctx, num_heads_q,
+                    num_heads_kv, head_dim, block_size, num_pages, dtype, softmax_scale, num_splits,
+                    workspace, workspace_bytes, nullptr, nullptr, 0, D2F_ATTN_ALL, nullptr, nullptr,
+                    err_word, stream);
 }
 
 int d2f_commit_workspace_size(int total_q, int vocab, int dtype, int block_size, int num_splits,

@@ -47,6 +47,9 @@ struct AttnArgs {
   const int32_t *app_src;  // tensor-core path, fused append: window rows of finished blocks
   const int32_t *app_dst;  // ... and their pages; n_append = 0: no append
   int n_append;
+  int part;                // tensor-core path: keys attended: 0 all, 1 cached only, 2 window only
+  const void *prev_out;    // part 2: a kept cached part to compose with ([total_q][Hq][D], as out)
+  const float *prev_lse;   // ... its natural-log normaliser [total_q][Hq]; NULL: no composition
   int32_t *counters;     // [batch * Hkv * m_tiles] merge arrival counters (zero at rest)
   float2 *ws_ml;         // [num_splits][total_q * Hq] (max in log2 units, sum)
   float *ws_o;           // [num_splits][total_q * Hq][head_dim] unnormalised partial output

@@ -32,9 +32,12 @@ STATUS = {0: "D2F_OK", 1: "D2F_ERR_INVALID_ARG", 2: "D2F_ERR_UNSUPPORTED", 3: "D
 # Every symbol include/d2f.h declares.
 EXPORTS = ("d2f_version", "d2f_status_string", "d2f_last_error_string",
            "d2f_block_attn_workspace_size", "d2f_block_attn", "d2f_block_attn_append",
+           "d2f_block_attn_part",
            "d2f_commit_workspace_size",
            "d2f_commit", "d2f_commit_metric", "d2f_commit_noalloc", "d2f_kv_append")
 
+# attention parts of block_attn(part=...) (include/d2f.h D2F_ATTN_*)
+ATTN_ALL, ATTN_CACHED, ATTN_WINDOW = 0, 1, 2
 # confidence metrics of commit(metric=...) (include/d2f.h D2F_CONF_*)
 CONF_PMAX, CONF_NEG_ENTROPY, CONF_MARGIN, CONF_LOGIT_GAP = 0, 1, 2, 3
 
@@ -71,6 +74,9 @@ def load(path=LIB_PATH):
     lib.d2f_block_attn_append.restype = _I
     lib.d2f_block_attn_append.argtypes = ([_P] * 6 + [_I] + [_P] * 2 + [_P, _P] + [_I] * 10 +
                                           [ctypes.c_float, _I, _P, _SZ, _P, _P, _I, _P, _P])
+    lib.d2f_block_attn_part.restype = _I
+    lib.d2f_block_attn_part.argtypes = ([_P] * 6 + [_I] + [_P] * 2 + [_P, _P] + [_I] * 10 +
+                                        [ctypes.c_float, _I, _P, _SZ, _I, _P, _P, _P, _P])
     lib.d2f_commit_workspace_size.restype = _I
     lib.d2f_commit_workspace_size.argtypes = [_I] * 5 + [ctypes.POINTER(_SZ)]
     lib.d2f_commit.restype = _I
@@ -152,10 +158,12 @@ def attn_workspace(device, **kw):
 def block_attn(q, k_win, v_win, k_pool, v_pool, page_table, ctx_len, q_start, *, block_size,
                max_q_per_seq, max_ctx, softmax_scale=None, num_splits=0, out=None, lse=None,
                want_lse=True, workspace=None, err=None, stream=None, append_src_row=None,
-               append_dst_page=None):
+               append_dst_page=None, part=ATTN_ALL, prev_out=None, prev_lse=None):
     """Block-causal attention of the window over [paged cache ; window] (one layer).
     With append_src_row / append_dst_page (int32 [n_append]) the finished blocks
     are appended to their pages in the same launch (d2f_block_attn_append).
+    part ATTN_CACHED / ATTN_WINDOW (d2f_block_attn_part): one part of the keys; the
+    window part composes a kept cached part given as prev_out / prev_lse.
 
     Returns (out [total_q, Hq, D] like q, lse [total_q, Hq] float32 or None)."""
     lib = load()
@@ -186,7 +194,14 @@ def block_attn(q, k_win, v_win, k_pool, v_pool, page_table, ctx_len, q_start, *,
             _ptr(out), _ptr(lse), batch, total_q, max_q_per_seq, max_ctx, hq, hkv, d, block_size,
             k_pool.shape[0] if k_pool is not None else 0, dt, float(softmax_scale), num_splits,
             _ptr(workspace), workspace.numel() * workspace.element_size())
-    if append_src_row is None:
+    if part != ATTN_ALL:
+        if append_src_row is not None:
+            raise ValueError("an append goes with the whole attention (part ATTN_ALL)")
+        _dev(prev_out, "prev_out", q.dtype)
+        _dev(prev_lse, "prev_lse", torch.float32)
+        _check(lib.d2f_block_attn_part(*args, int(part), _ptr(prev_out), _ptr(prev_lse), _ptr(err),
+                                       _stream(stream)))
+    elif append_src_row is None:
         _check(lib.d2f_block_attn(*args, _ptr(err), _stream(stream)))
     else:
         _dev(append_src_row, "append_src_row", torch.int32)

@@ -65,6 +65,8 @@ typedef enum d2f_dtype { D2F_BF16 = 0, D2F_F32 = 1 } d2f_dtype;
 
 /* Block phases ([P2] §쉽게 이해하기). */
 enum { D2F_PHASE_CONSERVATIVE = 0, D2F_PHASE_AGGRESSIVE = 1 };
+/* Keys attended by d2f_block_attn_part (d2f_block_attn attends to all). */
+enum { D2F_ATTN_ALL = 0, D2F_ATTN_CACHED = 1, D2F_ATTN_WINDOW = 2 };
 /* Confidence metrics of d2f_commit_metric (d2f_commit uses D2F_CONF_PMAX). */
 enum {
   D2F_CONF_PMAX = 0,         /* largest softmax probability */
@@ -175,6 +177,45 @@ int d2f_block_attn_append(const void *q, const void *k_win, const void *v_win, c
                           void *workspace, size_t workspace_bytes, const int32_t *src_row,
                           const int32_t *dst_page, int n_append, int32_t *err_word,
                           void *stream);
+
+/*
+ * d2f_block_attn_part -- the attention over one part of the keys, and the reuse
+ * of a kept cached part.
+ *
+ * "확산 언어 모델(Diffusion LLM)이란 무엇인가", §FlashBlock: 블록 외부 어텐션 캐싱:
+ * the attention output and normaliser over the tokens outside the blocks being
+ * decoded are kept from one step; at the next step only the attention inside
+ * is recomputed and the two are recombined in log space; when more tokens than
+ * a threshold have changed, the kept part is recomputed instead (the caller's
+ * choice: it calls D2F_ATTN_CACHED again).
+ *
+ *   part D2F_ATTN_ALL     d2f_block_attn.
+ *   part D2F_ATTN_CACHED  only the cached tokens (lse_out required); a row of a
+ *                         sequence without cached tokens gets out 0, lse -inf.
+ *                         out / lse_out are the part to keep.
+ *   part D2F_ATTN_WINDOW  only the window keys (no cached page is read:
+ *                         k_pool / v_pool / page_table may be NULL, max_ctx is
+ *                         ignored); with prev_out / prev_lse (a kept
+ *                         D2F_ATTN_CACHED result, of this step or an earlier
+ *                         one) the output is the composition
+ *                           out = (e^{lse_p} prev + e^{lse_w} out_w) / (e^{lse_p} + e^{lse_w}),
+ *                           lse = ln(e^{lse_p} + e^{lse_w}).
+ *                         With the same queries this is the full attention (up
+ *                         to the kept part's bf16 rounding); with the kept part of
+ *                         earlier queries it is the softmax whose cached scores use
+ *                         those.
+ * Other arguments as d2f_block_attn; prev_out is laid out as out, prev_lse as
+ * lse_out. Tensor-core path only (bf16, head_dim 64/128, block_size 8/16/32):
+ * D2F_ERR_UNSUPPORTED otherwise.
+ */
+int d2f_block_attn_part(const void *q, const void *k_win, const void *v_win, const void *k_pool,
+                        const void *v_pool, const int32_t *page_table, int max_pages_per_seq,
+                        const int32_t *ctx_len, const int32_t *q_start, void *out, float *lse_out,
+                        int batch, int total_q, int max_q_per_seq, int max_ctx, int num_heads_q,
+                        int num_heads_kv, int head_dim, int block_size, int num_pages, int dtype,
+                        float softmax_scale, int num_splits, void *workspace,
+                        size_t workspace_bytes, int part, const void *prev_out,
+                        const float *prev_lse, int32_t *err_word, void *stream);
 
 /* ------------------------------------------------------------------------- */
 /* Confidence commit over the vocabulary                                    */

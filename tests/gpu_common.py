@@ -2,7 +2,11 @@
 
 Tolerances
   attention, bf16 operands: max |gpu - oracle| <= 2e-2 and mean <= 2e-3 on the
-      output (the hot path's stated bar); lse within 5e-3.
+      output (the hot path's stated bar); lse within 1.1e-2: P is exponentiated
+      from a bf16-rounded argument x (relative rounding 2^-9), and with the lazy
+      rescale x reaches +8 (log2 units) before the reference moves, so a dominant
+      term can be off by 8 * 2^-9 * ln 2 relative: ln(1 + 0.0108) = 0.0108 on the
+      natural-log normaliser.
   attention, float32 operands: the CUDA-core path accumulates in float32 over at
       most a few thousand keys of unit-scale values, so its error is ~1e-6; the
       bar is 1e-4 max / 1e-5 mean.
@@ -17,7 +21,7 @@ import torch
 import oracle
 
 ATTN_TOL = {torch.bfloat16: (2e-2, 2e-3), torch.float32: (1e-4, 1e-5)}
-LSE_TOL = 5e-3
+LSE_TOL = 1.1e-2
 CONF_RTOL = 1e-5
 BAND = 1e-5
 
@@ -40,7 +44,11 @@ def check_attention(out, lse, ref, ref_lse, dtype, label=""):
     tmax, tmean = ATTN_TOL[dtype]
     assert mx <= tmax and mean <= tmean, "%s max %.3g mean %.3g" % (label, mx, mean)
     if lse is not None:
-        le = float((lse.double().cpu() - ref_lse).abs().max())
+        lg, lr = lse.double().cpu(), ref_lse
+        # rows without any visible key carry lse = -inf on both sides
+        inf = torch.isneginf(lr)
+        assert torch.equal(torch.isneginf(lg), inf), "%s lse -inf rows differ" % label
+        le = float((lg[~inf] - lr[~inf]).abs().max()) if (~inf).any() else 0.0
         assert le <= LSE_TOL, "%s lse err %.3g" % (label, le)
     return mx, mean
 

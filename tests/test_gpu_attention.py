@@ -238,3 +238,64 @@ def test_full_size_sampled(name):
                                p.w.block_size, want_lse=False)
     mx, mean = check_attention(out[rows], None, ref, None, torch.bfloat16, name + " full")
     print("%s full (sequence %d): max-abs %.3e mean-abs %.3e" % (name, b, mx, mean))
+
+
+def _part(g, p, part, q=None, prev=None, splits=0):
+    out, lse = d2f.block_attn(g.q if q is None else q, g.k_win, g.v_win, g.k_pool, g.v_pool,
+                              g.page_table, g.ctx_len, g.q_start, block_size=p.w.block_size,
+                              max_q_per_seq=p.max_q_per_seq, max_ctx=p.max_ctx,
+                              num_splits=splits, part=part,
+                              prev_out=None if prev is None else prev[0],
+                              prev_lse=None if prev is None else prev[1])
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def _ref_part(p, part, q=None, prev=None):
+    return oracle.block_attn_part(p.q if q is None else q, p.k_win, p.v_win, p.k_pool, p.v_pool,
+                                  p.page_table, p.ctx_len, p.q_start, p.w.block_size, part,
+                                  prev_out=None if prev is None else prev[0].double(),
+                                  prev_lse=None if prev is None else prev[1].double())
+
+
+def _cached_ctx_zero(w):
+    # a ragged batch whose second sequence has no cached token
+    return synth.Workload("pz", 3, 8, 4, 128, 16, torch.bfloat16, [300, 0, 700], [2, 3, 1], 64,
+                          permute_pages=True, extra_pages=2, seed=900)
+
+
+@pytest.mark.parametrize("name", ["llada", "dream", "long_b32", "ragged", "ctx0"])
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_cached_and_window_parts(name, splits):
+    """d2f_block_attn_part: the cached part alone and the window part alone match
+    the oracle's parts; the window part composed with the kept cached part of the
+    same queries matches the full attention; composed with the kept part of
+    earlier queries it matches the oracle's composition of that kept part."""
+    dev = device()
+    w = _cached_ctx_zero(None) if name == "ctx0" else synth.small(name)
+    p = synth.make_problem(w)
+    g = p.to(dev)
+    oc, lc = _part(g, p, d2f.ATTN_CACHED, splits=splits)
+    rc, rlc = _ref_part(p, oracle.ATTN_CACHED)
+    check_attention(oc, lc, rc, rlc, torch.bfloat16, "cached/%s/s%d" % (name, splits))
+    ow, lw = _part(g, p, d2f.ATTN_WINDOW, splits=splits)
+    rw, rlw = _ref_part(p, oracle.ATTN_WINDOW)
+    check_attention(ow, lw, rw, rlw, torch.bfloat16, "window/%s/s%d" % (name, splits))
+    # the same queries: the full attention
+    of, lf = _part(g, p, d2f.ATTN_WINDOW, prev=(oc, lc), splits=splits)
+    ref, ref_lse = _ref(p)
+    check_attention(of, lf, ref, ref_lse, torch.bfloat16, "composed/%s/s%d" % (name, splits))
+    # the next step's queries with the kept part: the oracle's composition of it
+    q1 = (p.q.float() + 0.25 * torch.randn(p.q.shape, generator=torch.Generator().manual_seed(5))
+          ).to(p.q.dtype)
+    o1, l1 = _part(g, p, d2f.ATTN_WINDOW, q=q1.to(dev), prev=(oc, lc), splits=splits)
+    r1, rl1 = _ref_part(p, oracle.ATTN_WINDOW, q=q1, prev=(oc.cpu(), lc.cpu()))
+    check_attention(o1, l1, r1, rl1, torch.bfloat16, "reuse/%s/s%d" % (name, splits))
+
+
+def test_attention_parts_need_the_tensor_core_path():
+    dev = device()
+    p = synth.make_problem(synth.workload("tiny"))
+    g = p.to(dev)
+    with pytest.raises(d2f.D2FError):
+        _part(g, p, d2f.ATTN_CACHED)
