@@ -53,6 +53,11 @@ def parse():
     ap.add_argument("--early-gap", type=float, default=None,
                     help="early commit of whole sequences at this logit-gap threshold "
                          "(d2f_commit_metric; every sequence)")
+    ap.add_argument("--reuse-cached", action="store_true",
+                    help="steps inside a block's denoising: the window part of the attention "
+                         "composed with a kept cached part (d2f_block_attn_part); the cached "
+                         "part is computed once per input set, before the timed region, and "
+                         "timed on its own")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -98,27 +103,36 @@ def max_over_ranks(x, world):
 # ---------------------------------------------------------------------------
 # workload accounting
 # ---------------------------------------------------------------------------
-def algorithmic_bytes(p):
+def algorithmic_bytes(p, part="all"):
     """Bytes a step must move at minimum: cached K+V once per (sequence, KV
-    head), window K/V, Q, O, page ids; logits of masked rows; appended blocks."""
+    head), window K/V, Q, O, page ids; logits of masked rows; appended blocks.
+    part "window" (composed with a kept cached part): window K/V, Q, O and the
+    kept part's output and normaliser, no cached page; part "cached": cached K+V,
+    page ids, Q, and its output and normaliser."""
     w = p.w
     elt = 2 if w.dtype == torch.bfloat16 else 4
     Hk, H, D = w.num_heads_kv, w.num_heads_q, w.head_dim
     ctx = sum(w.ctx_lens)
     tq = w.total_q
     pages = sum((c + w.block_size - 1) // w.block_size for c in w.ctx_lens)
-    attn = 2 * ctx * Hk * D * elt + 2 * tq * Hk * D * elt + 2 * tq * H * D * elt + pages * 4 * Hk
+    if part == "window":
+        attn = 2 * tq * Hk * D * elt + 3 * tq * H * D * elt + tq * H * 4
+    elif part == "cached":
+        attn = 2 * ctx * Hk * D * elt + pages * 4 * Hk + 2 * tq * H * D * elt + tq * H * 4
+    else:
+        attn = 2 * ctx * Hk * D * elt + 2 * tq * Hk * D * elt + 2 * tq * H * D * elt + pages * 4 * Hk
     masked_rows = int(p.masked.sum())
     commit = masked_rows * w.vocab * elt + tq * 6
     append = 2 * 2 * len(p.src_row) * w.block_size * Hk * D * elt
     return attn, commit, append
 
 
-def flops(p):
+def flops(p, reuse=False):
     w = p.w
     f = 0
     for c, nb in zip(w.ctx_lens, w.window_blocks):
         n = nb * w.block_size
+        c = 0 if reuse else c
         keys = sum(c + (i // w.block_size + 1) * w.block_size for i in range(n))
         f += 4 * w.num_heads_q * w.head_dim * keys
     return f
@@ -145,6 +159,9 @@ def source_sha(files):
 KERNEL_SOURCES = {
     "attn": ["block_causal_kv_gb300/csrc/attn_tc.cu", "block_causal_kv_gb300/csrc/attn_common.cuh",
              "block_causal_kv_gb300/csrc/d2f_internal.cuh"],
+    "attn_window": ["block_causal_kv_gb300/csrc/attn_tc.cu",
+                    "block_causal_kv_gb300/csrc/attn_common.cuh",
+                    "block_causal_kv_gb300/csrc/d2f_internal.cuh"],
     "commit": ["block_causal_kv_gb300/csrc/commit.cu", "block_causal_kv_gb300/csrc/d2f_internal.cuh"],
 }
 
@@ -230,22 +247,31 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # CPU oracle timing (reference arm and cpu_baseline)
 # ---------------------------------------------------------------------------
-def time_oracle(p, seconds, nthreads, metric=0):
+def time_oracle(p, seconds, nthreads, metric=0, reuse=False):
     """Time the CPU oracle on a bounded sample of one step and extrapolate to
     full steps: attention over a subset of KV heads (its cost is linear in heads)
     and the commit over a subset of rows (linear in rows), with the commit's
-    confidence `metric`."""
+    confidence `metric`. reuse: the attention is the window part composed with a
+    cached part that is computed once per sample size, untimed."""
     import oracle
     w = p.w
     Hk, G = w.num_heads_kv, w.num_heads_q // w.num_heads_kv
+    kept = {}
+
     # calibrate with one KV head and one block of rows
     def attn_sample(nh):
         hk = list(range(nh))
         hq = [h for g in hk for h in range(g * G, (g + 1) * G)]
+        args = (p.q[:, hq], p.k_win[:, hk], p.v_win[:, hk], p.k_pool[:, hk], p.v_pool[:, hk],
+                p.page_table, p.ctx_len, p.q_start, w.block_size)
+        if reuse and nh not in kept:
+            kept[nh] = oracle.block_attn_part(*args, oracle.ATTN_CACHED, nthreads=nthreads)
         t0 = time.perf_counter()
-        oracle.block_attn(p.q[:, hq], p.k_win[:, hk], p.v_win[:, hk], p.k_pool[:, hk],
-                          p.v_pool[:, hk], p.page_table, p.ctx_len, p.q_start, w.block_size,
-                          nthreads=nthreads, want_lse=False)
+        if reuse:
+            oracle.block_attn_part(*args, oracle.ATTN_WINDOW, prev_out=kept[nh][0],
+                                   prev_lse=kept[nh][1], nthreads=nthreads)
+        else:
+            oracle.block_attn(*args, nthreads=nthreads, want_lse=False)
         return time.perf_counter() - t0
 
     def commit_sample(nb):
@@ -275,8 +301,10 @@ def time_oracle(p, seconds, nthreads, metric=0):
         if time.perf_counter() - t_start >= seconds:
             break
     step_s = (ta / reps) * Hk / nh + (tc / reps) * n_blocks / nb
-    sample = ("%d x [attention for %d of %d KV heads + commit for %d of %d window blocks], "
-              "extrapolated linearly to full steps" % (reps, nh, Hk, nb, n_blocks))
+    sample = ("%d x [%s for %d of %d KV heads + commit for %d of %d window blocks], "
+              "extrapolated linearly to full steps" % (
+                  reps, "window-part attention with a kept cached part" if reuse else "attention",
+                  nh, Hk, nb, n_blocks))
     return 1.0 / step_s, sample
 
 
@@ -296,8 +324,9 @@ def run_reference(args, world, rank):
     # bounded: the whole run takes about --ref-seconds regardless of K
     budget = args.ref_seconds
     for _ in range(max(0, min(args.warmup, 1))):
-        time_oracle(p, 0.1, nthreads, CONF_METRICS[args.conf_metric])
-    value, sample = time_oracle(p, budget, nthreads, CONF_METRICS[args.conf_metric])
+        time_oracle(p, 0.1, nthreads, CONF_METRICS[args.conf_metric], args.reuse_cached)
+    value, sample = time_oracle(p, budget, nthreads, CONF_METRICS[args.conf_metric],
+                                args.reuse_cached)
     ms = 1000.0 / value
     cfg = workload_config(p, args)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s",
@@ -323,6 +352,11 @@ def workload_config(p, args):
         extra["early_commit_gap"] = args.early_gap
     if args.fused_append and w.appends_per_seq:
         extra["append"] = "fused into the attention (d2f_block_attn_append)"
+    if args.reuse_cached:
+        extra["attention"] = ("window part composed with a kept cached part (d2f_block_attn_part): "
+                              "a step inside a block's denoising, no append; the cached part of "
+                              "each input set is computed before the timed region and timed on "
+                              "its own in kernels.cached_part")
     return {**extra,"workload": "%s: batch %d, Hq %d / Hkv %d, head_dim %d, block %d, context %s, "
                         "window %s blocks, vocab %d" % (
                             w.name, w.batch, w.num_heads_q, w.num_heads_kv, w.head_dim,
@@ -380,8 +414,11 @@ def run_ours(args, world, rank, local):
     tokens_all, masked_all = tokens0.clone(), masked0.clone()
     for i, st in enumerate(sets):
         st.tokens, st.masked = tokens_all[i], masked_all[i]
+    reuse = args.reuse_cached
+    if reuse and args.fused_append:
+        raise SystemExit("--reuse-cached times steps without an append: drop --fused-append")
     fused = args.fused_append and len(p.src_row) > 0
-    appends = len(p.src_row) > 0 and not fused
+    appends = len(p.src_row) > 0 and not fused and not reuse
 
     dcode = d2f.F32 if w.dtype == torch.float32 else d2f.BF16
     ws_attn = d2f.attn_workspace(dev, batch=w.batch, total_q=w.total_q, dtype=dcode,
@@ -396,11 +433,29 @@ def run_ours(args, world, rank, local):
     rem = torch.empty(w.total_q // B, dtype=torch.int32, device=dev)
 
     def attn(s):
-        kw = dict(append_src_row=s.src_row, append_dst_page=s.dst_page) if fused else {}
+        if reuse:
+            kw = dict(part=d2f.ATTN_WINDOW, prev_out=s.prev_out, prev_lse=s.prev_lse)
+        elif fused:
+            kw = dict(append_src_row=s.src_row, append_dst_page=s.dst_page)
+        else:
+            kw = {}
         d2f.block_attn(s.q, s.k_win, s.v_win, s.k_pool, s.v_pool, s.page_table, s.ctx_len,
                        s.q_start, block_size=B, max_q_per_seq=p.max_q_per_seq, max_ctx=p.max_ctx,
                        num_splits=args.num_splits, out=s.out, want_lse=False, workspace=ws_attn,
                        err=err, **kw)
+
+    def cached_part(s):
+        d2f.block_attn(s.q, s.k_win, s.v_win, s.k_pool, s.v_pool, s.page_table, s.ctx_len,
+                       s.q_start, block_size=B, max_q_per_seq=p.max_q_per_seq, max_ctx=p.max_ctx,
+                       num_splits=args.num_splits, out=s.prev_out, lse=s.prev_lse,
+                       workspace=ws_attn, err=err, part=d2f.ATTN_CACHED)
+
+    if reuse:
+        for s in sets:
+            s.prev_out = torch.empty_like(s.q)
+            s.prev_lse = torch.empty(s.q.shape[:2], dtype=torch.float32, device=dev)
+            cached_part(s)
+        torch.cuda.synchronize()
 
     early_gap = stopped = None
     if args.early_gap is not None:
@@ -514,7 +569,8 @@ def run_ours(args, world, rank, local):
     # so that number is reported for reference only. Events between kernels
     # would add their own latency to every bracket.)
     per_kernel = {}
-    kernel_fns = [("attn", attn), ("commit", commit)] + ([("append", append)] if appends else [])
+    kernel_fns = [("attn", attn), ("commit", commit)] + ([("append", append)] if appends else []) \
+        + ([("cached_part", cached_part)] if reuse else [])
     for which, fn in kernel_fns:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
@@ -541,7 +597,7 @@ def run_ours(args, world, rank, local):
     steps_total = K * world
     value = steps_total / (elapsed_ms / 1000.0)
     ms_per_step = elapsed_ms / K
-    attn_b, commit_b, append_b = algorithmic_bytes(p)
+    attn_b, commit_b, append_b = algorithmic_bytes(p, "window" if reuse else "all")
     if fused:  # the appended pages' writes (their window rows are read by the attention anyway)
         attn_b += append_b // 2
     hbm, tflops, peak_kind = peaks()
@@ -551,11 +607,17 @@ def run_ours(args, world, rank, local):
     if t_attn:
         kernels["block_attn"] = {"us": t_attn, "bytes": attn_b, "GB/s": attn_b / t_attn / 1e3,
                                  "frac": attn_b / t_attn / 1e3 / hbm,
-                                 "TFLOP/s": flops(p) / t_attn / 1e6,
+                                 "TFLOP/s": flops(p, reuse) / t_attn / 1e6,
                                  "us_attention_only_graph": per_kernel["attn"]}
     if t_commit:
         kernels["commit"] = {"us": t_commit, "bytes": commit_b, "GB/s": commit_b / t_commit / 1e3,
                              "frac": commit_b / t_commit / 1e3 / hbm}
+    if reuse:
+        cb = algorithmic_bytes(p, "cached")[0]
+        t_cp = per_kernel["cached_part"]
+        kernels["cached_part"] = {"us": t_cp, "bytes": cb, "GB/s": cb / t_cp / 1e3,
+                                  "frac": cb / t_cp / 1e3 / hbm,
+                                  "note": "once per cache change (a finished block), not per step"}
     if appends:
         t_app = per_kernel["append"]
         kernels["kv_append"] = {"us": t_app, "bytes": append_b, "GB/s": append_b / t_app / 1e3,
@@ -571,7 +633,8 @@ def run_ours(args, world, rank, local):
                             "sets, CUDA events around whole replays",
                 "achieved": dk.get("GB/s"), "peak": hbm,
                 "unit": "GB/s", "frac": dk.get("frac"), "peak_kind": peak_kind,
-                "traffic": recorded_traffic("attn" if dom == "block_attn" else "commit", w.name)}
+                "traffic": recorded_traffic(("attn_window" if reuse else "attn")
+                                            if dom == "block_attn" else "commit", w.name)}
 
     # end to end through the C ABI from pinned host buffers
     e2e = None
@@ -597,7 +660,7 @@ def run_ours(args, world, rank, local):
     if rank == 0 and not args.no_cpu_baseline:
         value_cpu, sample = time_oracle(p if p.q.device.type == "cpu" else p.to("cpu"),
                                         args.cpu_seconds, oracle_threads(),
-                                        CONF_METRICS[args.conf_metric])
+                                        CONF_METRICS[args.conf_metric], reuse)
         line["cpu_baseline"] = {"value": value_cpu, "unit": "steps/s", "cores": oracle_threads(),
                                 "kind": "oracle", "sample": sample}
     if rank == 0:

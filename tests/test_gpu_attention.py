@@ -293,6 +293,28 @@ def test_cached_and_window_parts(name, splits):
     check_attention(o1, l1, r1, rl1, torch.bfloat16, "reuse/%s/s%d" % (name, splits))
 
 
+@pytest.mark.parametrize("name", ["dream", "long_b32"])
+def test_full_size_parts_sampled(name):
+    """Full-size workloads in the bench's launch configuration: the cached part,
+    then the window part composed with it, against the oracle's full attention
+    of one sampled sequence (its window rows, all heads)."""
+    dev = device()
+    p = synth.make_problem(synth.workload(name))
+    g = p.to(dev)
+    oc, lc = _part(g, p, d2f.ATTN_CACHED)
+    of, lf = _part(g, p, d2f.ATTN_WINDOW, prev=(oc, lc))
+    b = p.w.batch // 2
+    qs = p.q_start.tolist()
+    rows = slice(qs[b], qs[b + 1])
+    ref, ref_lse = oracle.block_attn(p.q[rows], p.k_win[rows], p.v_win[rows], p.k_pool, p.v_pool,
+                                     p.page_table[b:b + 1], p.ctx_len[b:b + 1],
+                                     torch.tensor([0, qs[b + 1] - qs[b]], dtype=torch.int32),
+                                     p.w.block_size)
+    mx, mean = check_attention(of[rows], lf[rows], ref, ref_lse, torch.bfloat16,
+                               name + " parts full")
+    print("%s parts full (sequence %d): max-abs %.3e mean-abs %.3e" % (name, b, mx, mean))
+
+
 def test_attention_parts_need_the_tensor_core_path():
     dev = device()
     p = synth.make_problem(synth.workload("tiny"))
