@@ -11,6 +11,8 @@ Functions:
   commit      -- per-position max-probability confidence, threshold /
                  aggressive commit per block, remasking.
   kv_append   -- bitwise copy of finished blocks into their pages.
+  window_step -- the pipelined window scheduler between two steps (block
+                 entry, phases, append list, pages, repacked window).
 """
 import ctypes
 import os
@@ -53,6 +55,10 @@ def _load():
             _P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P,
             _P, _P, _P, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int32,
             _P, _P, _P, ctypes.c_int, _P, _P, ctypes.c_int]
+        lib.d2f_oracle_window_step.restype = ctypes.c_int
+        lib.d2f_oracle_window_step.argtypes = [
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int32,
+            ctypes.c_float, ctypes.c_float] + [_P] * 17
         lib.d2f_oracle_kv_append.restype = ctypes.c_int
         lib.d2f_oracle_kv_append.argtypes = [
             _P, _P, _P, _P, ctypes.c_int, ctypes.c_int, _P, _P,
@@ -223,3 +229,52 @@ def kv_append(k_win, v_win, src_row, dst_page, k_pool, v_pool, block_size):
     if rc != 0:
         raise ValueError("oracle kv_append rejected its input (code %d)" % rc)
     return k_pool, v_pool
+
+
+# keys of the window scheduler's state (see window_step)
+WINDOW_STATE = ("q_start", "tokens", "masked", "ctx_len", "page_table", "next_block",
+                "gen_blocks", "n_leaving", "stopped", "free_pages", "free_count")
+
+
+def window_step(state, block_size, max_blocks, mask_id, tau_add, tau_act):
+    """One call of the pipelined window scheduler on a copy of `state` (a dict of
+    CPU tensors: q_start int32 [batch+1], tokens int32 [capacity], masked uint8
+    [capacity], ctx_len / next_block / gen_blocks / n_leaving int32 [batch],
+    page_table int32 [batch, max_pages], stopped uint8 [batch] or None,
+    free_pages int32 [F], free_count int). Returns the new state plus
+    block_phase uint8 [capacity / B], row_pos int32 [capacity], app_src /
+    app_dst int32 [n_append], n_append and err (ints). Raises on bad sizes or an
+    inconsistent state (the oracle writes nothing then)."""
+    lib = _load()
+    st = {}
+    for k in ("q_start", "tokens", "ctx_len", "page_table", "next_block", "gen_blocks",
+              "n_leaving", "free_pages"):
+        st[k] = _cpu(state[k], torch.int32).clone().contiguous()
+    st["masked"] = _cpu(state["masked"], torch.uint8).clone().contiguous()
+    stopped = state.get("stopped")
+    st["stopped"] = None if stopped is None else _cpu(stopped, torch.uint8).clone().contiguous()
+    batch = st["q_start"].shape[0] - 1
+    capacity = st["tokens"].shape[0]
+    max_pages = st["page_table"].shape[1] if st["page_table"].dim() == 2 else 0
+    free_count = torch.tensor([int(state["free_count"])], dtype=torch.int32)
+    phase = torch.zeros(max(capacity // block_size, 1), dtype=torch.uint8)
+    row_pos = torch.empty(max(capacity, 1), dtype=torch.int32)
+    app_src = torch.empty(max(capacity // block_size, 1), dtype=torch.int32)
+    app_dst = torch.empty_like(app_src)
+    n_append = torch.zeros(1, dtype=torch.int32)
+    err = torch.zeros(1, dtype=torch.int32)
+    rc = lib.d2f_oracle_window_step(
+        batch, block_size, max_blocks, capacity, max_pages, int(mask_id), float(tau_add),
+        float(tau_act), _ptr(st["q_start"]), _ptr(st["tokens"]), _ptr(st["masked"]), _ptr(phase),
+        _ptr(row_pos), _ptr(st["ctx_len"]), _ptr(st["page_table"]), _ptr(st["next_block"]),
+        _ptr(st["gen_blocks"]), _ptr(st["n_leaving"]), _ptr(st["stopped"]),
+        _ptr(st["free_pages"]), _ptr(free_count), _ptr(app_src), _ptr(app_dst), _ptr(n_append),
+        _ptr(err))
+    if rc != 0:
+        raise ValueError("oracle window_step rejected its input (code %d)" % rc)
+    n = int(n_append.item())
+    st["free_count"] = int(free_count.item())
+    st.update(block_phase=phase[:capacity // block_size], row_pos=row_pos[:capacity],
+              app_src=app_src[:n].clone(), app_dst=app_dst[:n].clone(), n_append=n,
+              err=int(err.item()))
+    return st

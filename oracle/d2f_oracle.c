@@ -547,3 +547,163 @@ int d2f_oracle_kv_append(const void *k_win, const void *v_win,
   }
   return 0;
 }
+
+/*
+ * One step of the pipelined window scheduler, run after the commit of a step:
+ * it turns the decode state left by that commit into the window of the next step.
+ *
+ * [P2] §쉽게 이해하기 (pipelined parallel decoding): an active window of blocks is
+ * kept; when the progress of the window's last block passes a threshold a new
+ * block is added behind it, so the window's size stays bounded; a new block
+ * starts conservative (it commits only positions above the confidence threshold)
+ * and turns aggressive (it also commits its most confident position) once the
+ * block before it has progressed far enough; what is not committed stays masked.
+ * [P1] §블록 단위 인과 어텐션 and §운영 관점: a completed block's K/V are final and
+ * are persisted to the paged cache; block completion is the signal.
+ *
+ * Readings (the pages give neither values nor an order of these steps):
+ *  - progress of a block = committed positions c out of B. "Passes the threshold"
+ *    is c > tau_add * B and "far enough" is c >= tau_act * B, both products and
+ *    comparisons in float. The block before the oldest window block is the cache
+ *    (complete).
+ *  - max_blocks bounds every block whose rows a step computes, including complete
+ *    blocks waiting for their append. At most one block enters a sequence's
+ *    window per step; an empty window takes one if any are left
+ *    (next_block < gen_blocks) and the sequence was not stopped by the early
+ *    commit.
+ *  - a block that completed is appended during the next step (whose forward pass
+ *    computes its K/V from final tokens), and only as part of a complete oldest
+ *    prefix of the window (the cache stays in order). The blocks appended during
+ *    a step leave the window at the next call (n_leaving), and ctx_len grows by B
+ *    for each.
+ *  - pages are taken from the top of the free list (free_pages[free_count - 1]
+ *    first) in the order (sequence, block); the page of the i-th appended block of
+ *    sequence b is written to page_table[b][ctx_len[b] / B + i] at once. A block
+ *    that gets no page (list empty, or the page-table row full) stays in the
+ *    window and err = 7.
+ *
+ * State, packed like the rest of the path (window rows of sequence b are
+ * q_start[b] .. q_start[b+1]-1, block by block, oldest first), all in/out unless
+ * said: q_start [batch+1]; tokens [capacity]; masked [capacity]; ctx_len [batch];
+ * page_table [batch][max_pages_per_seq]; next_block [batch] (generation blocks
+ * that have entered so far); gen_blocks [batch] (in); n_leaving [batch];
+ * stopped [batch] (in, may be NULL); free_pages (in) and free_count.
+ * Out: block_phase [capacity / B] (1 = aggressive); row_pos [capacity] (position
+ * of the row's token in its sequence, -1 past the window); app_src / app_dst /
+ * n_append (the append list of the next step: first window row of the block in
+ * the new layout, its page). Rows past the new window: tokens = mask_id,
+ * masked = 0, row_pos = -1; their blocks' phase 0.
+ *
+ * Returns 0; -1 bad sizes (nothing written); -2 inconsistent state (a window not
+ * made of whole blocks, beyond capacity or longer than max_blocks, n_leaving
+ * larger than the window, ctx_len negative or not a multiple of B): nothing
+ * written. *err (first error wins, 0 = none) takes 7 when a block gets no page.
+ */
+int d2f_oracle_window_step(int batch, int block_size, int max_blocks, int capacity,
+                           int max_pages_per_seq, int32_t mask_id, float tau_add, float tau_act,
+                           int32_t *q_start, int32_t *tokens, uint8_t *masked,
+                           uint8_t *block_phase, int32_t *row_pos, int32_t *ctx_len,
+                           int32_t *page_table, int32_t *next_block, const int32_t *gen_blocks,
+                           int32_t *n_leaving, const uint8_t *stopped,
+                           const int32_t *free_pages, int32_t *free_count,
+                           int32_t *app_src, int32_t *app_dst, int32_t *n_append, int32_t *err) {
+  const int B = block_size;
+  if (batch < 0 || B < 1 || max_blocks < 1 || capacity < 0 || capacity % B != 0 ||
+      (long long)batch * max_blocks * B > capacity || max_pages_per_seq < 0 || *free_count < 0)
+    return -1;
+  /* the state must be consistent before anything is changed */
+  if (q_start[0] != 0) return -2;
+  for (int b = 0; b < batch; ++b) {
+    const int n = q_start[b + 1] - q_start[b];
+    if (n < 0 || n % B != 0 || n / B > max_blocks || q_start[b + 1] > capacity) return -2;
+    if (n_leaving[b] < 0 || n_leaving[b] > n / B) return -2;
+    if (ctx_len[b] < 0 || ctx_len[b] % B != 0) return -2;
+  }
+  /* the rows of the old window, read before any is overwritten */
+  const int old_rows = q_start[batch];
+  int32_t *tok0 = (int32_t *)malloc(sizeof(int32_t) * (size_t)(old_rows > 0 ? old_rows : 1));
+  uint8_t *msk0 = (uint8_t *)malloc((size_t)(old_rows > 0 ? old_rows : 1));
+  int32_t *qs0 = (int32_t *)malloc(sizeof(int32_t) * (size_t)(batch + 1));
+  int *committed = (int *)malloc(sizeof(int) * (size_t)(max_blocks + 1));
+  if (!tok0 || !msk0 || !qs0 || !committed) {
+    free(tok0);
+    free(msk0);
+    free(qs0);
+    free(committed);
+    return -1;
+  }
+  memcpy(tok0, tokens, sizeof(int32_t) * (size_t)old_rows);
+  memcpy(msk0, masked, (size_t)old_rows);
+  memcpy(qs0, q_start, sizeof(int32_t) * (size_t)(batch + 1));
+
+  int free_left = *free_count, n_app = 0, row = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int old_blocks = (qs0[b + 1] - qs0[b]) / B;
+    /* 1. the blocks appended during the step just run leave the window */
+    const int nl = n_leaving[b];
+    ctx_len[b] += nl * B;
+    const int first_old = qs0[b] / B + nl; /* oldest surviving block (old layout) */
+    const int n_surv = old_blocks - nl;
+    /* committed positions of each block of the new window (a new block: none) */
+    for (int k = 0; k < n_surv; ++k) {
+      int c = 0;
+      for (int u = 0; u < B; ++u) c += msk0[(first_old + k) * B + u] == 0;
+      committed[k] = c;
+    }
+    /* 2. a new block behind the last one */
+    const int is_stopped = stopped != NULL && stopped[b] != 0;
+    int add = !is_stopped && next_block[b] < gen_blocks[b] && n_surv < max_blocks;
+    if (add && n_surv > 0) add = (float)committed[n_surv - 1] > tau_add * (float)B;
+    const int n_new = n_surv + add;
+    if (add) committed[n_surv] = 0;
+    q_start[b] = row;
+    /* 3. the complete oldest blocks are appended during the next step */
+    int want = 0;
+    while (want < n_surv && committed[want] == B) ++want;
+    int granted = 0;
+    for (int i = 0; i < want; ++i) {
+      const int slot = ctx_len[b] / B + i;
+      if (free_left == 0 || slot >= max_pages_per_seq) {
+        if (*err == 0) *err = 7;
+        break;
+      }
+      const int page = free_pages[--free_left];
+      page_table[(int64_t)b * max_pages_per_seq + slot] = page;
+      app_src[n_app] = row + i * B;
+      app_dst[n_app] = page;
+      ++n_app;
+      ++granted;
+    }
+    n_leaving[b] = granted;
+    /* 4. phases and rows of the new window */
+    for (int k = 0; k < n_new; ++k) {
+      const int pred = k == 0 ? B : committed[k - 1];
+      block_phase[row / B] = (float)pred >= tau_act * (float)B ? 1 : 0;
+      for (int u = 0; u < B; ++u, ++row) {
+        if (k < n_surv) {
+          tokens[row] = tok0[(first_old + k) * B + u];
+          masked[row] = msk0[(first_old + k) * B + u];
+        } else {
+          tokens[row] = mask_id;
+          masked[row] = 1;
+        }
+        row_pos[row] = ctx_len[b] + k * B + u;
+      }
+    }
+    next_block[b] += add;
+  }
+  q_start[batch] = row;
+  for (int r = row; r < capacity; ++r) {
+    tokens[r] = mask_id;
+    masked[r] = 0;
+    row_pos[r] = -1;
+    if (r % B == 0) block_phase[r / B] = 0;
+  }
+  *free_count = free_left;
+  *n_append = n_app;
+  free(tok0);
+  free(msk0);
+  free(qs0);
+  free(committed);
+  return 0;
+}
