@@ -19,6 +19,8 @@ template <bool VEC>
 __global__ void __launch_bounds__(kThreads) append_kernel(const AppendArgs a) {
   const int ap = blockIdx.x / a.num_heads_kv;
   const int g = blockIdx.x % a.num_heads_kv;
+  // a list whose length is in device memory: the launch covers its capacity
+  if (a.n_dev != nullptr && ap >= min(max(*a.n_dev, 0), a.n_append)) return;
   const int src = a.src_row[ap];
   const int dst = a.dst_page[ap];
   if (src < 0 || src + a.block_size > a.total_q || dst < 0 || dst >= a.num_pages) {

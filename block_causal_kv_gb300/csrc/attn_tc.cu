@@ -397,7 +397,9 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
       // stage before this thread can refill it.
       if (a.n_append > 0 && mt == 0 && t >= Tc && src >= 0) {
         bool landed = false;
-        for (int ap = 0; ap < a.n_append; ++ap) {
+        // list length: the host's, or (bounded by it) the one in device memory
+        const int napp = a.app_n_dev ? min(max(*a.app_n_dev, 0), a.n_append) : a.n_append;
+        for (int ap = 0; ap < napp; ++ap) {
           if (__ldg(a.app_src + ap) != src) continue;
           const int dp = __ldg(a.app_dst + ap);
           if (dp < 0 || dp >= a.num_pages) {

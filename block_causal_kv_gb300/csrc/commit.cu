@@ -280,6 +280,9 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
   grid_launch_dependents();
   grid_dependency_wait();  // logits / state may come from the previous kernel
   if (tid == 0) D2F_TRACE_MARK(1, 1);
+  // Rows past the last window (a launch sized for a capacity, the layout written
+  // on the device): the whole block leaves before touching any counter.
+  if (jb * B >= __ldg(a.q_start + a.batch)) return;
 
   // Decision metadata of this block, fetched now, used only by the last arriver:
   // lane u of warp 0 holds row u's masked flag, thread 0 the block's tau and phase.

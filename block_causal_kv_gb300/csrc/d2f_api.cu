@@ -301,6 +301,7 @@ const char *d2f_status_string(int status) {
     case D2F_ERR_BAD_INDEX: return "index out of range (device)";
     case D2F_ERR_TIMEOUT: return "bounded wait timed out (device)";
     case D2F_ERR_WORKSPACE: return "workspace missing or too small";
+    case D2F_ERR_NO_PAGE: return "a finished block got no page (device)";
     default: return "unknown status";
   }
 }
@@ -326,8 +327,9 @@ int attn_entry(const void *q, const void *k_win, const void *v_win, const void *
                int batch, int total_q, int max_q_per_seq, int max_ctx, int num_heads_q,
                int num_heads_kv, int head_dim, int block_size, int num_pages, int dtype,
                float softmax_scale, int num_splits, void *workspace, size_t workspace_bytes,
-               const int32_t *src_row, const int32_t *dst_page, int n_append, int part,
-               const void *prev_out, const float *prev_lse, int32_t *err_word, void *stream) {
+               const int32_t *src_row, const int32_t *dst_page, int n_append,
+               const int32_t *n_append_dev, int part, const void *prev_out,
+               const float *prev_lse, int32_t *err_word, void *stream) {
   if (n_append < 0) return fail(D2F_ERR_INVALID_ARG, "n_append %d < 0", n_append);
   if (part < D2F_ATTN_ALL || part > D2F_ATTN_WINDOW)
     return fail(D2F_ERR_INVALID_ARG, "part %d is not a D2F_ATTN_* value", part);
@@ -405,6 +407,7 @@ int attn_entry(const void *q, const void *k_win, const void *v_win, const void *
   a.prev_lse = prev_lse;
   // fused append on the tensor-core path; the CUDA-core path appends after
   a.n_append = p.tc ? n_append : 0;
+  a.app_n_dev = n_append_dev;
   a.app_src = src_row;
   a.app_dst = dst_page;
   if (num_pages <= 0 && max_ctx > 0) return fail(D2F_ERR_INVALID_ARG, "no pages");
@@ -420,6 +423,11 @@ int attn_entry(const void *q, const void *k_win, const void *v_win, const void *
   } else {
     e = launch_attn_simt(a, dtype, s);
     if (e != cudaSuccess) return cuda_fail(e, "CUDA-core attention launch");
+    if (n_append > 0 && n_append_dev)
+      return d2f_kv_append_dev(k_win, v_win, src_row, dst_page, n_append_dev, n_append, total_q,
+                               const_cast<void *>(k_pool), const_cast<void *>(v_pool),
+                               num_heads_kv, head_dim, block_size, num_pages, dtype, err_word,
+                               stream);
     if (n_append > 0)
       return d2f_kv_append(k_win, v_win, src_row, dst_page, n_append, total_q, const_cast<void *>(k_pool),
                            const_cast<void *>(v_pool), num_heads_kv, head_dim, block_size, num_pages,
@@ -441,8 +449,26 @@ int d2f_block_attn_append(const void *q, const void *k_win, const void *v_win, c
   return attn_entry(q, k_win, v_win, k_pool, v_pool, page_table, max_pages_per_seq, ctx_len,
                     q_start, out, lse_out, batch, total_q, max_q_per_seq, max_ctx, num_heads_q,
                     num_heads_kv, head_dim, block_size, num_pages, dtype, softmax_scale, num_splits,
-                    workspace, workspace_bytes, src_row, dst_page, n_append, D2F_ATTN_ALL, nullptr,
-                    nullptr, err_word, stream);
+                    workspace, workspace_bytes, src_row, dst_page, n_append, nullptr, D2F_ATTN_ALL,
+                    nullptr, nullptr, err_word, stream);
+}
+
+int d2f_block_attn_append_dev(const void *q, const void *k_win, const void *v_win,
+                              const void *k_pool, const void *v_pool, const int32_t *page_table,
+                              int max_pages_per_seq, const int32_t *ctx_len,
+                              const int32_t *q_start, void *out, float *lse_out, int batch,
+                              int total_q, int max_q_per_seq, int max_ctx, int num_heads_q,
+                              int num_heads_kv, int head_dim, int block_size, int num_pages,
+                              int dtype, float softmax_scale, int num_splits, void *workspace,
+                              size_t workspace_bytes, const int32_t *src_row,
+                              const int32_t *dst_page, const int32_t *n_append_dev,
+                              int max_append, int32_t *err_word, void *stream) {
+  if (!n_append_dev) return fail(D2F_ERR_INVALID_ARG, "n_append_dev is NULL");
+  return attn_entry(q, k_win, v_win, k_pool, v_pool, page_table, max_pages_per_seq, ctx_len,
+                    q_start, out, lse_out, batch, total_q, max_q_per_seq, max_ctx, num_heads_q,
+                    num_heads_kv, head_dim, block_size, num_pages, dtype, softmax_scale, num_splits,
+                    workspace, workspace_bytes, src_row, dst_page, max_append, n_append_dev,
+                    D2F_ATTN_ALL, nullptr, nullptr, err_word, stream);
 }
 
 int d2f_block_attn_part(const void *q, const void *k_win, const void *v_win, const void *k_pool,
@@ -456,8 +482,8 @@ int d2f_block_attn_part(const void *q, const void *k_win, const void *v_win, con
   return attn_entry(q, k_win, v_win, k_pool, v_pool, page_table, max_pages_per_seq, ctx_len,
                     q_start, out, lse_out, batch, total_q, max_q_per_seq, max_ctx, num_heads_q,
                     num_heads_kv, head_dim, block_size, num_pages, dtype, softmax_scale, num_splits,
-                    workspace, workspace_bytes, nullptr, nullptr, 0, part, prev_out, prev_lse,
-                    err_word, stream);
+                    workspace, workspace_bytes, nullptr, nullptr, 0, nullptr, part, prev_out,
+                    prev_lse, err_word, stream);
 }
 
 int d2f_block_attn(const void *q, const void *k_win, const void *v_win, const void *k_pool,
@@ -470,8 +496,8 @@ int d2f_block_attn(const void *q, const void *k_win, const void *v_win, const vo
   return attn_entry(q, k_win, v_win, k_pool, v_pool, page_table, max_pages_per_seq, ctx_len,
                     q_start, out, lse_out, batch, total_q, max_q_per_seq, max_ctx, num_heads_q,
                     num_heads_kv, head_dim, block_size, num_pages, dtype, softmax_scale, num_splits,
-                    workspace, workspace_bytes, nullptr, nullptr, 0, D2F_ATTN_ALL, nullptr, nullptr,
-                    err_word, stream);
+                    workspace, workspace_bytes, nullptr, nullptr, 0, nullptr, D2F_ATTN_ALL, nullptr,
+                    nullptr, err_word, stream);
 }
 
 int d2f_commit_workspace_size(int total_q, int vocab, int dtype, int block_size, int num_splits,
@@ -558,10 +584,11 @@ int d2f_commit(const void *logits, int64_t row_stride, int dtype, int vocab, int
                            num_splits, workspace, workspace_bytes, err_word, stream);
 }
 
-int d2f_kv_append(const void *k_win, const void *v_win, const int32_t *src_row,
-                  const int32_t *dst_page, int n_append, int total_q, void *k_pool,
-                  void *v_pool, int num_heads_kv, int head_dim, int block_size, int num_pages,
-                  int dtype, int32_t *err_word, void *stream) {
+namespace {
+int append_entry(const void *k_win, const void *v_win, const int32_t *src_row,
+                 const int32_t *dst_page, int n_append, const int32_t *n_append_dev, int total_q,
+                 void *k_pool, void *v_pool, int num_heads_kv, int head_dim, int block_size,
+                 int num_pages, int dtype, int32_t *err_word, void *stream) {
   if (n_append < 0 || total_q < 0 || num_heads_kv <= 0 || head_dim <= 0 || block_size < 1 ||
       num_pages < 0)
     return fail(D2F_ERR_INVALID_ARG, "size out of range");
@@ -579,6 +606,7 @@ int d2f_kv_append(const void *k_win, const void *v_win, const int32_t *src_row,
   a.src_row = src_row;
   a.dst_page = dst_page;
   a.n_append = n_append;
+  a.n_dev = n_append_dev;
   a.total_q = total_q;
   a.k_pool = k_pool;
   a.v_pool = v_pool;
@@ -591,6 +619,81 @@ int d2f_kv_append(const void *k_win, const void *v_win, const int32_t *src_row,
                       aligned16(v_pool) && (a.row_bytes % 16 == 0);
   const cudaError_t e = launch_append(a, vec_ok, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
+  return D2F_OK;
+}
+}  // namespace
+
+int d2f_kv_append(const void *k_win, const void *v_win, const int32_t *src_row,
+                  const int32_t *dst_page, int n_append, int total_q, void *k_pool,
+                  void *v_pool, int num_heads_kv, int head_dim, int block_size, int num_pages,
+                  int dtype, int32_t *err_word, void *stream) {
+  return append_entry(k_win, v_win, src_row, dst_page, n_append, nullptr, total_q, k_pool, v_pool,
+                      num_heads_kv, head_dim, block_size, num_pages, dtype, err_word, stream);
+}
+
+int d2f_kv_append_dev(const void *k_win, const void *v_win, const int32_t *src_row,
+                      const int32_t *dst_page, const int32_t *n_append_dev, int max_append,
+                      int total_q, void *k_pool, void *v_pool, int num_heads_kv, int head_dim,
+                      int block_size, int num_pages, int dtype, int32_t *err_word, void *stream) {
+  if (!n_append_dev) return fail(D2F_ERR_INVALID_ARG, "n_append_dev is NULL");
+  return append_entry(k_win, v_win, src_row, dst_page, max_append, n_append_dev, total_q, k_pool,
+                      v_pool, num_heads_kv, head_dim, block_size, num_pages, dtype, err_word,
+                      stream);
+}
+
+int d2f_window_step(int batch, int block_size, int max_blocks, int capacity,
+                    int max_pages_per_seq, int32_t mask_id, float tau_add, float tau_act,
+                    int32_t *q_start, int32_t *tokens, uint8_t *masked, uint8_t *block_phase,
+                    int32_t *row_pos, int32_t *ctx_len, int32_t *page_table, int32_t *next_block,
+                    const int32_t *gen_blocks, int32_t *n_leaving, const uint8_t *stopped,
+                    const int32_t *free_pages, int32_t *free_count, int32_t *app_src,
+                    int32_t *app_dst, int32_t *n_append, int32_t *err_word, void *stream) {
+  if (batch < 0 || block_size < 1 || max_blocks < 1 || capacity < 0 || max_pages_per_seq < 0)
+    return fail(D2F_ERR_INVALID_ARG, "size out of range");
+  if (capacity % block_size != 0)
+    return fail(D2F_ERR_INVALID_ARG, "capacity %d is not a multiple of block_size %d", capacity,
+                block_size);
+  if ((long long)batch * max_blocks * block_size > capacity)
+    return fail(D2F_ERR_INVALID_ARG, "capacity %d < batch * max_blocks * block_size", capacity);
+  if (tau_add != tau_add || tau_act != tau_act)
+    return fail(D2F_ERR_INVALID_ARG, "tau_add / tau_act must not be NaN");
+  if (block_size > 128) return fail(D2F_ERR_UNSUPPORTED, "block_size > 128");
+  const size_t smem = d2f::window_smem_bytes(batch, capacity, block_size);
+  if (smem > 227 * 1024)
+    return fail(D2F_ERR_UNSUPPORTED, "window state of %zu bytes exceeds one CTA's shared memory",
+                smem);
+  if (!q_start || !tokens || !masked || !block_phase || !row_pos || !ctx_len || !next_block ||
+      !gen_blocks || !n_leaving || !free_pages || !free_count || !app_src || !app_dst ||
+      !n_append || (!page_table && max_pages_per_seq > 0))
+    return fail(D2F_ERR_INVALID_ARG, "a required pointer is NULL");
+  d2f::WindowArgs a;
+  a.batch = batch;
+  a.block_size = block_size;
+  a.max_blocks = max_blocks;
+  a.capacity = capacity;
+  a.max_pages_per_seq = max_pages_per_seq;
+  a.mask_id = mask_id;
+  a.tau_add = tau_add;
+  a.tau_act = tau_act;
+  a.q_start = q_start;
+  a.tokens = tokens;
+  a.masked = masked;
+  a.block_phase = block_phase;
+  a.row_pos = row_pos;
+  a.ctx_len = ctx_len;
+  a.page_table = page_table;
+  a.next_block = next_block;
+  a.gen_blocks = gen_blocks;
+  a.n_leaving = n_leaving;
+  a.stopped = stopped;
+  a.free_pages = free_pages;
+  a.free_count = free_count;
+  a.app_src = app_src;
+  a.app_dst = app_dst;
+  a.n_append = n_append;
+  a.err = err_word;
+  const cudaError_t e = d2f::launch_window(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "window step launch");
   return D2F_OK;
 }
 

@@ -46,7 +46,8 @@ struct AttnArgs {
   int longest_first;     // tensor-core path: map blockIdx.z to sequences longest context first
   const int32_t *app_src;  // tensor-core path, fused append: window rows of finished blocks
   const int32_t *app_dst;  // ... and their pages; n_append = 0: no append
-  int n_append;
+  int n_append;            // entries (with app_n_dev: the most the list can hold)
+  const int32_t *app_n_dev;  // non-null: the list's length, read on the device
   int part;                // tensor-core path: keys attended: 0 all, 1 cached only, 2 window only
   const void *prev_out;    // part 2: a kept cached part to compose with ([total_q][Hq][D], as out)
   const float *prev_lse;   // ... its natural-log normaliser [total_q][Hq]; NULL: no composition
@@ -86,10 +87,26 @@ struct CommitArgs {
 struct AppendArgs {
   const void *k_win, *v_win;
   const int32_t *src_row, *dst_page;
-  int n_append, total_q;
+  int n_append, total_q;   // n_append: entries (with n_dev: the most the list can hold)
+  const int32_t *n_dev;    // non-null: the list's length, read on the device
   void *k_pool, *v_pool;
   int num_heads_kv, block_size, num_pages;
   int row_bytes;         // head_dim * element size
+  int32_t *err;
+};
+
+struct WindowArgs {
+  int batch, block_size, max_blocks, capacity, max_pages_per_seq;
+  int32_t mask_id;
+  float tau_add, tau_act;
+  int32_t *q_start, *tokens;
+  uint8_t *masked, *block_phase;
+  int32_t *row_pos, *ctx_len, *page_table, *next_block;
+  const int32_t *gen_blocks;
+  int32_t *n_leaving;
+  const uint8_t *stopped;
+  const int32_t *free_pages;
+  int32_t *free_count, *app_src, *app_dst, *n_append;
   int32_t *err;
 };
 
@@ -97,6 +114,8 @@ struct AppendArgs {
 // path: 0 scalar loads, 1 128-bit loads (see commit.cu)
 cudaError_t launch_commit(const CommitArgs &a, int dtype, int path, cudaStream_t s);
 cudaError_t launch_append(const AppendArgs &a, bool vec_ok, cudaStream_t s);
+cudaError_t launch_window(const WindowArgs &a, cudaStream_t s);
+size_t window_smem_bytes(int batch, int capacity, int block_size);
 cudaError_t launch_attn_simt(const AttnArgs &a, int dtype, cudaStream_t s);
 cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t s, char *why, size_t why_len);
 int attn_tc_deep_slots(int cs);  // resident CTAs of the 6-stage head_dim-128 variant

@@ -27,14 +27,16 @@ PHASE_CONSERVATIVE = 0
 PHASE_AGGRESSIVE = 1
 
 STATUS = {0: "D2F_OK", 1: "D2F_ERR_INVALID_ARG", 2: "D2F_ERR_UNSUPPORTED", 3: "D2F_ERR_CUDA",
-          4: "D2F_ERR_BAD_INDEX", 5: "D2F_ERR_TIMEOUT", 6: "D2F_ERR_WORKSPACE"}
+          4: "D2F_ERR_BAD_INDEX", 5: "D2F_ERR_TIMEOUT", 6: "D2F_ERR_WORKSPACE",
+          7: "D2F_ERR_NO_PAGE"}
 
 # Every symbol include/d2f.h declares.
 EXPORTS = ("d2f_version", "d2f_status_string", "d2f_last_error_string",
            "d2f_block_attn_workspace_size", "d2f_block_attn", "d2f_block_attn_append",
            "d2f_block_attn_part",
            "d2f_commit_workspace_size",
-           "d2f_commit", "d2f_commit_metric", "d2f_commit_noalloc", "d2f_kv_append")
+           "d2f_commit", "d2f_commit_metric", "d2f_commit_noalloc", "d2f_kv_append",
+           "d2f_kv_append_dev", "d2f_block_attn_append_dev", "d2f_window_step")
 
 # attention parts of block_attn(part=...) (include/d2f.h D2F_ATTN_*)
 ATTN_ALL, ATTN_CACHED, ATTN_WINDOW = 0, 1, 2
@@ -91,6 +93,16 @@ def load(path=LIB_PATH):
                                         _I, _I, ctypes.c_int32, _P, _P, _P, _I, _P, _P])
     lib.d2f_kv_append.restype = _I
     lib.d2f_kv_append.argtypes = [_P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P]
+    lib.d2f_kv_append_dev.restype = _I
+    lib.d2f_kv_append_dev.argtypes = [_P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _I, _I, _I,
+                                      _P, _P]
+    lib.d2f_block_attn_append_dev.restype = _I
+    lib.d2f_block_attn_append_dev.argtypes = ([_P] * 6 + [_I] + [_P] * 2 + [_P, _P] + [_I] * 10 +
+                                              [ctypes.c_float, _I, _P, _SZ, _P, _P, _P, _I, _P,
+                                               _P])
+    lib.d2f_window_step.restype = _I
+    lib.d2f_window_step.argtypes = ([_I] * 5 + [ctypes.c_int32, ctypes.c_float, ctypes.c_float] +
+                                    [_P] * 18)
     _lib = lib
     return lib
 
@@ -158,10 +170,13 @@ def attn_workspace(device, **kw):
 def block_attn(q, k_win, v_win, k_pool, v_pool, page_table, ctx_len, q_start, *, block_size,
                max_q_per_seq, max_ctx, softmax_scale=None, num_splits=0, out=None, lse=None,
                want_lse=True, workspace=None, err=None, stream=None, append_src_row=None,
-               append_dst_page=None, part=ATTN_ALL, prev_out=None, prev_lse=None):
+               append_dst_page=None, part=ATTN_ALL, prev_out=None, prev_lse=None,
+               append_n_dev=None):
     """Block-causal attention of the window over [paged cache ; window] (one layer).
     With append_src_row / append_dst_page (int32 [n_append]) the finished blocks
     are appended to their pages in the same launch (d2f_block_attn_append).
+    With append_n_dev (int32 [1] on the device, d2f_block_attn_append_dev) the list's
+    length is read there, at most len(append_src_row).
     part ATTN_CACHED / ATTN_WINDOW (d2f_block_attn_part): one part of the keys; the
     window part composes a kept cached part given as prev_out / prev_lse.
 
@@ -203,6 +218,13 @@ def block_attn(q, k_win, v_win, k_pool, v_pool, page_table, ctx_len, q_start, *,
                                        _stream(stream)))
     elif append_src_row is None:
         _check(lib.d2f_block_attn(*args, _ptr(err), _stream(stream)))
+    elif append_n_dev is not None:
+        _dev(append_src_row, "append_src_row", torch.int32)
+        _dev(append_dst_page, "append_dst_page", torch.int32)
+        _dev(append_n_dev, "append_n_dev", torch.int32)
+        _check(lib.d2f_block_attn_append_dev(*args, _ptr(append_src_row), _ptr(append_dst_page),
+                                             _ptr(append_n_dev), append_src_row.shape[0],
+                                             _ptr(err), _stream(stream)))
     else:
         _dev(append_src_row, "append_src_row", torch.int32)
         _dev(append_dst_page, "append_dst_page", torch.int32)
@@ -304,15 +326,73 @@ def commit_noalloc(logits, tokens, masked, q_start, block_phase, tau, *, block_s
 # KV append
 # ---------------------------------------------------------------------------
 def kv_append(k_win, v_win, src_row, dst_page, k_pool, v_pool, *, block_size, err=None,
-              stream=None):
-    """Copy finished blocks (rows src_row[a] .. +B of the window K/V) into pages dst_page[a]."""
+              stream=None, n_append_dev=None):
+    """Copy finished blocks (rows src_row[a] .. +B of the window K/V) into pages dst_page[a].
+    n_append_dev (int32 [1] on the device, d2f_kv_append_dev): the list's length is
+    read there, at most len(src_row)."""
     lib = load()
     for name, t in (("k_win", k_win), ("v_win", v_win), ("k_pool", k_pool), ("v_pool", v_pool)):
         _dev(t, name, k_win.dtype)
     _dev(src_row, "src_row", torch.int32)
     _dev(dst_page, "dst_page", torch.int32)
     total_q, hkv, d = k_win.shape
+    if n_append_dev is not None:
+        _dev(n_append_dev, "n_append_dev", torch.int32)
+        _check(lib.d2f_kv_append_dev(
+            _ptr(k_win), _ptr(v_win), _ptr(src_row), _ptr(dst_page), _ptr(n_append_dev),
+            src_row.shape[0], total_q, _ptr(k_pool), _ptr(v_pool), hkv, d, block_size,
+            k_pool.shape[0], _dtype_code(k_win), _ptr(err), _stream(stream)))
+        return
     _check(lib.d2f_kv_append(
         _ptr(k_win), _ptr(v_win), _ptr(src_row), _ptr(dst_page), src_row.shape[0], total_q,
         _ptr(k_pool), _ptr(v_pool), hkv, d, block_size, k_pool.shape[0], _dtype_code(k_win),
         _ptr(err), _stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# pipelined window scheduler
+# ---------------------------------------------------------------------------
+class WindowState:
+    """Device buffers of the window scheduler (d2f_window_step), one attribute per
+    argument of that name: q_start, tokens, masked, block_phase, row_pos,
+    ctx_len, page_table, next_block, gen_blocks, n_leaving, stopped, free_pages,
+    free_count, app_src, app_dst, n_append. Created empty (no window, nothing
+    listed); the caller fills ctx_len / page_table (prompt pages), gen_blocks
+    and the free list."""
+
+    def __init__(self, device, *, batch, block_size, max_blocks, max_pages_per_seq, num_free,
+                 mask_id, capacity=None):
+        i32 = dict(dtype=torch.int32, device=device)
+        u8 = dict(dtype=torch.uint8, device=device)
+        cap = batch * max_blocks * block_size if capacity is None else capacity
+        self.batch, self.block_size, self.max_blocks, self.capacity = (batch, block_size,
+                                                                       max_blocks, cap)
+        self.mask_id = mask_id
+        self.q_start = torch.zeros(batch + 1, **i32)
+        self.tokens = torch.full((cap,), mask_id, **i32)
+        self.masked = torch.zeros(cap, **u8)
+        self.block_phase = torch.zeros(max(cap // block_size, 1), **u8)
+        self.row_pos = torch.full((cap,), -1, **i32)
+        self.ctx_len = torch.zeros(batch, **i32)
+        self.page_table = torch.full((batch, max_pages_per_seq), -1, **i32)
+        self.next_block = torch.zeros(batch, **i32)
+        self.gen_blocks = torch.zeros(batch, **i32)
+        self.n_leaving = torch.zeros(batch, **i32)
+        self.stopped = torch.zeros(batch, **u8)
+        self.free_pages = torch.zeros(max(num_free, 1), **i32)
+        self.free_count = torch.zeros(1, **i32)
+        self.app_src = torch.zeros(max(cap // block_size, 1), **i32)
+        self.app_dst = torch.zeros_like(self.app_src)
+        self.n_append = torch.zeros(1, **i32)
+
+
+def window_step(st, *, tau_add, tau_act, err=None, stream=None, use_stopped=True):
+    """One call of the device window scheduler on WindowState `st` (in place)."""
+    lib = load()
+    _check(lib.d2f_window_step(
+        st.batch, st.block_size, st.max_blocks, st.capacity, st.page_table.shape[1],
+        int(st.mask_id), float(tau_add), float(tau_act), _ptr(st.q_start), _ptr(st.tokens),
+        _ptr(st.masked), _ptr(st.block_phase), _ptr(st.row_pos), _ptr(st.ctx_len),
+        _ptr(st.page_table), _ptr(st.next_block), _ptr(st.gen_blocks), _ptr(st.n_leaving),
+        _ptr(st.stopped) if use_stopped else None, _ptr(st.free_pages), _ptr(st.free_count),
+        _ptr(st.app_src), _ptr(st.app_dst), _ptr(st.n_append), _ptr(err), _stream(stream)))

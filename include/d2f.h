@@ -58,7 +58,9 @@ typedef enum d2f_status {
   D2F_ERR_CUDA = 3,        /* a CUDA runtime / launch error                      */
   D2F_ERR_BAD_INDEX = 4,   /* device: page id / row index out of range          */
   D2F_ERR_TIMEOUT = 5,     /* device: a bounded wait gave up                     */
-  D2F_ERR_WORKSPACE = 6    /* workspace missing or smaller than required         */
+  D2F_ERR_WORKSPACE = 6,   /* workspace missing or smaller than required         */
+  D2F_ERR_NO_PAGE = 7      /* device: a finished block got no page (free list    */
+                           /* empty or its page-table row full); it stays put    */
 } d2f_status;
 
 typedef enum d2f_dtype { D2F_BF16 = 0, D2F_F32 = 1 } d2f_dtype;
@@ -356,6 +358,110 @@ int d2f_kv_append(const void *k_win, const void *v_win, const int32_t *src_row,
                   const int32_t *dst_page, int n_append, int total_q, void *k_pool,
                   void *v_pool, int num_heads_kv, int head_dim, int block_size, int num_pages,
                   int dtype, int32_t *err_word, void *stream);
+
+/*
+ * d2f_kv_append_dev -- d2f_kv_append whose list length lives in device memory
+ * (written by d2f_window_step), so that no host readback sits between steps.
+ *
+ *   n_append_dev  device int32 [1]: entries of src_row / dst_page to apply, read
+ *                 on the device; values above max_append are taken as max_append,
+ *                 negative ones as 0. max_append >= 0 sizes the launch.
+ * Everything else as d2f_kv_append.
+ */
+int d2f_kv_append_dev(const void *k_win, const void *v_win, const int32_t *src_row,
+                      const int32_t *dst_page, const int32_t *n_append_dev, int max_append,
+                      int total_q, void *k_pool, void *v_pool, int num_heads_kv, int head_dim,
+                      int block_size, int num_pages, int dtype, int32_t *err_word, void *stream);
+
+/*
+ * d2f_block_attn_append_dev -- d2f_block_attn_append whose list length lives in
+ * device memory (n_append_dev, at most max_append entries, as d2f_kv_append_dev).
+ */
+int d2f_block_attn_append_dev(const void *q, const void *k_win, const void *v_win,
+                              const void *k_pool, const void *v_pool, const int32_t *page_table,
+                              int max_pages_per_seq, const int32_t *ctx_len,
+                              const int32_t *q_start, void *out, float *lse_out, int batch,
+                              int total_q, int max_q_per_seq, int max_ctx, int num_heads_q,
+                              int num_heads_kv, int head_dim, int block_size, int num_pages,
+                              int dtype, float softmax_scale, int num_splits, void *workspace,
+                              size_t workspace_bytes, const int32_t *src_row,
+                              const int32_t *dst_page, const int32_t *n_append_dev,
+                              int max_append, int32_t *err_word, void *stream);
+
+/* ------------------------------------------------------------------------- */
+/* Pipelined window scheduler                                               */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * d2f_window_step -- between two decode steps, on the device: turn the state the
+ * commit left into the window, phases, append list and cache bookkeeping of the
+ * next step, so a whole step (attention with its appends, commit, scheduler)
+ * replays from one CUDA graph with no host readback.
+ *
+ * [P2] §쉽게 이해하기 (pipelined parallel decoding): an active window of blocks;
+ * once the last block's progress passes a threshold a new block enters behind
+ * it; a new block is conservative and turns aggressive once the block before it
+ * has progressed enough; uncommitted positions stay masked. [P1] §운영 관점: a
+ * completed block is persisted to the paged cache (completion is the signal).
+ *
+ * Rule (readings of the pages, which give no values and no order):
+ *  - progress of a block = its committed positions c out of B. A new block
+ *    enters a sequence's window when c(last block) > tau_add * B, or the window is
+ *    empty, and next_block < gen_blocks, the window holds fewer than max_blocks
+ *    blocks and the sequence is not stopped; at most one per step.
+ *  - block k of the new window is aggressive (phase 1) when the block before it
+ *    has c >= tau_act * B; the block before the oldest is the cache (c = B).
+ *  - complete blocks forming the oldest prefix of the window are listed for the
+ *    next step's append (its forward pass computes their K/V from final tokens);
+ *    they stay in the window for that step and leave at the next call (their
+ *    count is n_leaving), when ctx_len grows by B each.
+ *  - pages come from the top of the free list, free_pages[*free_count - 1] first,
+ *    in (sequence, block) order; the page of the i-th listed block of sequence b
+ *    is written to page_table[b][ctx_len[b] / B + i] at once. A block that gets no
+ *    page (list empty or page-table row full) stays in the window, listed again
+ *    later, and err_word takes D2F_ERR_NO_PAGE.
+ *  - the products tau * B and the comparisons are float.
+ *
+ * Layout: the window rows of sequence b are q_start[b] .. q_start[b+1]-1, block by
+ * block, oldest first, as every other entry point takes them. capacity rows are
+ * allocated; capacity % block_size == 0 and capacity >= batch * max_blocks *
+ * block_size, so the window always fits. All pointers are device memory owned by
+ * the caller; in/out unless said:
+ *   q_start      int32 [batch+1]
+ *   tokens       int32 [capacity];  masked uint8 [capacity]
+ *   block_phase  uint8 [capacity / block_size] (out)
+ *   row_pos      int32 [capacity] (out): position of the row's token in its
+ *                sequence (ctx_len + offset in the window), -1 past the window
+ *   ctx_len      int32 [batch]; page_table int32 [batch][max_pages_per_seq]
+ *   next_block   int32 [batch]: generation blocks that have entered so far
+ *   gen_blocks   int32 [batch] (in): generation blocks of each sequence
+ *   n_leaving    int32 [batch]: blocks listed for append by the previous call
+ *   stopped      uint8 [batch] (in, may be NULL): the early commit's flags
+ *   free_pages   int32 [>= *free_count] (in); free_count int32 [1]
+ *   app_src, app_dst  int32 [capacity / block_size] (out); n_append int32 [1] (out):
+ *                the next step's append list (first window row of the block in the
+ *                new layout, its page), for d2f_block_attn_append_dev or
+ *                d2f_kv_append_dev
+ * Rows past the new window read tokens = mask_id, masked = 0, row_pos = -1 and
+ * their blocks phase 0, so the commit skips them. A sequence is finished when its
+ * window is empty after a call. ctx_len must be a multiple of block_size (pad the
+ * prompt).
+ *
+ * Errors: D2F_ERR_INVALID_ARG for bad sizes (host), or, in err_word, for a state
+ * that is not consistent (a window not made of whole blocks, beyond capacity or
+ * longer than max_blocks, n_leaving larger than the window, ctx_len negative or
+ * not a multiple of block_size, q_start[0] != 0, *free_count < 0): then nothing is
+ * written. D2F_ERR_UNSUPPORTED when the state does not fit one CTA's shared
+ * memory (about 5 bytes per capacity row + 36 per sequence, 227 KB in all) or
+ * block_size > 128.
+ */
+int d2f_window_step(int batch, int block_size, int max_blocks, int capacity,
+                    int max_pages_per_seq, int32_t mask_id, float tau_add, float tau_act,
+                    int32_t *q_start, int32_t *tokens, uint8_t *masked, uint8_t *block_phase,
+                    int32_t *row_pos, int32_t *ctx_len, int32_t *page_table, int32_t *next_block,
+                    const int32_t *gen_blocks, int32_t *n_leaving, const uint8_t *stopped,
+                    const int32_t *free_pages, int32_t *free_count, int32_t *app_src,
+                    int32_t *app_dst, int32_t *n_append, int32_t *err_word, void *stream);
 
 #ifdef __cplusplus
 }
