@@ -58,6 +58,15 @@ def parse():
                          "composed with a kept cached part (d2f_block_attn_part); the cached "
                          "part is computed once per input set, before the timed region, and "
                          "timed on its own")
+    ap.add_argument("--scheduler", action="store_true",
+                    help="the step of a device-driven decode: attention (appending the listed "
+                         "blocks, d2f_block_attn_append_dev), commit and the window scheduler "
+                         "(d2f_window_step), the scheduler's state reset per step")
+    ap.add_argument("--tau-add", type=float, default=0.5,
+                    help="window scheduler: progress of the last block that lets a block enter")
+    ap.add_argument("--tau-act", type=float, default=1.0,
+                    help="window scheduler: progress of the block before that makes a block "
+                         "aggressive")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -352,6 +361,11 @@ def workload_config(p, args):
         extra["early_commit_gap"] = args.early_gap
     if args.fused_append and w.appends_per_seq:
         extra["append"] = "fused into the attention (d2f_block_attn_append)"
+    if args.scheduler:
+        extra["scheduler"] = ("d2f_window_step after the commit (tau_add %g, tau_act %g); the "
+                              "append of listed blocks inside the attention "
+                              "(d2f_block_attn_append_dev); the scheduler's state starts every "
+                              "step from the same device snapshot" % (args.tau_add, args.tau_act))
     if args.reuse_cached:
         extra["attention"] = ("window part composed with a kept cached part (d2f_block_attn_part): "
                               "a step inside a block's denoising, no append; the cached part of "
@@ -392,6 +406,57 @@ class StepSet:
                    (self.q, self.k_win, self.v_win, self.k_pool, self.v_pool, self.logits, self.out))
 
 
+def sched_snapshot(p, dev, W):
+    """The window scheduler's state at the start of a step of problem `p`: its
+    layout, its phases, its cache bookkeeping and the appends listed for the step.
+    Returns (int32 row, uint8 row, {field: (offset, shape)}, constants)."""
+    w = p.w
+    B, batch, cap = w.block_size, w.batch, w.total_q
+    maxp = p.page_table.shape[1] + W + 1
+    pt = torch.full((batch, maxp), -1, dtype=torch.int32)
+    pt[:, :p.page_table.shape[1]] = p.page_table.cpu()
+    src, dst = p.src_row.cpu(), p.dst_page.cpu()
+    qs = p.q_start.cpu()
+    leaving = torch.zeros(batch, dtype=torch.int32)
+    for r in src.tolist():
+        leaving[int(torch.searchsorted(qs, torch.tensor(r), right=True)) - 1] += 1
+    app_src = torch.zeros(cap // B, dtype=torch.int32)
+    app_dst = torch.zeros(cap // B, dtype=torch.int32)
+    app_src[:len(src)], app_dst[:len(dst)] = src, dst
+    parts = [("q_start", qs.to(torch.int32)), ("ctx_len", p.ctx_len.cpu().to(torch.int32)),
+             ("page_table", pt),
+             ("next_block", torch.tensor(w.window_blocks, dtype=torch.int32)),
+             ("n_leaving", leaving), ("free_count", torch.tensor([p.k_pool.shape[0]],
+                                                                 dtype=torch.int32)),
+             ("app_src", app_src), ("app_dst", app_dst),
+             ("n_append", torch.tensor([len(src)], dtype=torch.int32)),
+             ("row_pos", torch.full((cap,), -1, dtype=torch.int32))]
+    fields, off, rows = {}, 0, []
+    for name, t in parts:
+        fields[name] = (off, tuple(t.shape))
+        off += t.numel()
+        rows.append(t.reshape(-1))
+    const = {"gen_blocks": torch.tensor([wb + 10 ** 6 for wb in w.window_blocks],
+                                        dtype=torch.int32, device=dev),
+             "free_pages": torch.arange(p.k_pool.shape[0], dtype=torch.int32, device=dev)}
+    return (torch.cat(rows).to(dev), p.block_phase.cpu().to(torch.uint8).to(dev), fields, const)
+
+
+def sched_views(tokens, masked, i32, u8, fields, const, p, W):
+    """A d2f.window_step state whose fields are views of one int32 and one uint8 row."""
+    from types import SimpleNamespace
+    w = p.w
+    st = SimpleNamespace(batch=w.batch, block_size=w.block_size, max_blocks=W,
+                         capacity=w.total_q, mask_id=p.mask_id, tokens=tokens, masked=masked,
+                         block_phase=u8, stopped=None, **const)
+    for name, (off, shape) in fields.items():
+        n = 1
+        for x in shape:
+            n *= x
+        setattr(st, name, i32[off:off + n].view(shape))
+    return st
+
+
 def run_ours(args, world, rank, local):
     from block_causal_kv_gb300 import d2f, synth
     import __graft_entry__
@@ -415,9 +480,14 @@ def run_ours(args, world, rank, local):
     for i, st in enumerate(sets):
         st.tokens, st.masked = tokens_all[i], masked_all[i]
     reuse = args.reuse_cached
+    sched = args.scheduler
     if reuse and args.fused_append:
         raise SystemExit("--reuse-cached times steps without an append: drop --fused-append")
-    fused = args.fused_append and len(p.src_row) > 0
+    if sched and (reuse or args.fused_append):
+        raise SystemExit("--scheduler appends inside the attention by itself; it goes alone")
+    if sched and w.total_q != w.batch * max(w.window_blocks) * B:
+        raise SystemExit("--scheduler takes workloads whose windows all hold the same blocks")
+    fused = (args.fused_append or sched) and len(p.src_row) > 0
     appends = len(p.src_row) > 0 and not fused and not reuse
 
     dcode = d2f.F32 if w.dtype == torch.float32 else d2f.BF16
@@ -432,17 +502,38 @@ def run_ours(args, world, rank, local):
     amax = torch.empty(w.total_q, dtype=torch.int32, device=dev)
     rem = torch.empty(w.total_q // B, dtype=torch.int32, device=dev)
 
+    # the scheduler's state (one int32 and one uint8 row per input set, so that one
+    # copy of each resets every set)
+    if sched:
+        Wmax = max(w.window_blocks)
+        sched_i32_0, sched_u8_0, sched_fields, sched_const = sched_snapshot(p, dev, Wmax)
+        sched_i32_rep = sched_i32_0.repeat(n_sets, 1)
+        sched_u8_rep = sched_u8_0.repeat(n_sets, 1)
+        sched_i32_all, sched_u8_all = sched_i32_rep.clone(), sched_u8_rep.clone()
+        for i, st in enumerate(sets):
+            st.ws = sched_views(st.tokens, st.masked, sched_i32_all[i], sched_u8_all[i],
+                                sched_fields, sched_const, p, Wmax)
+
     def attn(s):
+        pt, cl, qs = s.page_table, s.ctx_len, s.q_start
         if reuse:
             kw = dict(part=d2f.ATTN_WINDOW, prev_out=s.prev_out, prev_lse=s.prev_lse)
+        elif sched:
+            pt, cl, qs = s.ws.page_table, s.ws.ctx_len, s.ws.q_start
+            kw = dict(append_src_row=s.ws.app_src, append_dst_page=s.ws.app_dst,
+                      append_n_dev=s.ws.n_append)
         elif fused:
             kw = dict(append_src_row=s.src_row, append_dst_page=s.dst_page)
         else:
             kw = {}
-        d2f.block_attn(s.q, s.k_win, s.v_win, s.k_pool, s.v_pool, s.page_table, s.ctx_len,
-                       s.q_start, block_size=B, max_q_per_seq=p.max_q_per_seq, max_ctx=p.max_ctx,
+        d2f.block_attn(s.q, s.k_win, s.v_win, s.k_pool, s.v_pool, pt, cl, qs, block_size=B,
+                       max_q_per_seq=p.max_q_per_seq, max_ctx=p.max_ctx,
                        num_splits=args.num_splits, out=s.out, want_lse=False, workspace=ws_attn,
                        err=err, **kw)
+
+    def window(s):
+        d2f.window_step(s.ws, tau_add=args.tau_add, tau_act=args.tau_act, err=err,
+                        use_stopped=False)
 
     def cached_part(s):
         d2f.block_attn(s.q, s.k_win, s.v_win, s.k_pool, s.v_pool, s.page_table, s.ctx_len,
@@ -463,7 +554,8 @@ def run_ours(args, world, rank, local):
         stopped = torch.zeros(w.batch, dtype=torch.uint8, device=dev)
 
     def commit(s):
-        d2f.commit(s.logits, s.tokens, s.masked, s.q_start, s.block_phase, s.tau, block_size=B,
+        qs, ph = (s.ws.q_start, s.ws.block_phase) if sched else (s.q_start, s.block_phase)
+        d2f.commit(s.logits, s.tokens, s.masked, qs, ph, s.tau, block_size=B,
                    mask_id=p.mask_id, num_splits=args.commit_splits, conf=conf, argmax=amax,
                    block_remaining=rem, workspace=ws_commit, err=err,
                    metric=CONF_METRICS[args.conf_metric], early_gap=early_gap, stopped=stopped)
@@ -475,20 +567,31 @@ def run_ours(args, world, rank, local):
     def reset_all():
         tokens_all.copy_(tokens0)
         masked_all.copy_(masked0)
+        if sched:
+            sched_i32_all.copy_(sched_i32_rep)
+            sched_u8_all.copy_(sched_u8_rep)
 
     def reset(s):
         i = sets.index(s)
         s.tokens.copy_(tokens0[i])
         s.masked.copy_(masked0[i])
+        if sched:
+            sched_i32_all[i].copy_(sched_i32_0)
+            sched_u8_all[i].copy_(sched_u8_0)
+
+    def step_kernels(s):
+        attn(s)
+        commit(s)
+        if appends:
+            append(s)
+        if sched:
+            window(s)
 
     if args.profile_steps:
         for i in range(args.profile_steps):
             s = sets[i % n_sets]
             reset(s)
-            attn(s)
-            commit(s)
-            if appends:
-                append(s)
+            step_kernels(s)
         torch.cuda.synchronize()
         assert int(err.item()) == 0, "device error %d" % int(err.item())
         return
@@ -499,10 +602,7 @@ def run_ours(args, world, rank, local):
         for i in range(max(3, min(args.warmup, n_sets))):
             s = sets[i % n_sets]
             reset(s)
-            attn(s)
-            commit(s)
-            if appends:
-                append(s)
+            step_kernels(s)
     stream.synchronize()
 
     def capture(indices):
@@ -514,10 +614,7 @@ def run_ours(args, world, rank, local):
                 s = sets[i]
                 if len(indices) != n_sets:
                     reset(s)
-                attn(s)
-                commit(s)
-                if appends:
-                    append(s)
+                step_kernels(s)
         return g
 
     g_all = capture(range(n_sets))
@@ -570,11 +667,12 @@ def run_ours(args, world, rank, local):
     # would add their own latency to every bracket.)
     per_kernel = {}
     kernel_fns = [("attn", attn), ("commit", commit)] + ([("append", append)] if appends else []) \
-        + ([("cached_part", cached_part)] if reuse else [])
+        + ([("cached_part", cached_part)] if reuse else []) \
+        + ([("window", window)] if sched else [])
     for which, fn in kernel_fns:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
-            if which == "commit":
+            if which in ("commit", "window"):
                 reset_all()
             for i in range(n_sets):
                 fn(sets[i])
@@ -591,7 +689,8 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         per_kernel[which] = a.elapsed_time(b) * 1000.0 / (reps * n_sets)
     step_us = elapsed_ms * 1000.0 / K
-    attn_in_step = step_us - per_kernel["commit"] - per_kernel.get("append", 0.0)
+    attn_in_step = (step_us - per_kernel["commit"] - per_kernel.get("append", 0.0)
+                    - per_kernel.get("window", 0.0))
     attn_us, commit_us = [attn_in_step], [per_kernel["commit"]]
 
     steps_total = K * world
@@ -618,6 +717,9 @@ def run_ours(args, world, rank, local):
         kernels["cached_part"] = {"us": t_cp, "bytes": cb, "GB/s": cb / t_cp / 1e3,
                                   "frac": cb / t_cp / 1e3 / hbm,
                                   "note": "once per cache change (a finished block), not per step"}
+    if sched:
+        kernels["window_step"] = {"us": per_kernel["window"],
+                                  "note": "one CTA; integer work on a few KB of state"}
     if appends:
         t_app = per_kernel["append"]
         kernels["kv_append"] = {"us": t_app, "bytes": append_b, "GB/s": append_b / t_app / 1e3,
@@ -639,8 +741,20 @@ def run_ours(args, world, rank, local):
     # end to end through the C ABI from pinned host buffers
     e2e = None
     if not args.no_e2e:
+        hooks = None
+        if sched:
+            def make_ws(d):
+                d.ws_i32, d.ws_u8 = sched_i32_0.clone(), sched_u8_0.clone()
+                d.ws = sched_views(d.tokens, d.masked, d.ws_i32, d.ws_u8, sched_fields,
+                                   sched_const, p, Wmax)
+
+            def pre_step(d):
+                d.ws_i32.copy_(sched_i32_0)
+                d.ws_u8.copy_(sched_u8_0)
+
+            hooks = (make_ws, pre_step, window)
         e2e = run_e2e(p, dev, sets[0], attn, commit, append if appends else None, K, stream,
-                      tokens0[0], masked0[0])
+                      tokens0[0], masked0[0], hooks)
 
     line = {"metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": K,
             "warmup": W, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -655,7 +769,7 @@ def run_ours(args, world, rank, local):
                            attn_splits=args.num_splits or "auto",
                            commit_splits=args.commit_splits or "auto"),
             "roofline": roofline, "kernels": kernels,
-            "gpu_launches": K * (2 + (1 if appends else 0)),
+            "gpu_launches": K * (2 + (1 if appends else 0) + (1 if sched else 0)),
             "clocks": clocks, "e2e": e2e}
     if rank == 0 and not args.no_cpu_baseline:
         value_cpu, sample = time_oracle(p if p.q.device.type == "cpu" else p.to("cpu"),
@@ -667,7 +781,7 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def run_e2e(p, dev, s, attn, commit, append, K, stream, tokens0, masked0):
+def run_e2e(p, dev, s, attn, commit, append, K, stream, tokens0, masked0, hooks=None):
     """Same step through the public API with host inputs: every step copies its
     inputs (Q, window K/V, logits, decode state) from pinned host memory and
     reads back its results (output, tokens, masked). The inputs of a step travel
@@ -704,6 +818,8 @@ def run_e2e(p, dev, s, attn, commit, append, K, stream, tokens0, masked0):
         d.out = torch.empty_like(s.out)
         d.ready = torch.cuda.Event()   # inputs landed
         d.read = torch.cuda.Event()    # results read back
+        if hooks:
+            hooks[0](d)                # its own scheduler state over its tokens / masked
         dsets.append(d)
     h_out = torch.empty(s.out.shape, dtype=s.out.dtype).pin_memory()
     h_tok_o = torch.empty(tokens0.shape, dtype=tokens0.dtype).pin_memory()
@@ -722,10 +838,14 @@ def run_e2e(p, dev, s, attn, commit, append, K, stream, tokens0, masked0):
             d.ready.record(cstream)
         with torch.cuda.stream(stream):
             stream.wait_event(d.ready)
+            if hooks:
+                hooks[1](d)            # the scheduler's state of the step (device copy)
             attn(d)
             commit(d)
             if append:
                 append(d)
+            if hooks:
+                hooks[2](d)
             # results back right after the kernels (on this stream, so the copy
             # stream stays free for the next step's inputs)
             h_out.copy_(d.out, non_blocking=True)

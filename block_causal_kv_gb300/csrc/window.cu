@@ -11,9 +11,10 @@
 //
 // One CTA does it all: the work is a few integers per sequence and a few bytes
 // per window row, and a single CTA can order the whole step with __syncthreads:
-//   1. check the state (nothing is written if it is inconsistent);
-//   2. stage the old window rows in shared memory and count each block's
-//      committed positions;
+//   1. bring the whole state into shared memory in one wave of loads (the top of
+//      the free list follows, its latency hidden behind steps 2-4);
+//   2. check the state (nothing is written if it is inconsistent) and count each
+//      old block's committed positions;
 //   3. decide per sequence: blocks leaving, a block entering, blocks to append;
 //   4. one block-wide exclusive scan gives the new layout (blocks before each
 //      sequence) and the pages before each sequence's appends, so pages come off
@@ -78,46 +79,60 @@ __global__ void __launch_bounds__(kThreads, 1) window_kernel(const WindowArgs a)
   const int B = a.block_size, batch = a.batch, cap = a.capacity;
   const int tid = threadIdx.x;
   // shared layout: scan totals, per-sequence arrays, then rows (window_smem_bytes)
-  int2 *s_warp = reinterpret_cast<int2 *>(smem);                  // [kThreads / 32 + 1]
+  int2 *s_warp = reinterpret_cast<int2 *>(smem);                      // [kThreads / 32 + 1]
   int *s_qold = reinterpret_cast<int *>(s_warp + kThreads / 32 + 1);  // [batch + 1]
-  int *s_qnew = s_qold + (batch + 1);                             // [batch + 1] in blocks
-  int *s_abase = s_qnew + (batch + 1);                            // [batch] pages before b
-  SeqDecision *s_dec = reinterpret_cast<SeqDecision *>(s_abase + batch);
-  int32_t *s_tok = reinterpret_cast<int32_t *>(s_dec + batch);    // [cap]
-  uint8_t *s_msk = reinterpret_cast<uint8_t *>(s_tok + cap);      // [cap]
-  uint8_t *s_cnt = s_msk + cap;                                   // [cap / B]
-  __shared__ int s_bad, s_free;
+  int *s_qnew = s_qold + (batch + 1);                                 // [batch + 1] in blocks
+  int *s_abase = s_qnew + (batch + 1);                                // [batch] pages before b
+  int *s_nl = s_abase + batch;                                        // [batch] n_leaving
+  int *s_ctx = s_nl + batch;                                          // [batch] ctx_len
+  int *s_nb = s_ctx + batch;                                          // [batch] next_block
+  int *s_gen = s_nb + batch;                                          // [batch] gen_blocks
+  int *s_fp = s_gen + batch;                                          // [kThreads] list top
+  SeqDecision *s_dec = reinterpret_cast<SeqDecision *>(s_fp + kThreads);
+  int32_t *s_tok = reinterpret_cast<int32_t *>(s_dec + batch);        // [cap]
+  uint8_t *s_msk = reinterpret_cast<uint8_t *>(s_tok + cap);          // [cap]
+  uint8_t *s_cnt = s_msk + cap;                                       // [cap / B]
+  uint8_t *s_stop = s_cnt + cap / B;                                  // [batch]
+  __shared__ int s_free;
 
   grid_launch_dependents();
   grid_dependency_wait();  // the commit (or the caller) wrote the state
 
-  // ---- 1. consistency of the state -------------------------------------------
-  if (tid == 0) {
-    s_free = a.free_count[0];
-    s_bad = (a.q_start[0] != 0 || s_free < 0) ? 1 : 0;
-  }
+  // ---- 1. the whole state in one wave of independent loads ----------------------
+  if (tid == 0) s_free = a.free_count[0];
   for (int b = tid; b <= batch; b += kThreads) s_qold[b] = a.q_start[b];
-  __syncthreads();
-  int bad = 0;
   for (int b = tid; b < batch; b += kThreads) {
-    const int n = s_qold[b + 1] - s_qold[b];
-    const int nl = a.n_leaving[b], ctx = a.ctx_len[b];
-    bad |= n < 0 || n % B != 0 || n / B > a.max_blocks || s_qold[b + 1] > cap || nl < 0 ||
-           nl > n / B || ctx < 0 || ctx % B != 0;
+    s_nl[b] = a.n_leaving[b];
+    s_ctx[b] = a.ctx_len[b];
+    s_nb[b] = a.next_block[b];
+    s_gen[b] = a.gen_blocks[b];
+    s_stop[b] = a.stopped != nullptr ? a.stopped[b] : 0;
   }
-  bad = __syncthreads_or(bad) | s_bad;
-  if (bad) {
-    if (tid == 0) set_err(a.err, D2F_ERR_INVALID_ARG);
-    return;
-  }
-
-  // ---- 2. stage the old rows, count committed positions per block ------------
-  const int old_rows = s_qold[batch];
-  for (int r = tid; r < old_rows; r += kThreads) {
+  for (int r = tid; r < cap; r += kThreads) {
     s_tok[r] = a.tokens[r];
     s_msk[r] = a.masked[r];
   }
   __syncthreads();
+  // The top of the free list, loaded now and stored to shared memory only after
+  // the checks and decisions below, which hide its latency.
+  const int free0 = s_free;
+  const int n_pre = min(max(free0, 0), min(kThreads, cap / B));
+  const int fp = tid < n_pre ? a.free_pages[free0 - 1 - tid] : 0;
+
+  // ---- 2. consistency of the state (nothing is written if it fails) --------------
+  int bad = tid == 0 && (s_qold[0] != 0 || free0 < 0);
+  for (int b = tid; b < batch; b += kThreads) {
+    const int n = s_qold[b + 1] - s_qold[b];
+    bad |= n < 0 || n % B != 0 || n / B > a.max_blocks || s_qold[b + 1] > cap || s_nl[b] < 0 ||
+           s_nl[b] > n / B || s_ctx[b] < 0 || s_ctx[b] % B != 0;
+  }
+  if (__syncthreads_or(bad)) {
+    if (tid == 0) set_err(a.err, D2F_ERR_INVALID_ARG);
+    return;
+  }
+
+  // ---- 2b. committed positions of every old block --------------------------------
+  const int old_rows = s_qold[batch];
   for (int jb = tid; jb < old_rows / B; jb += kThreads) {
     int c = 0;
     for (int u = 0; u < B; ++u) c += s_msk[jb * B + u] == 0;
@@ -125,19 +140,18 @@ __global__ void __launch_bounds__(kThreads, 1) window_kernel(const WindowArgs a)
   }
   __syncthreads();
 
-  // ---- 3. per-sequence decisions (each thread a contiguous chunk) -------------
+  // ---- 3. per-sequence decisions (each thread a contiguous chunk) -----------------
   const int chunk = (batch + kThreads - 1) / kThreads;
   const int b0 = min(batch, tid * chunk), b1 = min(batch, b0 + chunk);
   int my_blocks = 0, my_want = 0;
   for (int b = b0; b < b1; ++b) {
     SeqDecision d;
     const int nblk = (s_qold[b + 1] - s_qold[b]) / B;
-    const int nl = a.n_leaving[b];
-    d.ctx = a.ctx_len[b] + nl * B;
+    const int nl = s_nl[b];
+    d.ctx = s_ctx[b] + nl * B;
     d.first = s_qold[b] / B + nl;
     d.surv = nblk - nl;
-    const bool stopped = a.stopped != nullptr && a.stopped[b] != 0;
-    int add = !stopped && a.next_block[b] < a.gen_blocks[b] && d.surv < a.max_blocks;
+    int add = !s_stop[b] && s_nb[b] < s_gen[b] && d.surv < a.max_blocks;
     if (add && d.surv > 0) add = (float)s_cnt[d.first + d.surv - 1] > a.tau_add * (float)B;
     d.add = add;
     int want = 0;
@@ -150,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1) window_kernel(const WindowArgs a)
     my_want += d.want;
   }
 
-  // ---- 4. layout and page bases ----------------------------------------------
+  // ---- 4. layout and page bases -------------------------------------------------
   int ex_blocks, ex_want, tot_blocks, tot_want;
   block_scan2(my_blocks, my_want, ex_blocks, ex_want, tot_blocks, tot_want, s_warp);
   for (int b = b0; b < b1; ++b) {
@@ -160,10 +174,10 @@ __global__ void __launch_bounds__(kThreads, 1) window_kernel(const WindowArgs a)
     ex_want += s_dec[b].want;
   }
   if (tid == 0) s_qnew[batch] = tot_blocks;
+  if (tid < n_pre) s_fp[tid] = fp;
   __syncthreads();
 
-  // ---- 5. per-sequence state, append list, phases ----------------------------
-  const int free0 = s_free;
+  // ---- 5. per-sequence state, append list, phases --------------------------------
   for (int b = b0; b < b1; ++b) {
     const SeqDecision d = s_dec[b];
     const int row0 = s_qnew[b] * B;
@@ -172,14 +186,14 @@ __global__ void __launch_bounds__(kThreads, 1) window_kernel(const WindowArgs a)
     if (granted < d.want || d.short_) set_err(a.err, D2F_ERR_NO_PAGE);
     for (int i = 0; i < granted; ++i) {
       const int slot = s_abase[b] + i;
-      const int page = a.free_pages[free0 - 1 - slot];
+      const int page = slot < n_pre ? s_fp[slot] : a.free_pages[free0 - 1 - slot];
       a.page_table[(int64_t)b * a.max_pages_per_seq + d.ctx / B + i] = page;
       a.app_src[slot] = row0 + i * B;
       a.app_dst[slot] = page;
     }
     a.n_leaving[b] = granted;
     a.ctx_len[b] = d.ctx;
-    a.next_block[b] += d.add;
+    a.next_block[b] = s_nb[b] + d.add;
     a.q_start[b] = row0;
     for (int k = 0; k < d.surv + d.add; ++k) {
       const int pred = k == 0 ? B : (k - 1 < d.surv ? (int)s_cnt[d.first + k - 1] : 0);
@@ -193,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) window_kernel(const WindowArgs a)
     a.n_append[0] = n_app;
   }
 
-  // ---- 6. rows of the new window (and the idle rows past it) -----------------
+  // ---- 6. rows of the new window (and the idle rows past it) ----------------------
   const int new_rows = tot_blocks * B;
   for (int r = tid; r < cap; r += kThreads) {
     int32_t tok = a.mask_id, pos = -1;
@@ -227,9 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1) window_kernel(const WindowArgs a)
 }  // namespace
 
 size_t window_smem_bytes(int batch, int capacity, int block_size) {
-  size_t b = (size_t)(batch + 1) * 2 * sizeof(int) + (size_t)batch * sizeof(int) +
-             (size_t)batch * sizeof(SeqDecision) + (kThreads / 32 + 1) * sizeof(int2);
-  b += (size_t)capacity * (sizeof(int32_t) + 1) + (size_t)(capacity / block_size);
+  size_t b = (kThreads / 32 + 1) * sizeof(int2) + (size_t)(batch + 1) * 2 * sizeof(int) +
+             (size_t)batch * 5 * sizeof(int) + kThreads * sizeof(int) +
+             (size_t)batch * sizeof(SeqDecision);
+  b += (size_t)capacity * (sizeof(int32_t) + 1) + (size_t)(capacity / block_size) + batch;
   return (b + 15) & ~(size_t)15;
 }
 
