@@ -280,14 +280,12 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
   grid_launch_dependents();
   grid_dependency_wait();  // logits / state may come from the previous kernel
   if (tid == 0) D2F_TRACE_MARK(1, 1);
-  // Rows past the last window (a launch sized for a capacity, the layout written
-  // on the device): the whole block leaves before touching any counter.
-  if (jb * B >= __ldg(a.q_start + a.batch)) return;
 
   // Decision metadata of this block, fetched now, used only by the last arriver:
   // lane u of warp 0 holds row u's masked flag, thread 0 the block's tau and phase.
   float tau_b = 0.f;
   int phase = 0, seq_b = 0;
+  bool live = true;  // thread 0: the block lies inside the window layout
   const bool blk_masked = warp == 0 && lane < B && a.masked[jb * B + lane] != 0;
   if (tid == 0) {
     int lo = 0, hi = a.batch - 1;
@@ -299,6 +297,10 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
     tau_b = __ldg(a.tau + lo);
     phase = __ldg(a.block_phase + jb);
     seq_b = lo;
+    // Rows past the last window (a launch sized for a capacity, the layout written
+    // on the device) are not masked, so they fold nothing; their block must not
+    // arrive either, or it would decide for a sequence it does not belong to.
+    live = r0 < __ldg(a.q_start + a.batch);
   }
   const bool is_masked = a.masked[r] != 0;
 
@@ -391,7 +393,7 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const CommitArgs a) {
 
   // ---- arrival on the block's counter ----------------------------------------
   if (tid == 0) D2F_TRACE_MARK(1, 5);
-  if (tid == 0) is_last = atomic_add_acq_rel(a.blk_cnt + jb, 1) == B * a.splits - 1;
+  if (tid == 0) is_last = live && atomic_add_acq_rel(a.blk_cnt + jb, 1) == B * a.splits - 1;
   __syncthreads();
   if (tid == 0) D2F_TRACE_MARK(1, 6);
   if (!is_last) return;
