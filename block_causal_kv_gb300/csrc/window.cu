@@ -250,9 +250,17 @@ size_t window_smem_bytes(int batch, int capacity, int block_size) {
 
 cudaError_t launch_window(const WindowArgs &a, cudaStream_t stream) {
   const size_t smem = window_smem_bytes(a.batch, a.capacity, a.block_size);
-  cudaError_t e = cudaFuncSetAttribute(window_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  // The opt-in above 48 KB is a per-device function attribute: set it when a larger
+  // size is first needed, not on every launch.
+  static int opted[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (smem > 48 * 1024 && (dev >= 64 || (int)smem > opted[dev])) {
+    e = cudaFuncSetAttribute(window_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) opted[dev] = (int)smem;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1);
   cfg.blockDim = dim3(kThreads);
