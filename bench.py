@@ -256,12 +256,14 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # CPU oracle timing (reference arm and cpu_baseline)
 # ---------------------------------------------------------------------------
-def time_oracle(p, seconds, nthreads, metric=0, reuse=False):
+def time_oracle(p, seconds, nthreads, metric=0, reuse=False, sched=None):
     """Time the CPU oracle on a bounded sample of one step and extrapolate to
     full steps: attention over a subset of KV heads (its cost is linear in heads)
     and the commit over a subset of rows (linear in rows), with the commit's
     confidence `metric`. reuse: the attention is the window part composed with a
-    cached part that is computed once per sample size, untimed."""
+    cached part that is computed once per sample size, untimed. sched (tau_add,
+    tau_act): each step also runs the oracle's window scheduler over the whole
+    batch, from the state the device-driven step starts from."""
     import oracle
     w = p.w
     Hk, G = w.num_heads_kv, w.num_heads_q // w.num_heads_kv
@@ -293,6 +295,17 @@ def time_oracle(p, seconds, nthreads, metric=0, reuse=False):
                       metric=metric)
         return time.perf_counter() - t0
 
+    t_window = 0.0
+    if sched is not None:
+        W = max(w.window_blocks)
+        state = sched_state_dict(p, W)
+        t0 = time.perf_counter()
+        n_win = 0
+        while n_win < 3 or time.perf_counter() - t0 < 0.05:
+            oracle.window_step(state, w.block_size, W, p.mask_id, sched[0], sched[1])
+            n_win += 1
+        t_window = (time.perf_counter() - t0) / n_win
+
     ta1 = attn_sample(1)
     tc1 = commit_sample(1)
     n_blocks = w.total_q // w.block_size
@@ -309,11 +322,13 @@ def time_oracle(p, seconds, nthreads, metric=0, reuse=False):
         reps += 1
         if time.perf_counter() - t_start >= seconds:
             break
-    step_s = (ta / reps) * Hk / nh + (tc / reps) * n_blocks / nb
+    step_s = (ta / reps) * Hk / nh + (tc / reps) * n_blocks / nb + t_window
     sample = ("%d x [%s for %d of %d KV heads + commit for %d of %d window blocks], "
               "extrapolated linearly to full steps" % (
                   reps, "window-part attention with a kept cached part" if reuse else "attention",
                   nh, Hk, nb, n_blocks))
+    if sched is not None:
+        sample += " + the window scheduler over the whole batch (%.1f us)" % (t_window * 1e6)
     return 1.0 / step_s, sample
 
 
@@ -332,10 +347,11 @@ def run_reference(args, world, rank):
     nthreads = oracle_threads()
     # bounded: the whole run takes about --ref-seconds regardless of K
     budget = args.ref_seconds
+    sched = (args.tau_add, args.tau_act) if args.scheduler else None
     for _ in range(max(0, min(args.warmup, 1))):
-        time_oracle(p, 0.1, nthreads, CONF_METRICS[args.conf_metric], args.reuse_cached)
+        time_oracle(p, 0.1, nthreads, CONF_METRICS[args.conf_metric], args.reuse_cached, sched)
     value, sample = time_oracle(p, budget, nthreads, CONF_METRICS[args.conf_metric],
-                                args.reuse_cached)
+                                args.reuse_cached, sched)
     ms = 1000.0 / value
     cfg = workload_config(p, args)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s",
@@ -442,6 +458,24 @@ def sched_snapshot(p, dev, W):
     return (torch.cat(rows).to(dev), p.block_phase.cpu().to(torch.uint8).to(dev), fields, const)
 
 
+def sched_state_dict(p, W):
+    """The same starting state as sched_snapshot, as the oracle's window_step takes it
+    (CPU tensors)."""
+    i32, u8, fields, const = sched_snapshot(p, "cpu", W)
+    st = {}
+    for name, (off, shape) in fields.items():
+        n = 1
+        for x in shape:
+            n *= x
+        st[name] = i32[off:off + n].view(shape).clone()
+    st.update(tokens=p.tokens.cpu().clone(), masked=p.masked.cpu().clone(), stopped=None,
+              gen_blocks=const["gen_blocks"].cpu(), free_pages=const["free_pages"].cpu(),
+              free_count=int(st.pop("free_count")[0]))
+    for k in ("app_src", "app_dst", "n_append", "row_pos"):
+        st.pop(k)
+    return st
+
+
 def sched_views(tokens, masked, i32, u8, fields, const, p, W):
     """A d2f.window_step state whose fields are views of one int32 and one uint8 row."""
     from types import SimpleNamespace
@@ -487,6 +521,8 @@ def run_ours(args, world, rank, local):
         raise SystemExit("--scheduler appends inside the attention by itself; it goes alone")
     if sched and w.total_q != w.batch * max(w.window_blocks) * B:
         raise SystemExit("--scheduler takes workloads whose windows all hold the same blocks")
+    if sched and any(c % B for c in w.ctx_lens):
+        raise SystemExit("--scheduler takes prompts padded to whole blocks")
     fused = (args.fused_append or sched) and len(p.src_row) > 0
     appends = len(p.src_row) > 0 and not fused and not reuse
 
@@ -774,7 +810,8 @@ def run_ours(args, world, rank, local):
     if rank == 0 and not args.no_cpu_baseline:
         value_cpu, sample = time_oracle(p if p.q.device.type == "cpu" else p.to("cpu"),
                                         args.cpu_seconds, oracle_threads(),
-                                        CONF_METRICS[args.conf_metric], reuse)
+                                        CONF_METRICS[args.conf_metric], reuse,
+                                        (args.tau_add, args.tau_act) if sched else None)
         line["cpu_baseline"] = {"value": value_cpu, "unit": "steps/s", "cores": oracle_threads(),
                                 "kind": "oracle", "sample": sample}
     if rank == 0:
