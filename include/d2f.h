@@ -28,9 +28,13 @@
  *   skipped without any out-of-range access, and the caller reads the word
  *   after its own synchronisation. Kernels never trap or assert.
  * - Window metadata: sequence b owns window rows q_start[b] .. q_start[b+1]-1
- *   (n_b rows; q_start[0] = 0, q_start[batch] = total_q, every q_start value a
+ *   (n_b rows; q_start[0] = 0, q_start[batch] <= total_q, every q_start value a
  *   multiple of block_size). Row i of sequence b lies in window block i / B.
- *   Global window block jb covers rows jb*B .. jb*B+B-1.
+ *   Global window block jb covers rows jb*B .. jb*B+B-1. total_q may exceed
+ *   q_start[batch] (a launch sized for a capacity while the layout is written on
+ *   the device, as d2f_window_step does): the rows past q_start[batch] belong to
+ *   no sequence, the attention writes nothing for them, and the commit wants them
+ *   not masked (masked = 0) and leaves them as they are.
  * - K/V pool layout: [num_pages][num_heads_kv][block_size][head_dim], one page
  *   = one block of B tokens of one sequence ([P1] §운영 관점: block completion
  *   is the cache-persistence signal, so a page holds exactly one block). Token t
