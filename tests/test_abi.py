@@ -94,3 +94,34 @@ def test_null_pointers_are_rejected_before_any_launch(lib):
                             1, 16, 16, 0, 4, 4, 64, 16, 4, 0, ctypes.c_float(0.125), 1, None, 0,
                             None, None)
     assert st == 1
+
+
+def _window(lib, batch=2, B=16, W=3, cap=None, maxp=8, tau_add=0.5, tau_act=1.0, ptr=1):
+    """d2f_window_step with every pointer set to `ptr` (never dereferenced: each call
+    here must be refused on the host)."""
+    cap = batch * W * B if cap is None else cap
+    p = ctypes.c_void_p(ptr) if ptr else None
+    return lib.d2f_window_step(batch, B, W, cap, maxp, 99, ctypes.c_float(tau_add),
+                               ctypes.c_float(tau_act), *([p] * 18))
+
+
+def test_window_step_host_checks(lib):
+    assert _window(lib, cap=100) == 1                  # not a multiple of block_size
+    assert _window(lib, cap=64) == 1                   # < batch * max_blocks * block_size
+    assert _window(lib, B=256, cap=2 * 3 * 256) == 2   # block_size > 128
+    assert _window(lib, batch=1, W=1, B=16, cap=64000) == 2   # past one CTA's shared memory
+    assert _window(lib, tau_add=float("nan")) == 1
+    assert _window(lib, W=0) == 1
+    assert _window(lib, ptr=0) == 1                    # NULL state
+    assert b"NULL" in lib.d2f_last_error_string()
+
+
+def test_device_count_appends_need_the_count(lib):
+    st = lib.d2f_kv_append_dev(None, None, None, None, None, 4, 16, None, None, 4, 128, 16, 8,
+                               0, None, None)
+    assert st == 1 and b"n_append_dev" in lib.d2f_last_error_string()
+    st = lib.d2f_block_attn_append_dev(None, None, None, None, None, None, 4, None, None, None,
+                                       None, 1, 16, 16, 0, 4, 4, 64, 16, 4, 0,
+                                       ctypes.c_float(0.125), 1, None, 0, None, None, None, 4,
+                                       None, None)
+    assert st == 1 and b"n_append_dev" in lib.d2f_last_error_string()
