@@ -53,12 +53,13 @@ def test_two_gloo_ranks_time_with_the_slowest():
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="the gloo path is the one without GPUs")
-def test_reference_arm_under_torchrun_prints_once():
+@pytest.mark.parametrize("mode", [[], ["--scheduler"], ["--reuse-cached"]])
+def test_reference_arm_under_torchrun_prints_once(mode):
     port = _free_port()
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
            "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl",
            "reference", "--gpus", "2", "--workload", "tiny", "--steps", "2", "--warmup", "1",
-           "--ref-seconds", "0.5"]
+           "--ref-seconds", "0.5"] + mode
     r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
@@ -66,3 +67,7 @@ def test_reference_arm_under_torchrun_prints_once():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle"
+    if mode == ["--scheduler"]:
+        assert "window scheduler" in d["cpu_baseline"]["sample"] and "scheduler" in d["config"]
+    if mode == ["--reuse-cached"]:
+        assert "kept cached part" in d["cpu_baseline"]["sample"]
