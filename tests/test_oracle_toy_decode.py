@@ -186,3 +186,103 @@ def test_cached_decode_equals_full_recompute(oracle):
             page = phys[t // B]
             np.testing.assert_allclose(k_pool[l][page, :, t % B].numpy(), ks[l][t], rtol=0, atol=1e-12)
             np.testing.assert_allclose(v_pool[l][page, :, t % B].numpy(), vs[l][t], rtol=0, atol=1e-12)
+
+
+def test_scheduled_decode_equals_full_recompute(oracle):
+    """The same toy decode with the window driven by the window scheduler
+    (oracle.window_step): block entry on the progress threshold, phases, positions,
+    the one-step-delayed append list, pages off a free list and the page table. The
+    invariants are the pages' own: every step's logits equal a full recomputation
+    with the explicit block-causal mask, cached pages never change, and at the end
+    the cache holds the full recomputation's K/V of the final sequence."""
+    model = Toy(0)
+    rng = np.random.default_rng(2)
+    prompt = rng.integers(0, VOCAB, PROMPT)
+    n_pages = PROMPT // B + NBLOCKS + 3
+    phys = rng.permutation(n_pages)
+    prompt_pages = [int(x) for x in phys[:PROMPT // B]]
+    free = [int(x) for x in phys[PROMPT // B:]]
+    k_pool = [torch.zeros(n_pages, HEADS, B, HD, dtype=torch.float64) for _ in range(LAYERS)]
+    v_pool = [torch.zeros(n_pages, HEADS, B, HD, dtype=torch.float64) for _ in range(LAYERS)]
+
+    def f64(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float64))
+
+    _, pk, pv = full_recompute(model, prompt, np.full(PROMPT, -1))
+    for l in range(LAYERS):
+        for t in range(PROMPT):
+            k_pool[l][prompt_pages[t // B], :, t % B] = f64(pk[l][t])
+            v_pool[l][prompt_pages[t // B], :, t % B] = f64(pv[l][t])
+    max_pages = PROMPT // B + NBLOCKS
+    pt = torch.full((1, max_pages), -1, dtype=torch.int32)
+    pt[0, :len(prompt_pages)] = torch.tensor(prompt_pages, dtype=torch.int32)
+    cap = WMAX * B
+    st = {"q_start": torch.zeros(2, dtype=torch.int32),
+          "tokens": torch.full((cap,), MASK, dtype=torch.int32),
+          "masked": torch.zeros(cap, dtype=torch.uint8),
+          "ctx_len": torch.tensor([PROMPT], dtype=torch.int32), "page_table": pt,
+          "next_block": torch.zeros(1, dtype=torch.int32),
+          "gen_blocks": torch.tensor([NBLOCKS], dtype=torch.int32),
+          "n_leaving": torch.zeros(1, dtype=torch.int32), "stopped": None,
+          "free_pages": torch.tensor(free, dtype=torch.int32), "free_count": len(free)}
+    tau_add, tau_act = 0.5, 1.0
+    st = oracle.window_step(st, B, WMAX, MASK, tau_add, tau_act)
+    committed = {}                       # position -> token
+    snapshots = {}
+    steps = 0
+    while int(st["q_start"][1]) > 0:
+        steps += 1
+        assert steps < 80 and st["err"] == 0
+        n = int(st["q_start"][1])
+        rows_tok = st["tokens"][:n].numpy()
+        rows_pos = st["row_pos"][:n].numpy()
+        ctx = int(st["ctx_len"][0])
+        assert rows_pos[0] == ctx and (np.diff(rows_pos) == 1).all()
+        x = model.embed(rows_tok, rows_pos)
+        win_k, win_v = [], []
+        for l in range(LAYERS):
+            q, k, v = (f64(a) for a in model.qkv(x, l))
+            win_k.append(k)
+            win_v.append(v)
+            out, _ = oracle.block_attn(q, k, v, k_pool[l], v_pool[l], st["page_table"],
+                                       st["ctx_len"], torch.tensor([0, n], dtype=torch.int32), B)
+            x = model.post(x, out.numpy(), l)
+        logits = x @ model.Wlm
+        # the full recomputation over [prompt ; every block up to the window's last]
+        last = (int(rows_pos[-1]) - PROMPT) // B
+        toks = [committed.get(PROMPT + t, MASK) for t in range((last + 1) * B)]
+        all_tok = np.concatenate([prompt, np.array(toks)])
+        ids = np.concatenate([np.full(PROMPT, -1), np.repeat(np.arange(last + 1), B)])
+        ref_logits, _, _ = full_recompute(model, all_tok, ids)
+        np.testing.assert_allclose(logits, ref_logits[rows_pos], rtol=0, atol=1e-12)
+        for (l, page), (kk, vv) in snapshots.items():
+            assert torch.equal(k_pool[l][page], kk) and torch.equal(v_pool[l][page], vv)
+        # the appends listed for this step read this step's K/V (final tokens)
+        for src, page in zip(st["app_src"].tolist(), st["app_dst"].tolist()):
+            assert not st["masked"][src:src + B].any()
+            for l in range(LAYERS):
+                kp, vp = oracle.kv_append(win_k[l], win_v[l], torch.tensor([src], dtype=torch.int32),
+                                          torch.tensor([page], dtype=torch.int32), k_pool[l],
+                                          v_pool[l], B)
+                k_pool[l], v_pool[l] = kp, vp
+                snapshots[(l, page)] = (kp[page].clone(), vp[page].clone())
+        # commit on this step's logits, then the scheduler
+        res = oracle.commit(torch.from_numpy(logits.astype(np.float32)), st["tokens"][:n],
+                            st["masked"][:n], st["q_start"], st["block_phase"][:n // B],
+                            torch.tensor([TAU]), B, MASK)
+        tok, msk = st["tokens"].clone(), st["masked"].clone()
+        tok[:n], msk[:n] = res["tokens"], res["masked"]
+        for r in range(n):
+            if st["masked"][r] and not msk[r]:
+                committed[int(rows_pos[r])] = int(tok[r])
+        st = oracle.window_step(dict(st, tokens=tok, masked=msk), B, WMAX, MASK, tau_add, tau_act)
+
+    assert int(st["ctx_len"][0]) == PROMPT + NBLOCKS * B and len(committed) == NBLOCKS * B
+    final = np.concatenate([prompt, np.array([committed[PROMPT + t] for t in range(NBLOCKS * B)])])
+    ids = np.concatenate([np.full(PROMPT, -1), np.repeat(np.arange(NBLOCKS), B)])
+    _, ks, vs = full_recompute(model, final, ids)
+    for l in range(LAYERS):
+        for t in range(len(final)):
+            page = int(st["page_table"][0, t // B])
+            np.testing.assert_allclose(k_pool[l][page, :, t % B].numpy(), ks[l][t], rtol=0, atol=1e-12)
+            np.testing.assert_allclose(v_pool[l][page, :, t % B].numpy(), vs[l][t], rtol=0, atol=1e-12)
