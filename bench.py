@@ -4,18 +4,24 @@
 One step = d2f_block_attn (one layer, the whole active window) + d2f_commit
 (every still-masked window position), + d2f_kv_append where the workload
 appends, preceded by a 2-copy reset of the decode state (tokens, masked) so that
-every step does the same work. Default workload: the LLaDA-8B-shaped layer
-(batch 1, 32 MHA heads, head_dim 128, bf16, context 1024 in 16-token pages,
-window 3 blocks = 48 queries, vocabulary 126464).
+every step does the same work.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload llada]
+By default every workload is measured, each on its own: tiny, llada, ragged,
+dream, long_b8, long_b16, long_b32. The line's headline fields (value, roofline,
+kernels, e2e, cpu_baseline) are those of long_b32, the largest configuration
+that fits one GPU (batch 4, 32 MHA heads, head_dim 128, context 32768, window 4
+blocks of 32, vocabulary 126464), timed over exactly --steps steps; per_config
+holds the same fields for every workload (the others timed over at least a few
+hundred milliseconds of steps).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload all|llada|...]
     python bench.py --impl reference ...   # the CPU oracle, timed the same way
 
 Timing: inputs resident in HBM; the step cycles through enough independent
 input sets (> 4x L2) that no step finds its inputs in L2; K steps replayed from
 CUDA graphs between CUDA events, barrier + synchronize on both sides, max over
-ranks. Per-kernel durations come from CUDA events captured in the same graphs.
-Prints one JSON line (rank 0).
+ranks. Per-kernel durations come from graphs of each kernel over the same input
+sets. Prints one JSON line (rank 0).
 """
 import argparse
 import hashlib
@@ -38,10 +44,12 @@ PROFILES = os.path.join(ROOT, "profiles")
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="llada")
+    ap.add_argument("--workload", default="all",
+                    help="one workload, or all (default): the headline on %s and per_config "
+                         "results for every workload" % "long_b32")
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--commit-splits", type=int, default=0)
     ap.add_argument("--conf-metric", default="pmax", choices=list(CONF_METRICS),
@@ -69,7 +77,10 @@ def parse():
                          "aggressive")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=4.0,
+                    help="time budget of the oracle on all host cores, per workload")
+    ap.add_argument("--cpu-seconds-1t", type=float, default=3.0,
+                    help="time budget of the oracle on one host thread, per workload")
     ap.add_argument("--ref-seconds", type=float, default=60.0,
                     help="oracle time budget of the reference arm")
     ap.add_argument("--profile-steps", type=int, default=0,
@@ -342,7 +353,7 @@ def run_reference(args, world, rank):
     from block_causal_kv_gb300 import synth
     import oracle
     oracle._load()
-    w = synth.workload(args.workload)
+    w = synth.workload(HEADLINE if args.workload == "all" else args.workload)
     p = synth.make_problem(w)
     nthreads = oracle_threads()
     # bounded: the whole run takes about --ref-seconds regardless of K
@@ -491,13 +502,11 @@ def sched_views(tokens, masked, i32, u8, fields, const, p, W):
     return st
 
 
-def run_ours(args, world, rank, local):
+def measure(args, name, K, W, world, rank, dev, cpu=True):
+    """Time K steps of workload `name` (after W warm-up steps) on `dev`; returns
+    the workload's result object (the JSON line's fields for it)."""
     from block_causal_kv_gb300 import d2f, synth
-    import __graft_entry__
-    __graft_entry__.build()
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    w = synth.workload(args.workload)
+    w = synth.workload(name)
     big = w.name.startswith("long") or w.name in ("dream", "ragged")
     p = synth.make_problem(w, device="cuda" if big else "cpu")
     base = StepSet(p, dev)
@@ -635,7 +644,7 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.Stream(device=dev)
     # warm-up (library init, function attributes) outside capture
     with torch.cuda.stream(stream):
-        for i in range(max(3, min(args.warmup, n_sets))):
+        for i in range(max(3, min(W, n_sets))):
             s = sets[i % n_sets]
             reset(s)
             step_kernels(s)
@@ -656,7 +665,6 @@ def run_ours(args, world, rank, local):
     g_all = capture(range(n_sets))
     singles = [capture([i]) for i in range(n_sets)]
 
-    K, W = args.steps, args.warmup
     full, rest = divmod(K, n_sets)
 
     # warm-up replays (untimed) plus a short pre-roll so clock samples overlap load
@@ -807,13 +815,90 @@ def run_ours(args, world, rank, local):
             "roofline": roofline, "kernels": kernels,
             "gpu_launches": K * (2 + (1 if appends else 0) + (1 if sched else 0)),
             "clocks": clocks, "e2e": e2e}
-    if rank == 0 and not args.no_cpu_baseline:
-        value_cpu, sample = time_oracle(p if p.q.device.type == "cpu" else p.to("cpu"),
-                                        args.cpu_seconds, oracle_threads(),
-                                        CONF_METRICS[args.conf_metric], reuse,
-                                        (args.tau_add, args.tau_act) if sched else None)
-        line["cpu_baseline"] = {"value": value_cpu, "unit": "steps/s", "cores": oracle_threads(),
-                                "kind": "oracle", "sample": sample}
+    # free the device buffers before the CPU legs (and the next workload)
+    del sets, base
+    torch.cuda.synchronize()
+    if rank == 0 and cpu and not args.no_cpu_baseline:
+        pc = p if p.q.device.type == "cpu" else p.to("cpu")
+        del p
+        torch.cuda.empty_cache()
+        line["cpu_baseline"] = cpu_baseline(pc, args, reuse, sched)
+    return line
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def cpu_baseline(p, args, reuse, sched):
+    """The oracle as it stands on this host: all cores, then one thread, each on
+    a bounded sample of the step (time_oracle)."""
+    metric = CONF_METRICS[args.conf_metric]
+    sch = (args.tau_add, args.tau_act) if sched else None
+    n = oracle_threads()
+    v_all, s_all = time_oracle(p, args.cpu_seconds, n, metric, reuse, sch)
+    res = {"value": v_all, "unit": "steps/s", "cores": n, "kind": "oracle", "sample": s_all,
+           "cpu_model": cpu_model()}
+    if n > 1 and args.cpu_seconds_1t > 0:
+        v1, s1 = time_oracle(p, args.cpu_seconds_1t, 1, metric, reuse, sch)
+        res["one_thread"] = {"value": v1, "unit": "steps/s", "cores": 1, "sample": s1}
+    return res
+
+
+# Order of the per-workload results; the headline is the largest configuration
+# that fits one GPU (long context, block size 32: 2.16 GB of cached K/V and
+# 129.5 MB of logits per step).
+HEADLINE = "long_b32"
+ALL_WORKLOADS = ("tiny", "llada", "ragged", "dream", "long_b8", "long_b16", "long_b32")
+# steps timed for the workloads other than the headline (which times exactly
+# --steps): enough for a timed region of a few hundred milliseconds
+MIN_STEPS = {"tiny": 20000, "llada": 20000, "ragged": 3000, "dream": 3000, "long_b8": 1000,
+             "long_b16": 1000, "long_b32": 1000}
+# per-workload fields kept in the per_config object
+PER_CONFIG_KEYS = ("value", "unit", "steps", "ms_per_step", "dtype", "config", "roofline",
+                   "kernels", "clocks", "e2e", "cpu_baseline")
+
+
+def run_ours(args, world, rank, local):
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    K, W = args.steps, args.warmup
+    if args.profile_steps and args.workload == "all":
+        raise SystemExit("--profile-steps takes one --workload")
+    if args.workload != "all":
+        line = measure(args, args.workload, K, W, world, rank, dev)
+        if rank == 0 and line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    per = {}
+    for name in ALL_WORKLOADS:
+        k = K if name == HEADLINE else max(K, MIN_STEPS[name])
+        per[name] = measure(args, name, k, W, world, rank, dev)
+        torch.cuda.empty_cache()
+    line = dict(per[HEADLINE])
+    line["per_config"] = {n: {k: v for k, v in r.items() if k in PER_CONFIG_KEYS}
+                          for n, r in per.items()}
+    line["config"] = dict(line["config"], headline=(
+        "%s: the largest configuration that fits one GPU; per_config holds every workload, each "
+        "timed on its own" % HEADLINE))
     if rank == 0:
         print(json.dumps(line), flush=True)
 

@@ -11,9 +11,13 @@ Tolerances
       most a few thousand keys of unit-scale values, so its error is ~1e-6; the
       bar is 1e-4 max / 1e-5 mean.
   commit: greedy tokens bit-exact; confidence relative error <= 1e-5; tokens and
-      masks bit-exact except positions with |p - tau| < 1e-5 and aggressive
-      blocks whose two best masked confidences differ by < 1e-5 (both reported).
+      masks bit-exact except positions with |p - tau| < 1e-5 and, in aggressive
+      blocks, the rows within 1e-5 of the block's best masked confidence when
+      there are several (their commit count must still match); both reported.
 """
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -53,12 +57,32 @@ def check_attention(out, lse, ref, ref_lse, dtype, label=""):
     return mx, mean
 
 
+def record_excluded(label, n_masked, n_band, n_tie, max_frac=None, n_tie_blocks=0):
+    """The positions a commit comparison left out of the bit-exact check are
+    reported separately: appended as one JSON line to the file named by
+    D2F_PARITY_LOG (when set). With max_frac they are also bounded: band
+    positions at most that fraction of the masked ones (at least one allowed),
+    near-tied rows at most four per aggressive block that has them."""
+    path = os.environ.get("D2F_PARITY_LOG")
+    if path and label:
+        with open(path, "a") as f:
+            f.write(json.dumps({"case": label, "masked": n_masked, "band": n_band,
+                                "near_tie_rows": n_tie, "near_tie_blocks": n_tie_blocks}) + "\n")
+    if max_frac is not None:
+        lim = max(1, int(max_frac * n_masked))
+        assert n_band <= lim, "%s: %d band positions excluded of %d masked" % (
+            label, n_band, n_masked)
+        assert n_tie <= 4 * n_tie_blocks, "%s: %d near-tied rows in %d blocks" % (
+            label, n_tie, n_tie_blocks)
+
+
 def commit_compare(p, gpu_tokens, gpu_masked, gpu_conf, gpu_arg, gpu_rem, phase, tau, ref,
-                   band=None, atol=0.0):
+                   band=None, atol=0.0, label=None, max_frac=None):
     """Compare a GPU commit with the oracle's. Returns (n_band, n_tie) positions
     excluded from the bit-exact check. band: the |c - tau| (and top-two) band
     excluded from it (default BAND); atol: absolute slack on the confidence
-    besides CONF_RTOL (for metrics that can be near 0)."""
+    besides CONF_RTOL (for metrics that can be near 0); label / max_frac: see
+    record_excluded."""
     BAND_ = BAND if band is None else band
     m0 = p.masked.cpu().bool()
     conf = gpu_conf.cpu()
@@ -70,7 +94,9 @@ def commit_compare(p, gpu_tokens, gpu_masked, gpu_conf, gpu_arg, gpu_rem, phase,
     err = ((conf[m0].double() - rc).abs() - atol).clamp(min=0.0)
     rel = (err / (rc.abs() + 1e-30)).max().item() if m0.any() else 0.0
     assert rel <= CONF_RTOL, "conf rel err %.3g" % rel
-    # excluded positions
+    # excluded positions: the |c - tau| band, and in aggressive blocks the masked
+    # rows within the band of the block's most confident row when there are
+    # several (which of them is the extra top-1 commit depends on rounding)
     B = p.w.block_size
     q_start = p.q_start.cpu()
     seq = torch.searchsorted(q_start, torch.arange(len(m0), dtype=torch.int32), right=True) - 1
@@ -79,19 +105,35 @@ def commit_compare(p, gpu_tokens, gpu_masked, gpu_conf, gpu_arg, gpu_rem, phase,
     tie_rows = torch.zeros_like(m0)
     nb = len(m0) // B
     ph = phase.cpu()
+    tie_blocks = []
     for jb in range(nb):
         if ph[jb] != 1:
             continue
         sl = slice(jb * B, (jb + 1) * B)
+        if m0[sl].sum() < 2:
+            continue
         c = torch.where(m0[sl], ref["conf"][sl], torch.tensor(float("-inf")))
-        top = torch.sort(c, descending=True).values
-        if m0[sl].sum() >= 2 and float(top[0] - top[1]) < BAND_:
-            tie_rows[sl] = True
+        tied = m0[sl] & (c >= c.max() - BAND_)
+        if tied.sum() >= 2:
+            tie_rows[sl] |= tied
+            tie_blocks.append(jb)
     excl = band | tie_rows
     tok = gpu_tokens.cpu()
     msk = gpu_masked.cpu()
     assert torch.equal(tok[~excl], ref["tokens"][~excl]), "token mismatch"
     assert torch.equal(msk[~excl], ref["masked"][~excl]), "mask mismatch"
-    blk_ok = ~excl.view(-1, B).any(1)
+    # near-tied rows: as many commits among them as the oracle makes, each with
+    # its greedy token; the others stay masked
+    for jb in tie_blocks:
+        sl = slice(jb * B, (jb + 1) * B)
+        t = tie_rows[sl] & ~band[sl]
+        assert int((msk[sl][t] == 0).sum()) == int((ref["masked"][sl][t] == 0).sum()), \
+            "block %d: commits among near-tied rows differ" % jb
+        com = t & (msk[sl] == 0)
+        assert torch.equal(tok[sl][com], ref["argmax"][sl][com])
+        assert bool((tok[sl][t & (msk[sl] != 0)] == p.mask_id).all())
+    blk_ok = ~band.view(-1, B).any(1)
     assert torch.equal(gpu_rem.cpu()[blk_ok], ref["block_remaining"][blk_ok])
-    return int(band.sum()), int(tie_rows.sum())
+    n_band, n_tie = int(band.sum()), int((tie_rows & ~band).sum())
+    record_excluded(label, int(m0.sum()), n_band, n_tie, max_frac, len(tie_blocks))
+    return n_band, n_tie

@@ -222,7 +222,7 @@ def test_full_size_llada_layer():
     print("llada full: max-abs %.3e mean-abs %.3e" % (mx, mean))
 
 
-@pytest.mark.parametrize("name", ["dream", "ragged", "long_b16"])
+@pytest.mark.parametrize("name", ["dream", "ragged", "long_b8", "long_b16", "long_b32"])
 def test_full_size_sampled(name):
     """Full-size workloads: the GPU runs the whole batch; the oracle recomputes
     one sampled sequence (its window rows, all heads) one by one."""

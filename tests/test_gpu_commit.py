@@ -34,14 +34,16 @@ def _gpu_commit(p, dev, phase=None, tau=None, num_splits=0, logit_row=None, logi
 METRIC_TOL = {0: (0.0, None), 1: (2e-5, 1e-4), 2: (2e-6, 1e-5), 3: (0.0, 1e-6)}
 
 
-def _check(p, dev, phase=None, tau=None, num_splits=0, logit_row=None, logits=None, metric=0):
+def _check(p, dev, phase=None, tau=None, num_splits=0, logit_row=None, logits=None, metric=0,
+           label=None, max_frac=None):
     g, res, phase, tau = _gpu_commit(p, dev, phase, tau, num_splits, logit_row, logits, metric)
     ref = oracle.commit(p.logits if logits is None else logits, p.tokens, p.masked, p.q_start,
                         phase.cpu(), tau.cpu(), p.w.block_size, p.mask_id,
                         logit_row=logit_row, metric=metric)
     atol, band = METRIC_TOL[metric]
     return commit_compare(p, g.tokens, g.masked, res["conf"], res["argmax"],
-                          res["block_remaining"], phase, tau, ref, band=band, atol=atol)
+                          res["block_remaining"], phase, tau, ref, band=band, atol=atol,
+                          label=label, max_frac=max_frac)
 
 
 @pytest.mark.parametrize("name", ["tiny", "llada", "ragged", "dream", "long_b8", "long_b32"])
@@ -49,15 +51,19 @@ def _check(p, dev, phase=None, tau=None, num_splits=0, logit_row=None, logits=No
 def test_small_workloads(name, splits):
     dev = device()
     w = synth.workload("tiny") if name == "tiny" else synth.small(name)
-    nb, nt = _check(synth.make_problem(w), dev, num_splits=splits)
+    nb, nt = _check(synth.make_problem(w), dev, num_splits=splits,
+                    label="%s small, splits %d" % (name, splits), max_frac=0.02)
     print("%s s%d: band %d tie %d" % (name, splits, nb, nt))
 
 
-@pytest.mark.parametrize("name", ["llada", "ragged", "dream"])
+@pytest.mark.parametrize("name", ["llada", "ragged", "dream", "long_b8", "long_b16", "long_b32"])
 def test_full_size(name):
+    """Every full-size workload in the bench's launch configuration (automatic
+    plan): the excluded positions are recorded and stay below 2 % of the masked
+    ones."""
     dev = device()
     p = synth.make_problem(synth.workload(name))
-    nb, nt = _check(p, dev)
+    nb, nt = _check(p, dev, label="%s full size" % name, max_frac=0.02)
     print("%s full: rows %d, excluded band %d tie %d" % (name, p.w.total_q, nb, nt))
 
 
@@ -276,3 +282,49 @@ def test_early_commit_rejects_entropy():
         d2f.commit(g.logits, g.tokens, g.masked, g.q_start, g.block_phase, g.tau,
                    block_size=p.w.block_size, mask_id=p.mask_id, metric=1,
                    early_gap=torch.zeros(p.w.batch, device=dev))
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_planted_threshold_boundary(dtype):
+    """Rows planted just outside the reported band: every sequence holds one
+    block whose row 0 is the planted row, and its tau is that row's confidence
+    (from the oracle) moved by +-2e-5 or +-1e-4, in conservative and aggressive
+    blocks (in aggressive blocks row 1 is made clearly more confident, so the
+    planted row's fate is the threshold test), at the full LLaDA vocabulary.
+    Every decision outside the 1e-5 band is bit-exact, and each planted row
+    commits exactly when tau lies below its confidence."""
+    dev = device()
+    V, B = 126464, 16
+    deltas = [2e-5, -2e-5, 1e-4, -1e-4]
+    nseq = 2 * 2 * len(deltas)
+    w = synth.Workload("plant", nseq, 1, 1, 8, B, dtype, [0] * nseq, [1] * nseq, V,
+                       masked_frac=0.75, seed=77)
+    p = synth.make_problem(w)
+    p.masked[0::B] = 1          # the planted row is masked
+    p.tokens[0::B] = p.mask_id
+    phase = torch.tensor([(b // len(deltas)) % 2 for b in range(nseq)], dtype=torch.uint8)
+    for b in range(nseq):
+        if phase[b] == 1:       # a clearly more confident row ahead of the planted one
+            r = b * B
+            row = p.logits[r].clone()
+            row[int(torch.argmax(row.float()))] += 8
+            p.logits[r + 1] = row
+            p.masked[r + 1] = 1
+            p.tokens[r + 1] = p.mask_id
+    conf = oracle.commit(p.logits, p.tokens, p.masked, p.q_start, phase,
+                         torch.full((nseq,), 2.0), B, p.mask_id)["conf"]
+    d = torch.tensor([deltas[b % len(deltas)] for b in range(nseq)], dtype=torch.float64)
+    tau = (conf[0::B].double() + d).float()
+    assert bool(((tau.double() - conf[0::B].double()).abs() >= 1.5e-5).all())
+    p.tau = tau
+    p.block_phase = phase
+    g, res, _, _ = _gpu_commit(p, dev, phase=phase, tau=tau)
+    ref = oracle.commit(p.logits, p.tokens, p.masked, p.q_start, phase, tau, B, p.mask_id)
+    nb, nt = commit_compare(p, g.tokens, g.masked, res["conf"], res["argmax"],
+                            res["block_remaining"], phase, tau, ref,
+                            label="planted boundary %s" % str(dtype).split(".")[-1])
+    planted = torch.arange(nseq) * B
+    gm = g.masked.cpu()[planted]
+    expect_commit = d < 0        # tau below p: p > tau holds
+    assert torch.equal(gm == 0, expect_commit), (gm, d)
+    assert torch.equal(g.tokens.cpu()[planted][expect_commit], ref["argmax"][planted][expect_commit])
