@@ -353,7 +353,7 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
       if (u >= NS) {
         bool ok = true;
         if (lane == 0)
-          ok = mbar_wait(smem_u32(&bars->empty[stage]), ((u / NS) - 1) & 1, abort_flag, a.err);
+          ok = mbar_wait(smem_u32(&bars->empty[stage]), ((u / NS) - 1) & 1, abort_flag, a.err, a.wait_cycles);
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       }
       // Source of this lane's slot: a physical page or a window row; -1 = nothing
@@ -406,7 +406,7 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
             set_err(a.err, D2F_ERR_BAD_INDEX);
             continue;
           }
-          if (!landed && !mbar_wait(full, (u / NS) & 1, abort_flag, a.err)) break;
+          if (!landed && !mbar_wait(full, (u / NS) & 1, abort_flag, a.err, a.wait_cycles)) break;
           landed = true;
           tma_store_5d(tensor ? &tm_vpool : &tm_kpool, dst, 0, 0, 0, 0, dp * a.num_heads_kv + g);
         }
@@ -424,7 +424,7 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
     if (lane == 0) {
       for (int u = max(0, issued - NS); u < issued; ++u) {
         volatile int no_abort = 0;
-        mbar_wait(smem_u32(&bars->full[u % NS]), (u / NS) & 1, &no_abort, a.err);
+        mbar_wait(smem_u32(&bars->full[u % NS]), (u / NS) & 1, &no_abort, a.err, kDrainCycles);
       }
     }
   } else if (has_work && L::kSplit && warp <= 2) {
@@ -432,15 +432,15 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(M, N, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(M, D, 0, 1);
-      bool ok = mbar_wait(smem_u32(&bars->q_full), 0, abort_flag, a.err);
+      bool ok = mbar_wait(smem_u32(&bars->q_full), 0, abort_flag, a.err, a.wait_cycles);
       for (int u = 0; u < T && ok; ++u) {
         const int stage = u % NS;
-        ok = mbar_wait(smem_u32(&bars->full[stage]), (u / NS) & 1, abort_flag, a.err);
+        ok = mbar_wait(smem_u32(&bars->full[stage]), (u / NS) & 1, abort_flag, a.err, a.wait_cycles);
         if (!ok) break;
         if (warp == 1) {
           // S_u overwrites the S/P buffer of P_{u-2}: its P.V must be complete
           if (u >= 2 && !mbar_wait(smem_u32(&bars->pv_done[0][u & 1]), ((u - 2) >> 1) & 1,
-                                   abort_flag, a.err)) {
+                                   abort_flag, a.err, a.wait_cycles)) {
             ok = false;
             break;
           }
@@ -457,7 +457,7 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
           }
           umma_commit(smem_u32(&bars->s_full[0][u & 1]));
         } else {
-          if (!mbar_wait(smem_u32(&bars->p_full[0][u & 1]), (u >> 1) & 1, abort_flag, a.err)) {
+          if (!mbar_wait(smem_u32(&bars->p_full[0][u & 1]), (u >> 1) & 1, abort_flag, a.err, a.wait_cycles)) {
             ok = false;
             break;
           }
@@ -475,7 +475,7 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
       }
       umma_commit(smem_u32(&bars->drain));
       volatile int no_abort = 0;
-      mbar_wait(smem_u32(&bars->drain), 0, &no_abort, a.err);
+      mbar_wait(smem_u32(&bars->drain), 0, &no_abort, a.err, kDrainCycles);
     }
   } else if (has_work && !L::kSplit && warp <= MT) {
     // ============ MMA issuer of row tile wi (one lane) ===========================
@@ -487,11 +487,11 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
       constexpr uint32_t idesc_qk = idesc_bf16_f32(M, N, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(M, D, 0, 1);
       const uint32_t q_base = sb + L::kQ;
-      bool ok = mbar_wait(smem_u32(&bars->q_full), 0, abort_flag, a.err);
+      bool ok = mbar_wait(smem_u32(&bars->q_full), 0, abort_flag, a.err, a.wait_cycles);
       // Key tile u: S goes to S/P buffer u % 2 of warpgroup wi; P.V_u accumulates
       // into warpgroup wi's O.
       auto issue_pv = [&](int u, int i) -> bool {
-        if (!mbar_wait(smem_u32(&bars->p_full[i][u & 1]), (u >> 1) & 1, abort_flag, a.err))
+        if (!mbar_wait(smem_u32(&bars->p_full[i][u & 1]), (u >> 1) & 1, abort_flag, a.err, a.wait_cycles))
           return false;
         tc_fence_after();
         D2F_PASS_MARK(2, 3 + i, u);
@@ -516,7 +516,7 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
       const bool idle = wi >= mt_live;  // a row tile without rows: only release stages
       for (int u = 0; u < T && ok; ++u) {
         const int stage = u % NS;
-        if (!mbar_wait(smem_u32(&bars->full[stage]), (u / NS) & 1, abort_flag, a.err)) {
+        if (!mbar_wait(smem_u32(&bars->full[stage]), (u / NS) & 1, abort_flag, a.err, a.wait_cycles)) {
           ok = false;
           break;
         }
@@ -550,7 +550,7 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
       // Drain: wait until every MMA issued above has completed.
       umma_commit(smem_u32(&bars->drain));
       volatile int no_abort = 0;
-      mbar_wait(smem_u32(&bars->drain), 0, &no_abort, a.err);
+      mbar_wait(smem_u32(&bars->drain), 0, &no_abort, a.err, kDrainCycles);
     }
   } else if (has_work) {
     // ============ softmax (a warpgroup per row tile, a thread per TMEM lane) =====
@@ -584,7 +584,7 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
     for (int u = 0; u < T && ok && live; ++u) {
       const int t = t0 + u;
       const int tile_lim = t < Tc ? C - t * N : n - (t - Tc) * N;  // valid keys of the tile
-      ok = mbar_wait(smem_u32(&bars->s_full[wg][u & 1]), (u >> 1) & 1, abort_flag, a.err);
+      ok = mbar_wait(smem_u32(&bars->s_full[wg][u & 1]), (u >> 1) & 1, abort_flag, a.err, a.wait_cycles);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       const bool pm = lane == 0 && warp == L::kFirstSoft + 4 * wg;  // first thread of the warpgroup
@@ -630,7 +630,7 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
         if (u > 0) {
           // every earlier P.V (MMAs complete in order) has landed in O
           ok = mbar_wait(smem_u32(&bars->pv_done[wg][(u - 1) & 1]), ((u - 1) >> 1) & 1, abort_flag,
-                         a.err);
+                         a.err, a.wait_cycles);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
@@ -704,7 +704,7 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
     }
     if (ok && live) {  // the last P.V product
       const int last = T - 1;
-      ok = mbar_wait(smem_u32(&bars->pv_done[wg][last & 1]), (last >> 1) & 1, abort_flag, a.err);
+      ok = mbar_wait(smem_u32(&bars->pv_done[wg][last & 1]), (last >> 1) & 1, abort_flag, a.err, a.wait_cycles);
       ok = __all_sync(0xffffffffu, ok);
     }
     tc_fence_after();
@@ -840,8 +840,15 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
     // 4) wait for the cs blocks this CTA owns, then arrive on the closing
     //    cluster barrier: once every CTA has arrived, every copy has landed and
     //    no staging block is still being read.
+    // The copies into this CTA are always issued (step 3 runs whatever happened
+    // before), so this wait ignores the abort flag and takes the full budget: a
+    // CTA must not leave while another CTA's copy may still land in its shared
+    // memory.
     bool got = true;
-    if (warp >= L::kFirstSoft) got = __all_sync(0xffffffffu, mbar_wait(recv_bar, 0, abort_flag, a.err));
+    if (warp >= L::kFirstSoft) {
+      volatile int no_abort = 0;
+      got = __all_sync(0xffffffffu, mbar_wait(recv_bar, 0, &no_abort, a.err, kDrainCycles));
+    }
     if (tid == 64) D2F_TRACE_MARK(0, 9);
     __syncwarp();
     cluster_arrive_relaxed();

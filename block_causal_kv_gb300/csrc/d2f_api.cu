@@ -283,6 +283,19 @@ int plan_commit(int total_q, int vocab, int dtype, int B, int num_splits, Commit
 }
 
 }  // namespace
+
+// The leading bytes of a commit workspace that must be zero before a call (the
+// per-block and per-sequence arrival counters; the rest is written before it is
+// read).
+int commit_zeroed_prefix(int total_q, int vocab, int dtype, int block_size, int num_splits,
+                         size_t *bytes) {
+  CommitPlan p{};
+  const int st = plan_commit(total_q, vocab, dtype, block_size, num_splits, &p);
+  if (st != D2F_OK) return st;
+  *bytes = p.off_blkgap;
+  return D2F_OK;
+}
+
 }  // namespace d2f
 
 using namespace d2f;
@@ -395,6 +408,13 @@ int attn_entry(const void *q, const void *k_win, const void *v_win, const void *
   a.tc_stages = p.stages;
   a.tc_mt = p.mt > 0 ? p.mt : 1;
   a.longest_first = p.longest_first ? 1 : 0;
+  // D2F_WAIT_CYCLES shortens the budget of the waits on another role's work (a
+  // test switch for the give-up path; copies and MMAs are still drained in full)
+  a.wait_cycles = kWaitCycles;
+  if (const char *e = getenv("D2F_WAIT_CYCLES")) {
+    const long long v = atoll(e);
+    if (v > 0 && v < kWaitCycles) a.wait_cycles = v;
+  }
   a.counters = reinterpret_cast<int32_t *>(workspace);
   a.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) + p.off_ml);
   a.ws_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + p.off_o);

@@ -16,6 +16,10 @@ namespace d2f {
 // ---------------------------------------------------------------------------
 void set_last_error(const char *fmt, ...);
 int num_sms_current_device();
+// Bytes at the start of a commit workspace that must be zero before a call (its
+// arrival counters); the plan of d2f_commit_workspace_size.
+int commit_zeroed_prefix(int total_q, int vocab, int dtype, int block_size, int num_splits,
+                         size_t *bytes);
 // Programmatic dependent launch on every kernel launch unless D2F_PDL=0 (a
 // switch for comparing launch overlap; results are identical either way).
 bool pdl_enabled();
@@ -23,6 +27,12 @@ bool pdl_enabled();
 // Bounded waits give up after this many SM clock cycles (about one second at
 // the GB300's clocks), set D2F_ERR_TIMEOUT in the error word and unwind.
 constexpr long long kWaitCycles = 2000000000LL;
+// Waits that only drain work this CTA already issued (copies landing, MMAs
+// completing) give up after ~1 ms: far longer than a copy or an MMA takes.
+// After another role gave up, such a wait may be on a phase that can no longer
+// complete (a stage that one producer issued and another abandoned); it then
+// ends here instead of after kWaitCycles.
+constexpr long long kDrainCycles = 2000000LL;
 
 // ---------------------------------------------------------------------------
 // Launch arguments
@@ -51,6 +61,8 @@ struct AttnArgs {
   int part;                // tensor-core path: keys attended: 0 all, 1 cached only, 2 window only
   const void *prev_out;    // part 2: a kept cached part to compose with ([total_q][Hq][D], as out)
   const float *prev_lse;   // ... its natural-log normaliser [total_q][Hq]; NULL: no composition
+  long long wait_cycles; // tensor-core path: budget of each wait on another role's work
+                         // (kWaitCycles; less only to test the give-up path)
   int32_t *counters;     // [batch * Hkv * m_tiles] merge arrival counters (zero at rest)
   float2 *ws_ml;         // [num_splits][total_q * Hq] (max in log2 units, sum)
   float *ws_o;           // [num_splits][total_q * Hq][head_dim] unnormalised partial output
@@ -202,15 +214,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Wait for the phase with the given parity; gives up after kWaitCycles or when
-// another thread of the CTA has already given up (shared abort flag).
+// Wait for the phase with the given parity; gives up after `budget` SM cycles
+// (kWaitCycles unless a caller passes less) or when another thread of the CTA
+// has already given up (shared abort flag).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          int32_t *err) {
+                                          int32_t *err, long long budget = kWaitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > budget) {
       *abort_flag = 1;
       set_err(err, D2F_ERR_TIMEOUT);
       return false;

@@ -251,3 +251,35 @@ def test_append_writes_stay_inside_the_pool():
     _canary_intact(vb, "v_pool")
     kp, vp = oracle.kv_append(p.k_win, p.v_win, p.src_row, p.dst_page, p.k_pool, p.v_pool, 16)
     assert torch.equal(kpool.cpu(), kp) and torch.equal(vpool.cpu(), vp)
+
+
+ERR_TIMEOUT = 5
+
+
+@pytest.mark.parametrize("name,deep", [("llada", None), ("dream", "0"), ("dream", "1"),
+                                       ("long_b32", "1")])
+@pytest.mark.parametrize("splits", [1, 3])
+def test_wait_budget_runs_out_cleanly(name, deep, splits, monkeypatch):
+    """The tensor-core attention's waits on another role's work are bounded. With
+    their budget cut to one cycle (D2F_WAIT_CYCLES, a test switch) they run out:
+    the kernel records D2F_ERR_TIMEOUT, every CTA drains the copies and MMAs it
+    issued (those waits keep their own budget) and returns, cluster peers still
+    exchange their partials; the launch completes. A normal call right after, on
+    the same buffers, matches the oracle. Single-split and cluster-composed
+    launches, the one-issuer and the split-issuer variants."""
+    dev = device()
+    if deep is not None:
+        monkeypatch.setenv("D2F_TC_DEEP", deep)
+    p = synth.make_problem(synth.small(name))
+    g = p.to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    monkeypatch.setenv("D2F_WAIT_CYCLES", "1")
+    _attn(g, p, splits, err=err)
+    assert int(err.item()) == ERR_TIMEOUT
+    monkeypatch.delenv("D2F_WAIT_CYCLES")
+    err.zero_()
+    out, lse = _attn(g, p, splits, err=err)
+    assert int(err.item()) == 0
+    ref, ref_lse = oracle.block_attn(p.q, p.k_win, p.v_win, p.k_pool, p.v_pool, p.page_table,
+                                     p.ctx_len, p.q_start, p.w.block_size)
+    check_attention(out, lse, ref, ref_lse, torch.bfloat16, "after the timeout " + name)

@@ -71,3 +71,73 @@ def test_rejects_requests_beyond_its_scratch():
                                 None, None)
     assert st == 6
     assert b"scratch" in lib.d2f_last_error_string()
+
+
+def _random_problem(dev, total_q, vocab, B, seed):
+    """A decode state over `total_q` rows (every row masked, random phases and
+    thresholds) with N(0, 3) logits drawn on the device."""
+    g = torch.Generator(device=dev).manual_seed(seed)
+    logits = (torch.randn((total_q, vocab), generator=g, device=dev) * 3).to(torch.bfloat16)
+    tokens = torch.full((total_q,), vocab, dtype=torch.int32, device=dev)
+    masked = torch.ones(total_q, dtype=torch.uint8, device=dev)
+    q_start = torch.tensor([0, total_q], dtype=torch.int32, device=dev)
+    phase = torch.randint(0, 2, (total_q // B,), generator=g, device=dev).to(torch.uint8)
+    tau = torch.full((1,), 1e-4, dtype=torch.float32, device=dev)
+    return logits, tokens, masked, q_start, phase, tau
+
+
+@pytest.mark.parametrize("num_splits,total_q,vocab", [(64, 2032, 126464), (1, 65520, 2048)])
+def test_largest_requests_that_fit(num_splits, total_q, vocab):
+    """At block size 16 the scratch holds 2,032 rows at 64 vocabulary slices (the
+    largest multiple of the block that fits) and the API's largest row count at
+    one slice; both run and match d2f_commit. Sixteen rows more at 64 slices are
+    refused before anything is enqueued."""
+    dev = device()
+    B = 16
+    logits, tokens, masked, q_start, phase, tau = _random_problem(dev, total_q, vocab, B, 5)
+    need = d2f.commit_workspace_size(total_q, vocab, B, d2f.BF16, num_splits)
+    assert need <= 2 << 20
+    tok_a, msk_a, tok_b, msk_b = tokens.clone(), masked.clone(), tokens.clone(), masked.clone()
+    kw = dict(block_size=B, mask_id=vocab, num_splits=num_splits)
+    res_a = {k: torch.empty(n, dtype=t, device=dev) for k, n, t in (
+        ("conf", total_q, torch.float32), ("argmax", total_q, torch.int32),
+        ("block_remaining", total_q // B, torch.int32))}
+    d2f.commit_noalloc(logits, tok_a, msk_a, q_start, phase, tau, conf=res_a["conf"],
+                       argmax=res_a["argmax"], block_remaining=res_a["block_remaining"], **kw)
+    res_b = d2f.commit(logits, tok_b, msk_b, q_start, phase, tau, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(tok_a, tok_b) and torch.equal(msk_a, msk_b)
+    assert torch.equal(res_a["argmax"], res_b["argmax"])
+    assert torch.equal(res_a["block_remaining"], res_b["block_remaining"])
+    rel = ((res_a["conf"] - res_b["conf"]).abs() / res_b["conf"]).max().item()
+    assert rel <= CONF_RTOL
+    if num_splits == 64:
+        lib = d2f.load()
+        st = lib.d2f_commit_noalloc(None, vocab, d2f.BF16, vocab, total_q + 16, None, None, None,
+                                    None, None, None, 1, total_q + 16, B, ctypes.c_int32(0), None,
+                                    None, None, num_splits, None, None)
+        assert st == 6
+
+
+def test_python_wrapper_across_shapes():
+    """d2f.commit_noalloc (the binding) on three differently shaped calls in a row
+    on the one shared scratch -- each call clears only the counters it needs --
+    against d2f_commit with its own workspace."""
+    dev = device()
+    for name in ("llada", "ragged", "dream", "llada"):
+        p = synth.make_problem(synth.small(name))
+        g = p.to(dev)
+        B = p.w.block_size
+        n = p.w.total_q
+        tok_a, msk_a, tok_b, msk_b = g.tokens.clone(), g.masked.clone(), g.tokens.clone(), g.masked.clone()
+        outs = [torch.empty(n, dtype=torch.float32, device=dev),
+                torch.empty(n, dtype=torch.int32, device=dev),
+                torch.empty(n // B, dtype=torch.int32, device=dev)]
+        d2f.commit_noalloc(g.logits, tok_a, msk_a, g.q_start, g.block_phase, g.tau, block_size=B,
+                           mask_id=p.mask_id, conf=outs[0], argmax=outs[1],
+                           block_remaining=outs[2])
+        ref = d2f.commit(g.logits, tok_b, msk_b, g.q_start, g.block_phase, g.tau, block_size=B,
+                         mask_id=p.mask_id)
+        torch.cuda.synchronize()
+        assert torch.equal(tok_a, tok_b) and torch.equal(msk_a, msk_b), name
+        assert torch.equal(outs[1], ref["argmax"]) and torch.equal(outs[2], ref["block_remaining"])
