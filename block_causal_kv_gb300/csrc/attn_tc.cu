@@ -74,6 +74,7 @@ constexpr int N = kTcKeys;                     // 64 keys per tile
 constexpr uint32_t kTmemO = 128;               // O within a warpgroup's columns (S / P: 2 x 64 before it)
 constexpr int kMaxCluster = 8;
 constexpr int kBarSetup = 1;                   // named barrier: MMA warp + softmax warps
+constexpr int kBarSk = 2;                      // named barrier: the softmax warps (stream-K form)
 constexpr int kSmemTwoPerSm = 115712;          // dynamic bytes that still let 2 CTAs share an SM
 static_assert(kMaxLongestFirstBatch * 4 + 4 <= 2 * 64 * 64 * 2, "ordering scratch fits a ring stage");
 
@@ -152,6 +153,7 @@ struct Bars {
       drain, recv;
   uint32_t tmem_base;
   int abort_flag;
+  int sk[6];  // stream-K form: the share's first (sequence, KV head, tile), length, W (lo, hi)
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
@@ -939,6 +941,602 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
 }
 
 // ---------------------------------------------------------------------------
+// Stream-K form (head_dim 128, one 128-row tile per (sequence, KV head), the
+// 6-stage ring at one CTA per SM)
+//
+// With one split per (sequence, KV head) and fewer of them than SMs, the split
+// layout above leaves SMs idle (long-context batch 4 x 32 heads: 128 CTAs on
+// 152 SMs, each streaming at the ~50 GB/s its MMA / softmax chain allows). Here
+// the key tiles of every (sequence, KV head) are laid end to end (pair p =
+// b * Hkv + g, tiles cache first then window, the order above) and each of
+// `grid` CTAs takes an equal contiguous share: a few whole pairs plus a piece
+// of a pair at either end. The roles are those of the one-CTA variant (warp 0
+// loads, warp 1 issues Q K^T, warp 2 P V, warps 3-6 softmax); they walk the
+// share's segments in the same order with one running tile count, so the ring
+// stages and the S / P buffers keep their phases across segments. At the start
+// of a segment the softmax warps load its Q rows (the previous segment's last
+// Q K^T has completed: they waited for its S) and the Q K^T issuer waits for
+// them; the first P V of a segment overwrites O (the softmax warps read the
+// previous O before they release the segment's first P).
+//
+// A segment that is a whole pair writes its output directly. A piece of a
+// pair writes its rows normalised (O / l, bf16) with their (max, sum) into one
+// of the CTA's two partial slots (0: the share's first segment, 1: its last)
+// and arrives on the pair's counter; the last CTA to arrive composes the
+// pair's pieces in log space and writes the output (the same composition as
+// the cluster path, through global memory). Every wait is bounded as above.
+// ---------------------------------------------------------------------------
+
+// The key tiles of sequence b (cache, then window) and its window layout;
+// T = 0 for a sequence without window rows or whose metadata contradicts the
+// host sizes (recorded as D2F_ERR_INVALID_ARG by warp 0).
+struct SkSeq {
+  int q0, n, C, Tc, T;
+  bool ok;
+};
+__device__ __forceinline__ SkSeq sk_seq(const AttnArgs &a, int b) {
+  SkSeq s;
+  s.ok = load_seq_meta(a, b, s.q0, s.n, s.C) && a.group * s.n <= kTcRows;
+  s.Tc = s.ok ? (s.C + N - 1) / N : 0;
+  s.T = (s.ok && s.n > 0) ? s.Tc + (s.n + N - 1) / N : 0;
+  return s;
+}
+
+// The CTA whose share holds tile position u of the line of W tiles.
+__device__ __forceinline__ int sk_cta_of(long long u, long long W, int grid) {
+  return (int)(((u + 1) * grid - 1) / W);
+}
+__device__ __forceinline__ long long sk_start(int c, long long W, int grid) {
+  return (long long)c * W / grid;
+}
+
+template <int D>
+__global__ void __launch_bounds__((Layout<D, 6, 128, 1>::kThreads), 1)
+    attn_sk_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tm_kpool,
+                   const __grid_constant__ CUtensorMap tm_vpool,
+                   const __grid_constant__ CUtensorMap tm_kwin,
+                   const __grid_constant__ CUtensorMap tm_vwin) {
+  constexpr int NS = 6, QR = 128;
+  using L = Layout<D, NS, QR, 1>;
+  static_assert(L::kSplit && L::kProducers == 1 && L::kFirstSoft == 3, "one-CTA roles");
+  extern __shared__ uint8_t smem_raw[];
+  {
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    uint32_t dyn;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+    if (pad + L::kBytes > dyn) {
+      if (threadIdx.x == 0) set_err(a.err, D2F_ERR_UNSUPPORTED);
+      return;
+    }
+  }
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  Bars *bars = reinterpret_cast<Bars *>(smem + L::kBars);
+  volatile int *abort_flag = &bars->abort_flag;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c = blockIdx.x, grid = gridDim.x;
+  const int Hkv = a.num_heads_kv, G = a.group, H = a.num_heads_q, B = a.block_size;
+  const int ppt = N / B;  // pages (or window blocks) per tile
+
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(smem_u32(&bars->full[i]), 1);
+      mbar_init(smem_u32(&bars->empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bars->s_full[0][i]), 1);
+      mbar_init(smem_u32(&bars->p_full[0][i]), QR);
+      mbar_init(smem_u32(&bars->pv_done[0][i]), 1);
+    }
+    mbar_init(smem_u32(&bars->q_full), QR);
+    mbar_init(smem_u32(&bars->drain), 2);
+    bars->abort_flag = 0;
+    mbar_fence_init();
+    tma_prefetch_desc(&tm_kpool);
+    tma_prefetch_desc(&tm_vpool);
+    tma_prefetch_desc(&tm_kwin);
+    tma_prefetch_desc(&tm_vwin);
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&bars->tmem_base), L::kTmemCols);
+    tmem_relinquish();
+  }
+  grid_dependency_wait();  // inputs may come from the previous kernel in the stream
+
+  // ---- the share: W tiles in all, this CTA's [s0, s1); warp 0 locates s0 ----
+  if (warp == 0) {
+    long long tot = 0;
+    bool bad = false;
+    for (int b = lane; b < a.batch; b += 32) {
+      const SkSeq q = sk_seq(a, b);
+      tot += (long long)q.T * Hkv;
+      bad |= !q.ok;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    if (__any_sync(0xffffffffu, bad) && lane == 0 && c == 0) set_err(a.err, D2F_ERR_INVALID_ARG);
+    const long long W = tot;
+    const long long s0 = W > 0 ? sk_start(c, W, grid) : 0, s1 = W > 0 ? sk_start(c + 1, W, grid) : 0;
+    int b0 = 0, g0 = 0, ta0 = 0;
+    long long run = 0;
+    for (int base = 0; base < a.batch && s1 > s0; base += 32) {
+      const int b = base + lane;
+      const SkSeq q = b < a.batch ? sk_seq(a, b) : SkSeq{0, 0, 0, 0, 0, false};
+      const long long t = (long long)q.T * Hkv;
+      long long incl = t;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const long long excl = run + incl - t;
+      const bool hit = t > 0 && excl <= s0 && s0 < excl + t;
+      const unsigned who = __ballot_sync(0xffffffffu, hit);
+      if (hit) {
+        const long long rel = s0 - excl;
+        b0 = b;
+        g0 = (int)(rel / q.T);
+        ta0 = (int)(rel - (long long)g0 * q.T);
+      }
+      if (who) {
+        const int src = __ffs(who) - 1;
+        b0 = __shfl_sync(0xffffffffu, b0, src);
+        g0 = __shfl_sync(0xffffffffu, g0, src);
+        ta0 = __shfl_sync(0xffffffffu, ta0, src);
+        break;
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      bars->sk[0] = b0;
+      bars->sk[1] = g0;
+      bars->sk[2] = ta0;
+      bars->sk[3] = (int)(s1 - s0);
+      bars->sk[4] = (int)(W & 0xffffffffLL);
+      bars->sk[5] = (int)(W >> 32);
+    }
+  }
+  if (warp >= 1) {  // TMEM address, published by warp 1
+    tc_fence_before();
+    named_sync(kBarSetup, L::kThreads - 32);
+    tc_fence_after();
+  }
+  __syncthreads();
+  const uint32_t tmem = bars->tmem_base;
+  const int b0 = bars->sk[0], g0 = bars->sk[1], ta0 = bars->sk[2], R = bars->sk[3];
+  const long long W = (long long)(uint32_t)bars->sk[4] | ((long long)bars->sk[5] << 32);
+  const long long s0 = W > 0 ? sk_start(c, W, grid) : 0;
+  grid_launch_dependents();
+
+  // Every role walks the share's segments in the same order: tiles [ta, tb) of
+  // pair (b, g), then the next pair from its first tile, until R tiles are done.
+  // `gu` counts the tiles of the whole share (ring stage gu % NS, S / P buffer
+  // gu % 2, and their phases).
+  if (warp == 0) {
+    // ======================= TMA producer ======================================
+    const int box = lane;  // box i: tensor i / ppt (0 = K, 1 = V), page or block i % ppt
+    const bool lane_on = box < 2 * ppt;
+    const int tensor = lane_on ? box / ppt : 0, slot = lane_on ? box % ppt : 0;
+    int gu = 0;
+    bool ok = true;
+    int b = b0, g = g0, ta = ta0, rem = R;
+    while (ok && rem > 0 && b < a.batch) {
+      const SkSeq q = sk_seq(a, b);
+      const int tb = min(q.T, ta + rem);
+      const int n_pages = (q.C + B - 1) / B;
+      const int32_t *pt = a.page_table + (int64_t)b * a.max_pages_per_seq;
+      auto fetch = [&](int base) -> int {
+        const int lp = base + lane;
+        return (lp < n_pages && lp < tb * ppt) ? __ldg(pt + lp) : -1;
+      };
+      int chunk = ta * ppt;  // logical page held by lane 0 of ids_cur
+      int ids_cur = ta < q.Tc ? fetch(chunk) : -1;
+      int ids_next = ta < q.Tc ? fetch(chunk + 32) : -1;
+      for (int t = ta; t < tb; ++t, ++gu) {
+        const int stage = gu % NS;
+        if (gu >= NS) {
+          int w = 1;
+          if (lane == 0)
+            w = mbar_wait(smem_u32(&bars->empty[stage]), ((gu / NS) - 1) & 1, abort_flag, a.err,
+                          a.wait_cycles);
+          if (!__shfl_sync(0xffffffffu, w, 0)) {
+            ok = false;
+            break;
+          }
+        }
+        int src = -1;  // a physical page or a window row; -1: nothing to load
+        if (t < q.Tc) {
+          const int lp0 = t * ppt;
+          if (lp0 - chunk >= 32) {  // warp-uniform: move to the next 32 ids
+            chunk += 32;
+            ids_cur = ids_next;
+            ids_next = fetch(chunk + 32);
+          }
+          const int pg = __shfl_sync(0xffffffffu, ids_cur, (lp0 - chunk + slot) & 31);
+          if (lane_on && (lp0 + slot) * B < q.C) {
+            if (pg >= 0 && pg < a.num_pages)
+              src = pg;
+            else
+              set_err(a.err, D2F_ERR_BAD_INDEX);
+          }
+        } else if (lane_on) {
+          const int w0 = (t - q.Tc) * N + slot * B;  // first window row of this block
+          if (w0 < q.n) src = q.q0 + w0;
+        }
+        const unsigned have = __ballot_sync(0xffffffffu, src >= 0);
+        const uint32_t full = smem_u32(&bars->full[stage]);
+        if (lane == 0) mbar_arrive_expect_tx(full, __popc(have) * (uint32_t)B * D * 2u);
+        __syncwarp();
+        const uint32_t dst = sb + L::kRing + stage * L::kStage + tensor * L::kKBytes +
+                             slot * (B / 8) * L::kGroupBytes;
+        if (src >= 0) {
+          if (t < q.Tc)
+            tma_load_5d(dst, tensor ? &tm_vpool : &tm_kpool, full, 0, 0, 0, 0, src * Hkv + g);
+          else
+            tma_load_5d(dst, tensor ? &tm_vwin : &tm_kwin, full, 0, 0, 0, src >> 3, g);
+        }
+      }
+      rem -= max(0, tb - ta);
+      ta = 0;
+      if (++g == Hkv) {
+        g = 0;
+        ++b;
+      }
+    }
+    // Drain: every issued stage has landed before the CTA moves on.
+    if (lane == 0) {
+      for (int u = max(0, gu - NS); u < gu; ++u) {
+        volatile int no_abort = 0;
+        mbar_wait(smem_u32(&bars->full[u % NS]), (u / NS) & 1, &no_abort, a.err, kDrainCycles);
+      }
+    }
+  } else if (warp == 1 || warp == 2) {
+    // ============ MMA issuers: warp 1 S = Q K^T, warp 2 O += P V =============
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(M, N, 0, 0);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(M, D, 0, 1);
+      int gu = 0, k = 0;  // tiles and segments so far
+      bool ok = true;
+      int b = b0, g = g0, ta = ta0, rem = R;
+      while (ok && rem > 0 && b < a.batch) {
+        const SkSeq q = sk_seq(a, b);
+        const int tb = min(q.T, ta + rem);
+        if (tb > ta && warp == 1)  // this segment's Q rows are in shared memory
+          ok = mbar_wait(smem_u32(&bars->q_full), k & 1, abort_flag, a.err, a.wait_cycles);
+        for (int t = ta; t < tb && ok; ++t, ++gu) {
+          const int stage = gu % NS;
+          ok = mbar_wait(smem_u32(&bars->full[stage]), (gu / NS) & 1, abort_flag, a.err, a.wait_cycles);
+          if (!ok) break;
+          if (warp == 1) {
+            // S_gu overwrites the S / P buffer of P_{gu-2}: its P V must be complete
+            if (gu >= 2 && !mbar_wait(smem_u32(&bars->pv_done[0][gu & 1]), ((gu - 2) >> 1) & 1,
+                                      abort_flag, a.err, a.wait_cycles)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t k_base = sb + L::kRing + stage * L::kStage;
+#pragma unroll
+            for (int h = 0; h < L::kHalves; ++h) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t ad = smem_desc_sw128(sb + L::kQ + h * L::kQHalf + kk * 32, 16, 1024);
+                const uint64_t bd = smem_desc_sw128(k_base + h * 1024 + kk * 32, 16, L::kGroupBytes);
+                umma_bf16(tmem + (gu & 1) * N, ad, bd, idesc_qk, (h | kk) ? 1u : 0u);
+              }
+            }
+            umma_commit(smem_u32(&bars->s_full[0][gu & 1]));
+          } else {
+            if (!mbar_wait(smem_u32(&bars->p_full[0][gu & 1]), (gu >> 1) & 1, abort_flag, a.err,
+                           a.wait_cycles)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t v_base = sb + L::kRing + stage * L::kStage + L::kKBytes;
+            const bool first = t == ta;  // the segment's first P V overwrites O
+#pragma unroll
+            for (int ks = 0; ks < N / 16; ++ks) {
+              const uint64_t bd = smem_desc_sw128(v_base + ks * 2 * L::kGroupBytes, 1024, L::kGroupBytes);
+              umma_bf16_tmem_a(tmem + kTmemO, tmem + (gu & 1) * N + ks * 8, bd, idesc_pv,
+                               (!first || ks > 0) ? 1u : 0u);
+            }
+            umma_commit(smem_u32(&bars->pv_done[0][gu & 1]));
+            umma_commit(smem_u32(&bars->empty[stage]));
+          }
+        }
+        if (tb > ta) ++k;
+        rem -= max(0, tb - ta);
+        ta = 0;
+        if (++g == Hkv) {
+          g = 0;
+          ++b;
+        }
+      }
+      umma_commit(smem_u32(&bars->drain));
+      volatile int no_abort = 0;
+      mbar_wait(smem_u32(&bars->drain), 0, &no_abort, a.err, kDrainCycles);
+    }
+  } else {
+    // ============ softmax: one warpgroup, a thread per query row (TMEM lane) =====
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
+    const float sl2 = a.scale_log2;
+    int gu = 0;
+    bool ok = true;
+    int b = b0, g = g0, ta = ta0, rem = R;
+    long long pre_p = s0 - ta0;  // position of the current pair's first tile on the line
+    while (ok && rem > 0 && b < a.batch) {
+      const SkSeq q = sk_seq(a, b);
+      const int tb = min(q.T, ta + rem);
+      if (tb > ta) {
+        const int rows_total = G * q.n;
+        const bool rv = row < rows_total;
+        const int64_t hr = (int64_t)(q.q0 + row / G) * H + g * G + row % G;  // valid where rv
+        {
+          // This segment's Q rows into the 128-byte-swizzled K-major layout (the
+          // previous segment's Q K^T have all completed: their S were waited for).
+          constexpr int kQc = D / 8;
+          uint4 qv[kQc];
+          const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(a.q) + hr * D);
+#pragma unroll
+          for (int cq = 0; cq < kQc; ++cq) qv[cq] = rv ? __ldg(src + cq) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int cq = 0; cq < kQc; ++cq) {
+            const uint32_t dst = sb + L::kQ + (cq >> 3) * L::kQHalf + (row >> 3) * 1024 + (row & 7) * 128 +
+                                 (((cq & 7) ^ (row & 7)) << 4);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(qv[cq].x),
+                         "r"(qv[cq].y), "r"(qv[cq].z), "r"(qv[cq].w)
+                         : "memory");
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(smem_u32(&bars->q_full));
+        }
+        const int win_end = rv ? ((row / G) / B + 1) * B : 0;
+        float m_ref = -INFINITY, l = 0.f;
+        for (int t = ta; t < tb && ok; ++t, ++gu) {
+          const int tile_lim = t < q.Tc ? q.C - t * N : q.n - (t - q.Tc) * N;  // valid keys
+          ok = mbar_wait(smem_u32(&bars->s_full[0][gu & 1]), (gu >> 1) & 1, abort_flag, a.err,
+                         a.wait_cycles);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint32_t sv[N];
+          const uint32_t s_addr = lane_addr + (gu & 1) * N;
+          tmem_ld64(s_addr, sv);
+          int lim = t < q.Tc ? tile_lim : win_end - (t - q.Tc) * N;
+          lim = rv ? max(0, min(lim, N)) : 0;
+          float sf[N];
+#pragma unroll
+          for (int cc = 0; cc < N; ++cc) sf[cc] = __uint_as_float(sv[cc]);
+          if (!__all_sync(0xffffffffu, lim >= N)) {  // ragged tile: hide masked keys
+#pragma unroll
+            for (int cc = 0; cc < N; ++cc)
+              if (cc >= lim) sf[cc] = -INFINITY;
+          }
+          float t1[22], t2[8];
+#pragma unroll
+          for (int cc = 0; cc < 21; ++cc) t1[cc] = fmax3(sf[3 * cc], sf[3 * cc + 1], sf[3 * cc + 2]);
+          t1[21] = sf[63];
+#pragma unroll
+          for (int cc = 0; cc < 7; ++cc) t2[cc] = fmax3(t1[3 * cc], t1[3 * cc + 1], t1[3 * cc + 2]);
+          t2[7] = t1[21];
+          const float tmax = fmax3(fmax3(t2[0], t2[1], t2[2]), fmax3(t2[3], t2[4], t2[5]),
+                                   fmaxf(t2[6], t2[7])) * sl2;
+          // lazy rescale: keep the reference max unless the tile max exceeds it by 2^8
+          const bool need = tmax > m_ref + 8.0f;
+          if (__any_sync(0xffffffffu, need)) {
+            const float m_new = need ? tmax : m_ref;
+            const float alpha = need ? fast_exp2(m_ref - m_new) : 1.0f;
+            l *= alpha;
+            if (t > ta) {  // every earlier P V of this segment has landed in O
+              ok = mbar_wait(smem_u32(&bars->pv_done[0][(gu - 1) & 1]), ((gu - 1) >> 1) & 1,
+                             abort_flag, a.err, a.wait_cycles);
+              if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+#pragma unroll
+              for (int ch = 0; ch < D / 32; ++ch) {
+                uint32_t o[32];
+                const uint32_t oa = lane_addr + kTmemO + ch * 32;
+                tmem_ld32(oa, o);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                tmem_st32(oa, o);
+              }
+              tmem_wait_st();
+            }
+            m_ref = m_new;
+          }
+          const float mb = m_ref == -INFINITY ? 0.f : m_ref;
+          uint32_t pk[N / 2];
+#pragma unroll
+          for (int j = 0; j < N / 2; ++j) {
+            float x0, x1;
+            fma2_bc(x0, x1, sf[2 * j], sf[2 * j + 1], sl2, -mb);
+            pk[j] = ex2_bf16x2(pack_bf16x2(x0, x1));
+          }
+          float ps0[N / 4], ps1[N / 4];
+#pragma unroll
+          for (int j = 0; j < N / 4; ++j)
+            add2(ps0[j], ps1[j], __uint_as_float(pk[2 * j] << 16),
+                 __uint_as_float(pk[2 * j] & 0xffff0000u), __uint_as_float(pk[2 * j + 1] << 16),
+                 __uint_as_float(pk[2 * j + 1] & 0xffff0000u));
+#pragma unroll
+          for (int w = N / 8; w >= 1; w >>= 1)
+#pragma unroll
+            for (int cc = 0; cc < w; ++cc)
+              add2(ps0[cc], ps1[cc], ps0[2 * cc], ps1[2 * cc], ps0[2 * cc + 1], ps1[2 * cc + 1]);
+          l += ps0[0] + ps1[0];
+          tmem_st32(s_addr, pk);
+          tmem_wait_st();
+          // a ragged tile's V rows past its valid keys: cleared before its P V (0 * NaN)
+          if (row < N && row >= tile_lim) {
+            const uint32_t v_row = sb + L::kRing + (gu % NS) * L::kStage + L::kKBytes +
+                                   (row >> 3) * L::kGroupBytes + (row & 7) * 128;
+#pragma unroll
+            for (int h = 0; h < L::kHalves; ++h)
+#pragma unroll
+              for (int cc = 0; cc < 8; ++cc)
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(v_row + h * 1024 + (cc << 4)),
+                             "r"(0u)
+                             : "memory");
+            fence_proxy_async_smem();
+          }
+          tc_fence_before();
+          mbar_arrive(smem_u32(&bars->p_full[0][gu & 1]));
+        }
+        // the segment's last P V product (when every tile went through)
+        if (ok) {
+          ok = mbar_wait(smem_u32(&bars->pv_done[0][(gu - 1) & 1]), ((gu - 1) >> 1) & 1, abort_flag,
+                         a.err, a.wait_cycles);
+          ok = __all_sync(0xffffffffu, ok);
+        }
+        // Every softmax thread arrives here for every segment it started, so a
+        // give-up in any of the four warps is known to all before the epilogue's
+        // barriers (a warp that passed its waits must not wait there for one that
+        // left).
+        ok = named_sync_and(kBarSk, QR, ok);
+        if (!ok) break;
+        tc_fence_after();
+
+        // ---- epilogue of the segment ----
+        const int cf = sk_cta_of(pre_p, W, grid), cl = sk_cta_of(pre_p + q.T - 1, W, grid);
+        const bool any = __any_sync(0xffffffffu, rv);  // warp-uniform TMEM reads
+        if (cf == cl) {  // the whole pair: the output directly
+          const float inv = l > 0.f ? 1.0f / l : 0.f;
+#pragma unroll
+          for (int ch = 0; ch < D / 32 && any; ++ch) {
+            uint32_t o[32];
+            tmem_ld32(lane_addr + kTmemO + ch * 32, o);
+            if (rv) {
+              uint32_t w[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                w[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
+              uint4 *d4 = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(a.out) + hr * D + ch * 32);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) d4[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+            }
+          }
+          if (rv && a.lse_out)
+            a.lse_out[hr] = l > 0.f ? (m_ref + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+        } else {
+          // A piece: its rows (O / l, bf16) and (max, sum) into this CTA's slot,
+          // then one arrival on the pair's counter.
+          const int which = (c == cf && s0 < pre_p) ? 1 : 0;  // the share's last segment : first
+          uint8_t *slot = a.sk_slots + (size_t)(2 * c + which) * kSkSlotBytes;
+          const bool keep = rv && l > 0.f;
+          const float inv = keep ? 1.0f / l : 0.f;
+#pragma unroll
+          for (int ch = 0; ch < D / 32 && any; ++ch) {
+            uint32_t o[32];
+            tmem_ld32(lane_addr + kTmemO + ch * 32, o);
+            if (keep) {
+              uint32_t w[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                w[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
+              uint4 *d4 = reinterpret_cast<uint4 *>(slot + (size_t)row * D * 2 + ch * 64);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) d4[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+            }
+          }
+          reinterpret_cast<float2 *>(slot + (size_t)QR * D * 2)[row] =
+              make_float2(keep ? m_ref : -INFINITY, keep ? l : 0.f);
+          __threadfence();  // this row's piece before the arrival
+          named_sync(kBarSk, QR);
+          if (row == 0) {
+            int target = 0;  // CTAs with a share that touch the pair
+            for (int cc = cf; cc <= cl; ++cc) target += sk_start(cc + 1, W, grid) > sk_start(cc, W, grid);
+            const int pair = b * Hkv + g;
+            const int last = atomic_add_acq_rel(a.sk_cnt + pair, 1) == target - 1;
+            if (last) a.sk_cnt[pair] = 0;  // every piece of this launch is in
+            bars->sk[0] = last;
+          }
+          named_sync(kBarSk, QR);
+          if (bars->sk[0] && rv) {
+            // The last piece in: compose the pair's pieces of this row in log space.
+            float mx = -INFINITY;
+            for (int cc = cf; cc <= cl; ++cc) {
+              if (sk_start(cc + 1, W, grid) <= sk_start(cc, W, grid)) continue;
+              const int wc = (cc == cf && sk_start(cc, W, grid) < pre_p) ? 1 : 0;
+              const float2 ml = __ldcg(reinterpret_cast<const float2 *>(
+                  a.sk_slots + (size_t)(2 * cc + wc) * kSkSlotBytes + (size_t)QR * D * 2) + row);
+              if (ml.y > 0.f) mx = fmaxf(mx, ml.x);
+            }
+            float ws = 0.f;
+            for (int cc = cf; cc <= cl; ++cc) {
+              if (sk_start(cc + 1, W, grid) <= sk_start(cc, W, grid)) continue;
+              const int wc = (cc == cf && sk_start(cc, W, grid) < pre_p) ? 1 : 0;
+              const float2 ml = __ldcg(reinterpret_cast<const float2 *>(
+                  a.sk_slots + (size_t)(2 * cc + wc) * kSkSlotBytes + (size_t)QR * D * 2) + row);
+              if (ml.y > 0.f) ws += fast_exp2(ml.x - mx) * ml.y;
+            }
+            const float invs = ws > 0.f ? 1.0f / ws : 0.f;
+            for (int ch = 0; ch < D / 32; ++ch) {
+              float acc[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+              for (int cc = cf; cc <= cl; ++cc) {
+                if (sk_start(cc + 1, W, grid) <= sk_start(cc, W, grid)) continue;
+                const int wc = (cc == cf && sk_start(cc, W, grid) < pre_p) ? 1 : 0;
+                const uint8_t *sl = a.sk_slots + (size_t)(2 * cc + wc) * kSkSlotBytes;
+                const float2 ml = __ldcg(reinterpret_cast<const float2 *>(sl + (size_t)QR * D * 2) + row);
+                if (!(ml.y > 0.f)) continue;
+                const float wj = fast_exp2(ml.x - mx) * ml.y * invs;
+                const uint4 *p4 = reinterpret_cast<const uint4 *>(sl + (size_t)row * D * 2 + ch * 64);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const uint4 v = __ldcg(p4 + j);
+                  const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    acc[8 * j + 2 * e] = fmaf(wj, bf16_bits_to_float(vv[e] & 0xffffu), acc[8 * j + 2 * e]);
+                    acc[8 * j + 2 * e + 1] = fmaf(wj, bf16_bits_to_float(vv[e] >> 16), acc[8 * j + 2 * e + 1]);
+                  }
+                }
+              }
+              uint32_t w[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(acc[2 * j], acc[2 * j + 1]);
+              uint4 *d4 = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(a.out) + hr * D + ch * 32);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) d4[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+            }
+            if (a.lse_out) a.lse_out[hr] = ws > 0.f ? (mx + __log2f(ws)) * 0.6931471805599453f : -INFINITY;
+          }
+          named_sync(kBarSk, QR);  // bars->sk[0] is reused by the next piece
+        }
+      }
+      rem -= max(0, tb - ta);
+      pre_p += q.T;
+      ta = 0;
+      if (++g == Hkv) {
+        g = 0;
+        ++b;
+      }
+    }
+    tc_fence_before();
+  }
+
+  // ---- teardown ---------------------------------------------------------------
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(bars->tmem_base, L::kTmemCols);
+}
+
+// ---------------------------------------------------------------------------
 // Host side: tensor maps and launch
 // ---------------------------------------------------------------------------
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -990,14 +1588,15 @@ cudaError_t ensure_attrs() {
   return e;
 }
 
-template <int D, int NS, int QR, int MT>
-cudaError_t launch_d(const AttnArgs &a, cudaStream_t s, char *why, size_t why_len) {
+// The four K/V tensor maps of a launch (pool K, pool V, window K, window V).
+template <int D>
+cudaError_t encode_maps(const AttnArgs &a, CUtensorMap &kp, CUtensorMap &vp, CUtensorMap &kw,
+                        CUtensorMap &vw, char *why, size_t why_len) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) {
     snprintf(why, why_len, "cuTensorMapEncodeTiled is not available from the driver");
     return cudaErrorNotSupported;
   }
-  CUtensorMap kp, vp, kw, vw;
   // 5-D views whose box is one page (or window block) of one KV head, both
   // column halves, landing group-major in shared memory (see Layout):
   // (64 columns, 8 rows, column half, 8-row group, page x head | token group x head).
@@ -1018,7 +1617,15 @@ cudaError_t launch_d(const AttnArgs &a, cudaStream_t s, char *why, size_t why_le
     snprintf(why, why_len, "cuTensorMapEncodeTiled rejected a K/V tensor (alignment or size)");
     return cudaErrorInvalidValue;
   }
-  cudaError_t e = ensure_attrs<D, NS, QR, MT>();
+  return cudaSuccess;
+}
+
+template <int D, int NS, int QR, int MT>
+cudaError_t launch_d(const AttnArgs &a, cudaStream_t s, char *why, size_t why_len) {
+  CUtensorMap kp, vp, kw, vw;
+  cudaError_t e = encode_maps<D>(a, kp, vp, kw, vw, why, why_len);
+  if (e != cudaSuccess) return e;
+  e = ensure_attrs<D, NS, QR, MT>();
   if (e != cudaSuccess) return e;
   const int cs = a.num_splits;
   cudaLaunchConfig_t cfg = {};
@@ -1036,6 +1643,43 @@ cudaError_t launch_d(const AttnArgs &a, cudaStream_t s, char *why, size_t why_le
   cfg.attrs = attr;
   cfg.numAttrs = pdl_enabled() ? 2 : 1;
   e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<D, NS, QR, MT>, a, kp, vp, kw, vw);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_sk(const AttnArgs &a, cudaStream_t s, char *why, size_t why_len) {
+  CUtensorMap kp, vp, kw, vw;
+  cudaError_t e = encode_maps<D>(a, kp, vp, kw, vw, why, why_len);
+  if (e != cudaSuccess) return e;
+  using L = Layout<D, 6, 128, 1>;
+  {
+    static std::mutex mu;
+    static bool done[64] = {};
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 0 || dev >= 64 || !done[dev]) {
+      e = cudaFuncSetAttribute(attn_sk_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(attn_sk_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+      if (e != cudaSuccess) return e;
+      if (dev >= 0 && dev < 64) done[dev] = true;
+    }
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.sk);
+  cfg.blockDim = dim3(L::kThreads);
+  cfg.dynamicSmemBytes = L::kAlloc;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, attn_sk_kernel<D>, a, kp, vp, kw, vw);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1089,6 +1733,8 @@ cudaError_t launch_attn_tc(const AttnArgs &a, cudaStream_t s, char *why, size_t 
   // softmax warpgroup each (GQA groups of 129..384 rows): every K/V tile is
   // loaded once for both, and the CTA takes a whole SM.
   const int rows = a.tc_rows, ns = a.tc_stages, mt = a.tc_mt;
+  if (a.sk > 0 && a.head_dim == 128 && rows == 128 && ns == 6 && mt == 1)
+    return launch_sk<128>(a, s, why, why_len);
   if (a.head_dim == 128) {
     if (rows == 64 && ns == 3 && mt == 1) return launch_d<128, 3, 64, 1>(a, s, why, why_len);
     if (rows == 128 && ns == 2 && mt == 1) return launch_d<128, 2, 128, 1>(a, s, why, why_len);

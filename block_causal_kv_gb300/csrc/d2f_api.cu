@@ -66,8 +66,18 @@ struct AttnPlan {
   int splits;
   int tiles_per_split;
   int n_counters;
-  size_t off_ml, off_o, bytes;
+  int sk;         // stream-K form: its grid (CTAs), else 0
+  size_t off_ml, off_o, off_sk, bytes;
 };
+
+// D2F_ATTN_SK=1 / 0 forces / forbids the stream-K form of the one-CTA-per-SM
+// variant (tests); unset = planner.
+int force_sk() {
+  const char *e = getenv("D2F_ATTN_SK");
+  if (!e || !e[0]) return -1;
+  return e[0] == '1' ? 1 : 0;
+}
+constexpr int kSkMaxBatch = 4096;
 
 bool force_simt() {
   const char *e = getenv("D2F_ATTN_PATH");
@@ -75,11 +85,15 @@ bool force_simt() {
 }
 
 // D2F_TC_ROWS=128 keeps the tensor-core path on 128-row tiles even where every
-// sequence fits a 64-row tile (for comparing the two; results agree within
-// rounding).
+// sequence fits a 64-row tile; D2F_TC_ROWS=64 cuts every (sequence, KV head) into
+// 64-row tiles (for comparing the two; results agree within rounding).
 bool force_full_rows() {
   const char *e = getenv("D2F_TC_ROWS");
   return e && strcmp(e, "128") == 0;
+}
+bool force_half_rows() {
+  const char *e = getenv("D2F_TC_ROWS");
+  return e && strcmp(e, "64") == 0;
 }
 
 // D2F_TC_DEEP=1 / 0 forces / forbids the one-CTA-per-SM 6-stage variant for
@@ -125,7 +139,8 @@ int plan_attn(int batch, int total_q, int max_q, int max_ctx, int Hq, int Hkv, i
   const int G = Hq / Hkv;
   // tensor-core tiles hold 64 rows when every sequence's G * max_q rows fit
   const int rows = !tc ? kSimtRows
-                       : ((long long)G * max_q <= 64 && !force_full_rows() ? 64 : kTcRows);
+                       : (((long long)G * max_q <= 64 && !force_full_rows()) || force_half_rows()
+                              ? 64 : kTcRows);
   const int keys = tc ? kTcKeys : kSimtKeys;
   p->tc = tc;
   p->rows = rows;
@@ -195,6 +210,22 @@ int plan_attn(int batch, int total_q, int max_q, int max_ctx, int Hq, int Hkv, i
       }
     }
     p->splits = min(splits, kTcMaxSplits);
+    // Stream-K: the one-CTA variant with one split per (sequence, KV head) and
+    // fewer of them than resident CTAs leaves SMs idle (batch 4 x 32 heads at
+    // context 32768: 128 of 152 SMs, each at the ~50 GB/s its MMA / softmax
+    // chain streams). Instead one wave of CTAs takes equal shares of all the key
+    // tiles. Each CTA owns two partial slots; the pairs count arrivals.
+    p->sk = 0;
+    if (D == 128 && rows == 128 && p->mt == 1 && p->stages == 6 && batch <= kSkMaxBatch) {
+      const int slots1 = attn_tc_deep_slots(1);
+      bool sk = num_splits == 0 && p->splits == 1 && slots1 > 0 && base < slots1;
+      if (force_sk() >= 0) sk = force_sk() == 1 && slots1 > 0;
+      if (sk) p->sk = slots1;
+      // D2F_ATTN_SK_GRID moves the share boundaries (a test switch; any grid is
+      // correct, the CTAs never wait on one another)
+      if (const char *e = getenv("D2F_ATTN_SK_GRID"))
+        if (sk && atoi(e) > 0) p->sk = min(atoi(e), 65535);
+    }
     {
       const long long ctas = (long long)max(batch, 1) * Hkv * p->m_tiles * p->splits;
       const bool whole_sm = D == 128 && (p->stages == 6 || p->mt > 1);
@@ -205,9 +236,15 @@ int plan_attn(int batch, int total_q, int max_q, int max_ctx, int Hq, int Hkv, i
     }
     p->tiles_per_split = cdiv(t_max, p->splits);
     p->n_counters = 0;
-    p->off_ml = p->off_o = p->bytes = 0;
+    p->off_ml = p->off_o = p->off_sk = p->bytes = 0;
+    if (p->sk) {  // pair counters, then 2 slots per CTA
+      p->off_sk = align_up((size_t)max(batch, 1) * Hkv * sizeof(int32_t));
+      p->bytes = p->off_sk + (size_t)2 * p->sk * kSkSlotBytes;
+    }
     return D2F_OK;
   }
+  p->sk = 0;
+  p->off_sk = 0;
   if (splits == 0) {
     const int sms = num_sms_current_device();
     const long long target = sms > 0 ? 4LL * sms : 1;
@@ -415,6 +452,10 @@ int attn_entry(const void *q, const void *k_win, const void *v_win, const void *
     const long long v = atoll(e);
     if (v > 0 && v < kWaitCycles) a.wait_cycles = v;
   }
+  // the stream-K form computes the whole attention only: no fused append, no part
+  a.sk = (p.sk > 0 && part == D2F_ATTN_ALL && n_append == 0 && !prev_out) ? p.sk : 0;
+  a.sk_cnt = reinterpret_cast<int32_t *>(workspace);
+  a.sk_slots = reinterpret_cast<uint8_t *>(static_cast<char *>(workspace) + p.off_sk);
   a.counters = reinterpret_cast<int32_t *>(workspace);
   a.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) + p.off_ml);
   a.ws_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + p.off_o);

@@ -63,6 +63,9 @@ struct AttnArgs {
   const float *prev_lse;   // ... its natural-log normaliser [total_q][Hq]; NULL: no composition
   long long wait_cycles; // tensor-core path: budget of each wait on another role's work
                          // (kWaitCycles; less only to test the give-up path)
+  int sk;                // tensor-core path: stream-K form (see attn_tc.cu), else 0
+  int32_t *sk_cnt;       // stream-K: [batch * Hkv] arrival counters (zero at rest)
+  uint8_t *sk_slots;     // stream-K: [2 * grid] partial slots of kSkSlotBytes
   int32_t *counters;     // [batch * Hkv * m_tiles] merge arrival counters (zero at rest)
   float2 *ws_ml;         // [num_splits][total_q * Hq] (max in log2 units, sum)
   float *ws_o;           // [num_splits][total_q * Hq][head_dim] unnormalised partial output
@@ -139,6 +142,10 @@ constexpr int kTcRows = 128;    // query rows per CTA (UMMA M), tensor-core path
 constexpr int kTcKeys = 64;     // keys per tile (UMMA N of Q.K^T), tensor-core path
 constexpr int kTcMaxSplits = 8; // CTAs per cluster sharing one row tile, tensor-core path
 constexpr int kMaxLongestFirstBatch = 256;  // largest batch the longest-first order covers
+// Stream-K form of the tensor-core attention (head_dim 128, one 128-row tile per
+// (sequence, KV head)): a partial slot holds 128 rows of 128 bf16 then 128
+// (max, sum) float pairs; each CTA owns two.
+constexpr int kSkSlotBytes = 128 * 128 * 2 + 128 * 8;
 
 // ---------------------------------------------------------------------------
 // Device helpers
@@ -387,6 +394,18 @@ __device__ __forceinline__ int atomic_add_acq_rel(int32_t *p, int v) {
   asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
                : "memory");
   return old;
+}
+// Named barrier among `count` threads (a multiple of 32) of the CTA that also
+// returns whether `v` held in every one of them.
+__device__ __forceinline__ bool named_sync_and(int id, int count, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
 }
 // Named barrier among `count` threads (a multiple of 32) of the CTA.
 __device__ __forceinline__ void named_sync(int id, int count) {

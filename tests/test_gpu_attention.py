@@ -321,3 +321,68 @@ def test_attention_parts_need_the_tensor_core_path():
     g = p.to(dev)
     with pytest.raises(d2f.D2FError):
         _part(g, p, d2f.ATTN_CACHED)
+
+
+def _sk_env(monkeypatch, grid=None):
+    monkeypatch.setenv("D2F_ATTN_SK", "1")
+    monkeypatch.setenv("D2F_TC_DEEP", "1")
+    monkeypatch.setenv("D2F_TC_ROWS", "128")
+    if grid is not None:
+        monkeypatch.setenv("D2F_ATTN_SK_GRID", str(grid))
+
+
+def _gqa2_small():
+    # GQA 8 / 4, window 1-3 blocks of 16: up to 96 rows per (sequence, KV head)
+    return synth.Workload("gqa2sk", 3, 8, 4, 128, 16, torch.bfloat16, [700, 0, 1234], [3, 2, 1],
+                          64, permute_pages=True, seed=77)
+
+
+@pytest.mark.parametrize("name", ["llada", "ragged", "long_b8", "long_b16", "long_b32", "gqa2"])
+@pytest.mark.parametrize("grid", [None, 1, 3, 7, 40])
+def test_stream_k_form(name, grid, monkeypatch):
+    """The stream-K form of the one-CTA variant: every (sequence, KV head)'s key
+    tiles laid end to end and cut into equal shares, pieces of a pair composed in
+    log space by the last CTA to finish one. Grids of 1 (one CTA walks every pair),
+    3, 7, 40 and one per SM move every share boundary (pieces that start and end
+    inside the cache or the window, pairs over three or more CTAs, CTAs with no
+    share). Output and lse against the oracle; two calls in a row on one
+    workspace (the pair counters reset themselves)."""
+    dev = device()
+    _sk_env(monkeypatch, grid)
+    w = _gqa2_small() if name == "gqa2" else synth.small(name)
+    p = synth.make_problem(w)
+    g = p.to(dev)
+    ws = d2f.attn_workspace(dev, batch=w.batch, total_q=w.total_q, max_q_per_seq=p.max_q_per_seq,
+                            max_ctx=p.max_ctx, num_heads_q=w.num_heads_q,
+                            num_heads_kv=w.num_heads_kv, head_dim=w.head_dim,
+                            block_size=w.block_size)
+    ref, ref_lse = _ref(p)
+    for call in range(2):
+        out, lse = d2f.block_attn(g.q, g.k_win, g.v_win, g.k_pool, g.v_pool, g.page_table,
+                                  g.ctx_len, g.q_start, block_size=w.block_size,
+                                  max_q_per_seq=p.max_q_per_seq, max_ctx=p.max_ctx, workspace=ws)
+        torch.cuda.synchronize()
+        check_attention(out, lse, ref, ref_lse, torch.bfloat16, "sk %s grid %s call %d" % (name, grid, call))
+
+
+def test_stream_k_falls_back_for_appends_and_parts(monkeypatch):
+    """Calls the stream-K form does not compute (a fused append, an attention
+    part) take the split layout on the same plan and workspace."""
+    dev = device()
+    _sk_env(monkeypatch, 5)
+    w = synth.Workload("skapp", 2, 4, 4, 128, 16, torch.bfloat16, [300, 500], [3, 2], 64,
+                       appends_per_seq=1, permute_pages=True, seed=78)
+    p = synth.make_problem(w)
+    g = p.to(dev)
+    out, _ = d2f.block_attn(g.q, g.k_win, g.v_win, g.k_pool, g.v_pool, g.page_table, g.ctx_len,
+                            g.q_start, block_size=16, max_q_per_seq=p.max_q_per_seq,
+                            max_ctx=p.max_ctx, want_lse=False, append_src_row=g.src_row,
+                            append_dst_page=g.dst_page)
+    torch.cuda.synchronize()
+    ref, _ = _ref(p)
+    check_attention(out, None, ref, None, torch.bfloat16, "sk fallback, fused append")
+    for s_, d_ in zip(p.src_row.tolist(), p.dst_page.tolist()):
+        assert torch.equal(g.k_pool[d_].cpu(), p.k_win[s_:s_ + 16].transpose(0, 1))
+    cached, lse_c = _part(g, p, d2f.ATTN_CACHED)
+    ref_c, ref_lse_c = _ref_part(p, oracle.ATTN_CACHED)
+    check_attention(cached, lse_c, ref_c, ref_lse_c, torch.bfloat16, "sk fallback, cached part")

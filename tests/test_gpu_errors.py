@@ -182,13 +182,20 @@ def test_bad_logit_row_sets_the_error_word(splits):
 # ---------------------------------------------------------------------------
 # canary bytes around outputs and workspaces
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("path", ["tc", "simt"])
+@pytest.mark.parametrize("path", ["tc", "simt", "sk"])
 @pytest.mark.parametrize("name", ["ragged", "dream", "long_b32"])
 @pytest.mark.parametrize("splits", [0, 3])
 def test_attention_writes_stay_inside_its_buffers(path, name, splits, monkeypatch):
     dev = device()
     if path == "simt":
         monkeypatch.setenv("D2F_ATTN_PATH", "simt")
+    if path == "sk":
+        if name == "dream" or splits:
+            pytest.skip("the stream-K form takes one 128-row tile per (sequence, KV head), auto splits")
+        monkeypatch.setenv("D2F_ATTN_SK", "1")
+        monkeypatch.setenv("D2F_ATTN_SK_GRID", "7")
+        monkeypatch.setenv("D2F_TC_DEEP", "1")
+        monkeypatch.setenv("D2F_TC_ROWS", "128")
     p = synth.make_problem(synth.small(name))
     g = p.to(dev)
     w = p.w
@@ -257,7 +264,7 @@ ERR_TIMEOUT = 5
 
 
 @pytest.mark.parametrize("name,deep", [("llada", None), ("dream", "0"), ("dream", "1"),
-                                       ("long_b32", "1")])
+                                       ("long_b32", "1"), ("long_b32", "sk")])
 @pytest.mark.parametrize("splits", [1, 3])
 def test_wait_budget_runs_out_cleanly(name, deep, splits, monkeypatch):
     """The tensor-core attention's waits on another role's work are bounded. With
@@ -268,7 +275,12 @@ def test_wait_budget_runs_out_cleanly(name, deep, splits, monkeypatch):
     the same buffers, matches the oracle. Single-split and cluster-composed
     launches, the one-issuer and the split-issuer variants."""
     dev = device()
-    if deep is not None:
+    if deep == "sk":  # the stream-K form: five CTAs over every (sequence, KV head)
+        monkeypatch.setenv("D2F_ATTN_SK", "1")
+        monkeypatch.setenv("D2F_ATTN_SK_GRID", "5")
+        monkeypatch.setenv("D2F_TC_DEEP", "1")
+        splits = 0
+    elif deep is not None:
         monkeypatch.setenv("D2F_TC_DEEP", deep)
     p = synth.make_problem(synth.small(name))
     g = p.to(dev)
@@ -278,7 +290,7 @@ def test_wait_budget_runs_out_cleanly(name, deep, splits, monkeypatch):
     assert int(err.item()) == ERR_TIMEOUT
     monkeypatch.delenv("D2F_WAIT_CYCLES")
     err.zero_()
-    out, lse = _attn(g, p, splits, err=err)
+    out, lse = _attn(g, p, splits, err=err)  # a fresh (zeroed) workspace, as after any device error
     assert int(err.item()) == 0
     ref, ref_lse = oracle.block_attn(p.q, p.k_win, p.v_win, p.k_pool, p.v_pool, p.page_table,
                                      p.ctx_len, p.q_start, p.w.block_size)
