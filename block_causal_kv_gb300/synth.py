@@ -78,6 +78,11 @@ def workload(name: str, seed: Optional[int] = None) -> Workload:
     elif name == "dream":
         w = Workload("dream", 8, 28, 4, 128, 16, torch.bfloat16, [8192] * 8, [3] * 8, 152064,
                      appends_per_seq=1, permute_pages=False, seed=1237)
+    elif name == "long_b32_ctx8k":
+        # the long-context layout at a quarter of the context: a case small enough
+        # for multi-pass profiler captures of the same kernels (0.5 GB of K/V)
+        w = Workload(name, 4, 32, 32, 128, 32, torch.bfloat16, [8192] * 4, [4] * 4, 126464,
+                     permute_pages=False, seed=1239)
     elif name.startswith("long_b"):
         B = int(name[len("long_b"):])
         if B not in (8, 16, 32):
