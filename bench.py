@@ -75,6 +75,9 @@ def parse():
     ap.add_argument("--tau-act", type=float, default=1.0,
                     help="window scheduler: progress of the block before that makes a block "
                          "aggressive")
+    ap.add_argument("--cache-ready", type=int, default=1, choices=[0, 1],
+                    help="pass D2F_ATTN_CACHE_READY with the plain step's attention (the cache "
+                         "is written by no kernel of the step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=4.0,
@@ -570,7 +573,10 @@ def measure(args, name, K, W, world, rank, dev, cpu=True):
         elif fused:
             kw = dict(append_src_row=s.src_row, append_dst_page=s.dst_page)
         else:
-            kw = {}
+            # without an append the cache, page table and layout are written by
+            # no kernel of the step: the attention may load cached tiles before
+            # its dependency wait
+            kw = dict(cache_ready=bool(args.cache_ready) and not appends)
         d2f.block_attn(s.q, s.k_win, s.v_win, s.k_pool, s.v_pool, pt, cl, qs, block_size=B,
                        max_q_per_seq=p.max_q_per_seq, max_ctx=p.max_ctx,
                        num_splits=args.num_splits, out=s.out, want_lse=False, workspace=ws_attn,
@@ -811,7 +817,9 @@ def measure(args, name, K, W, world, rank, dev, cpu=True):
                                        "at the start of each %d-step graph" % (5 * w.total_q,
                                                                               n_sets),
                            attn_splits=args.num_splits or "auto",
-                           commit_splits=args.commit_splits or "auto"),
+                           commit_splits=args.commit_splits or "auto",
+                           cache_ready=bool(args.cache_ready) and not (reuse or fused or
+                                                                       appends)),
             "roofline": roofline, "kernels": kernels,
             "gpu_launches": K * (2 + (1 if appends else 0) + (1 if sched else 0)),
             "clocks": clocks, "e2e": e2e}

@@ -242,7 +242,19 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
     }
   }
 
-  grid_dependency_wait();  // inputs may come from the previous kernel in the stream
+  // producer index of this warp (-1: not a producer)
+  const int prod = warp == 0 ? 0
+                   : (MT == 2 && warp == 1 + MT) ? 1
+                   : (QR == 64 && warp >= L::kFirstSoft && (warp & 3) >= 2) ? 1 + (MT == 2) + ((warp & 3) - 2)
+                   : -1;
+  // D2F_ATTN_CACHE_READY: the page table, context lengths, window layout and
+  // cached pages are final before the previous kernel started, so the producers
+  // may read them and load cached tiles before waiting for it; they wait before
+  // their first window tile or once the ring is full. Every other read (Q, window
+  // K/V) and every write comes after the wait.
+  const bool early = a.cache_ready && prod >= 0;
+  bool waited = !early;
+  if (!early) grid_dependency_wait();  // inputs may come from the previous kernel in the stream
   if (tid == 0) D2F_TRACE_MARK(0, 1);
 
   if (a.longest_first) {
@@ -274,11 +286,6 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
   // its first logical page is known up front.
   const int ppt = N / a.block_size;  // pages (or window blocks) per tile
   const int pre_chunk = split * a.tiles_per_split * ppt;
-  // producer index of this warp (-1: not a producer)
-  const int prod = warp == 0 ? 0
-                   : (MT == 2 && warp == 1 + MT) ? 1
-                   : (QR == 64 && warp >= L::kFirstSoft && (warp & 3) >= 2) ? 1 + (MT == 2) + ((warp & 3) - 2)
-                   : -1;
   int pre_ids = -1;
   if (prod >= 0 && pre_chunk + lane < a.max_pages_per_seq)
     pre_ids = __ldg(a.page_table + (int64_t)b * a.max_pages_per_seq + pre_chunk + lane);
@@ -352,6 +359,10 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
     for (int u = 0; u < T; ++u) {
       const int stage = u % NS;
       const int t = t0 + u;
+      if (!waited && (t >= Tc || u >= NS)) {  // warp-uniform
+        grid_dependency_wait();
+        waited = true;
+      }
       if (u >= NS) {
         bool ok = true;
         if (lane == 0)
@@ -713,6 +724,9 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
   }
 
   // ---- epilogue ---------------------------------------------------------------
+  // A producer that loaded only cached tiles (or had none) has not waited yet;
+  // the epilogue's writes come after the previous kernel in every thread.
+  if (!waited) grid_dependency_wait();
   __syncwarp();
   __syncthreads();  // every role is done; Q and the ring are free
   if (tid == 0) D2F_TRACE_MARK(0, 7);

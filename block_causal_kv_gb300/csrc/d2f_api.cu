@@ -291,16 +291,22 @@ int plan_commit(int total_q, int vocab, int dtype, int B, int num_splits, Commit
   const int vec = 16 / elt;
   int splits = num_splits;
   if (splits == 0) {
-    // About four CTAs per SM over the whole grid, at least two slices per row and
-    // at least 2048 logits per slice: long slices amortise each CTA's fixed chain
-    // (decode-state read, reduction, arrival), enough CTAs keep every SM's loads
-    // in flight. Measured on GB300 (commit µs): LLaDA layer 48 rows -> 12 slices
-    // 9.5 (vs 9.8 at 6, 13.4 at 2); Dream layer 384 rows -> 2 slices 34.5 (vs
-    // 37.5 at 8, 43.0 at 12).
+    // At most four CTAs per SM over the whole grid (one slice per row once the
+    // rows alone fill that), and at least 2048 logits per slice: long slices
+    // amortise each CTA's fixed chain (decode-state read, reduction, arrival),
+    // enough CTAs keep every SM's loads in flight. Measured on GB300 (commit µs,
+    // 126,464 or 152,064 bf16 logits per row, every row masked): 48 rows -> 12
+    // slices 9.6 (10.2 at 8 or 16, 13.4 at 2); 128 rows -> 4 slices 18.5 (20.5
+    // at 2 or 5); 256 -> 2 slices 24.7 (27.4 at 1, 27.6 at 3); 384 -> 1 slice
+    // 32.2 (34.7 at 2); 512 -> 1 slice 37.1 (42.1 at 2). Rows that are no
+    // longer masked read nothing, so the count over-states the work of a window
+    // with many committed rows: 464 rows of which half are masked take 34.3 at
+    // one slice, 31.2 at two, 27.3 at three. A caller that knows its masked
+    // count passes num_splits.
     const int sms = max(1, num_sms_current_device());
     const long long rows = max(total_q, 1);
-    splits = (int)((4LL * sms + rows / 2) / rows);
-    splits = max(2, min(splits, kCommitMaxSplits));
+    splits = (int)((4LL * sms) / rows);
+    splits = max(1, min(splits, kCommitMaxSplits));
     splits = max(1, min(splits, vocab / 2048));
   }
   const int chunk = cdiv(cdiv(vocab, splits), vec) * vec;
@@ -379,8 +385,9 @@ int attn_entry(const void *q, const void *k_win, const void *v_win, const void *
                float softmax_scale, int num_splits, void *workspace, size_t workspace_bytes,
                const int32_t *src_row, const int32_t *dst_page, int n_append,
                const int32_t *n_append_dev, int part, const void *prev_out,
-               const float *prev_lse, int32_t *err_word, void *stream) {
+               const float *prev_lse, int32_t *err_word, void *stream, unsigned flags = 0) {
   if (n_append < 0) return fail(D2F_ERR_INVALID_ARG, "n_append %d < 0", n_append);
+  if (flags & ~D2F_ATTN_CACHE_READY) return fail(D2F_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
   if (part < D2F_ATTN_ALL || part > D2F_ATTN_WINDOW)
     return fail(D2F_ERR_INVALID_ARG, "part %d is not a D2F_ATTN_* value", part);
   if (part == D2F_ATTN_CACHED && !lse_out)
@@ -452,6 +459,7 @@ int attn_entry(const void *q, const void *k_win, const void *v_win, const void *
     const long long v = atoll(e);
     if (v > 0 && v < kWaitCycles) a.wait_cycles = v;
   }
+  a.cache_ready = (flags & D2F_ATTN_CACHE_READY) ? 1 : 0;
   // the stream-K form computes the whole attention only: no fused append, no part
   a.sk = (p.sk > 0 && part == D2F_ATTN_ALL && n_append == 0 && !prev_out) ? p.sk : 0;
   a.sk_cnt = reinterpret_cast<int32_t *>(workspace);
@@ -559,6 +567,21 @@ int d2f_block_attn(const void *q, const void *k_win, const void *v_win, const vo
                     num_heads_kv, head_dim, block_size, num_pages, dtype, softmax_scale, num_splits,
                     workspace, workspace_bytes, nullptr, nullptr, 0, nullptr, D2F_ATTN_ALL, nullptr,
                     nullptr, err_word, stream);
+}
+
+int d2f_block_attn_flags(const void *q, const void *k_win, const void *v_win, const void *k_pool,
+                         const void *v_pool, const int32_t *page_table, int max_pages_per_seq,
+                         const int32_t *ctx_len, const int32_t *q_start, void *out,
+                         float *lse_out, int batch, int total_q, int max_q_per_seq, int max_ctx,
+                         int num_heads_q, int num_heads_kv, int head_dim, int block_size,
+                         int num_pages, int dtype, float softmax_scale, int num_splits,
+                         void *workspace, size_t workspace_bytes, unsigned flags,
+                         int32_t *err_word, void *stream) {
+  return attn_entry(q, k_win, v_win, k_pool, v_pool, page_table, max_pages_per_seq, ctx_len,
+                    q_start, out, lse_out, batch, total_q, max_q_per_seq, max_ctx, num_heads_q,
+                    num_heads_kv, head_dim, block_size, num_pages, dtype, softmax_scale, num_splits,
+                    workspace, workspace_bytes, nullptr, nullptr, 0, nullptr, D2F_ATTN_ALL, nullptr,
+                    nullptr, err_word, stream, flags);
 }
 
 int d2f_commit_workspace_size(int total_q, int vocab, int dtype, int block_size, int num_splits,

@@ -63,6 +63,8 @@ struct AttnArgs {
   const float *prev_lse;   // ... its natural-log normaliser [total_q][Hq]; NULL: no composition
   long long wait_cycles; // tensor-core path: budget of each wait on another role's work
                          // (kWaitCycles; less only to test the give-up path)
+  int cache_ready;        // D2F_ATTN_CACHE_READY: producers may load cached tiles before
+                         // the dependency wait
   int sk;                // tensor-core path: stream-K form (see attn_tc.cu), else 0
   int32_t *sk_cnt;       // stream-K: [batch * Hkv] arrival counters (zero at rest)
   uint8_t *sk_slots;     // stream-K: [2 * grid] partial slots of kSkSlotBytes

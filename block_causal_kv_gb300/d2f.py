@@ -32,14 +32,16 @@ STATUS = {0: "D2F_OK", 1: "D2F_ERR_INVALID_ARG", 2: "D2F_ERR_UNSUPPORTED", 3: "D
 
 # Every symbol include/d2f.h declares.
 EXPORTS = ("d2f_version", "d2f_status_string", "d2f_last_error_string",
-           "d2f_block_attn_workspace_size", "d2f_block_attn", "d2f_block_attn_append",
-           "d2f_block_attn_part",
+           "d2f_block_attn_workspace_size", "d2f_block_attn", "d2f_block_attn_flags",
+           "d2f_block_attn_append", "d2f_block_attn_part",
            "d2f_commit_workspace_size",
            "d2f_commit", "d2f_commit_metric", "d2f_commit_noalloc", "d2f_kv_append",
            "d2f_kv_append_dev", "d2f_block_attn_append_dev", "d2f_window_step")
 
 # attention parts of block_attn(part=...) (include/d2f.h D2F_ATTN_*)
 ATTN_ALL, ATTN_CACHED, ATTN_WINDOW = 0, 1, 2
+# d2f_block_attn_flags: the cache and window layout are final before the preceding kernel
+CACHE_READY = 1
 # confidence metrics of commit(metric=...) (include/d2f.h D2F_CONF_*)
 CONF_PMAX, CONF_NEG_ENTROPY, CONF_MARGIN, CONF_LOGIT_GAP = 0, 1, 2, 3
 
@@ -73,6 +75,9 @@ def load(path=LIB_PATH):
     lib.d2f_block_attn.restype = _I
     lib.d2f_block_attn.argtypes = ([_P] * 6 + [_I] + [_P] * 2 + [_P, _P] + [_I] * 10 +
                                    [ctypes.c_float, _I, _P, _SZ, _P, _P])
+    lib.d2f_block_attn_flags.restype = _I
+    lib.d2f_block_attn_flags.argtypes = ([_P] * 6 + [_I] + [_P] * 2 + [_P, _P] + [_I] * 10 +
+                                         [ctypes.c_float, _I, _P, _SZ, ctypes.c_uint, _P, _P])
     lib.d2f_block_attn_append.restype = _I
     lib.d2f_block_attn_append.argtypes = ([_P] * 6 + [_I] + [_P] * 2 + [_P, _P] + [_I] * 10 +
                                           [ctypes.c_float, _I, _P, _SZ, _P, _P, _I, _P, _P])
@@ -171,7 +176,7 @@ def block_attn(q, k_win, v_win, k_pool, v_pool, page_table, ctx_len, q_start, *,
                max_q_per_seq, max_ctx, softmax_scale=None, num_splits=0, out=None, lse=None,
                want_lse=True, workspace=None, err=None, stream=None, append_src_row=None,
                append_dst_page=None, part=ATTN_ALL, prev_out=None, prev_lse=None,
-               append_n_dev=None):
+               append_n_dev=None, cache_ready=False):
     """Block-causal attention of the window over [paged cache ; window] (one layer).
     With append_src_row / append_dst_page (int32 [n_append]) the finished blocks
     are appended to their pages in the same launch (d2f_block_attn_append).
@@ -179,6 +184,9 @@ def block_attn(q, k_win, v_win, k_pool, v_pool, page_table, ctx_len, q_start, *,
     length is read there, at most len(append_src_row).
     part ATTN_CACHED / ATTN_WINDOW (d2f_block_attn_part): one part of the keys; the
     window part composes a kept cached part given as prev_out / prev_lse.
+    cache_ready=True (d2f_block_attn_flags with D2F_ATTN_CACHE_READY, the whole
+    attention only): page_table, ctx_len, q_start and the cached pages are not
+    written by the kernel that precedes this call in the stream.
 
     Returns (out [total_q, Hq, D] like q, lse [total_q, Hq] float32 or None)."""
     lib = load()
@@ -209,6 +217,8 @@ def block_attn(q, k_win, v_win, k_pool, v_pool, page_table, ctx_len, q_start, *,
             _ptr(out), _ptr(lse), batch, total_q, max_q_per_seq, max_ctx, hq, hkv, d, block_size,
             k_pool.shape[0] if k_pool is not None else 0, dt, float(softmax_scale), num_splits,
             _ptr(workspace), workspace.numel() * workspace.element_size())
+    if cache_ready and (part != ATTN_ALL or append_src_row is not None):
+        raise ValueError("cache_ready goes with the whole attention, without an append")
     if part != ATTN_ALL:
         if append_src_row is not None:
             raise ValueError("an append goes with the whole attention (part ATTN_ALL)")
@@ -216,6 +226,8 @@ def block_attn(q, k_win, v_win, k_pool, v_pool, page_table, ctx_len, q_start, *,
         _dev(prev_lse, "prev_lse", torch.float32)
         _check(lib.d2f_block_attn_part(*args, int(part), _ptr(prev_out), _ptr(prev_lse), _ptr(err),
                                        _stream(stream)))
+    elif append_src_row is None and cache_ready:
+        _check(lib.d2f_block_attn_flags(*args, CACHE_READY, _ptr(err), _stream(stream)))
     elif append_src_row is None:
         _check(lib.d2f_block_attn(*args, _ptr(err), _stream(stream)))
     elif append_n_dev is not None:

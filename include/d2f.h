@@ -142,7 +142,11 @@ int d2f_block_attn_workspace_size(int batch, int total_q, int max_q_per_seq, int
  *               are clamped to 8). CUDA-core path: any count; partials go through
  *               the workspace.
  *   workspace   device, >= d2f_block_attn_workspace_size(...) bytes, zeroed once
- *               (0 bytes on the tensor-core path: NULL is accepted there)
+ *               (and again after a device error). The tensor-core path needs none
+ *               (NULL is accepted), except its stream-K form: the one-CTA-per-SM
+ *               variant with fewer (sequence, KV head) pairs than SMs takes a
+ *               counter per pair and two 33 KB partial slots per CTA (~10 MB on
+ *               GB300).
  *
  * Alignment: every device buffer 16-byte aligned.
  */
@@ -153,6 +157,31 @@ int d2f_block_attn(const void *q, const void *k_win, const void *v_win, const vo
                    int num_heads_kv, int head_dim, int block_size, int num_pages, int dtype,
                    float softmax_scale, int num_splits, void *workspace, size_t workspace_bytes,
                    int32_t *err_word, void *stream);
+
+/*
+ * d2f_block_attn_flags -- d2f_block_attn with launch flags.
+ *
+ *   flags  0 or D2F_ATTN_CACHE_READY. D2F_ATTN_CACHE_READY is the caller's promise
+ *          that page_table, ctx_len, q_start and the cached K/V pages those name
+ *          are final before the kernel that precedes this call in `stream`
+ *          starts: that kernel writes none of them. Q, the window K/V and the
+ *          outputs carry no such promise. The attention may then load its first
+ *          cached tiles before it waits for the preceding kernel. Under
+ *          programmatic dependent launch, its CTAs start while that kernel
+ *          finishes, so the first tiles land sooner. Results are those of
+ *          d2f_block_attn. Do not pass it when the preceding kernel writes the
+ *          cache or the window layout: a d2f_kv_append, or d2f_window_step, as in
+ *          a device-driven decode. Unknown bits give D2F_ERR_INVALID_ARG.
+ */
+#define D2F_ATTN_CACHE_READY 1u
+int d2f_block_attn_flags(const void *q, const void *k_win, const void *v_win, const void *k_pool,
+                         const void *v_pool, const int32_t *page_table, int max_pages_per_seq,
+                         const int32_t *ctx_len, const int32_t *q_start, void *out,
+                         float *lse_out, int batch, int total_q, int max_q_per_seq, int max_ctx,
+                         int num_heads_q, int num_heads_kv, int head_dim, int block_size,
+                         int num_pages, int dtype, float softmax_scale, int num_splits,
+                         void *workspace, size_t workspace_bytes, unsigned flags,
+                         int32_t *err_word, void *stream);
 
 /*
  * d2f_block_attn_append -- d2f_block_attn, then d2f_kv_append of finished

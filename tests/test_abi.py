@@ -53,7 +53,9 @@ def _attn_ws(**over):
 
 def test_attention_workspace_size(lib, monkeypatch):
     # tensor-core path: splits compose in distributed shared memory, no workspace
+    monkeypatch.setenv("D2F_ATTN_SK", "0")
     assert _attn_ws() == 0
+    monkeypatch.delenv("D2F_ATTN_SK")
     # CUDA-core path: counters + 4 splits x (max, sum) + 4 splits x fp32 partial rows
     monkeypatch.setenv("D2F_ATTN_PATH", "simt")
     n4 = _attn_ws()
@@ -125,3 +127,12 @@ def test_device_count_appends_need_the_count(lib):
                                        ctypes.c_float(0.125), 1, None, 0, None, None, None, 4,
                                        None, None)
     assert st == 1 and b"n_append_dev" in lib.d2f_last_error_string()
+
+
+def test_attention_flags_are_checked(lib):
+    """d2f_block_attn_flags refuses unknown flag bits before any launch."""
+    st = lib.d2f_block_attn_flags(None, None, None, None, None, None, 4, None, None, None, None,
+                                  1, 16, 16, 0, 4, 4, 64, 16, 4, 0, ctypes.c_float(0.125), 1, None,
+                                  0, 2, None, None)
+    assert st == 1
+    assert b"flags" in lib.d2f_last_error_string()

@@ -386,3 +386,48 @@ def test_stream_k_falls_back_for_appends_and_parts(monkeypatch):
     cached, lse_c = _part(g, p, d2f.ATTN_CACHED)
     ref_c, ref_lse_c = _ref_part(p, oracle.ATTN_CACHED)
     check_attention(cached, lse_c, ref_c, ref_lse_c, torch.bfloat16, "sk fallback, cached part")
+
+
+@pytest.mark.parametrize("name", ["llada", "ragged", "dream", "long_b16", "long_b32"])
+def test_cache_ready_flag(name):
+    """D2F_ATTN_CACHE_READY: the producers read the page table and layout and load
+    cached tiles before waiting for the preceding kernel. Same results, alone and
+    replayed from a CUDA graph where each attention follows a commit (which writes
+    no cache) under programmatic dependent launch."""
+    dev = device()
+    w = synth.small(name)
+    p = synth.make_problem(w)
+    g = p.to(dev)
+    ref, ref_lse = _ref(p)
+    kw = dict(block_size=w.block_size, max_q_per_seq=p.max_q_per_seq, max_ctx=p.max_ctx,
+              cache_ready=True)
+    out, lse = d2f.block_attn(g.q, g.k_win, g.v_win, g.k_pool, g.v_pool, g.page_table, g.ctx_len,
+                              g.q_start, **kw)
+    torch.cuda.synchronize()
+    check_attention(out, lse, ref, ref_lse, w.dtype, "cache_ready " + name)
+    ws = d2f.attn_workspace(dev, batch=w.batch, total_q=w.total_q, max_q_per_seq=p.max_q_per_seq,
+                            max_ctx=p.max_ctx, num_heads_q=w.num_heads_q,
+                            num_heads_kv=w.num_heads_kv, head_dim=w.head_dim,
+                            block_size=w.block_size)
+    wsc = d2f.commit_workspace(dev, total_q=w.total_q, vocab=w.vocab, block_size=w.block_size)
+    outs = [torch.empty_like(g.q) for _ in range(3)]
+    lses = [torch.empty(g.q.shape[:2], dtype=torch.float32, device=dev) for _ in range(3)]
+    toks = [g.tokens.clone() for _ in range(3)]
+    msks = [g.masked.clone() for _ in range(3)]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):  # warm-up outside the capture (function attributes)
+        d2f.commit(g.logits, g.tokens.clone(), g.masked.clone(), g.q_start, g.block_phase, g.tau,
+                   block_size=w.block_size, mask_id=p.mask_id, workspace=wsc)
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        for i in range(3):
+            d2f.commit(g.logits, toks[i], msks[i], g.q_start, g.block_phase, g.tau,
+                       block_size=w.block_size, mask_id=p.mask_id, workspace=wsc)
+            d2f.block_attn(g.q, g.k_win, g.v_win, g.k_pool, g.v_pool, g.page_table, g.ctx_len,
+                           g.q_start, out=outs[i], lse=lses[i], workspace=ws, **kw)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    for i in range(3):
+        check_attention(outs[i], lses[i], ref, ref_lse, w.dtype, "cache_ready graph %d" % i)
