@@ -1003,6 +1003,189 @@ __device__ __forceinline__ int sk_cta_of(long long u, long long W, int grid) {
 __device__ __forceinline__ long long sk_start(int c, long long W, int grid) {
   return (long long)c * W / grid;
 }
+// The same share boundaries without a 64-bit division per call (compositions
+// walk them per row): with W = Wq grid + Wr, c W / grid = c Wq + c Wr / grid,
+// and c Wr < grid^2 < 2^32 for grids of at most 65535 CTAs (the planner's bound).
+struct SkShares {
+  long long Wq;
+  unsigned Wr, grid;
+  __device__ __forceinline__ long long start(int c) const {
+    return (long long)c * Wq + (long long)(((unsigned)c * Wr) / grid);
+  }
+};
+__device__ __forceinline__ SkShares sk_shares(long long W, int grid) {
+  return SkShares{W / grid, (unsigned)(W % grid), (unsigned)grid};
+}
+// The first tile of a pair (line position P, T tiles) at or after line position x.
+__device__ __forceinline__ int sk_first_tile(long long x, long long P, int T) {
+  if (x <= P) return 0;
+  const long long d = x - P;
+  return d >= T ? T : (int)d;
+}
+
+// The last piece of a pair is in: compose its rows from the pieces of the CTAs
+// cf..cl that hold a tile of it, in log space, and write them (bf16) with their
+// lse. CTA cc's piece: slot 2 cc + 1 if cc = cf and its share began before the
+// pair (the pair is its last segment), else slot 2 cc. The slots were written by
+// other CTAs: read from L2. The pieces are gathered once, up to eight at a time
+// (the share boundaries take integer divisions).
+constexpr int kComposeGroup = 8;
+struct SkPieces {
+  const uint8_t *p[kComposeGroup];
+  int n;
+};
+// The next pieces from CTA cc on (lo: its share's start), at most eight.
+__device__ __forceinline__ SkPieces sk_gather(const uint8_t *slots, int cf, int cl, long long P, int T,
+                                              SkShares sh, int &cc, long long &lo) {
+  SkPieces g;
+  g.n = 0;
+#pragma unroll
+  for (int i = 0; i < kComposeGroup; ++i) g.p[i] = slots;
+  while (cc <= cl && g.n < kComposeGroup) {
+    const long long hi = sh.start(cc + 1);
+    if (sk_first_tile(lo, P, T) < sk_first_tile(hi, P, T)) {
+      const int wc = (cc == cf && lo < P) ? 1 : 0;
+      const uint8_t *pp = slots + (size_t)(2 * cc + wc) * kSkSlotBytes;
+#pragma unroll
+      for (int i = 0; i < kComposeGroup; ++i)
+        if (i == g.n) g.p[i] = pp;
+      ++g.n;
+    }
+    lo = hi;
+    ++cc;
+  }
+  return g;
+}
+// Called by every lane of each warp of the composing warpgroup (lane = row %
+// 32 of the warp's 32 rows; rv: the lane's row is a query row, hr its output
+// row). Pass 1, lane = row: the pieces' (max, sum) and each piece's weight for
+// the row. Pass 2, coalesced: a warp load covers two rows (16 lanes x 16 bytes
+// each), the weights come by shuffle; four rows and four pieces in flight.
+__device__ __noinline__ void sk_compose(const uint8_t *slots, uint16_t *out, float *lse_out, int64_t hr,
+                                        bool rv, int row, int cf, int cl, long long P, int T,
+                                        SkShares sh) {
+  constexpr int D = 128;
+  constexpr size_t kMl = (size_t)kTcRows * D * 2;  // (max, sum) pairs after the rows
+  const int lane = threadIdx.x & 31;
+  const int row0 = row - lane;  // the warp's first row
+  int cc = cf;
+  long long lo = sh.start(cf);
+  const SkPieces g0 = sk_gather(slots, cf, cl, P, T, sh, cc, lo);
+  const bool more = cc <= cl;  // more than eight pieces: the rest below, one by one
+  float2 ml[kComposeGroup];
+#pragma unroll
+  for (int i = 0; i < kComposeGroup; ++i)
+    ml[i] = i < g0.n ? __ldcg(reinterpret_cast<const float2 *>(g0.p[i] + kMl) + row) : make_float2(0.f, 0.f);
+  float mx = -INFINITY, ws = 0.f;
+  auto fold = [&](float2 m) {
+    if (!(m.y > 0.f)) return;
+    if (m.x > mx) {
+      ws = ws * fast_exp2(mx - m.x) + m.y;
+      mx = m.x;
+    } else {
+      ws += fast_exp2(m.x - mx) * m.y;
+    }
+  };
+#pragma unroll
+  for (int i = 0; i < kComposeGroup; ++i)
+    if (i < g0.n) fold(ml[i]);
+  if (more) {
+    int c2 = cc;
+    long long l2 = lo;
+    while (c2 <= cl) {
+      const SkPieces g = sk_gather(slots, cf, cl, P, T, sh, c2, l2);
+      for (int i = 0; i < g.n; ++i) fold(__ldcg(reinterpret_cast<const float2 *>(g.p[i & 7] + kMl) + row));
+    }
+  }
+  const float invs = ws > 0.f ? 1.0f / ws : 0.f;
+  float wt[kComposeGroup];  // this lane's row: weight of each of the first eight pieces
+#pragma unroll
+  for (int i = 0; i < kComposeGroup; ++i)
+    wt[i] = (i < g0.n && ml[i].y > 0.f) ? fast_exp2(ml[i].x - mx) * ml[i].y * invs : 0.f;
+  if (rv && lse_out) lse_out[hr] = ws > 0.f ? (mx + __log2f(ws)) * 0.6931471805599453f : -INFINITY;
+  const int chunk = lane & 15;  // 16-byte chunk (8 columns) of a row
+  for (int k = 0; k < 16; k += 4) {  // rows row0 + 2 (k + u) + lane / 16, u < 4
+    float acc[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[u][e] = 0.f;
+#pragma unroll
+    for (int pb = 0; pb < kComposeGroup; pb += 4) {
+      if (pb >= g0.n) break;
+      uint4 v[4][4];
+      float wv[4][4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int r = 2 * (k + u) + (lane >> 4);  // row within the warp
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          wv[u][i] = __shfl_sync(0xffffffffu, wt[pb + i], r);
+          const bool on = pb + i < g0.n;
+          const uint4 *q4 = reinterpret_cast<const uint4 *>(g0.p[pb + i] + (size_t)(row0 + r) * D * 2) + chunk;
+          v[u][i] = on ? __ldcg(q4) : make_uint4(0, 0, 0, 0);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t x[4] = {v[u][i].x, v[u][i].y, v[u][i].z, v[u][i].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            acc[u][2 * e] = fmaf(wv[u][i], bf16_bits_to_float(x[e] & 0xffffu), acc[u][2 * e]);
+            acc[u][2 * e + 1] = fmaf(wv[u][i], bf16_bits_to_float(x[e] >> 16), acc[u][2 * e + 1]);
+          }
+        }
+    }
+    if (more) {  // pieces past the first eight, one at a time (their weights per row)
+      int c2 = cc;
+      long long l2 = lo;
+      while (c2 <= cl) {
+        const SkPieces g = sk_gather(slots, cf, cl, P, T, sh, c2, l2);
+        for (int i = 0; i < g.n; ++i) {
+          const float2 m = __ldcg(reinterpret_cast<const float2 *>(g.p[i & 7] + kMl) + row);
+          const float wrow = m.y > 0.f ? fast_exp2(m.x - mx) * m.y * invs : 0.f;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int r = 2 * (k + u) + (lane >> 4);
+            const float wgt = __shfl_sync(0xffffffffu, wrow, r);
+            const uint4 vv = __ldcg(reinterpret_cast<const uint4 *>(g.p[i & 7] + (size_t)(row0 + r) * D * 2) + chunk);
+            const uint32_t x[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              acc[u][2 * e] = fmaf(wgt, bf16_bits_to_float(x[e] & 0xffffu), acc[u][2 * e]);
+              acc[u][2 * e + 1] = fmaf(wgt, bf16_bits_to_float(x[e] >> 16), acc[u][2 * e + 1]);
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int r = 2 * (k + u) + (lane >> 4);
+      const long long hr_r = __shfl_sync(0xffffffffu, (long long)hr, r);
+      const int rv_r = __shfl_sync(0xffffffffu, rv ? 1 : 0, r);
+      if (rv_r) {
+        uint4 *d = reinterpret_cast<uint4 *>(out + hr_r * D) + chunk;
+        *d = make_uint4(pack_bf16x2(acc[u][0], acc[u][1]), pack_bf16x2(acc[u][2], acc[u][3]),
+                        pack_bf16x2(acc[u][4], acc[u][5]), pack_bf16x2(acc[u][6], acc[u][7]));
+      }
+    }
+  }
+  if (row == 0) D2F_TRACE_MARK(0, 12);
+}
+// CTAs cf..cl that hold a tile of the pair (the arrivals its last piece waits for)
+__device__ __forceinline__ int sk_pieces(int cf, int cl, long long P, int T, SkShares sh) {
+  int n = 0;
+  long long lo = sh.start(cf);
+  for (int cc = cf; cc <= cl; ++cc) {
+    const long long hi = sh.start(cc + 1);
+    n += sk_first_tile(lo, P, T) < sk_first_tile(hi, P, T);
+    lo = hi;
+  }
+  return n;
+}
 
 template <int D>
 __global__ void __launch_bounds__((Layout<D, 6, 128, 1>::kThreads), 1)
@@ -1034,6 +1217,7 @@ __global__ void __launch_bounds__((Layout<D, 6, 128, 1>::kThreads), 1)
   const int Hkv = a.num_heads_kv, G = a.group, H = a.num_heads_q, B = a.block_size;
   const int ppt = N / B;  // pages (or window blocks) per tile
 
+  if (tid == 0) D2F_TRACE_MARK(0, 0);
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(&bars->full[i]), 1);
@@ -1123,6 +1307,7 @@ __global__ void __launch_bounds__((Layout<D, 6, 128, 1>::kThreads), 1)
   const int b0 = bars->sk[0], g0 = bars->sk[1], ta0 = bars->sk[2], R = bars->sk[3];
   const long long W = (long long)(uint32_t)bars->sk[4] | ((long long)bars->sk[5] << 32);
   const long long s0 = W > 0 ? sk_start(c, W, grid) : 0;
+  const SkShares sh = sk_shares(W > 0 ? W : 1, grid);
   grid_launch_dependents();
 
   // Every role walks the share's segments in the same order: tiles [ta, tb) of
@@ -1134,6 +1319,8 @@ __global__ void __launch_bounds__((Layout<D, 6, 128, 1>::kThreads), 1)
     const int box = lane;  // box i: tensor i / ppt (0 = K, 1 = V), page or block i % ppt
     const bool lane_on = box < 2 * ppt;
     const int tensor = lane_on ? box / ppt : 0, slot = lane_on ? box % ppt : 0;
+    // K/V are read once: evict them first, so the partial slots stay in L2
+    const uint64_t kv_policy = l2_policy_evict_first();
     int gu = 0;
     bool ok = true;
     int b = b0, g = g0, ta = ta0, rem = R;
@@ -1188,9 +1375,9 @@ __global__ void __launch_bounds__((Layout<D, 6, 128, 1>::kThreads), 1)
                              slot * (B / 8) * L::kGroupBytes;
         if (src >= 0) {
           if (t < q.Tc)
-            tma_load_5d(dst, tensor ? &tm_vpool : &tm_kpool, full, 0, 0, 0, 0, src * Hkv + g);
+            tma_load_5d_hint(dst, tensor ? &tm_vpool : &tm_kpool, full, 0, 0, 0, 0, src * Hkv + g, kv_policy);
           else
-            tma_load_5d(dst, tensor ? &tm_vwin : &tm_kwin, full, 0, 0, 0, src >> 3, g);
+            tma_load_5d_hint(dst, tensor ? &tm_vwin : &tm_kwin, full, 0, 0, 0, src >> 3, g, kv_policy);
         }
       }
       rem -= max(0, tb - ta);
@@ -1284,6 +1471,9 @@ __global__ void __launch_bounds__((Layout<D, 6, 128, 1>::kThreads), 1)
     bool ok = true;
     int b = b0, g = g0, ta = ta0, rem = R;
     long long pre_p = s0 - ta0;  // position of the current pair's first tile on the line
+#ifdef D2F_TRACE
+    int seg_no = 0;
+#endif
     while (ok && rem > 0 && b < a.batch) {
       const SkSeq q = sk_seq(a, b);
       const int tb = min(q.T, ta + rem);
@@ -1419,6 +1609,7 @@ __global__ void __launch_bounds__((Layout<D, 6, 128, 1>::kThreads), 1)
         // barriers (a warp that passed its waits must not wait there for one that
         // left).
         ok = named_sync_and(kBarSk, QR, ok);
+        if (row == 0) D2F_TRACE_MARK(0, 4 + min(seg_no++, 3));
         if (!ok) break;
         tc_fence_after();
 
@@ -1460,8 +1651,11 @@ __global__ void __launch_bounds__((Layout<D, 6, 128, 1>::kThreads), 1)
               for (int j = 0; j < 16; ++j)
                 w[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
               uint4 *d4 = reinterpret_cast<uint4 *>(slot + (size_t)row * D * 2 + ch * 64);
+              const uint64_t keep_policy = l2_policy_evict_last();  // read back by the last piece
 #pragma unroll
-              for (int j = 0; j < 4; ++j) d4[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+              for (int j = 0; j < 4; ++j)
+                st_global_v4_hint(d4 + j, make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]),
+                                  keep_policy);
             }
           }
           reinterpret_cast<float2 *>(slot + (size_t)QR * D * 2)[row] =
@@ -1469,65 +1663,17 @@ __global__ void __launch_bounds__((Layout<D, 6, 128, 1>::kThreads), 1)
           __threadfence();  // this row's piece before the arrival
           named_sync(kBarSk, QR);
           if (row == 0) {
-            int target = 0;  // CTAs with a share that touch the pair
-            for (int cc = cf; cc <= cl; ++cc) target += sk_start(cc + 1, W, grid) > sk_start(cc, W, grid);
+            const int target = sk_pieces(cf, cl, pre_p, q.T, sh);  // CTAs holding tiles of the pair
             const int pair = b * Hkv + g;
             const int last = atomic_add_acq_rel(a.sk_cnt + pair, 1) == target - 1;
             if (last) a.sk_cnt[pair] = 0;  // every piece of this launch is in
             bars->sk[0] = last;
           }
           named_sync(kBarSk, QR);
-          if (bars->sk[0] && rv) {
-            // The last piece in: compose the pair's pieces of this row in log space.
-            float mx = -INFINITY;
-            for (int cc = cf; cc <= cl; ++cc) {
-              if (sk_start(cc + 1, W, grid) <= sk_start(cc, W, grid)) continue;
-              const int wc = (cc == cf && sk_start(cc, W, grid) < pre_p) ? 1 : 0;
-              const float2 ml = __ldcg(reinterpret_cast<const float2 *>(
-                  a.sk_slots + (size_t)(2 * cc + wc) * kSkSlotBytes + (size_t)QR * D * 2) + row);
-              if (ml.y > 0.f) mx = fmaxf(mx, ml.x);
-            }
-            float ws = 0.f;
-            for (int cc = cf; cc <= cl; ++cc) {
-              if (sk_start(cc + 1, W, grid) <= sk_start(cc, W, grid)) continue;
-              const int wc = (cc == cf && sk_start(cc, W, grid) < pre_p) ? 1 : 0;
-              const float2 ml = __ldcg(reinterpret_cast<const float2 *>(
-                  a.sk_slots + (size_t)(2 * cc + wc) * kSkSlotBytes + (size_t)QR * D * 2) + row);
-              if (ml.y > 0.f) ws += fast_exp2(ml.x - mx) * ml.y;
-            }
-            const float invs = ws > 0.f ? 1.0f / ws : 0.f;
-            for (int ch = 0; ch < D / 32; ++ch) {
-              float acc[32];
-#pragma unroll
-              for (int j = 0; j < 32; ++j) acc[j] = 0.f;
-              for (int cc = cf; cc <= cl; ++cc) {
-                if (sk_start(cc + 1, W, grid) <= sk_start(cc, W, grid)) continue;
-                const int wc = (cc == cf && sk_start(cc, W, grid) < pre_p) ? 1 : 0;
-                const uint8_t *sl = a.sk_slots + (size_t)(2 * cc + wc) * kSkSlotBytes;
-                const float2 ml = __ldcg(reinterpret_cast<const float2 *>(sl + (size_t)QR * D * 2) + row);
-                if (!(ml.y > 0.f)) continue;
-                const float wj = fast_exp2(ml.x - mx) * ml.y * invs;
-                const uint4 *p4 = reinterpret_cast<const uint4 *>(sl + (size_t)row * D * 2 + ch * 64);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  const uint4 v = __ldcg(p4 + j);
-                  const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                  for (int e = 0; e < 4; ++e) {
-                    acc[8 * j + 2 * e] = fmaf(wj, bf16_bits_to_float(vv[e] & 0xffffu), acc[8 * j + 2 * e]);
-                    acc[8 * j + 2 * e + 1] = fmaf(wj, bf16_bits_to_float(vv[e] >> 16), acc[8 * j + 2 * e + 1]);
-                  }
-                }
-              }
-              uint32_t w[16];
-#pragma unroll
-              for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(acc[2 * j], acc[2 * j + 1]);
-              uint4 *d4 = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(a.out) + hr * D + ch * 32);
-#pragma unroll
-              for (int j = 0; j < 4; ++j) d4[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-            }
-            if (a.lse_out) a.lse_out[hr] = ws > 0.f ? (mx + __log2f(ws)) * 0.6931471805599453f : -INFINITY;
-          }
+          if (bars->sk[0] && row == 0) D2F_TRACE_MARK(0, 8);
+          if (bars->sk[0])  // the last piece in: compose the pair's pieces (every lane)
+            sk_compose(a.sk_slots, reinterpret_cast<uint16_t *>(a.out), a.lse_out, hr, rv, row, cf, cl,
+                       pre_p, q.T, sh);
           named_sync(kBarSk, QR);  // bars->sk[0] is reused by the next piece
         }
       }
@@ -1547,6 +1693,7 @@ __global__ void __launch_bounds__((Layout<D, 6, 128, 1>::kThreads), 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (tid == 0) D2F_TRACE_MARK(0, 3);
   if (warp == 1) tmem_dealloc(bars->tmem_base, L::kTmemCols);
 }
 
