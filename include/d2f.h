@@ -44,6 +44,19 @@
  *   *_workspace_size query returns. It must be zero-filled before its first use
  *   (e.g. cudaMemsetAsync); every call leaves it ready for the next call on the
  *   same stream. Calls that share one workspace must not overlap in time.
+ *
+ * Size limits (a call beyond one returns D2F_ERR_UNSUPPORTED before anything is
+ * enqueued):
+ * - attention: batch * num_heads_kv <= 65535 (one grid dimension); head_dim 64
+ *   or 128 with bf16 on the tensor-core path (block_size 8, 16 or 32), any other
+ *   case on the CUDA-core path, block_size <= 256;
+ * - commit: total_q <= 65535 window rows, block_size 1..32, num_splits <= 64;
+ * - window step: one CTA holds the whole window state in shared memory
+ *   (block_size <= 128; about 5 bytes per window row of capacity plus per-
+ *   sequence state against 227 KB: some 45,000 rows for a small batch);
+ * - the no-allocation commit: the scratch bound stated at d2f_commit_noalloc.
+ * The workloads this library is measured on (up to 512 window rows, batch 16,
+ * 32 KV heads, 32,768 cached tokens) are far inside all of them.
  */
 #ifndef D2F_H
 #define D2F_H
