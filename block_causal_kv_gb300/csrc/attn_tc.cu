@@ -248,11 +248,12 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
                    : (QR == 64 && warp >= L::kFirstSoft && (warp & 3) >= 2) ? 1 + (MT == 2) + ((warp & 3) - 2)
                    : -1;
   // D2F_ATTN_CACHE_READY: the page table, context lengths, window layout and
-  // cached pages are final before the previous kernel started, so the producers
-  // may read them and load cached tiles before waiting for it; they wait before
-  // their first window tile or once the ring is full. Every other read (Q, window
-  // K/V) and every write comes after the wait.
-  const bool early = a.cache_ready && prod >= 0;
+  // cached pages are final before the previous kernel started, so every thread
+  // may read them before waiting for it. The producers load cached tiles early
+  // and wait before their first window tile or once the ring is full; the softmax
+  // warps wait just before they load Q; the MMA issuers read no global memory.
+  // Every other read (Q, window K/V) and every write comes after a wait.
+  const bool early = a.cache_ready != 0;
   bool waited = !early;
   if (!early) grid_dependency_wait();  // inputs may come from the previous kernel in the stream
   if (tid == 0) D2F_TRACE_MARK(0, 1);
@@ -569,6 +570,10 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
     // ============ softmax (a warpgroup per row tile, a thread per TMEM lane) =====
     const bool live = wg < mt_live;  // warpgroup-uniform
     {
+      if (!waited) {  // Q may come from the previous kernel
+        grid_dependency_wait();
+        waited = true;
+      }
       // The Q rows into the 128-byte-swizzled K-major layout the MMA reads: in
       // row tile wg, 16-byte chunk c of column block h lands at
       //   wg*kTileQBytes + h*kQHalf + (row/8)*1024 + (row%8)*128 + ((c ^ (row%8)) * 16).
@@ -724,8 +729,9 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
   }
 
   // ---- epilogue ---------------------------------------------------------------
-  // A producer that loaded only cached tiles (or had none) has not waited yet;
-  // the epilogue's writes come after the previous kernel in every thread.
+  // A producer that loaded only cached tiles (or had none), an MMA issuer, or a
+  // thread without work has not waited yet; the epilogue's writes come after the
+  // previous kernel in every thread.
   if (!waited) grid_dependency_wait();
   __syncwarp();
   __syncthreads();  // every role is done; Q and the ring are free
