@@ -799,9 +799,7 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
   } else if (active) {
     const int LR = L::rows_per_owner(cs);  // rows a CTA owns (at most)
     const int BS = L::block_bytes(cs);     // one owner's block: LR rows + LR (max, sum)
-    const uint32_t recv = sb + L::kQ;      // [source split][BS], filled by the bulk copies
     const uint32_t stg = sb + L::staging(cs);  // [owner][BS], this CTA's rows
-    const uint32_t recv_bar = smem_u32(&bars->recv);
     // 1) stage this CTA's rows: local row lrow (wg*QR + lane row) -> owner
     //    lrow % cs, slot lrow / cs; the 16-byte chunks of a row are XOR-swizzled
     //    by (lrow % 8).
@@ -841,11 +839,9 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
                      "f"(mx), "f"(sm)
                      : "memory");
       }
-      fence_proxy_async_smem();  // the bulk copies read these blocks
     }
-    // 2) each owner expects cs blocks; the cluster barrier publishes the staged
-    //    blocks and frees every receive area (each CTA is past its ring).
-    if (tid == 0) mbar_arrive_expect_tx(recv_bar, (uint32_t)(cs * BS));
+    // 2) the cluster barrier publishes every CTA's staged blocks to the cluster
+    //    (release / acquire at cluster scope).
     __syncwarp();
     tc_fence_before();
     cluster_sync();
@@ -855,31 +851,16 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
       tmem_dealloc(bars->tmem_base, L::kTmemCols);
       tmem_freed = true;
     }
-    // 3) block j of this CTA -> receive slot [split] of CTA j
-    if (warp == 0 && lane < cs)
-      bulk_copy_to_cluster(dsmem_addr(recv + split * BS, lane), stg + lane * BS, BS,
-                           dsmem_addr(recv_bar, lane));
-    // 4) wait for the cs blocks this CTA owns, then arrive on the closing
-    //    cluster barrier: once every CTA has arrived, every copy has landed and
-    //    no staging block is still being read.
-    // The copies into this CTA are always issued (step 3 runs whatever happened
-    // before), so this wait ignores the abort flag and takes the full budget: a
-    // CTA must not leave while another CTA's copy may still land in its shared
-    // memory.
-    bool got = true;
-    if (warp >= L::kFirstSoft) {
-      volatile int no_abort = 0;
-      got = __all_sync(0xffffffffu, mbar_wait(recv_bar, 0, &no_abort, a.err, kDrainCycles));
-    }
-    if (tid == 64) D2F_TRACE_MARK(0, 9);
-    __syncwarp();
-    cluster_arrive_relaxed();
-    // 5) compose the rows this CTA owns: half a warp per row, lane c of the half
-    //    holds columns [c * D/16, (c + 1) * D/16).
+    // 3) compose the rows this CTA owns, reading each source CTA's block for this
+    //    owner (block `split` of its staging area) straight from its shared
+    //    memory: half a warp per row, lane c of the half holds columns
+    //    [c * D/16, (c + 1) * D/16); every source's chunk of a row is loaded before
+    //    any is used.
+    const uint32_t own_blk = stg + split * BS;  // the same offset in every CTA
     if (warp >= L::kFirstSoft) {
       constexpr int kCols = D / 16;
       const int hw = lane >> 4, sub = lane & 15;
-      for (int lr0 = (warp - L::kFirstSoft) * 2; got && lr0 * cs + split < nrows; lr0 += 2 * L::kSoftWarps) {
+      for (int lr0 = (warp - L::kFirstSoft) * 2; lr0 * cs + split < nrows; lr0 += 2 * L::kSoftWarps) {
         const int lr = lr0 + hw;
         const int crow = lr * cs + split;  // CTA row of this half-warp
         const bool valid = crow < nrows;
@@ -887,8 +868,7 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
         const int r2 = r_begin + crow;
         const int64_t hr2 = (int64_t)(q0 + r2 / G) * H + g * G + r2 % G;
         float2 ml = make_float2(-INFINITY, 0.f);
-        if (valid && sub < cs)
-          ml = *reinterpret_cast<const float2 *>(smem + sub * BS + LR * L::kRowBytes + lr * 8);
+        if (valid && sub < cs) ml = dsmem_ld_f2(dsmem_addr(own_blk + LR * L::kRowBytes + lr * 8, sub));
         // a kept cached part is one more normalised part: (its lse in log2 units, 1)
         const float lp = (a.prev_lse && valid) ? a.prev_lse[hr2] * 1.4426950408889634f : -INFINITY;
         float mx = fmaxf(ml.x, lp);
@@ -911,23 +891,32 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
         }
         const uint32_t off = lr * L::kRowBytes + (D == 128 ? ((sub ^ key) << 4)
                                                             : (((sub >> 1) ^ key) << 4) + (sub & 1) * 8);
+        float wj[kMaxCluster];
+        uint32_t v[kMaxCluster][kCols / 2];
 #pragma unroll
         for (int j = 0; j < kMaxCluster; ++j) {
-          const float wj = __shfl_sync(0xffffffffu, w, (hw << 4) + j);
-          if (j < cs && wj > 0.f) {
-            uint32_t v[kCols / 2];
-            if (D == 128) {
-              const uint4 q = *reinterpret_cast<const uint4 *>(smem + j * BS + off);
-              v[0] = q.x; v[1] = q.y; v[2 % (kCols / 2)] = q.z; v[3 % (kCols / 2)] = q.w;
-            } else {
-              const uint2 q = *reinterpret_cast<const uint2 *>(smem + j * BS + off);
-              v[0] = q.x; v[1 % (kCols / 2)] = q.y;
-            }
+          wj[j] = __shfl_sync(0xffffffffu, w, (hw << 4) + j);
 #pragma unroll
-            for (int c = 0; c < kCols / 2; ++c) {
-              acc[2 * c] = fmaf(wj, bf16_bits_to_float(v[c] & 0xffffu), acc[2 * c]);
-              acc[2 * c + 1] = fmaf(wj, bf16_bits_to_float(v[c] >> 16), acc[2 * c + 1]);
+          for (int c = 0; c < kCols / 2; ++c) v[j][c] = 0u;
+          if (j < cs && wj[j] > 0.f) {
+            const uint32_t src = dsmem_addr(own_blk + off, j);
+            if (D == 128) {
+              const float4 q = dsmem_ld_f4(src);
+              v[j][0] = __float_as_uint(q.x); v[j][1] = __float_as_uint(q.y);
+              v[j][2 % (kCols / 2)] = __float_as_uint(q.z); v[j][3 % (kCols / 2)] = __float_as_uint(q.w);
+            } else {
+              const float2 q = dsmem_ld_f2(src);
+              v[j][0] = __float_as_uint(q.x); v[j][1 % (kCols / 2)] = __float_as_uint(q.y);
             }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kMaxCluster; ++j) {
+          if (!(j < cs && wj[j] > 0.f)) continue;
+#pragma unroll
+          for (int c = 0; c < kCols / 2; ++c) {
+            acc[2 * c] = fmaf(wj[j], bf16_bits_to_float(v[j][c] & 0xffffu), acc[2 * c]);
+            acc[2 * c + 1] = fmaf(wj[j], bf16_bits_to_float(v[j][c] >> 16), acc[2 * c + 1]);
           }
         }
         if (valid && !aborted) {
@@ -947,7 +936,10 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
       }
     }
     if (tid == 64) D2F_TRACE_MARK(0, 12);
+    // 4) this CTA's reads of the other CTAs' staging blocks are done; they may
+    //    leave once every CTA has arrived
     __syncwarp();
+    cluster_arrive();
     cluster_wait();
   }
 
