@@ -48,10 +48,11 @@
 //
 // Composition. With cs > 1 every CTA writes its rows, normalised (O / l, bf16)
 // with their (max, sum), into a staging block per owning CTA (row r -> CTA
-// r mod cs). After one cluster barrier (every CTA done with its ring, which the
-// blocks overlay) each CTA sends block j to CTA j with one shared-to-shared bulk
-// copy; the owner waits on an mbarrier for the cs blocks it receives, composes
-// its rows in log space and writes the output. No partial goes to global
+// r mod cs), in its own shared memory (over its ring: every CTA is done with it).
+// One cluster barrier publishes the blocks; each owner reads its block from
+// every CTA of the cluster straight from that CTA's shared memory, composes its
+// rows in log space and writes the output; a closing cluster barrier keeps the
+// blocks alive until every owner has read them. No partial goes to global
 // memory.
 //
 // Set-up that reads no global memory (mbarriers, TMEM) runs before the
@@ -121,12 +122,9 @@ struct Layout {
   __host__ __device__ static constexpr int block_bytes(int cs) {
     return (rows_per_owner(cs) * (kRowBytes + 8) + 15) & ~15;
   }
-  __host__ __device__ static constexpr int staging(int cs) {  // after the receive blocks
-    return (cs * block_bytes(cs) + 127) & ~127;
-  }
-  static_assert(2 * ((MT * QR + kMaxCluster - 1) * (kRowBytes + 8) + 16 * kMaxCluster) + 128 <=
-                    kBars,
-                "receive and staging blocks must fit in the Q + ring area");
+  __host__ __device__ static constexpr int staging(int) { return 0; }  // over Q and the ring
+  static_assert((MT * QR + kMaxCluster - 1) * (kRowBytes + 8) + 16 * kMaxCluster <= kBars,
+                "staging blocks must fit in the Q + ring area");
   static_assert(MT == 1 || MT == 2, "one or two softmax warpgroups");
   static_assert(MT * kWgCols <= 512, "S / P buffers and accumulators fit TMEM");
   static_assert(kAlloc <= 232448, "shared memory per CTA");
@@ -150,7 +148,7 @@ static __device__ long long g_d2f_pass[3][8][64];
 struct Bars {
   // s_full / p_full / pv_done: [warpgroup][S/P buffer]
   uint64_t full[kMaxStages], empty[kMaxStages], s_full[2][2], p_full[2][2], pv_done[2][2], q_full,
-      drain, recv;
+      drain;
   uint32_t tmem_base;
   int abort_flag;
   int sk[6];  // stream-K form: the share's first (sequence, KV head, tile), length, W (lo, hi)
@@ -207,9 +205,8 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
       }
     mbar_init(smem_u32(&bars->q_full), QR * MT);
     mbar_init(smem_u32(&bars->drain), L::kIssuers);
-    mbar_init(smem_u32(&bars->recv), 1);
     bars->abort_flag = 0;
-    mbar_fence_init();  // cluster scope: other CTAs complete bytes on `recv`
+    mbar_fence_init();  // the initialised barriers, visible at cluster scope
     tma_prefetch_desc(&tm_kpool);
     tma_prefetch_desc(&tm_vpool);
     tma_prefetch_desc(&tm_kwin);

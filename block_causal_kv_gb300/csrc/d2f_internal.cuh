@@ -326,18 +326,6 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// 1-D bulk copy from this CTA's shared memory into another CTA of the cluster
-// (dst and bar are shared::cluster addresses in the destination CTA; 16-byte
-// aligned addresses, size a multiple of 16). Completion is counted on the
-// destination's mbarrier.
-__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes,
-                                                     uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
-      "[%3];" ::"r"(dst),
-      "r"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
 // Tensor copy from shared memory to global (bulk async-group completion).
 __device__ __forceinline__ void tma_store_5d(const CUtensorMap *map, uint32_t src, int c0, int c1,
                                              int c2, int c3, int c4) {
