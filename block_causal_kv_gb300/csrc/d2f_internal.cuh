@@ -28,11 +28,13 @@ bool pdl_enabled();
 // the GB300's clocks), set D2F_ERR_TIMEOUT in the error word and unwind.
 constexpr long long kWaitCycles = 2000000000LL;
 // Waits that only drain work this CTA already issued (copies landing, MMAs
-// completing) give up after ~1 ms: far longer than a copy or an MMA takes.
-// After another role gave up, such a wait may be on a phase that can no longer
-// complete (a stage that one producer issued and another abandoned); it then
-// ends here instead of after kWaitCycles.
-constexpr long long kDrainCycles = 2000000LL;
+// completing) give up after ~0.1 s: far longer than a copy or an MMA takes, even
+// under a profiler's instrumented replay (where a 2e6-cycle budget, ~1 ms, was
+// measured to run out and report a false time-out). After another role gave up,
+// such a wait may be on a phase that can no longer complete (a stage that one
+// producer issued and another abandoned); it then ends here instead of after
+// kWaitCycles.
+constexpr long long kDrainCycles = 200000000LL;
 
 // ---------------------------------------------------------------------------
 // Launch arguments
