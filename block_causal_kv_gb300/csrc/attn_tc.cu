@@ -443,6 +443,10 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(M, N, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(M, D, 0, 1);
+      // descriptors of Q and of stage 0's K and V; each MMA advances them by a constant
+      const uint64_t q_desc = smem_desc_sw128(sb + L::kQ, 16, 1024);
+      const uint64_t k_desc = smem_desc_sw128(sb + L::kRing, 16, L::kGroupBytes);
+      const uint64_t v_desc = smem_desc_sw128(sb + L::kRing + L::kKBytes, 1024, L::kGroupBytes);
       bool ok = mbar_wait(smem_u32(&bars->q_full), 0, abort_flag, a.err, a.wait_cycles);
       for (int u = 0; u < T && ok; ++u) {
         const int stage = u % NS;
@@ -456,13 +460,13 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
             break;
           }
           tc_fence_after();
-          const uint32_t k_base = sb + L::kRing + stage * L::kStage;
+          const uint64_t kd = smem_desc_advance(k_desc, stage * L::kStage);
 #pragma unroll
           for (int h = 0; h < L::kHalves; ++h) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = smem_desc_sw128(sb + L::kQ + h * L::kQHalf + kk * 32, 16, 1024);
-              const uint64_t bd = smem_desc_sw128(k_base + h * 1024 + kk * 32, 16, L::kGroupBytes);
+              const uint64_t ad = smem_desc_advance(q_desc, h * L::kQHalf + kk * 32);
+              const uint64_t bd = smem_desc_advance(kd, h * 1024 + kk * 32);
               umma_bf16(tmem + (u & 1) * N, ad, bd, idesc_qk, (h | kk) ? 1u : 0u);
             }
           }
@@ -473,10 +477,10 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
             break;
           }
           tc_fence_after();
-          const uint32_t v_base = sb + L::kRing + stage * L::kStage + L::kKBytes;
+          const uint64_t vd = smem_desc_advance(v_desc, stage * L::kStage);
 #pragma unroll
           for (int ks = 0; ks < N / 16; ++ks) {
-            const uint64_t bd = smem_desc_sw128(v_base + ks * 2 * L::kGroupBytes, 1024, L::kGroupBytes);
+            const uint64_t bd = smem_desc_advance(vd, ks * 2 * L::kGroupBytes);
             umma_bf16_tmem_a(tmem + kTmemO, tmem + (u & 1) * N + ks * 8, bd, idesc_pv,
                              (u > 0 || ks > 0) ? 1u : 0u);
           }
@@ -497,7 +501,11 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(M, N, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(M, D, 0, 1);
-      const uint32_t q_base = sb + L::kQ;
+      // descriptors of this row tile's Q and of stage 0's K and V; each MMA advances
+      // them by a constant
+      const uint64_t q_desc = smem_desc_sw128(sb + L::kQ + wi * L::kTileQBytes, 16, 1024);
+      const uint64_t k_desc = smem_desc_sw128(sb + L::kRing, 16, L::kGroupBytes);
+      const uint64_t v_desc = smem_desc_sw128(sb + L::kRing + L::kKBytes, 1024, L::kGroupBytes);
       bool ok = mbar_wait(smem_u32(&bars->q_full), 0, abort_flag, a.err, a.wait_cycles);
       // Key tile u: S goes to S/P buffer u % 2 of warpgroup wi; P.V_u accumulates
       // into warpgroup wi's O.
@@ -506,11 +514,11 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
           return false;
         tc_fence_after();
         D2F_PASS_MARK(2, 3 + i, u);
-        const uint32_t v_base = sb + L::kRing + (u % NS) * L::kStage + L::kKBytes;
+        const uint64_t vd = smem_desc_advance(v_desc, (u % NS) * L::kStage);
         const uint32_t tw = tmem + i * L::kWgCols;
 #pragma unroll
         for (int ks = 0; ks < N / 16; ++ks) {  // 16 keys = 8 TMEM columns of P per step
-          const uint64_t bd = smem_desc_sw128(v_base + ks * 2 * L::kGroupBytes, 1024, L::kGroupBytes);
+          const uint64_t bd = smem_desc_advance(vd, ks * 2 * L::kGroupBytes);
           umma_bf16_tmem_a(tw + kTmemO, tw + (u & 1) * N + ks * 8, bd, idesc_pv,
                            (u > 0 || ks > 0) ? 1u : 0u);
         }
@@ -541,14 +549,13 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
         if (u == T - 1) D2F_TRACE_MARK(0, 3);
         // S_u overwrites the S/P buffer that P_{u-2} occupied: P.V_{u-2} was issued
         // before this (MMAs of one thread execute in order).
-        const uint32_t k_base = sb + L::kRing + stage * L::kStage;
-        const uint32_t qi_base = q_base + wi * L::kTileQBytes;
+        const uint64_t kd = smem_desc_advance(k_desc, stage * L::kStage);
 #pragma unroll
         for (int h = 0; h < L::kHalves; ++h) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = smem_desc_sw128(qi_base + h * L::kQHalf + kk * 32, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(k_base + h * 1024 + kk * 32, 16, L::kGroupBytes);
+            const uint64_t ad = smem_desc_advance(q_desc, h * L::kQHalf + kk * 32);
+            const uint64_t bd = smem_desc_advance(kd, h * 1024 + kk * 32);
             umma_bf16(tmem + wi * L::kWgCols + (u & 1) * N, ad, bd, idesc_qk, (h | kk) ? 1u : 0u);
           }
         }
@@ -1394,6 +1401,10 @@ __global__ void __launch_bounds__((Layout<D, 6, 128, 1>::kThreads), 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(M, N, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(M, D, 0, 1);
+      // descriptors of Q and of stage 0's K and V; each MMA advances them by a constant
+      const uint64_t q_desc = smem_desc_sw128(sb + L::kQ, 16, 1024);
+      const uint64_t k_desc = smem_desc_sw128(sb + L::kRing, 16, L::kGroupBytes);
+      const uint64_t v_desc = smem_desc_sw128(sb + L::kRing + L::kKBytes, 1024, L::kGroupBytes);
       int gu = 0, k = 0;  // tiles and segments so far
       bool ok = true;
       int b = b0, g = g0, ta = ta0, rem = R;
@@ -1414,13 +1425,13 @@ __global__ void __launch_bounds__((Layout<D, 6, 128, 1>::kThreads), 1)
               break;
             }
             tc_fence_after();
-            const uint32_t k_base = sb + L::kRing + stage * L::kStage;
+            const uint64_t kd = smem_desc_advance(k_desc, stage * L::kStage);
 #pragma unroll
             for (int h = 0; h < L::kHalves; ++h) {
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t ad = smem_desc_sw128(sb + L::kQ + h * L::kQHalf + kk * 32, 16, 1024);
-                const uint64_t bd = smem_desc_sw128(k_base + h * 1024 + kk * 32, 16, L::kGroupBytes);
+                const uint64_t ad = smem_desc_advance(q_desc, h * L::kQHalf + kk * 32);
+                const uint64_t bd = smem_desc_advance(kd, h * 1024 + kk * 32);
                 umma_bf16(tmem + (gu & 1) * N, ad, bd, idesc_qk, (h | kk) ? 1u : 0u);
               }
             }
@@ -1432,11 +1443,11 @@ __global__ void __launch_bounds__((Layout<D, 6, 128, 1>::kThreads), 1)
               break;
             }
             tc_fence_after();
-            const uint32_t v_base = sb + L::kRing + stage * L::kStage + L::kKBytes;
+            const uint64_t vd = smem_desc_advance(v_desc, stage * L::kStage);
             const bool first = t == ta;  // the segment's first P V overwrites O
 #pragma unroll
             for (int ks = 0; ks < N / 16; ++ks) {
-              const uint64_t bd = smem_desc_sw128(v_base + ks * 2 * L::kGroupBytes, 1024, L::kGroupBytes);
+              const uint64_t bd = smem_desc_advance(vd, ks * 2 * L::kGroupBytes);
               umma_bf16_tmem_a(tmem + kTmemO, tmem + (gu & 1) * N + ks * 8, bd, idesc_pv,
                                (!first || ks > 0) ? 1u : 0u);
             }

@@ -603,6 +603,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// The descriptor of the same layout `bytes` further on in shared memory (bytes a
+// multiple of 16). Only the start-address field (bits 0-13: address >> 4) moves,
+// and it cannot carry into the fields above while the address stays below
+// 256 KB, so an issuing loop can build each descriptor with one add.
+__device__ __forceinline__ uint64_t smem_desc_advance(uint64_t d, uint32_t bytes) {
+  return d + (uint64_t)(bytes >> 4);
+}
+
 // Instruction descriptor, kind::f16 with bf16 A/B and f32 accumulator.
 //   D format f32 (bits 4-5 = 1), A and B format bf16 (bits 7-9 = 1, 10-12 = 1),
 //   A major (bit 15) and B major (bit 16): 0 = K-major, 1 = MN-major,

@@ -117,6 +117,33 @@ def test_unaligned_rows_use_the_scalar_path():
     _check(p, dev, num_splits=3)
 
 
+@pytest.mark.parametrize("splits", [0, 3, 7])
+def test_vector_path_with_a_ragged_row_end(splits):
+    # vocab 1001 with a 1008-element row stride: rows start 16-byte aligned (the
+    # 128-bit path), and each row ends inside a vector, so the last slice of every
+    # row finishes with scalar loads
+    dev = device()
+    w = synth.Workload("v", 2, 1, 1, 8, 8, torch.bfloat16, [0, 0], [3, 2], 1001,
+                       logit_row_pad=7, masked_frac=0.7, seed=23)
+    p = synth.make_problem(w)
+    assert (p.logits.stride(0) * 2) % 16 == 0 and p.w.vocab % 8 != 0
+    _check(p, dev, num_splits=splits)
+
+
+@pytest.mark.parametrize("B", [1, 4, 8])
+@pytest.mark.parametrize("metric", [0, 3])
+def test_small_vocabulary_many_blocks(B, metric):
+    # a 96-entry vocabulary over 224 rows: one slice per row, 28 to 224 blocks
+    # decided by their last-arriving CTAs, random phases
+    dev = device()
+    w = synth.Workload("m", 4, 1, 1, 8, B, torch.bfloat16, [0] * 4, [64 // B, 40 // B, 96 // B, 24 // B],
+                       96, masked_frac=0.6, taus=(0.05, 0.3, 0.6), logit_sigma=1.5, seed=40 + B)
+    p = synth.make_problem(w)
+    phase = torch.randint(0, 2, p.block_phase.shape, generator=torch.Generator().manual_seed(B),
+                          dtype=torch.uint8)
+    _check(p, dev, phase=phase, metric=metric)
+
+
 def test_float32_logits():
     dev = device()
     p = synth.make_problem(synth.workload("tiny"))
@@ -272,6 +299,26 @@ def test_early_commit_workloads(metric, name, splits):
     stop = _early_check(p, dev, metric, torch.tensor(thr, dtype=torch.float32), phase=phase,
                         num_splits=splits)
     print("%s m%d s%d: stopped %s" % (name, metric, splits, stop.tolist()))
+
+
+@pytest.mark.parametrize("B", [1, 4])
+def test_early_commit_small_vocabulary_many_blocks(B):
+    """The early commit over many small blocks (a 96-entry vocabulary, 224 rows):
+    thresholds 0.1 below / above each sequence's smallest gap, alternating."""
+    dev = device()
+    w = synth.Workload("m", 4, 1, 1, 8, B, torch.bfloat16, [0] * 4, [64 // B, 40 // B, 96 // B, 24 // B],
+                       96, masked_frac=0.6, taus=(0.05, 0.3, 0.6), logit_sigma=1.5, seed=50 + B)
+    p = synth.make_problem(w)
+    gaps = oracle.commit(p.logits, p.tokens, p.masked, p.q_start, p.block_phase, p.tau,
+                         p.w.block_size, p.mask_id, metric=3)["conf"]
+    m0 = p.masked.bool()
+    thr = []
+    for b in range(p.w.batch):
+        r0, r1 = int(p.q_start[b]), int(p.q_start[b + 1])
+        g = gaps[r0:r1][m0[r0:r1]]
+        thr.append((float(g.min()) if len(g) else 0.0) + (-0.1 if b % 2 == 0 else 0.1))
+    stop = _early_check(p, dev, 3, torch.tensor(thr, dtype=torch.float32))
+    assert stop.tolist() == [1, 0, 1, 0]
 
 
 def test_early_commit_rejects_entropy():
