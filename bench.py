@@ -171,6 +171,28 @@ def peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+def sustained_tflops():
+    """Dense bf16 TF/s sustained over seconds (the step loop is seconds long), else
+    the fallback's sustained figure."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 1700.0, "fallback"
+
+
+def attn_roofline(bytes_, flops_, hbm_gbs, tflops, us, tensor=True):
+    """The attention's two roofline terms (µs): its bytes at the HBM peak and its
+    flops at the dense bf16 peak (none on the CUDA-core path); the larger one
+    bounds it, and frac_of_roofline is that bound over the measured time."""
+    t_hbm = bytes_ / hbm_gbs / 1e3
+    t_tensor = flops_ / tflops / 1e6 if tensor else None
+    bound = "tensor" if (t_tensor or 0.0) > t_hbm else "hbm"
+    t_roof = max(t_hbm, t_tensor or 0.0)
+    return {"hbm_us": t_hbm, "tensor_us": t_tensor, "bound": bound,
+            "frac_of_roofline": t_roof / us if us else None}
+
+
 def source_sha(files):
     h = hashlib.sha256()
     for f in files:
@@ -738,6 +760,43 @@ def measure(args, name, K, W, world, rank, dev, cpu=True):
             b.record(stream)
         torch.cuda.synchronize()
         per_kernel[which] = a.elapsed_time(b) * 1000.0 / (reps * n_sets)
+    # Hot-L2 step (reported, never the headline): the same inputs every step, so
+    # they stay in L2, where one input set fits in half of L2. Like the timed
+    # graph, one graph runs many steps and resets their decode state once; each
+    # step has its own copy of that small state (the commit rewrites it), all
+    # other inputs are input set 0's. Plain steps only.
+    hot = None
+    if per_set <= l2 // 2 and not (reuse or sched or fused or appends):
+        import copy as _copy
+        n_hot = max(8, n_sets)
+        tok_h0, msk_h0 = tokens0[0].repeat(n_hot, 1), masked0[0].repeat(n_hot, 1)
+        tok_h, msk_h = tok_h0.clone(), msk_h0.clone()
+        hsets = []
+        for i in range(n_hot):
+            h = _copy.copy(sets[0])
+            h.tokens, h.masked = tok_h[i], msk_h[i]
+            hsets.append(h)
+        g_hot = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_hot, stream=stream, capture_error_mode="relaxed"):
+            tok_h.copy_(tok_h0)
+            msk_h.copy_(msk_h0)
+            for h in hsets:
+                step_kernels(h)
+        reps_hot = max(3, min(200, 20000 // n_hot))
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g_hot.replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for _ in range(reps_hot):
+                g_hot.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        hot_us = a.elapsed_time(b) * 1000.0 / (reps_hot * n_hot)
+        hot = {"us_per_step": hot_us, "steps_per_s": 1e6 / hot_us, "set_bytes": per_set,
+               "note": "input set 0 every step (L2-resident), decode state reset per graph "
+                       "as in the timed region: not counted"}
     step_us = elapsed_ms * 1000.0 / K
     attn_in_step = (step_us - per_kernel["commit"] - per_kernel.get("append", 0.0)
                     - per_kernel.get("window", 0.0))
@@ -754,9 +813,14 @@ def measure(args, name, K, W, world, rank, dev, cpu=True):
     t_commit = statistics.mean(commit_us) if commit_us else None
     kernels = {}
     if t_attn:
+        tf_sus, tf_kind = sustained_tflops()
         kernels["block_attn"] = {"us": t_attn, "bytes": attn_b, "GB/s": attn_b / t_attn / 1e3,
                                  "frac": attn_b / t_attn / 1e3 / hbm,
                                  "TFLOP/s": flops(p, reuse) / t_attn / 1e6,
+                                 "roofline": dict(attn_roofline(attn_b, flops(p, reuse), hbm, tf_sus,
+                                                                t_attn, dcode == d2f.BF16),
+                                                  tensor_peak_tflops=tf_sus,
+                                                  tensor_peak_kind=tf_kind + " sustained"),
                                  "us_attention_only_graph": per_kernel["attn"]}
     if t_commit:
         kernels["commit"] = {"us": t_commit, "bytes": commit_b, "GB/s": commit_b / t_commit / 1e3,
@@ -823,6 +887,8 @@ def measure(args, name, K, W, world, rank, dev, cpu=True):
             "roofline": roofline, "kernels": kernels,
             "gpu_launches": K * (2 + (1 if appends else 0) + (1 if sched else 0)),
             "clocks": clocks, "e2e": e2e}
+    if hot:
+        line["hot_l2"] = hot
     # free the device buffers before the CPU legs (and the next workload)
     del sets, base
     torch.cuda.synchronize()
@@ -880,7 +946,7 @@ MIN_STEPS = {"tiny": 20000, "llada": 20000, "ragged": 3000, "dream": 3000, "long
              "long_b16": 1000, "long_b32": 1000}
 # per-workload fields kept in the per_config object
 PER_CONFIG_KEYS = ("value", "unit", "steps", "ms_per_step", "dtype", "config", "roofline",
-                   "kernels", "clocks", "e2e", "cpu_baseline")
+                   "kernels", "clocks", "e2e", "cpu_baseline", "hot_l2")
 
 
 def run_ours(args, world, rank, local):

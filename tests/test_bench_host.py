@@ -63,3 +63,25 @@ def test_part_bytes_add_up():
     kept = tq * H * D * 2 + tq * H * 4
     q = tq * H * D * 2
     assert cached + window == full + q + 2 * kept
+
+
+def test_attention_roofline_terms():
+    """The attention's two roofline terms from the workload's own byte and flop
+    counts: the Dream-shaped layer sits past the ridge (tensor-bound at the
+    sustained dense peak), the LLaDA-shaped layer and the long context are
+    HBM-bound, and the float32 path has no tensor term."""
+    hbm, tf = 6791.7, 1714.0
+
+    def terms(name, tensor=True, us=100.0):
+        p = synth.make_problem(synth.workload(name))
+        b = bench.algorithmic_bytes(p)[0]
+        return b, bench.flops(p), bench.attn_roofline(b, bench.flops(p), hbm, tf, us, tensor)
+
+    b, f, r = terms("dream")
+    assert r["bound"] == "tensor"
+    assert r["hbm_us"] == pytest.approx(b / (hbm * 1e9) * 1e6)
+    assert r["tensor_us"] == pytest.approx(f / (tf * 1e12) * 1e6)
+    assert r["frac_of_roofline"] == pytest.approx(r["tensor_us"] / 100.0)
+    assert terms("llada")[2]["bound"] == "hbm"
+    r = terms("tiny", tensor=False)[2]
+    assert r["tensor_us"] is None and r["bound"] == "hbm"
