@@ -223,8 +223,13 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
   // (L2-only loads, nothing cached in L1; ids clamped to the pool): if the
   // previous kernel changes them, a prefetch is wasted, and every value the
   // attention uses is read again after the dependency wait. L2 is the point of
-  // coherence, so a prefetched line never hides a later write.
-  if (warp == 0 && a.page_table != nullptr && !a.longest_first && a.part != 2) {
+  // coherence, so a prefetched line never hides a later write. Only where the
+  // split's whole key range fits in the ring's first fill: there the prefetch
+  // shortens the latency chain (LLaDA layer: 10.4 -> 9.9 us), while over long
+  // ranges it only crowds the start (Dream layer 75.6 -> 76.4 us, Long B=16
+  // 331.7 -> 334.5 us with it).
+  if (warp == 0 && a.page_table != nullptr && !a.longest_first && a.part != 2 &&
+      a.tiles_per_split <= NS) {
     const int ppt0 = N / a.block_size;
     const int lp = split * a.tiles_per_split * ppt0 + lane;
     const int hint_c = __ldcg(a.ctx_len + b);
@@ -871,6 +876,28 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
         const int key = crow & 7;
         const int r2 = r_begin + crow;
         const int64_t hr2 = (int64_t)(q0 + r2 / G) * H + g * G + r2 % G;
+        // This lane's chunk of the row from every source CTA, requested before
+        // the weights are known, so the (max, sum) pairs and the values travel
+        // together; a part of weight 0 is skipped below, not loaded on demand.
+        const uint32_t off = lr * L::kRowBytes + (D == 128 ? ((sub ^ key) << 4)
+                                                            : (((sub >> 1) ^ key) << 4) + (sub & 1) * 8);
+        uint32_t v[kMaxCluster][kCols / 2];
+#pragma unroll
+        for (int j = 0; j < kMaxCluster; ++j) {
+#pragma unroll
+          for (int c = 0; c < kCols / 2; ++c) v[j][c] = 0u;
+          if (valid && j < cs) {
+            const uint32_t src = dsmem_addr(own_blk + off, j);
+            if (D == 128) {
+              const float4 q = dsmem_ld_f4(src);
+              v[j][0] = __float_as_uint(q.x); v[j][1] = __float_as_uint(q.y);
+              v[j][2 % (kCols / 2)] = __float_as_uint(q.z); v[j][3 % (kCols / 2)] = __float_as_uint(q.w);
+            } else {
+              const float2 q = dsmem_ld_f2(src);
+              v[j][0] = __float_as_uint(q.x); v[j][1 % (kCols / 2)] = __float_as_uint(q.y);
+            }
+          }
+        }
         float2 ml = make_float2(-INFINITY, 0.f);
         if (valid && sub < cs) ml = dsmem_ld_f2(dsmem_addr(own_blk + LR * L::kRowBytes + lr * 8, sub));
         // a kept cached part is one more normalised part: (its lse in log2 units, 1)
@@ -893,27 +920,9 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
 #pragma unroll
           for (int c = 0; c < kCols; ++c) acc[c] = wp * bf16_bits_to_float(pr[c]);
         }
-        const uint32_t off = lr * L::kRowBytes + (D == 128 ? ((sub ^ key) << 4)
-                                                            : (((sub >> 1) ^ key) << 4) + (sub & 1) * 8);
         float wj[kMaxCluster];
-        uint32_t v[kMaxCluster][kCols / 2];
 #pragma unroll
-        for (int j = 0; j < kMaxCluster; ++j) {
-          wj[j] = __shfl_sync(0xffffffffu, w, (hw << 4) + j);
-#pragma unroll
-          for (int c = 0; c < kCols / 2; ++c) v[j][c] = 0u;
-          if (j < cs && wj[j] > 0.f) {
-            const uint32_t src = dsmem_addr(own_blk + off, j);
-            if (D == 128) {
-              const float4 q = dsmem_ld_f4(src);
-              v[j][0] = __float_as_uint(q.x); v[j][1] = __float_as_uint(q.y);
-              v[j][2 % (kCols / 2)] = __float_as_uint(q.z); v[j][3 % (kCols / 2)] = __float_as_uint(q.w);
-            } else {
-              const float2 q = dsmem_ld_f2(src);
-              v[j][0] = __float_as_uint(q.x); v[j][1 % (kCols / 2)] = __float_as_uint(q.y);
-            }
-          }
-        }
+        for (int j = 0; j < kMaxCluster; ++j) wj[j] = __shfl_sync(0xffffffffu, w, (hw << 4) + j);
 #pragma unroll
         for (int j = 0; j < kMaxCluster; ++j) {
           if (!(j < cs && wj[j] > 0.f)) continue;
