@@ -862,14 +862,15 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
     }
     // 3) compose the rows this CTA owns, reading each source CTA's block for this
     //    owner (block `split` of its staging area) straight from its shared
-    //    memory: half a warp per row, lane c of the half holds columns
-    //    [c * D/16, (c + 1) * D/16); every source's chunk of a row is loaded before
-    //    any is used.
+    //    memory: every warp of the CTA (the producers and issuers are done), half
+    //    a warp per row, lane c of the half holds columns [c * D/16, (c + 1) *
+    //    D/16); every source's chunk of a row is loaded before any is used.
     const uint32_t own_blk = stg + split * BS;  // the same offset in every CTA
-    if (warp >= L::kFirstSoft) {
+    {
       constexpr int kCols = D / 16;
+      constexpr int kWarps = L::kThreads / 32;
       const int hw = lane >> 4, sub = lane & 15;
-      for (int lr0 = (warp - L::kFirstSoft) * 2; lr0 * cs + split < nrows; lr0 += 2 * L::kSoftWarps) {
+      for (int lr0 = warp * 2; lr0 * cs + split < nrows; lr0 += 2 * kWarps) {
         const int lr = lr0 + hw;
         const int crow = lr * cs + split;  // CTA row of this half-warp
         const bool valid = crow < nrows;
