@@ -862,40 +862,53 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
     }
     // 3) compose the rows this CTA owns, reading each source CTA's block for this
     //    owner (block `split` of its staging area) straight from its shared
-    //    memory: every warp of the CTA (the producers and issuers are done), half
-    //    a warp per row, lane c of the half holds columns [c * D/16, (c + 1) *
-    //    D/16); every source's chunk of a row is loaded before any is used.
+    //    memory: every warp of the CTA (the producers and issuers are done), LPR
+    //    lanes per row, lane c of a row's group holds columns [c * D/LPR,
+    //    (c + 1) * D/LPR); every source's chunks of a row are requested before any
+    //    is used. Eight lanes per row for 128-row tiles, whose CTAs own many
+    //    rows (twice the rows per round, twice the loads per lane: Dream layer
+    //    72.3 -> 71.0 us); sixteen for 64-row tiles, whose owners' rows fit one
+    //    round either way (LLaDA layer: 9.6 us, 10.5 with eight).
     const uint32_t own_blk = stg + split * BS;  // the same offset in every CTA
+    constexpr int kWarps = L::kThreads / 32;
     {
-      constexpr int kCols = D / 16;
-      constexpr int kWarps = L::kThreads / 32;
-      const int hw = lane >> 4, sub = lane & 15;
-      for (int lr0 = warp * 2; lr0 * cs + split < nrows; lr0 += 2 * kWarps) {
-        const int lr = lr0 + hw;
-        const int crow = lr * cs + split;  // CTA row of this half-warp
+      constexpr int LPR = QR == 128 ? 8 : 16;      // lanes per row
+      constexpr int kCols = D / LPR;               // columns per lane
+      constexpr int kBytes = 2 * kCols;            // 8, 16 or 32 bytes per lane
+      constexpr int kRowsPerWarp = 32 / LPR;
+      const int grp = lane / LPR, sub = lane % LPR;
+      for (int lr0 = warp * kRowsPerWarp; lr0 * cs + split < nrows; lr0 += kRowsPerWarp * kWarps) {
+        const int lr = lr0 + grp;
+        const int crow = lr * cs + split;  // CTA row of this lane group
         const bool valid = crow < nrows;
         const int key = crow & 7;
         const int r2 = r_begin + crow;
         const int64_t hr2 = (int64_t)(q0 + r2 / G) * H + g * G + r2 % G;
-        // This lane's chunk of the row from every source CTA, requested before
+        // This lane's bytes of the row from every source CTA, requested before
         // the weights are known, so the (max, sum) pairs and the values travel
         // together; a part of weight 0 is skipped below, not loaded on demand.
-        const uint32_t off = lr * L::kRowBytes + (D == 128 ? ((sub ^ key) << 4)
-                                                            : (((sub >> 1) ^ key) << 4) + (sub & 1) * 8);
         uint32_t v[kMaxCluster][kCols / 2];
 #pragma unroll
         for (int j = 0; j < kMaxCluster; ++j) {
 #pragma unroll
           for (int c = 0; c < kCols / 2; ++c) v[j][c] = 0u;
           if (valid && j < cs) {
-            const uint32_t src = dsmem_addr(own_blk + off, j);
-            if (D == 128) {
-              const float4 q = dsmem_ld_f4(src);
-              v[j][0] = __float_as_uint(q.x); v[j][1] = __float_as_uint(q.y);
-              v[j][2 % (kCols / 2)] = __float_as_uint(q.z); v[j][3 % (kCols / 2)] = __float_as_uint(q.w);
-            } else {
-              const float2 q = dsmem_ld_f2(src);
-              v[j][0] = __float_as_uint(q.x); v[j][1 % (kCols / 2)] = __float_as_uint(q.y);
+            if constexpr (kBytes >= 16) {
+#pragma unroll
+              for (int h = 0; h < kBytes / 16; ++h) {
+                const int chunk = sub * (kBytes / 16) + h;  // 16-byte chunk of the row
+                const float4 q =
+                    dsmem_ld_f4(dsmem_addr(own_blk + lr * L::kRowBytes + ((chunk ^ key) << 4), j));
+                v[j][4 * h] = __float_as_uint(q.x);
+                v[j][4 * h + 1] = __float_as_uint(q.y);
+                v[j][4 * h + 2] = __float_as_uint(q.z);
+                v[j][4 * h + 3] = __float_as_uint(q.w);
+              }
+            } else {  // half a chunk
+              const float2 q = dsmem_ld_f2(
+                  dsmem_addr(own_blk + lr * L::kRowBytes + (((sub >> 1) ^ key) << 4) + (sub & 1) * 8, j));
+              v[j][0] = __float_as_uint(q.x);
+              v[j][1] = __float_as_uint(q.y);
             }
           }
         }
@@ -905,13 +918,13 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
         const float lp = (a.prev_lse && valid) ? a.prev_lse[hr2] * 1.4426950408889634f : -INFINITY;
         float mx = fmaxf(ml.x, lp);
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        for (int o = LPR / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         // weight of a normalised part: 2^(m_j - M) * l_j
         const float w = (sub < cs && ml.y > 0.f) ? fast_exp2(ml.x - mx) * ml.y : 0.f;
         const float wp = lp > -INFINITY ? fast_exp2(lp - mx) : 0.f;
         float ws = w;
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+        for (int o = LPR / 2; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
         ws += wp;
         float acc[kCols];
 #pragma unroll
@@ -923,7 +936,7 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
         }
         float wj[kMaxCluster];
 #pragma unroll
-        for (int j = 0; j < kMaxCluster; ++j) wj[j] = __shfl_sync(0xffffffffu, w, (hw << 4) + j);
+        for (int j = 0; j < kMaxCluster; ++j) wj[j] = __shfl_sync(0xffffffffu, w, grp * LPR + j);
 #pragma unroll
         for (int j = 0; j < kMaxCluster; ++j) {
           if (!(j < cs && wj[j] > 0.f)) continue;
@@ -940,11 +953,13 @@ __global__ void __launch_bounds__((Layout<D, NS, QR, MT>::kThreads),
           for (int c = 0; c < kCols / 2; ++c)
             pk[c] = pack_bf16x2(acc[2 * c] * inv, acc[2 * c + 1] * inv);
           uint16_t *dst = reinterpret_cast<uint16_t *>(a.out) + hr2 * D + sub * kCols;
-          if (D == 128)
-            *reinterpret_cast<uint4 *>(dst) =
-                make_uint4(pk[0], pk[1], pk[2 % (kCols / 2)], pk[3 % (kCols / 2)]);
-          else
-            *reinterpret_cast<uint2 *>(dst) = make_uint2(pk[0], pk[1 % (kCols / 2)]);
+          if constexpr (kBytes >= 16) {
+#pragma unroll
+            for (int h = 0; h < kBytes / 16; ++h)
+              reinterpret_cast<uint4 *>(dst)[h] = make_uint4(pk[4 * h], pk[4 * h + 1], pk[4 * h + 2], pk[4 * h + 3]);
+          } else {
+            *reinterpret_cast<uint2 *>(dst) = make_uint2(pk[0], pk[1]);
+          }
           if (sub == 0 && a.lse_out) a.lse_out[hr2] = (mx + __log2f(ws)) * 0.6931471805599453f;
         }
       }
